@@ -1,0 +1,253 @@
+"""The oracle for the Kimi Delta Attention (KDA) token mixer.
+
+TEST INFRASTRUCTURE ONLY: the test suite, the package smoke check and the benchmark's
+CPU-baseline leg may import this package; the product path never does.  It shares no code
+with the CUDA library and never imports it.
+
+``kda_oracle.c`` holds the arithmetic (plain C, fp64, token by token).  This module only
+builds it with gcc and marshals numpy arrays into it.  Every function returns fp64 results
+computed from the exact stored values of its inputs (fp32 arrays, or bf16 given as the
+``torch.bfloat16`` / raw uint16 bit patterns).
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py`` (closed forms,
+invariants, brute force and library routines); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libkda_oracle.so")
+
+F32, BF16, F64 = 0, 1, 2
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compiles kda_oracle.c with gcc into oracle/_build/libkda_oracle.so (plain -O2)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _KdaArgs(ctypes.Structure):
+    _fields_ = [
+        ("H", ctypes.c_int), ("dk", ctypes.c_int), ("dv", ctypes.c_int),
+        ("n_seqs", ctypes.c_int), ("cu_seqlens", ctypes.c_void_p),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("qkv_dtype", ctypes.c_int),
+        ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+        ("init_state", ctypes.c_void_p), ("state_dtype", ctypes.c_int),
+        ("gate", ctypes.c_void_p), ("gate_dtype", ctypes.c_int),
+        ("norm_w", ctypes.c_void_p),
+        ("scale", ctypes.c_double), ("l2_eps", ctypes.c_double),
+        ("norm_eps", ctypes.c_double), ("g_min", ctypes.c_double),
+        ("qk_l2norm", ctypes.c_int),
+        ("n_units", ctypes.c_int), ("units", ctypes.c_void_p),
+        ("out_offset", ctypes.c_void_p), ("out", ctypes.c_void_p),
+        ("final_state", ctypes.c_void_p), ("state_norm", ctypes.c_void_p),
+        ("n_threads", ctypes.c_int),
+    ]
+
+
+class _ProArgs(ctypes.Structure):
+    _fields_ = [
+        ("n_seqs", ctypes.c_int), ("cu_seqlens", ctypes.c_void_p),
+        ("H", ctypes.c_int), ("d", ctypes.c_int),
+        ("x", ctypes.c_void_p), ("x_dtype", ctypes.c_int),
+        ("w", ctypes.c_void_p), ("w_dtype", ctypes.c_int),
+        ("conv_state_in", ctypes.c_void_p), ("conv_state_out", ctypes.c_void_p),
+        ("l2norm_qk", ctypes.c_int), ("l2_eps", ctypes.c_double),
+        ("y", ctypes.c_void_p),
+        ("beta_logit", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+        ("g_raw", ctypes.c_void_p), ("g", ctypes.c_void_p), ("g_min", ctypes.c_double),
+    ]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.oracle_kda_forward.argtypes = [ctypes.POINTER(_KdaArgs)]
+            lib.oracle_kda_forward.restype = ctypes.c_int
+            lib.oracle_prologue.argtypes = [ctypes.POINTER(_ProArgs)]
+            lib.oracle_prologue.restype = ctypes.c_int
+            lib.oracle_state_bytes.argtypes = [ctypes.c_int] * 4
+            lib.oracle_state_bytes.restype = ctypes.c_int64
+            lib.oracle_conv_tail_bytes.argtypes = [ctypes.c_int] * 4
+            lib.oracle_conv_tail_bytes.restype = ctypes.c_int64
+            _lib = lib
+    return _lib
+
+
+def _as_np(x):
+    """Returns (contiguous numpy array, dtype code).  bf16 torch tensors become uint16 bits."""
+    if x is None:
+        return None, F32
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            if x.dtype == torch.bfloat16:
+                return x.view(torch.int16).numpy().view(np.uint16), BF16
+            if x.dtype == torch.float32:
+                return x.numpy(), F32
+            if x.dtype == torch.float64:
+                return x.numpy(), F64
+            if x.dtype == torch.int32:
+                return x.numpy(), F32
+            raise TypeError(f"oracle: unsupported tensor dtype {x.dtype}")
+    except ImportError:  # pragma: no cover
+        pass
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        return x, BF16
+    if x.dtype == np.float32:
+        return x, F32
+    if x.dtype == np.float64:
+        return x, F64
+    if x.dtype == np.int32:
+        return x, F32
+    raise TypeError(f"oracle: unsupported array dtype {x.dtype}")
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def kda_forward(q, k, v, g, beta, cu_seqlens, *, init_state=None, gate=None, norm_w=None,
+                scale=1.0, l2_eps=1e-6, norm_eps=1e-6, g_min=-5.0, qk_l2norm=True,
+                units=None, n_threads=None, want_state_norm=False):
+    """Token-by-token fp64 KDA over a packed batch.
+
+    q, k: [T_tot, H, dk]; v: [T_tot, H, dv] (fp32 or bf16); g: [T_tot, H, dk] fp32 raw
+    log-retention (clamped at g_min here); beta: [T_tot, H] fp32 in (0, 1);
+    cu_seqlens: int32 [N + 1]; init_state: [N, H, dk, dv] or None; gate: [T_tot, H, dv]
+    output-gate logits or None (no output norm); norm_w: [dv] fp32 or None (ones).
+    units: list of (sequence, head) to compute, default all.
+
+    Returns dict(out=[T_tot, H, dv] fp64 when every unit is computed, otherwise
+    unit_out=list of [len, dv] arrays), final_state=[n_units, dk, dv] fp64 (in the units'
+    order; reshaped to [N, H, dk, dv] when all units are computed), and state_norm when asked.
+    """
+    lib = _load()
+    qn, qdt = _as_np(q)
+    kn, kdt = _as_np(k)
+    vn, vdt = _as_np(v)
+    if not (qdt == kdt == vdt):
+        raise TypeError("oracle: q, k, v must share a storage type")
+    gn, _ = _as_np(g)
+    bn, _ = _as_np(beta)
+    cu, _ = _as_np(cu_seqlens)
+    cu = cu.astype(np.int32)
+    T, H, dk = qn.shape
+    dv = vn.shape[2]
+    N = cu.shape[0] - 1
+    sn, sdt = _as_np(init_state)
+    gt, gdt = _as_np(gate)
+    wn, _ = _as_np(norm_w)
+    full = units is None
+    if full:
+        units = [(n, h) for n in range(N) for h in range(H)]
+    units_arr = np.ascontiguousarray(np.asarray(units, dtype=np.int32).reshape(-1, 2))
+    lens = np.array([cu[n + 1] - cu[n] for n, _ in units_arr], dtype=np.int64)
+    # each unit's [len, dv] block is written contiguously; the full [T, H, dv] view is
+    # scattered together afterwards
+    offs = np.zeros(len(units_arr), dtype=np.int64)
+    if len(units_arr):
+        offs[1:] = np.cumsum(lens[:-1] * dv)
+    out = np.zeros(int(lens.sum()) * dv, dtype=np.float64)
+    fin = np.zeros((len(units_arr), dk, dv), dtype=np.float64)
+    snorm = np.zeros(int(lens.sum()), dtype=np.float64) if want_state_norm else None
+    args = _KdaArgs(
+        H=H, dk=dk, dv=dv, n_seqs=N, cu_seqlens=_ptr(cu),
+        q=_ptr(qn), k=_ptr(kn), v=_ptr(vn), qkv_dtype=qdt,
+        g=_ptr(gn), beta=_ptr(bn),
+        init_state=_ptr(sn), state_dtype=sdt,
+        gate=_ptr(gt), gate_dtype=gdt, norm_w=_ptr(wn),
+        scale=scale, l2_eps=l2_eps, norm_eps=norm_eps, g_min=g_min,
+        qk_l2norm=1 if qk_l2norm else 0,
+        n_units=len(units_arr), units=_ptr(units_arr), out_offset=_ptr(offs),
+        out=_ptr(out), final_state=_ptr(fin), state_norm=_ptr(snorm),
+        n_threads=n_threads or (os.cpu_count() or 1),
+    )
+    if lib.oracle_kda_forward(ctypes.byref(args)) != 0:
+        raise ValueError("oracle_kda_forward rejected its arguments")
+    res = {}
+    unit_out = [out[o:o + l * dv].reshape(l, dv) for o, l in zip(offs, lens)]
+    if full:
+        o_full = np.zeros((T, H, dv), dtype=np.float64)
+        for (n, h), uo in zip(units_arr, unit_out):
+            o_full[cu[n]:cu[n + 1], h, :] = uo
+        res["out"] = o_full
+        res["final_state"] = fin.reshape(N, H, dk, dv)
+    else:
+        res["unit_out"] = unit_out
+        res["final_state"] = fin
+    if want_state_norm:
+        res["state_norm"] = [snorm[o // dv:o // dv + l] for o, l in zip(offs, lens)]
+    return res
+
+
+def prologue(x, conv_w, cu_seqlens, H, d, *, conv_state=None, l2norm_qk=False, l2_eps=1e-6,
+             beta_logit=None, g_raw=None, g_min=-5.0):
+    """Width-4 causal short convolution + SiLU over the concatenated q|k|v streams.
+
+    x: [T_tot, 3*H*d] (fp32 or bf16); conv_w: [3*H*d, 4]; conv_state: [N, 3, 3*H*d] in x's
+    storage type or None.  Returns dict(y=[T_tot, 3*H*d] fp64, conv_state=[N, 3, 3*H*d] in
+    x's storage type (numpy; uint16 bits for bf16), beta, g when their inputs are given).
+    """
+    lib = _load()
+    xn, xdt = _as_np(x)
+    wn, wdt = _as_np(conv_w)
+    cu, _ = _as_np(cu_seqlens)
+    cu = cu.astype(np.int32)
+    N = cu.shape[0] - 1
+    C = 3 * H * d
+    T = xn.shape[0]
+    sn, sdt = _as_np(conv_state)
+    if sn is not None and sdt != xdt:
+        raise TypeError("oracle: conv state must share x's storage type")
+    y = np.zeros((T, C), dtype=np.float64)
+    st_out = np.zeros((N, 3, C), dtype=xn.dtype)
+    bl, _ = _as_np(beta_logit)
+    gr, _ = _as_np(g_raw)
+    beta = np.zeros(bl.shape, dtype=np.float64) if bl is not None else None
+    g = np.zeros(gr.shape, dtype=np.float64) if gr is not None else None
+    args = _ProArgs(
+        n_seqs=N, cu_seqlens=_ptr(cu), H=H, d=d, x=_ptr(xn), x_dtype=xdt,
+        w=_ptr(wn), w_dtype=wdt, conv_state_in=_ptr(sn), conv_state_out=_ptr(st_out),
+        l2norm_qk=1 if l2norm_qk else 0, l2_eps=l2_eps, y=_ptr(y),
+        beta_logit=_ptr(bl), beta=_ptr(beta), g_raw=_ptr(gr), g=_ptr(g), g_min=g_min,
+    )
+    if lib.oracle_prologue(ctypes.byref(args)) != 0:
+        raise ValueError("oracle_prologue rejected its arguments")
+    res = {"y": y, "conv_state": st_out}
+    if beta is not None:
+        res["beta"] = beta
+    if g is not None:
+        res["g"] = g
+    return res
+
+
+def state_bytes(H, dk, dv, elem_bytes):
+    """Bytes of one layer's recurrent state for one sequence."""
+    return int(_load().oracle_state_bytes(H, dk, dv, elem_bytes))
+
+
+def conv_tail_bytes(H, d, width, elem_bytes):
+    """Bytes of one layer's short-convolution tail for one sequence."""
+    return int(_load().oracle_conv_tail_bytes(H, d, width, elem_bytes))
