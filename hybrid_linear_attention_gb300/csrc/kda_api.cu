@@ -1,0 +1,308 @@
+// kda_api.cu -- the C ABI (include/kda.h): host-side validation, then kernel launches.
+// Nothing here allocates device memory; every buffer belongs to the caller.
+#include "../../include/kda.h"
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "kda_internal.h"
+#include "kda_prefill_tc.h"
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+// Sticky error word written by kernels whose bounded waits ran out.
+__device__ int g_device_error = 0;
+
+constexpr int kMaxDevices = 64;
+int *g_err_ptr[kMaxDevices] = {nullptr};
+
+int *device_error_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_err_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int *>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool opt_aligned16(const void *p) { return p == nullptr || aligned16(p); }
+
+kda_status check_params(const kda_params *p) {
+  if (!p) return KDA_ERR_INVALID_ARG;
+  if (p->H < 1 || p->d_k < 1 || p->d_v < 1) return KDA_ERR_INVALID_ARG;
+  if (!(p->l2_eps >= 0.f) || !(p->norm_eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+  if (!(p->g_min <= 0.f)) return KDA_ERR_INVALID_ARG;  // also rejects NaN
+  if (p->scale != p->scale) return KDA_ERR_INVALID_ARG;
+  if ((p->io_dtype != KDA_F32 && p->io_dtype != KDA_BF16) ||
+      (p->state_dtype != KDA_F32 && p->state_dtype != KDA_BF16))
+    return KDA_ERR_INVALID_ARG;
+  if (p->d_k != p->d_v) return KDA_ERR_UNSUPPORTED;
+  if (p->d_k != 16 && p->d_k != 128) return KDA_ERR_UNSUPPORTED;
+  if (p->H > 21845) return KDA_ERR_UNSUPPORTED;  // 3*H grid rows of the prologue
+  return KDA_OK;
+}
+
+kda_status finish(cudaError_t e, int n_launches) {
+  g_launches += (uint64_t)n_launches;
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda::RecArgs base_args(const kda_params *p) {
+  kda::RecArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.H = p->H;
+  a.scale = p->scale;
+  a.l2_eps = p->l2_eps;
+  a.norm_eps = p->norm_eps;
+  a.g_min = p->g_min;
+  a.qk_l2norm = p->qk_l2norm ? 1 : 0;
+  a.err = device_error_ptr();
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+void kda_params_default(kda_params *p) {
+  if (!p) return;
+  p->H = 64;
+  p->d_k = p->d_v = 128;
+  p->scale = 1.0f;
+  p->l2_eps = 1e-6f;
+  p->norm_eps = 1e-6f;
+  p->g_min = -5.0f;
+  p->qk_l2norm = 1;
+  p->io_dtype = KDA_BF16;
+  p->state_dtype = KDA_F32;
+}
+
+const char *kda_status_string(kda_status s) {
+  switch (s) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: shape or dtype not supported";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA launch or runtime error";
+    case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace too small";
+    case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device wait ran out";
+  }
+  return "unknown kda_status";
+}
+
+size_t kda_state_bytes(const kda_params *p) {
+  if (!p || p->H < 1 || p->d_k < 1 || p->d_v < 1) return 0;
+  return (size_t)p->H * p->d_k * p->d_v * (p->state_dtype == KDA_BF16 ? 2 : 4);
+}
+
+size_t kda_prefill_workspace_size(const kda_params *p, int n_seqs, int64_t total_tokens) {
+  (void)n_seqs;
+  (void)total_tokens;
+  if (check_params(p) != KDA_OK) return 0;
+  return 0;
+}
+
+kda_status kda_prologue(const kda_params *p, const void *x_raw, const void *conv_w,
+                        void *conv_state, const int32_t *cu_seqlens, int n_seqs,
+                        int64_t total_tokens, int l2norm_qk, const float *beta_logit,
+                        const float *g_raw, void *q, void *k, void *v, float *beta, float *g,
+                        cudaStream_t stream) {
+  kda_status st = check_params(p);
+  if (st != KDA_OK) return st;
+  if (n_seqs < 0 || total_tokens < 0 || n_seqs > 65535) return KDA_ERR_INVALID_ARG;
+  if (n_seqs == 0 && total_tokens > 0) return KDA_ERR_INVALID_ARG;
+  if (total_tokens > (int64_t)INT32_MAX * 16) return KDA_ERR_UNSUPPORTED;  // prologue grid
+  if (n_seqs == 0) return KDA_OK;
+  if (!x_raw || !conv_w || !cu_seqlens || !q || !k || !v) return KDA_ERR_INVALID_ARG;
+  if ((beta_logit == nullptr) != (beta == nullptr)) return KDA_ERR_INVALID_ARG;
+  if ((g_raw == nullptr) != (g == nullptr)) return KDA_ERR_INVALID_ARG;
+  if (!aligned16(x_raw) || !aligned16(conv_w) || !opt_aligned16(conv_state) || !aligned16(q) ||
+      !aligned16(k) || !aligned16(v) || !opt_aligned16(beta_logit) || !opt_aligned16(g_raw) ||
+      !opt_aligned16(beta) || !opt_aligned16(g) || !aligned16(cu_seqlens))
+    return KDA_ERR_INVALID_ARG;
+  kda::ProArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.H = p->H;
+  a.n_seqs = n_seqs;
+  a.T = total_tokens;
+  a.l2_eps = p->l2_eps;
+  a.g_min = p->g_min;
+  a.l2norm_qk = l2norm_qk ? 1 : 0;
+  a.x = x_raw;
+  a.conv_w = conv_w;
+  a.conv_state = conv_state;
+  a.cu_seqlens = cu_seqlens;
+  a.beta_logit = beta_logit;
+  a.g_raw = g_raw;
+  a.q = q, a.k = k, a.v = v;
+  a.beta = beta, a.g = g;
+  const int n_launch = (total_tokens > 0 ? 1 : 0) + (conv_state ? 1 : 0);
+  return finish(kda::launch_prologue(a, p->d_k, p->io_dtype == KDA_BF16, stream), n_launch);
+}
+
+kda_status kda_prefill(const kda_params *p, const void *q, const void *k, const void *v,
+                       const float *g, const float *beta, const void *init_state,
+                       const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
+                       const void *gate_logit, const float *norm_w, void *out,
+                       void *final_state, void *workspace, size_t ws_bytes,
+                       cudaStream_t stream) {
+  kda_status st = check_params(p);
+  if (st != KDA_OK) return st;
+  if (n_seqs < 0 || total_tokens < 0 || n_seqs > 65535) return KDA_ERR_INVALID_ARG;
+  if (n_seqs == 0 && total_tokens > 0) return KDA_ERR_INVALID_ARG;
+  if (ws_bytes < kda_prefill_workspace_size(p, n_seqs, total_tokens)) return KDA_ERR_WORKSPACE;
+  (void)workspace;
+  if (n_seqs == 0) return KDA_OK;
+  if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
+  if (!opt_aligned16(q) || !opt_aligned16(k) || !opt_aligned16(v) || !opt_aligned16(g) ||
+      !opt_aligned16(beta) || !opt_aligned16(init_state) || !aligned16(cu_seqlens) ||
+      !opt_aligned16(gate_logit) || !opt_aligned16(norm_w) || !opt_aligned16(out) ||
+      !opt_aligned16(final_state))
+    return KDA_ERR_INVALID_ARG;
+
+  const bool io_bf16 = p->io_dtype == KDA_BF16, st_bf16 = p->state_dtype == KDA_BF16;
+  if (kda::prefill_tc_supported(p->d_k, io_bf16)) {
+    kda::TcArgs t;
+    std::memset(&t, 0, sizeof t);
+    t.H = p->H;
+    t.n_seqs = n_seqs;
+    t.scale = p->scale;
+    t.l2_eps = p->l2_eps;
+    t.norm_eps = p->norm_eps;
+    t.g_min = p->g_min;
+    t.qk_l2norm = p->qk_l2norm ? 1 : 0;
+    t.q = q, t.k = k, t.v = v, t.g = g, t.beta = beta;
+    t.init_state = init_state;
+    t.final_state = final_state;
+    t.cu_seqlens = cu_seqlens;
+    t.gate = gate_logit;
+    t.norm_w = norm_w;
+    t.out = out;
+    t.err = device_error_ptr();
+    return finish(kda::launch_prefill_tc(t, st_bf16, stream), 1);
+  }
+  kda::RecArgs a = base_args(p);
+  a.n_seqs = n_seqs;
+  a.q = q, a.k = k, a.v = v, a.g = g, a.beta = beta;
+  a.cu_seqlens = cu_seqlens;
+  a.state_in = init_state;
+  a.state_out = final_state;
+  a.gate = gate_logit;
+  a.norm_w = norm_w;
+  a.out = out;
+  return finish(kda::launch_recurrent(a, p->d_k, io_bf16, st_bf16, stream), 1);
+}
+
+static kda_status decode_common(const kda_params *p, const float *g, const float *beta,
+                                void *state, int n_slots, const int32_t *slot_idx, int n_seqs,
+                                const void *gate_logit, const float *norm_w, void *out) {
+  kda_status st = check_params(p);
+  if (st != KDA_OK) return st;
+  if (n_seqs < 0 || n_seqs > 65535 || n_slots < 0) return KDA_ERR_INVALID_ARG;
+  if (n_seqs == 0) return KDA_OK;
+  if (!g || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
+  if (!slot_idx && n_slots < n_seqs) return KDA_ERR_INVALID_ARG;
+  if (!aligned16(g) || !aligned16(beta) || !aligned16(state) || !aligned16(out) ||
+      !opt_aligned16(slot_idx) || !opt_aligned16(gate_logit) || !opt_aligned16(norm_w))
+    return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
+kda_status kda_decode_step(const kda_params *p, const void *q, const void *k, const void *v,
+                           const float *g, const float *beta, void *state, int n_slots,
+                           const int32_t *slot_idx, int n_seqs, const void *gate_logit,
+                           const float *norm_w, void *out, cudaStream_t stream) {
+  kda_status st = decode_common(p, g, beta, state, n_slots, slot_idx, n_seqs, gate_logit,
+                                norm_w, out);
+  if (st != KDA_OK || n_seqs == 0) return st;
+  if (!q || !k || !v || !aligned16(q) || !aligned16(k) || !aligned16(v))
+    return KDA_ERR_INVALID_ARG;
+  kda::RecArgs a = base_args(p);
+  a.n_seqs = n_seqs;
+  a.q = q, a.k = k, a.v = v, a.g = g, a.beta = beta;
+  a.slot_idx = slot_idx;
+  a.state_in = state;
+  a.state_out = state;
+  a.gate = gate_logit;
+  a.norm_w = norm_w;
+  a.out = out;
+  return finish(kda::launch_recurrent(a, p->d_k, p->io_dtype == KDA_BF16,
+                                      p->state_dtype == KDA_BF16, stream),
+                1);
+}
+
+kda_status kda_decode_step_fused(const kda_params *p, const void *x_raw, const void *conv_w,
+                                 void *conv_state, const float *g, const float *beta,
+                                 void *state, int n_slots, const int32_t *slot_idx, int n_seqs,
+                                 const void *gate_logit, const float *norm_w, void *out,
+                                 cudaStream_t stream) {
+  kda_status st = decode_common(p, g, beta, state, n_slots, slot_idx, n_seqs, gate_logit,
+                                norm_w, out);
+  if (st != KDA_OK || n_seqs == 0) return st;
+  if (!x_raw || !conv_w || !conv_state || !aligned16(x_raw) || !aligned16(conv_w) ||
+      !aligned16(conv_state))
+    return KDA_ERR_INVALID_ARG;
+  kda::RecArgs a = base_args(p);
+  a.n_seqs = n_seqs;
+  a.x_raw = x_raw;
+  a.conv_w = conv_w;
+  a.conv_state = conv_state;
+  a.g = g, a.beta = beta;
+  a.slot_idx = slot_idx;
+  a.state_in = state;
+  a.state_out = state;
+  a.gate = gate_logit;
+  a.norm_w = norm_w;
+  a.out = out;
+  return finish(kda::launch_recurrent(a, p->d_k, p->io_dtype == KDA_BF16,
+                                      p->state_dtype == KDA_BF16, stream),
+                1);
+}
+
+kda_status kda_conv_state_update(const kda_params *p, const void *x_new, const void *conv_w,
+                                 void *conv_state, int n_slots, const int32_t *slot_idx,
+                                 int n_seqs, int channels, void *y, cudaStream_t stream) {
+  if (!p) return KDA_ERR_INVALID_ARG;
+  if (p->io_dtype != KDA_F32 && p->io_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (n_seqs < 0 || n_seqs > 65535 || channels < 1 || n_slots < 0) return KDA_ERR_INVALID_ARG;
+  if (n_seqs == 0) return KDA_OK;
+  if (!slot_idx && n_slots < n_seqs) return KDA_ERR_INVALID_ARG;
+  if (!x_new || !conv_w || !conv_state || !y || !aligned16(x_new) || !aligned16(conv_w) ||
+      !aligned16(conv_state) || !aligned16(y) || !opt_aligned16(slot_idx))
+    return KDA_ERR_INVALID_ARG;
+  kda::ConvArgs a;
+  a.n_seqs = n_seqs;
+  a.channels = channels;
+  a.x_new = x_new;
+  a.conv_w = conv_w;
+  a.conv_state = conv_state;
+  a.slot_idx = slot_idx;
+  a.y = y;
+  return finish(kda::launch_conv_update(a, p->io_dtype == KDA_BF16, stream), 1);
+}
+
+kda_status kda_check_device_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return KDA_ERR_CUDA;
+  int *ptr = device_error_ptr();
+  if (!ptr) return KDA_ERR_CUDA;
+  int host = 0;
+  if (cudaMemcpy(&host, ptr, sizeof host, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  if (host != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(ptr, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    return KDA_ERR_TIMEOUT;
+  }
+  return KDA_OK;
+}
+
+uint64_t kda_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// kda_internal.h -- argument blocks and launchers shared between the ABI layer and kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace kda {
+
+// Token-serial recurrence (decode, and the exact-fp32 prefill path).
+struct RecArgs {
+  int H, n_seqs;
+  float scale, l2_eps, norm_eps, g_min;
+  int qk_l2norm;
+  const void *q, *k, *v;       // [T, H, D] io (unused when x_raw is set)
+  const float *g, *beta;       // [T, H, D], [T, H]
+  const void *x_raw;           // fused conv (decode): [N, 3HD] io, or nullptr
+  const void *conv_w;          // [3HD, 4] io
+  void *conv_state;            // [slots, 3, 3HD] io, updated in place
+  const int32_t *cu_seqlens;   // prefill: [N + 1]; nullptr for decode (seq n = token n)
+  const int32_t *slot_idx;     // decode: state/conv slot of each sequence, or nullptr
+  const void *state_in;        // [N or slots, H, D, D] state dtype, or nullptr (zeros)
+  void *state_out;             // same layout, or nullptr; may equal state_in
+  const void *gate;            // [T, H, D] io or nullptr
+  const float *norm_w;         // [D] or nullptr
+  void *out;                   // [T, H, D] io
+  int *err;
+};
+
+struct ProArgs {
+  int H, n_seqs;
+  int64_t T;
+  float l2_eps, g_min;
+  int l2norm_qk;
+  const void *x;               // [T, 3HD]
+  const void *conv_w;          // [3HD, 4]
+  void *conv_state;            // [N, 3, 3HD] or nullptr
+  const int32_t *cu_seqlens;
+  const float *beta_logit;     // [T, H] or nullptr
+  const float *g_raw;          // [T, H, D] or nullptr
+  void *q, *k, *v;             // [T, H, D]
+  float *beta, *g;
+};
+
+struct ConvArgs {
+  int n_seqs, channels;
+  const void *x_new;           // [N, C]
+  const void *conv_w;          // [C, 4]
+  void *conv_state;            // [slots, 3, C]
+  const int32_t *slot_idx;
+  void *y;                     // [N, C]
+};
+
+cudaError_t launch_recurrent(const RecArgs &a, int D, bool io_bf16, bool st_bf16,
+                             cudaStream_t s);
+cudaError_t launch_prologue(const ProArgs &a, int D, bool io_bf16, cudaStream_t s);
+cudaError_t launch_conv_update(const ConvArgs &a, bool io_bf16, cudaStream_t s);
+
+}  // namespace kda

@@ -1,0 +1,220 @@
+"""Python binding of libkda.so (include/kda.h), argument marshalling only.
+
+Each function has the name of the C entry point it calls, takes torch CUDA tensors (or None
+for a NULL pointer), checks dtypes/devices/contiguity, passes raw pointers and the current
+(or given) CUDA stream, and raises KdaError on a non-OK status.  All arithmetic runs in the
+library's CUDA kernels; there is no fallback.  If libkda.so has not been built, loading it
+raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_WORKSPACE, \
+    KDA_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+KDA_F32, KDA_BF16 = 0, 1
+
+_TORCH_OF = {KDA_F32: torch.float32, KDA_BF16: torch.bfloat16}
+
+EXPORTS = (
+    "kda_params_default", "kda_status_string", "kda_state_bytes", "kda_prefill_workspace_size",
+    "kda_prologue", "kda_prefill", "kda_decode_step", "kda_conv_state_update",
+    "kda_decode_step_fused", "kda_check_device_error", "kda_launch_count",
+)
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+class KdaParams(ctypes.Structure):
+    _fields_ = [
+        ("H", ctypes.c_int), ("d_k", ctypes.c_int), ("d_v", ctypes.c_int),
+        ("scale", ctypes.c_float), ("l2_eps", ctypes.c_float), ("norm_eps", ctypes.c_float),
+        ("g_min", ctypes.c_float), ("qk_l2norm", ctypes.c_int),
+        ("io_dtype", ctypes.c_int), ("state_dtype", ctypes.c_int),
+    ]
+
+    @property
+    def io_torch(self):
+        return _TORCH_OF[self.io_dtype]
+
+    @property
+    def state_torch(self):
+        return _TORCH_OF[self.state_dtype]
+
+
+_lock = threading.Lock()
+_lib = None
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+_P = ctypes.POINTER(KdaParams)
+
+
+def load():
+    """Loads libkda.so (built by hybrid_linear_attention_gb300.build.build())."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "hybrid_linear_attention_gb300.build.build() (nvcc, sm_103a)")
+        lib = ctypes.CDLL(LIB_PATH)
+        sig = {
+            "kda_params_default": (None, [_P]),
+            "kda_status_string": (ctypes.c_char_p, [_i32]),
+            "kda_state_bytes": (_sz, [_P]),
+            "kda_prefill_workspace_size": (_sz, [_P, _i32, _i64]),
+            "kda_prologue": (_i32, [_P, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _vp, _vp,
+                                    _vp, _vp, _vp, _vp, _vp, _vp]),
+            "kda_prefill": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp,
+                                   _vp, _vp, _vp, _sz, _vp]),
+            "kda_decode_step": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _vp,
+                                       _vp, _vp, _vp]),
+            "kda_conv_state_update": (_i32, [_P, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _vp,
+                                             _vp]),
+            "kda_decode_step_fused": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32,
+                                             _vp, _vp, _vp, _vp]),
+            "kda_check_device_error": (_i32, [_vp]),
+            "kda_launch_count": (ctypes.c_uint64, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def status_string(status):
+    try:
+        return load().kda_status_string(int(status)).decode()
+    except Exception:  # the library itself failed to load
+        return f"status {status}"
+
+
+def _check(status, where):
+    if status != KDA_OK:
+        raise KdaError(status, where)
+
+
+def params(H=64, d=128, *, scale=1.0, l2_eps=1e-6, norm_eps=1e-6, g_min=-5.0, qk_l2norm=True,
+           io_dtype=torch.bfloat16, state_dtype=torch.float32):
+    """Builds a kda_params struct (defaults: the pages' configuration)."""
+    code = {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16}
+    return KdaParams(H=H, d_k=d, d_v=d, scale=scale, l2_eps=l2_eps, norm_eps=norm_eps,
+                     g_min=g_min, qk_l2norm=1 if qk_l2norm else 0,
+                     io_dtype=code[io_dtype], state_dtype=code[state_dtype])
+
+
+def kda_params_default():
+    p = KdaParams()
+    load().kda_params_default(ctypes.byref(p))
+    return p
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch tensor or None")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor (device pointer)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
+
+
+def kda_state_bytes(p):
+    return int(load().kda_state_bytes(ctypes.byref(p)))
+
+
+def kda_prefill_workspace_size(p, n_seqs, total_tokens):
+    return int(load().kda_prefill_workspace_size(ctypes.byref(p), int(n_seqs), int(total_tokens)))
+
+
+def kda_launch_count():
+    return int(load().kda_launch_count())
+
+
+def kda_check_device_error(stream=None):
+    _check(load().kda_check_device_error(_stream(stream)), "kda_check_device_error")
+
+
+def kda_prologue(p, x_raw, conv_w, conv_state, cu_seqlens, q, k, v, *, l2norm_qk=False,
+                 beta_logit=None, g_raw=None, beta=None, g=None, stream=None):
+    io = p.io_torch
+    st = load().kda_prologue(
+        ctypes.byref(p), _ptr(x_raw, io, "x_raw"), _ptr(conv_w, io, "conv_w"),
+        _ptr(conv_state, io, "conv_state"), _ptr(cu_seqlens, torch.int32, "cu_seqlens"),
+        cu_seqlens.numel() - 1, x_raw.shape[0], 1 if l2norm_qk else 0,
+        _ptr(beta_logit, torch.float32, "beta_logit"), _ptr(g_raw, torch.float32, "g_raw"),
+        _ptr(q, io, "q"), _ptr(k, io, "k"), _ptr(v, io, "v"),
+        _ptr(beta, torch.float32, "beta"), _ptr(g, torch.float32, "g"), _stream(stream))
+    _check(st, "kda_prologue")
+
+
+def kda_prefill(p, q, k, v, g, beta, cu_seqlens, out, *, init_state=None, final_state=None,
+                gate_logit=None, norm_w=None, workspace=None, stream=None):
+    io, sd = p.io_torch, p.state_torch
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().kda_prefill(
+        ctypes.byref(p), _ptr(q, io, "q"), _ptr(k, io, "k"), _ptr(v, io, "v"),
+        _ptr(g, torch.float32, "g"), _ptr(beta, torch.float32, "beta"),
+        _ptr(init_state, sd, "init_state"), _ptr(cu_seqlens, torch.int32, "cu_seqlens"),
+        cu_seqlens.numel() - 1, q.shape[0], _ptr(gate_logit, io, "gate_logit"),
+        _ptr(norm_w, torch.float32, "norm_w"), _ptr(out, io, "out"),
+        _ptr(final_state, sd, "final_state"), _ptr(workspace, None, "workspace"), ws_bytes,
+        _stream(stream))
+    _check(st, "kda_prefill")
+
+
+def kda_decode_step(p, q, k, v, g, beta, state, out, *, slot_idx=None, gate_logit=None,
+                    norm_w=None, stream=None):
+    io, sd = p.io_torch, p.state_torch
+    st = load().kda_decode_step(
+        ctypes.byref(p), _ptr(q, io, "q"), _ptr(k, io, "k"), _ptr(v, io, "v"),
+        _ptr(g, torch.float32, "g"), _ptr(beta, torch.float32, "beta"),
+        _ptr(state, sd, "state"), state.shape[0], _ptr(slot_idx, torch.int32, "slot_idx"),
+        q.shape[0], _ptr(gate_logit, io, "gate_logit"), _ptr(norm_w, torch.float32, "norm_w"),
+        _ptr(out, io, "out"), _stream(stream))
+    _check(st, "kda_decode_step")
+
+
+def kda_decode_step_fused(p, x_raw, conv_w, conv_state, g, beta, state, out, *, slot_idx=None,
+                          gate_logit=None, norm_w=None, stream=None):
+    io, sd = p.io_torch, p.state_torch
+    st = load().kda_decode_step_fused(
+        ctypes.byref(p), _ptr(x_raw, io, "x_raw"), _ptr(conv_w, io, "conv_w"),
+        _ptr(conv_state, io, "conv_state"), _ptr(g, torch.float32, "g"),
+        _ptr(beta, torch.float32, "beta"), _ptr(state, sd, "state"), state.shape[0],
+        _ptr(slot_idx, torch.int32, "slot_idx"), x_raw.shape[0],
+        _ptr(gate_logit, io, "gate_logit"), _ptr(norm_w, torch.float32, "norm_w"),
+        _ptr(out, io, "out"), _stream(stream))
+    _check(st, "kda_decode_step_fused")
+
+
+def kda_conv_state_update(p, x_new, conv_w, conv_state, y, *, slot_idx=None, stream=None):
+    io = p.io_torch
+    st = load().kda_conv_state_update(
+        ctypes.byref(p), _ptr(x_new, io, "x_new"), _ptr(conv_w, io, "conv_w"),
+        _ptr(conv_state, io, "conv_state"), conv_state.shape[0],
+        _ptr(slot_idx, torch.int32, "slot_idx"), x_new.shape[0], x_new.shape[1],
+        _ptr(y, io, "y"), _stream(stream))
+    _check(st, "kda_conv_state_update")

@@ -1,0 +1,194 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention (KDA) token-mixer library.
+ *
+ * What the layer computes (web pages, cited by title and section):
+ *   [Grouped]  "Ling-3.1-flash: Grouped Routing and Two Different MLA Caches",
+ *              section "KDA replaces a token list with a recurrent matrix": q, k, v streams of
+ *              64 x 128 channels, each through its own causal short convolution of width 4
+ *              with SiLU; q and k normalised; channel-dependent retention; a delta-rule
+ *              write that corrects the state's prediction for k toward v; the safe forget
+ *              gate's log-retention lower bound -5; an output normalisation and sigmoid gate.
+ *   [Headers]  "Ling-3.1-flash: a 560B hybrid-attention MoE, counted from its safetensors
+ *              headers", section "How KDA and MLA split the work", the state equation:
+ *              a 128 x 128 state per head, decayed by Diag(alpha_t), written with strength
+ *              beta_t (one scalar per head), read as o_t = S_t^T q_t.
+ *   [Budget]   "Ling-3.1-flash: What 63 Linear-Attention Layers Do to the KV Budget",
+ *              section "The memory math": fp32 state of 64 x 128 x 128 values per layer and
+ *              sequence; the short-convolution tails.
+ *
+ * Per head and token (state S is d_k x d_v, row i = key channel, column j = value channel):
+ *     alpha = exp(max(g, g_min));  S' = Diag(alpha) S;  u = beta (v - S'^T k)
+ *     S = S' + k u^T;  o = scale * S^T q
+ * with q, k L2-normalised first when params->qk_l2norm is set, and, when gate logits are
+ * given, o <- o / sqrt(mean_j o_j^2 + norm_eps) * norm_w * sigmoid(gate).
+ *
+ * Conventions for every entry point:
+ *  - Every pointer is a DEVICE pointer unless stated otherwise; tensors are dense and
+ *    row-major in the layouts given.  The caller owns every buffer; the library allocates
+ *    no device memory.
+ *  - Calls are asynchronous on the given stream; they return after enqueueing.
+ *  - Arguments are validated on the host before anything is launched.  Errors are
+ *    returned (never thrown, never trapped on the device): KDA_ERR_INVALID_ARG for bad
+ *    pointers/sizes, KDA_ERR_UNSUPPORTED for valid but unimplemented shapes or dtypes,
+ *    KDA_ERR_CUDA when a launch fails.  Device-side waits are bounded; a wait that runs out
+ *    sets a sticky device flag read by kda_check_device_error().
+ *  - Packed sequences: token t of the batch lives at row t of every [T_tot, ...] tensor;
+ *    sequence n owns rows [cu_seqlens[n], cu_seqlens[n+1]).  cu_seqlens is a device int32
+ *    array of n_seqs + 1 non-decreasing offsets starting at 0 (the library does not read it
+ *    on the host; a decreasing array yields unspecified results for those sequences but no
+ *    out-of-bounds access as long as every entry lies in [0, total_tokens]).
+ *  - Supported: d_k == d_v == d in {16, 128}; any H >= 1; sequences of any length >= 0.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = -1,
+  KDA_ERR_UNSUPPORTED = -2,
+  KDA_ERR_CUDA = -3,
+  KDA_ERR_WORKSPACE = -4,
+  KDA_ERR_TIMEOUT = -5
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Layer configuration.  Defaults in brackets are the pages' configuration. */
+typedef struct {
+  int H;                 /* heads [64]                                                  */
+  int d_k, d_v;          /* head dims, equal, 16 or 128 [128]                           */
+  float scale;           /* read scale applied to S^T q [1.0]                           */
+  float l2_eps;          /* q/k L2 norm: x / sqrt(sum x^2 + l2_eps) [1e-6]              */
+  float norm_eps;        /* output RMS norm epsilon [1e-6]                              */
+  float g_min;           /* log-retention lower bound of the safe forget gate [-5]      */
+  int qk_l2norm;         /* 1: L2-normalise q and k inside the call [1]                 */
+  kda_dtype io_dtype;    /* q, k, v, raw x, conv weights/state, gate logits, out [BF16] */
+  kda_dtype state_dtype; /* recurrent state storage [F32]; BF16 = bf16 storage variant   */
+} kda_params;
+
+/* Fills *p with the pages' configuration (H 64, d 128, scale 1, eps 1e-6, g_min -5,
+ * qk_l2norm 1, bf16 I/O, fp32 state). */
+void kda_params_default(kda_params* p);
+
+/* Human-readable name of a status code (static storage). */
+const char* kda_status_string(kda_status s);
+
+/* Bytes of one sequence's recurrent state for one layer: H * d_k * d_v * sizeof(state).
+ * [Budget] "The memory math": 64 x 128 x 128 fp32 values = 4 MiB per layer. */
+size_t kda_state_bytes(const kda_params* p);
+
+/* Device workspace kda_prefill needs for this batch (0 today; kept so callers can size a
+ * buffer once).  Returns 0 for invalid params. */
+size_t kda_prefill_workspace_size(const kda_params* p, int n_seqs, int64_t total_tokens);
+
+/*
+ * kda_prologue -- short convolution + SiLU (+ optional q/k L2 norm) + gate activations for a
+ * packed batch ([Grouped]: "Each projection passes through its own causal short
+ * convolution of width four with SiLU activation").
+ *
+ *   x_raw       [T_tot, 3*H*d] io_dtype: the q, k and v projections side by side
+ *               (channels [0,Hd) = q, [Hd,2Hd) = k, [2Hd,3Hd) = v; head h of a stream is
+ *               channels h*d .. h*d+d-1 of it).
+ *   conv_w      [3*H*d, 4] io_dtype: y[t,c] = SiLU(sum_j conv_w[c][j] * x[t-3+j, c]).
+ *   conv_state  [n_seqs, 3, 3*H*d] io_dtype or NULL.  In: the three raw inputs before each
+ *               sequence (oldest first); taps before the sequence start read it (zeros if
+ *               NULL).  Out (updated in place when non-NULL): the last three raw inputs of
+ *               each sequence, reaching into the old tail for sequences shorter than 3;
+ *               a length-0 sequence keeps its tail.  Bit-exact copies.
+ *   q, k, v     [T_tot, H, d] io_dtype outputs (SiLU(conv) of each stream).
+ *   l2norm_qk   1: q and k outputs are L2-normalised per head (eps = p->l2_eps).
+ *   beta_logit  [T_tot, H] fp32 or NULL -> beta [T_tot, H] fp32 = sigmoid(beta_logit).
+ *   g_raw       [T_tot, H, d] fp32 or NULL -> g [T_tot, H, d] fp32 = max(g_raw, p->g_min).
+ */
+kda_status kda_prologue(const kda_params* p, const void* x_raw, const void* conv_w,
+                        void* conv_state, const int32_t* cu_seqlens, int n_seqs,
+                        int64_t total_tokens, int l2norm_qk, const float* beta_logit,
+                        const float* g_raw, void* q, void* k, void* v, float* beta, float* g,
+                        cudaStream_t stream);
+
+/*
+ * kda_prefill -- the recurrence over a packed batch of sequences ([Headers] state equation,
+ * [Grouped] delta-rule write), chunk-parallel inside each sequence.
+ *
+ *   q, k        [T_tot, H, d_k] io_dtype; v [T_tot, H, d_v] io_dtype.
+ *   g           [T_tot, H, d_k] fp32 log-retention (clamped at p->g_min inside).
+ *   beta        [T_tot, H] fp32 write strength in (0, 1).
+ *   init_state  [n_seqs, H, d_k, d_v] state_dtype, or NULL for zeros.
+ *   cu_seqlens  [n_seqs + 1] int32 (device).
+ *   gate_logit  [T_tot, H, d_v] io_dtype, or NULL: no output norm/gate (plain read).
+ *   norm_w      [d_v] fp32 output-norm weight, or NULL for ones (used only with a gate).
+ *   out         [T_tot, H, d_v] io_dtype.
+ *   final_state [n_seqs, H, d_k, d_v] state_dtype, or NULL.  May alias init_state.
+ *   workspace / ws_bytes: at least kda_prefill_workspace_size() bytes (may be NULL when 0).
+ * A length-0 sequence copies its initial state (or zeros) to final_state.
+ */
+kda_status kda_prefill(const kda_params* p, const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const void* init_state,
+                       const int32_t* cu_seqlens, int n_seqs, int64_t total_tokens,
+                       const void* gate_logit, const float* norm_w, void* out,
+                       void* final_state, void* workspace, size_t ws_bytes,
+                       cudaStream_t stream);
+
+/*
+ * kda_decode_step -- one token for each of n_seqs sequences, state updated in place.
+ *
+ *   q, k, v     [n_seqs, H, d] io_dtype (post-convolution streams).
+ *   g           [n_seqs, H, d] fp32 log-retention; beta [n_seqs, H] fp32.
+ *   state       [n_slots, H, d, d] state_dtype pool, updated in place.
+ *   slot_idx    [n_seqs] int32 (device): sequence n uses state slot slot_idx[n]; NULL means
+ *               slot n.  Slots must be distinct and in [0, n_slots).
+ *   gate_logit  [n_seqs, H, d] io_dtype or NULL; norm_w [d] fp32 or NULL.
+ *   out         [n_seqs, H, d] io_dtype.
+ * Each head's state is read from HBM once and written once.
+ */
+kda_status kda_decode_step(const kda_params* p, const void* q, const void* k, const void* v,
+                           const float* g, const float* beta, void* state, int n_slots,
+                           const int32_t* slot_idx, int n_seqs, const void* gate_logit,
+                           const float* norm_w, void* out, cudaStream_t stream);
+
+/*
+ * kda_conv_state_update -- decode-time short convolution: for each sequence n and channel c,
+ * y[n,c] = SiLU(sum_{j<3} conv_w[c][j] * conv_state[s][j][c] + conv_w[c][3] * x_new[n,c]),
+ * then conv_state[s] <- (conv_state[s][1], conv_state[s][2], x_new[n]) in place, where
+ * s = slot_idx[n] (or n when slot_idx is NULL).
+ *   x_new [n_seqs, channels], conv_w [channels, 4], conv_state [n_slots, 3, channels],
+ *   y [n_seqs, channels]; all io_dtype.  The state shift is bit-exact.
+ */
+kda_status kda_conv_state_update(const kda_params* p, const void* x_new, const void* conv_w,
+                                 void* conv_state, int n_slots, const int32_t* slot_idx,
+                                 int n_seqs, int channels, void* y, cudaStream_t stream);
+
+/*
+ * kda_decode_step_fused -- kda_conv_state_update and kda_decode_step in one launch, from
+ * the raw projections: x_raw [n_seqs, 3*H*d] (q|k|v as in kda_prologue), conv_w
+ * [3*H*d, 4], conv_state [n_slots, 3, 3*H*d] updated in place; the convolved q, k, v stay
+ * in fp32 on chip.  Other arguments as in kda_decode_step.
+ */
+kda_status kda_decode_step_fused(const kda_params* p, const void* x_raw, const void* conv_w,
+                                 void* conv_state, const float* g, const float* beta,
+                                 void* state, int n_slots, const int32_t* slot_idx, int n_seqs,
+                                 const void* gate_logit, const float* norm_w, void* out,
+                                 cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and clears the library's sticky device error flag
+ * (set when a bounded device wait ran out).  Returns KDA_OK, KDA_ERR_TIMEOUT or
+ * KDA_ERR_CUDA. */
+kda_status kda_check_device_error(cudaStream_t stream);
+
+/* Number of kernels the library launched since load (host-side counter, for benchmarks). */
+uint64_t kda_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,117 @@
+"""The C-ABI library loads, exports every entry point include/kda.h declares, and rejects
+bad arguments on the host before touching the GPU (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from hybrid_linear_attention_gb300 import build as kbuild
+from hybrid_linear_attention_gb300 import kda
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kda.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_contract_calls():
+    names = _declared_functions()
+    for must in ("kda_prefill", "kda_decode_step", "kda_conv_state_update", "kda_prologue",
+                 "kda_prefill_workspace_size", "kda_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"libkda.so does not export {name}"
+    assert set(_declared_functions()) <= set(kda.EXPORTS)
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert kda.status_string(code).startswith("KDA_")
+
+
+def test_defaults_are_the_pages_configuration(lib):
+    p = kda.kda_params_default()
+    assert (p.H, p.d_k, p.d_v, p.qk_l2norm) == (64, 128, 128, 1)
+    assert p.g_min == -5.0 and p.scale == 1.0
+    assert p.io_dtype == kda.KDA_BF16 and p.state_dtype == kda.KDA_F32
+
+
+def test_state_bytes_is_the_pages_payload(lib):
+    p = kda.params()
+    assert kda.kda_state_bytes(p) == 64 * 128 * 128 * 4            # 4 MiB per layer
+    assert 63 * kda.kda_state_bytes(p) == 252 * 2**20             # 252 MiB per sequence
+    pb = kda.params(state_dtype=torch.bfloat16)
+    assert 63 * kda.kda_state_bytes(pb) == 126 * 2**20
+
+
+def _raw_prefill(lib, p, **kw):
+    args = dict(q=16, k=16, v=16, g=16, beta=16, init=None, cu=16, n=1, T=4, gate=None,
+                w=None, out=16, fin=None, ws=None, wsb=0)
+    args.update(kw)
+    return lib.kda_prefill(ctypes.byref(p) if p is not None else None, args["q"], args["k"],
+                           args["v"], args["g"], args["beta"], args["init"], args["cu"],
+                           args["n"], args["T"], args["gate"], args["w"], args["out"],
+                           args["fin"], args["ws"], args["wsb"], None)
+
+
+def test_prefill_rejects_bad_arguments_on_host(lib):
+    p = kda.params()
+    assert _raw_prefill(lib, None) == kda.KDA_ERR_INVALID_ARG
+    assert _raw_prefill(lib, p, q=None) == kda.KDA_ERR_INVALID_ARG
+    assert _raw_prefill(lib, p, cu=None) == kda.KDA_ERR_INVALID_ARG
+    assert _raw_prefill(lib, p, n=-1) == kda.KDA_ERR_INVALID_ARG
+    assert _raw_prefill(lib, p, n=0, T=5) == kda.KDA_ERR_INVALID_ARG
+    assert _raw_prefill(lib, p, q=18) == kda.KDA_ERR_INVALID_ARG          # misaligned
+    assert _raw_prefill(lib, p, n=0, T=0) == kda.KDA_OK                   # nothing to do
+    bad = kda.params(d=64)
+    assert _raw_prefill(lib, bad) == kda.KDA_ERR_UNSUPPORTED
+    mixed = kda.params()
+    mixed.d_v = 16
+    assert _raw_prefill(lib, mixed) == kda.KDA_ERR_UNSUPPORTED
+    neg = kda.params(H=0)
+    assert _raw_prefill(lib, neg) == kda.KDA_ERR_INVALID_ARG
+    nan = kda.params(g_min=float("nan"))
+    assert _raw_prefill(lib, nan) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_decode_and_conv_reject_bad_arguments_on_host(lib):
+    p = kda.params()
+    P = ctypes.byref(p)
+    # state NULL
+    assert lib.kda_decode_step(P, 16, 16, 16, 16, 16, None, 4, None, 4, None, None, 16,
+                               None) == kda.KDA_ERR_INVALID_ARG
+    # identity slots but fewer slots than sequences
+    assert lib.kda_decode_step(P, 16, 16, 16, 16, 16, 16, 2, None, 4, None, None, 16,
+                               None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode_step(P, 16, 16, 16, 16, 16, 16, 4, None, 0, None, None, 16,
+                               None) == kda.KDA_OK
+    assert lib.kda_decode_step_fused(P, None, 16, 16, 16, 16, 16, 4, None, 4, None, None, 16,
+                                     None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_conv_state_update(P, 16, 16, 16, 4, None, 4, 0, 16,
+                                     None) == kda.KDA_ERR_INVALID_ARG      # zero channels
+    assert lib.kda_conv_state_update(P, 16, 16, 24, 4, None, 4, 64, 16,
+                                     None) == kda.KDA_ERR_INVALID_ARG      # misaligned
+    assert lib.kda_prologue(P, 16, 16, None, 16, 1, 4, 0, 16, None, 16, 16, 16, None, None,
+                            None) == kda.KDA_ERR_INVALID_ARG               # beta out missing
+
+
+def test_workspace_query(lib):
+    p = kda.params()
+    assert kda.kda_prefill_workspace_size(p, 32, 500_000) == 0
+    bad = kda.params(d=64)
+    assert kda.kda_prefill_workspace_size(bad, 1, 10) == 0
