@@ -1,0 +1,413 @@
+"""Benchmark of the KDA token-mixer hot path on GB300.
+
+Main line (value): prefill tokens/s per layer on the single-layer, Ling-shaped workload
+(B=1, T=4096, H=64, d=128, bf16 I/O, fp32 state, zero initial state, chunk 64).  One step is
+the whole prefill hot path over that batch: kda_prologue (width-4 causal conv + SiLU over the
+raw q|k|v projections, q/k L2 norm, beta = sigmoid, g clamp) then kda_prefill.
+Also reported: the prefill kernel alone, the decode workload (256 sequences x 1 token,
+H=64, d=128, fp32 state pool ~N(0,0.02), fused conv + decode, 100 consecutive steps) as
+state GB/s, the roofline of the dominant kernel against MEASURED_PEAKS.json, an end-to-end
+number through the same API with host buffers, and the oracle timed on the host cores.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+T_PREFILL, H, D = 4096, 64, 128
+N_DECODE, DECODE_STEPS = 256, 100
+METRIC = "KDA prefill tokens/s/layer"
+WORKLOAD = ("Single-layer KDA prefill, Ling-shaped: B=1, T=4096, H=64, d_k=d_v=128, bf16 "
+            "q/k/v (raw projections ~N(0,1) through the width-4 causal conv+SiLU prologue), "
+            "fp32 log-alpha ~U(-5,0) clamped at -5, beta=sigmoid(N(0,1)), fp32 state, zero "
+            "initial state, chunk 64")
+L2_BYTES = 129 * 2**20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), float(
+            pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _prefill_bytes(T, H, d, with_state_out=True):
+    """Algorithmic HBM bytes of one kda_prefill launch: q, k, v, out (bf16), g (fp32),
+    beta (fp32), plus the final fp32 state."""
+    per_tok = H * d * (2 * 3 + 4 + 2) + H * 4
+    return T * per_tok + (H * d * d * 4 if with_state_out else 0)
+
+
+def _prologue_bytes(T, H, d):
+    """kda_prologue: read raw x (3Hd bf16) + g_raw (Hd fp32) + beta logits; write q, k, v
+    (bf16), g (fp32), beta (fp32)."""
+    C = 3 * H * d
+    return T * (C * 2 * 2 + H * d * 4 * 2 + H * 4 * 2)
+
+
+def _decode_bytes(n, H, d):
+    """One fused decode step for n sequences: state read+write (fp32), conv tail read+write,
+    raw x, g, beta, conv weights, out."""
+    C = 3 * H * d
+    return (2 * n * H * d * d * 4 + 2 * n * 3 * C * 2 + n * C * 2 + n * H * d * 4 + n * H * 4
+            + C * 4 * 2 + n * H * d * 2)
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("nccl")
+        return dist, dist.get_rank(), ws
+    return None, 0, 1
+
+
+def _barrier(dist):
+    if dist:
+        dist.barrier()
+
+
+def _max_over_ranks(dist, x):
+    if not dist:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------
+# Oracle timing (host cores)
+# ---------------------------------------------------------------------------------------
+
+def _oracle_prefill_sample(heads, seed=0):
+    """The oracle on the prefill workload restricted to `heads` heads (the whole layer when
+    heads == H): prologue (conv+SiLU+L2 on the sampled heads' channels) then recurrence.
+    Returns (seconds, threads)."""
+    import numpy as np
+    import oracle
+    from hybrid_linear_attention_gb300 import inputs
+
+    pin = inputs.prologue_inputs([T_PREFILL], heads, D, seed=seed, conv_state=False)
+    threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    pr = oracle.prologue(pin["x"], pin["conv_w"], pin["cu_seqlens"], heads, D, l2norm_qk=True,
+                         beta_logit=pin["beta_logit"], g_raw=pin["g_raw"])
+    y = pr["y"].reshape(T_PREFILL, 3, heads, D)
+    oracle.kda_forward(np.ascontiguousarray(y[:, 0]), np.ascontiguousarray(y[:, 1]),
+                       np.ascontiguousarray(y[:, 2]), pr["g"].astype(np.float32),
+                       pr["beta"].astype(np.float32), pin["cu_seqlens"], qk_l2norm=False,
+                       n_threads=threads)
+    return time.perf_counter() - t0, threads
+
+
+CPU_SAMPLE_HEADS = 16
+
+
+def _cpu_baseline():
+    secs, threads = _oracle_prefill_sample(CPU_SAMPLE_HEADS)
+    # tokens/s/layer: the sample covers CPU_SAMPLE_HEADS of the layer's H heads
+    value = T_PREFILL * CPU_SAMPLE_HEADS / H / secs
+    return {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"T=4096 tokens x {CPU_SAMPLE_HEADS} of 64 heads (prologue + fp64 "
+                      f"recurrence), scaled to one full layer; {secs:.2f} s wall"}
+
+
+def run_reference(args):
+    dist, rank, ws = _dist()
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        _oracle_prefill_sample(CPU_SAMPLE_HEADS, seed=1)
+    times = []
+    threads = 1
+    for s in range(args.steps):
+        secs, threads = _oracle_prefill_sample(CPU_SAMPLE_HEADS, seed=2 + s)
+        times.append(secs)
+    per = sum(times) / len(times)
+    value = T_PREFILL * CPU_SAMPLE_HEADS / H / per
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": f"{CPU_SAMPLE_HEADS} of 64 heads per step"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"T=4096 x {CPU_SAMPLE_HEADS}/64 heads per step, scaled"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------
+
+class PrefillWorkload:
+    def __init__(self, dev, seed=0):
+        from hybrid_linear_attention_gb300 import inputs, kda
+        self.kda = kda
+        self.p = kda.params(H=H, d=D)
+        pin = inputs.prologue_inputs([T_PREFILL], H, D, seed=seed, device=dev, conv_state=False)
+        self.x, self.w = pin["x"], pin["conv_w"]
+        self.beta_logit, self.g_raw = pin["beta_logit"], pin["g_raw"]
+        self.cu = pin["cu_seqlens"]
+        T = T_PREFILL
+        self.q = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+        self.k, self.v = torch.empty_like(self.q), torch.empty_like(self.q)
+        self.beta = torch.empty((T, H), dtype=torch.float32, device=dev)
+        self.g = torch.empty((T, H, D), dtype=torch.float32, device=dev)
+        self.out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+        self.fin = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
+
+    def prologue(self, stream=None):
+        self.kda.kda_prologue(self.p, self.x, self.w, None, self.cu, self.q, self.k, self.v,
+                              l2norm_qk=True, beta_logit=self.beta_logit, g_raw=self.g_raw,
+                              beta=self.beta, g=self.g, stream=stream)
+
+    def prefill(self, stream=None):
+        self.kda.kda_prefill(self.p, self.q, self.k, self.v, self.g, self.beta, self.cu,
+                             self.out, final_state=self.fin, stream=stream)
+
+
+def run_ours(args):
+    dist, rank, ws = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from hybrid_linear_attention_gb300 import inputs, kda
+
+    hbm, tflops, tflops_sus, peak_kind = _peaks()
+    wl = PrefillWorkload(dev, seed=rank)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    for _ in range(max(args.warmup, 3)):
+        wl.prologue()
+        wl.prefill()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps (prologue + prefill), L2 flushed between steps ----------
+    step_ms, pro_ms, pf_ms = [], [], []
+    launches0 = kda.kda_launch_count()
+    _barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1, e2 = ev(), ev(), ev()
+            e0.record(stream)
+            wl.prologue()
+            e1.record(stream)
+            wl.prefill()
+            e2.record(stream)
+            e2.synchronize()
+            pro_ms.append(e0.elapsed_time(e1))
+            pf_ms.append(e1.elapsed_time(e2))
+            step_ms.append(e0.elapsed_time(e2))
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    _barrier(dist)
+    launches = kda.kda_launch_count() - launches0
+    kda.kda_check_device_error()
+    ms = _max_over_ranks(dist, sum(step_ms) / len(step_ms))
+    pf = _max_over_ranks(dist, sum(pf_ms) / len(pf_ms))
+    pro = _max_over_ranks(dist, sum(pro_ms) / len(pro_ms))
+    value = ws * T_PREFILL / (ms * 1e-3)
+
+    # ---- end to end through the same API with host buffers ---------------------------
+    hx = wl.x.cpu().pin_memory()
+    hg = wl.g_raw.cpu().pin_memory()
+    hb = wl.beta_logit.cpu().pin_memory()
+    hout = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
+    hfin = torch.empty(wl.fin.shape, dtype=wl.fin.dtype).pin_memory()
+    h2d = hx.numel() * 2 + hg.numel() * 4 + hb.numel() * 4
+    d2h = hout.numel() * 2 + hfin.numel() * 4
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        wl.x.copy_(hx, non_blocking=True)
+        wl.g_raw.copy_(hg, non_blocking=True)
+        wl.beta_logit.copy_(hb, non_blocking=True)
+        wl.prologue()
+        wl.prefill()
+        hout.copy_(wl.out, non_blocking=True)
+        hfin.copy_(wl.fin, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e = _max_over_ranks(dist, sum(e2e_ms) / len(e2e_ms))
+
+    # ---- decode: 256 sequences x 100 fused steps --------------------------------------
+    dec = None
+    if not args.no_decode:
+        dec = _decode_bench(dev, kda, inputs, hbm, rank, args)
+
+    if rank != 0:
+        return
+    pf_bytes = _prefill_bytes(T_PREFILL, H, D)
+    achieved = pf_bytes / (pf * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens_per_step": T_PREFILL, "heads": H, "d": D,
+                   "chunk": 64, "parallelism": f"replicas{ws}",
+                   "l2": "inputs larger than L2 (403 MB) and a 258 MB buffer written between "
+                         "steps"},
+        "breakdown_ms": {"prologue": pro, "prefill": pf},
+        "prefill_kernel_tokens_per_s": ws * T_PREFILL / (pf * 1e-3),
+        "roofline": {"kernel": "kda_prefill", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_kind": f"{peak_kind} hbm_gbs", "traffic": None,
+                     "algorithmic_bytes_per_launch": pf_bytes},
+        "e2e": {"value": ws * T_PREFILL / (e2e * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
+        "gpu_launches": int(launches),
+        "gpu_launches_per_step": launches / args.steps,
+        "wall_s_timed_region": wall,
+        "clocks": clk.summary(),
+    }
+    if dec:
+        line["decode"] = dec
+    if not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = _cpu_baseline()
+    print(json.dumps(line), flush=True)
+
+
+def _decode_bench(dev, kda, inputs, hbm, rank, args):
+    n, C = N_DECODE, 3 * H * D
+    p = kda.params(H=H, d=D)
+    state = inputs.normal((n, H, D, D), seed=300 + rank, device=dev, dtype=torch.float32,
+                          std=0.02)
+    cs = inputs.normal((n, 3, C), seed=301 + rank, device=dev)
+    w = inputs.normal((C, 4), seed=302 + rank, device=dev, std=0.5)
+    K = DECODE_STEPS
+    x = inputs.normal((K, n, C), seed=303 + rank, device=dev)
+    g = inputs.uniform((K, n, H, D), -5.0, 0.0, seed=304 + rank, device=dev)
+    beta = inputs.beta_draw((K, n, H), seed=305 + rank, device=dev)
+    out = torch.empty((K, n, H, D), dtype=torch.bfloat16, device=dev)
+    for t in range(3):
+        kda.kda_decode_step_fused(p, x[t], w, cs, g[t], beta[t], state, out[t])
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for t in range(K):
+        kda.kda_decode_step_fused(p, x[t], w, cs, g[t], beta[t], state, out[t])
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    b = _decode_bytes(n, H, D)
+    gbs = b / (ms * 1e-3) / 1e9
+    return {"metric": "KDA decode state GB/s", "value": gbs, "unit": "GB/s",
+            "workload": "256 sequences x 1 token, H=64, d=128, fp32 state pool [256,64,128,128]"
+                        " ~N(0,0.02) (1 GiB, > L2), bf16 conv tails, fused conv+decode, 100 "
+                        "consecutive steps",
+            "ms_per_step": ms, "tokens_per_s": n / (ms * 1e-3),
+            "roofline": {"kernel": "kda_decode_step_fused", "bound": "hbm", "achieved": gbs,
+                         "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
+                         "algorithmic_bytes_per_launch": b}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

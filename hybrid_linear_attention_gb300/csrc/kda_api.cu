@@ -185,7 +185,7 @@ kda_status kda_prefill(const kda_params *p, const void *q, const void *k, const 
     t.norm_w = norm_w;
     t.out = out;
     t.err = device_error_ptr();
-    return finish(kda::launch_prefill_tc(t, st_bf16, stream), 1);
+    return finish(kda::launch_prefill_tc(t, total_tokens, st_bf16, stream), 1);
   }
   kda::RecArgs a = base_args(p);
   a.n_seqs = n_seqs;

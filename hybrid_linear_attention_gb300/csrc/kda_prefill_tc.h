@@ -24,6 +24,6 @@ struct TcArgs {
 
 // True when the tensor-core path serves this shape (d = 128, bf16 I/O).
 bool prefill_tc_supported(int d, bool io_bf16);
-cudaError_t launch_prefill_tc(const TcArgs &a, bool st_bf16, cudaStream_t s);
+cudaError_t launch_prefill_tc(const TcArgs &a, int64_t total_tokens, bool st_bf16, cudaStream_t s);
 
 }  // namespace kda
