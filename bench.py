@@ -173,7 +173,7 @@ def _oracle_prefill_sample(heads, seed=0):
     return time.perf_counter() - t0, threads
 
 
-CPU_SAMPLE_HEADS = 16
+CPU_SAMPLE_HEADS = 32
 
 
 def _cpu_baseline():
@@ -296,29 +296,7 @@ def run_ours(args):
     value = ws * T_PREFILL / (ms * 1e-3)
 
     # ---- end to end through the same API with host buffers ---------------------------
-    hx = wl.x.cpu().pin_memory()
-    hg = wl.g_raw.cpu().pin_memory()
-    hb = wl.beta_logit.cpu().pin_memory()
-    hout = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
-    hfin = torch.empty(wl.fin.shape, dtype=wl.fin.dtype).pin_memory()
-    h2d = hx.numel() * 2 + hg.numel() * 4 + hb.numel() * 4
-    d2h = hout.numel() * 2 + hfin.numel() * 4
-    e2e_ms = []
-    for i in range(args.warmup + args.steps):
-        flush.zero_()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        wl.x.copy_(hx, non_blocking=True)
-        wl.g_raw.copy_(hg, non_blocking=True)
-        wl.beta_logit.copy_(hb, non_blocking=True)
-        wl.prologue()
-        wl.prefill()
-        hout.copy_(wl.out, non_blocking=True)
-        hfin.copy_(wl.fin, non_blocking=True)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            e2e_ms.append((time.perf_counter() - t0) * 1e3)
-    e2e = _max_over_ranks(dist, sum(e2e_ms) / len(e2e_ms))
+    e2e_line = _e2e(wl, flush, args, dist) if not args.no_e2e else None
 
     # ---- decode: 256 sequences x 100 fused steps --------------------------------------
     dec = None
@@ -344,18 +322,49 @@ def run_ours(args):
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_kind": f"{peak_kind} hbm_gbs", "traffic": None,
                      "algorithmic_bytes_per_launch": pf_bytes},
-        "e2e": {"value": ws * T_PREFILL / (e2e * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
         "gpu_launches": int(launches),
         "gpu_launches_per_step": launches / args.steps,
         "wall_s_timed_region": wall,
         "clocks": clk.summary(),
     }
+    if e2e_line:
+        line["e2e"] = e2e_line
     if dec:
         line["decode"] = dec
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = _cpu_baseline()
     print(json.dumps(line), flush=True)
+
+
+def _e2e(wl, flush, args, dist):
+    """The same step through the public API with pinned host buffers: H2D of the step's
+    inputs, prologue + prefill, D2H of the outputs, all inside the timed region."""
+    ws = dist.get_world_size() if dist else 1
+    hx = wl.x.cpu().pin_memory()
+    hg = wl.g_raw.cpu().pin_memory()
+    hb = wl.beta_logit.cpu().pin_memory()
+    hout = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
+    hfin = torch.empty(wl.fin.shape, dtype=wl.fin.dtype).pin_memory()
+    h2d = hx.numel() * 2 + hg.numel() * 4 + hb.numel() * 4
+    d2h = hout.numel() * 2 + hfin.numel() * 4
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        wl.x.copy_(hx, non_blocking=True)
+        wl.g_raw.copy_(hg, non_blocking=True)
+        wl.beta_logit.copy_(hb, non_blocking=True)
+        wl.prologue()
+        wl.prefill()
+        hout.copy_(wl.out, non_blocking=True)
+        hfin.copy_(wl.fin, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e = _max_over_ranks(dist, sum(e2e_ms) / len(e2e_ms))
+    return {"value": ws * T_PREFILL / (e2e * 1e-3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e}
 
 
 def _decode_bench(dev, kda, inputs, hbm, rank, args):
@@ -400,6 +409,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
