@@ -125,6 +125,44 @@ __device__ __forceinline__ void st_f32x8(uint8_t *p0, uint8_t *p1, const float (
   *reinterpret_cast<float4 *>(p1) = make_float4(o[4], o[5], o[6], o[7]);
 }
 
+// D(16x16) += A(16 x 8kk) B(8kk x 16) for row-major fp32 blocks in shared memory (row
+// strides la, lb), on the warp-level tensor-core MMA (m16n8k8, tf32 inputs, fp32
+// accumulate).  Accumulator fragment: d[nt][0..3] = rows g, g, g+8, g+8 and columns
+// 8nt + 2t, +1, 2t, +1 (g = lane / 4, t = lane % 4).
+__device__ __forceinline__ void warp_mma16(float (&d)[2][4], const float *A, int la,
+                                           const float *B, int lb, int ksteps, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  for (int kk = 0; kk < ksteps; ++kk) {
+    const float *a = A + 8 * kk;
+    const uint32_t a0 = __float_as_uint(to_tf32(a[g * la + t]));
+    const uint32_t a1 = __float_as_uint(to_tf32(a[(g + 8) * la + t]));
+    const uint32_t a2 = __float_as_uint(to_tf32(a[g * la + t + 4]));
+    const uint32_t a3 = __float_as_uint(to_tf32(a[(g + 8) * la + t + 4]));
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const float *b = B + (8 * kk) * lb + 8 * nt;
+      const uint32_t b0 = __float_as_uint(to_tf32(b[t * lb + g]));
+      const uint32_t b1 = __float_as_uint(to_tf32(b[(t + 4) * lb + g]));
+      asm volatile(
+          "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+          "{%8,%9}, {%0,%1,%2,%3};"
+          : "+f"(d[nt][0]), "+f"(d[nt][1]), "+f"(d[nt][2]), "+f"(d[nt][3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+  }
+}
+__device__ __forceinline__ void warp_store16(float *D, int ld, const float (&d)[2][4], int lane,
+                                             float sign) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    *reinterpret_cast<float2 *>(&D[g * ld + 8 * nt + 2 * t]) =
+        make_float2(sign * d[nt][0], sign * d[nt][1]);
+    *reinterpret_cast<float2 *>(&D[(g + 8) * ld + 8 * nt + 2 * t]) =
+        make_float2(sign * d[nt][2], sign * d[nt][3]);
+  }
+}
+
 struct Maps {
   CUtensorMap q, k, v, g;
 };
@@ -243,6 +281,8 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t ID_128 = idesc(2, 128, 128, 0, 0);
   const uint32_t ID_UPD = idesc(1, 128, 128, 0, 1);
   uint32_t mma_par = 0;
+  float beta_next = 0.f;  // beta of the next chunk, loaded one chunk ahead (threads 0..63)
+  if (tid < C && tid < eos - bos) beta_next = a.beta[(size_t)(bos + tid) * H + h];
 
   for (int c = 0; c < nchunks && ok; ++c) {
     const int64_t t0 = bos + (int64_t)c * C;
@@ -250,7 +290,11 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t par = (uint32_t)(c & 1);
     const bool more = c + 1 < nchunks;
 
-    if (tid < C) s_beta[tid] = tid < nv ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    if (tid < C) {
+      s_beta[tid] = tid < nv ? beta_next : 0.f;
+      const int64_t tn = t0 + C + tid;
+      beta_next = (more && tn < eos) ? a.beta[(size_t)tn * H + h] : 0.f;
+    }
     wait(BAR_Q, par);
     wait(BAR_K, par);
     wait(BAR_G, par);
@@ -279,18 +323,33 @@ __global__ void __launch_bounds__(NT, 1)
         const float rk = r < nv ? (a.qk_l2norm ? rsqrtf(sk + a.l2_eps) : 1.f) : 0.f;
         s_rq[r] = rq, s_rk[r] = rk, s_pd[r] = sqk * rq * rk;
       }
-    } else if (tid < 256) {
-      const int i = tid - 128;
-      float acc = 0.f;
-#pragma unroll 8
-      for (int r = 0; r < C; ++r) {
-        if ((r & 15) == 0) s_g0[r >> 4][i] = acc;
-        float *p = reinterpret_cast<float *>(sm + OFF_G + swz<4>(r, i));
-        if (r < nv) acc += fmaxf(*p, a.g_min) * LOG2E;
-        *p = acc;
+    } else {
+      // prefix sums of the clamped log2-retention per channel: two threads per channel
+      // (rows 0..31 and 32..63), the upper half offset by the lower half's total
+      const int t = tid - 128, i = t & 127, hf = t >> 7, r0 = 32 * hf;
+      float v[32];
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        const int r = r0 + x;
+        const float gv = *reinterpret_cast<const float *>(sm + OFF_G + swz<4>(r, i));
+        v[x] = r < nv ? fmaxf(gv, a.g_min) * LOG2E : 0.f;
       }
-      s_gC[i] = acc;
-      s_GC[i] = ex2(acc);
+#pragma unroll
+      for (int x = 1; x < 32; ++x) v[x] += v[x - 1];
+      if (hf == 0) s_M[i] = v[31];
+      asm volatile("bar.sync 2, 256;" ::: "memory");
+      const float base = hf ? s_M[i] : 0.f;
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        v[x] += base;
+        *reinterpret_cast<float *>(sm + OFF_G + swz<4>(r0 + x, i)) = v[x];
+      }
+      s_g0[2 * hf][i] = base;
+      s_g0[2 * hf + 1][i] = v[15];
+      if (hf) {
+        s_gC[i] = v[31];
+        s_GC[i] = ex2(v[31]);
+      }
     }
     if (!(ok = sync())) break;
 
@@ -327,30 +386,34 @@ __global__ void __launch_bounds__(NT, 1)
       }
       tmem_wait_st();
     } else {
-      const int row = tid - 256;  // 0..127
-      const int pi = row >> 6, w = row & 63;
-      const int R = 2 * pi + (w >> 5), isq = (w >> 4) & 1, r = 16 * R + (w & 15);
-      const bool live = r < nv;
-      const float rx = isq ? s_rq[r] : s_rk[r];
-      const uint8_t *src = sm + (isq ? OFF_Q : OFF_K);
-#pragma unroll 2
-      for (int c8 = 0; c8 < 16; ++c8) {
-        float o[8];
-        if (live) {
-          float xv[8], gg[8];
-          bf_row8(src, r, c8, xv);
+      // token r's rows: Ktil_r at 64 (R/2) + 32 (R&1) + r%16, Qtil_r 16 rows below
+      for (int it = tid - 256; it < C * 16; it += 128) {
+        const int r = it >> 4, c8 = it & 15;
+        const int R = r >> 4, rowk = 64 * (R >> 1) + 32 * (R & 1) + (r & 15);
+        float ok8[8], oq8[8];
+        if (r < nv) {
+          float kv[8], qv[8], gg[8];
+          bf_row8(sm + OFF_K, r, c8, kv);
+          bf_row8(sm + OFF_Q, r, c8, qv);
           f_row8(sm + OFF_G, r, c8, gg);
           const float4 r0 = *reinterpret_cast<const float4 *>(&s_g0[R][8 * c8]);
           const float4 r1 = *reinterpret_cast<const float4 *>(&s_g0[R][8 * c8 + 4]);
           const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+          const float rk = s_rk[r], rq = s_rq[r];
 #pragma unroll
-          for (int y = 0; y < 8; ++y) o[y] = to_tf32(xv[y] * rx * ex2(gg[y] - rr[y]));
+          for (int y = 0; y < 8; ++y) {
+            const float e = ex2(gg[y] - rr[y]);
+            ok8[y] = to_tf32(kv[y] * rk * e);
+            oq8[y] = to_tf32(qv[y] * rq * e);
+          }
         } else {
 #pragma unroll
-          for (int y = 0; y < 8; ++y) o[y] = 0.f;
+          for (int y = 0; y < 8; ++y) ok8[y] = oq8[y] = 0.f;
         }
-        st_f32x8(sm + OFF_X + kmaj_f32<128>(row, 8 * c8), sm + OFF_X + kmaj_f32<128>(row, 8 * c8 + 4),
-                 o);
+        st_f32x8(sm + OFF_X + kmaj_f32<128>(rowk, 8 * c8),
+                 sm + OFF_X + kmaj_f32<128>(rowk, 8 * c8 + 4), ok8);
+        st_f32x8(sm + OFF_X + kmaj_f32<128>(rowk + 16, 8 * c8),
+                 sm + OFF_X + kmaj_f32<128>(rowk + 16, 8 * c8 + 4), oq8);
       }
     }
     fence_proxy_async();
@@ -386,24 +449,28 @@ __global__ void __launch_bounds__(NT, 1)
         *reinterpret_cast<float *>(sm + OFF_P + kmaj_f32<64>(r, s)) = low ? to_tf32(v[16 + x]) : 0.f;
       }
     }
-    for (int it = tid; it < 128 * 16; it += NT) {  // (row, 8-channel group)
-      const int row = it >> 4, c8 = it & 15;
-      const int r = row & 63;
-      float o[8];
+    for (int it = tid; it < C * 16; it += NT) {  // (token, 8-channel group): rows r, 64 + r
+      const int r = it >> 4, c8 = it & 15;
+      float ok8[8], oq8[8];
       if (r < nv) {
-        const bool isq = row >= 64;
-        const float rx = isq ? s_rq[r] : s_rk[r];
-        float xv[8], gg[8];
-        bf_row8(sm + (isq ? OFF_Q : OFF_K), r, c8, xv);
+        float kv[8], qv[8], gg[8];
+        bf_row8(sm + OFF_K, r, c8, kv);
+        bf_row8(sm + OFF_Q, r, c8, qv);
         f_row8(sm + OFF_G, r, c8, gg);
+        const float rk = s_rk[r], rq = s_rq[r];
 #pragma unroll
-        for (int y = 0; y < 8; ++y) o[y] = to_tf32(xv[y] * rx * ex2(gg[y]));
+        for (int y = 0; y < 8; ++y) {
+          const float G = ex2(gg[y]);
+          ok8[y] = to_tf32(kv[y] * rk * G);
+          oq8[y] = to_tf32(qv[y] * rq * G);
+        }
       } else {
 #pragma unroll
-        for (int y = 0; y < 8; ++y) o[y] = 0.f;
+        for (int y = 0; y < 8; ++y) ok8[y] = oq8[y] = 0.f;
       }
-      st_f32x8(sm + OFF_X + kmaj_f32<128>(row, 8 * c8), sm + OFF_X + kmaj_f32<128>(row, 8 * c8 + 4),
-               o);
+      st_f32x8(sm + OFF_X + kmaj_f32<128>(r, 8 * c8), sm + OFF_X + kmaj_f32<128>(r, 8 * c8 + 4), ok8);
+      st_f32x8(sm + OFF_X + kmaj_f32<128>(64 + r, 8 * c8),
+               sm + OFF_X + kmaj_f32<128>(64 + r, 8 * c8 + 4), oq8);
     }
     fence_proxy_async();
     if (!(ok = sync())) break;
@@ -419,128 +486,118 @@ __global__ void __launch_bounds__(NT, 1)
       commit(mma_par);
     }
 
-    // ---- P4: T = (I + A)^-1 by 16x16 blocks (fp32, plain layout in the T region) ---------
-    {
+    // ---- P4 (warp group 2): T = (I + A)^-1 by 16x16 blocks, fp32, then tf32 K-major
+    //      [r][s] in the T region.  Meanwhile groups 0 and 1 wait for MMA1 and build
+    //      Y^T = beta (V - K Gamma S)^T (tf32 hi + lo in TA), decay S^T by Gamma_C, and
+    //      build Kbar = k Gamma_C / Gamma (bf16 hi | lo, MN-major) into X[0, 32K). ---------
+    if (grp == 2) {
+      const int t = tid - 256, wg = t >> 5;
       const float *Am = reinterpret_cast<const float *>(sm + OFF_A);
       float *Tm = reinterpret_cast<float *>(sm + OFF_T);
-      if (tid < 64) {  // diagonal blocks: right-looking substitution, one column per thread
-        const int R = tid >> 4, cc = tid & 15, b0 = 16 * R;
-        float x[16], p[16];
+      if (t < 64) {  // diagonal blocks: right-looking substitution, one column per thread
+        const int R = t >> 4, cc = t & 15, b0 = 16 * R;
+        float x[16], pacc[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) p[i] = 0.f;
+        for (int i = 0; i < 16; ++i) pacc[i] = 0.f;
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          x[k] = k < cc ? 0.f : (k == cc ? 1.f : -p[k]);
+          x[k] = k < cc ? 0.f : (k == cc ? 1.f : -pacc[k]);
 #pragma unroll
-          for (int i = k + 1; i < 16; ++i) p[i] = fmaf(Am[(b0 + i) * 64 + b0 + k], x[k], p[i]);
+          for (int i = k + 1; i < 16; ++i) pacc[i] = fmaf(Am[(b0 + i) * 64 + b0 + k], x[k], pacc[i]);
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) Tm[(b0 + i) * 64 + b0 + cc] = x[i];
       }
-      __syncthreads();
-      // off-diagonal blocks by distance: M = sum_Q A_RQ T_QS, then T_RS = -T_RR M; each
-      // thread owns a 4x4 patch of a 16x16 block
+      asm volatile("bar.sync 3, 128;" ::: "memory");
+      // off-diagonal blocks by distance, one warp per block: M = sum_Q A_RQ T_QS (the A
+      // blocks of row R are contiguous in Q), then T_RS = -T_RR M
       for (int dist = 1; dist <= 3; ++dist) {
-        const int npairs = 4 - dist;
-        const int pidx = tid >> 4, ai = ((tid >> 2) & 3) * 4, bi = (tid & 3) * 4;
-        if (tid < 16 * npairs) {
-          const int R = dist + pidx, S = R - dist;
-          float acc[4][4] = {};
+        if (wg < 4 - dist) {
+          const int R = dist + wg, S = R - dist;
+          float dacc[2][4] = {};
           for (int Q = S; Q < R; ++Q)
-#pragma unroll 4
-            for (int y = 0; y < 16; ++y) {
-              const float4 t4 = *reinterpret_cast<const float4 *>(&Tm[(16 * Q + y) * 64 + 16 * S + bi]);
-#pragma unroll
-              for (int x = 0; x < 4; ++x) {
-                const float av = Am[(16 * R + ai + x) * 64 + 16 * Q + y];
-                acc[x][0] = fmaf(av, t4.x, acc[x][0]);
-                acc[x][1] = fmaf(av, t4.y, acc[x][1]);
-                acc[x][2] = fmaf(av, t4.z, acc[x][2]);
-                acc[x][3] = fmaf(av, t4.w, acc[x][3]);
-              }
-            }
-#pragma unroll
-          for (int x = 0; x < 4; ++x)
-            *reinterpret_cast<float4 *>(&s_M[pidx * 256 + (ai + x) * 16 + bi]) =
-                make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
+            warp_mma16(dacc, Am + (16 * R) * 64 + 16 * Q, 64, Tm + (16 * Q) * 64 + 16 * S, 64, 2,
+                       lane);
+          warp_store16(s_M + wg * 256, 16, dacc, lane, 1.f);
+          __syncwarp();
+          float tacc[2][4] = {};
+          warp_mma16(tacc, Tm + (16 * R) * 64 + 16 * R, 64, s_M + wg * 256, 16, 2, lane);
+          warp_store16(Tm + (16 * R) * 64 + 16 * S, 64, tacc, lane, -1.f);
         }
-        __syncthreads();
-        if (tid < 16 * npairs) {
-          const int R = dist + pidx, S = R - dist;
-          float acc[4][4] = {};
-#pragma unroll 4
-          for (int y = 0; y < 16; ++y) {
-            const float4 m4 = *reinterpret_cast<const float4 *>(&s_M[pidx * 256 + y * 16 + bi]);
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const float tv = Tm[(16 * R + ai + x) * 64 + 16 * R + y];
-              acc[x][0] = fmaf(tv, m4.x, acc[x][0]);
-              acc[x][1] = fmaf(tv, m4.y, acc[x][1]);
-              acc[x][2] = fmaf(tv, m4.z, acc[x][2]);
-              acc[x][3] = fmaf(tv, m4.w, acc[x][3]);
-            }
-          }
-#pragma unroll
-          for (int x = 0; x < 4; ++x)
-            *reinterpret_cast<float4 *>(&Tm[(16 * R + ai + x) * 64 + 16 * S + bi]) =
-                make_float4(-acc[x][0], -acc[x][1], -acc[x][2], -acc[x][3]);
-        }
-        __syncthreads();
+        asm volatile("bar.sync 3, 128;" ::: "memory");
       }
       // T (lower triangle incl. the unit diagonal) -> tf32, K-major [r][s], in place
-      float tv[11];
+      float tv[32];
 #pragma unroll
-      for (int q = 0; q < 11; ++q) {
-        const int e = tid + NT * q;
-        tv[q] = 0.f;
-        if (e < 4096) {
-          const int r = e >> 6, s = e & 63;
-          tv[q] = s <= r ? to_tf32(Tm[e]) : 0.f;
-        }
+      for (int q = 0; q < 32; ++q) {
+        const int e = t + 128 * q, r = e >> 6, ss = e & 63;
+        tv[q] = ss <= r ? to_tf32(Tm[e]) : 0.f;
       }
-      __syncthreads();
+      asm volatile("bar.sync 3, 128;" ::: "memory");
 #pragma unroll
-      for (int q = 0; q < 11; ++q) {
-        const int e = tid + NT * q;
-        if (e < 4096)
-          *reinterpret_cast<float *>(sm + OFF_T + kmaj_f32<64>(e >> 6, e & 63)) = tv[q];
+      for (int q = 0; q < 32; ++q) {
+        const int e = t + 128 * q;
+        *reinterpret_cast<float *>(sm + OFF_T + kmaj_f32<64>(e >> 6, e & 63)) = tv[q];
       }
-    }
-    fence_proxy_async();
-    if (!(ok = sync())) break;
-    wait(BAR_MMA, mma_par);  // MMA1 done
-    mma_par ^= 1;
-    tc_fence_after();
-
-    // ---- P5: Y^T = beta (V - K Gamma S)^T as tf32 hi + lo in TA (groups 0, 1: 32 tokens
-    //      each); decay S^T by Gamma_C (group 2) ------------------------------------------
-    if (grp < 2) {
-      wait(BAR_V, par);
-      float xk[32], hi[32];
-      tmem_ld32(tm + lane_off + TM_C + 32 * grp, xk);
-      tmem_wait_ld();
-#pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        const int s = 32 * grp + x;
-        const float y = s < nv ? s_beta[s] * (bf_at(sm + OFF_V, s, j) - xk[x]) : 0.f;
-        hi[x] = to_tf32(y);
-        xk[x] = to_tf32(y - hi[x]);
-      }
-      tmem_st32(tm + lane_off + TM_A + 32 * grp, hi);
-      tmem_st32(tm + lane_off + TM_A + 64 + 32 * grp, xk);
-      tmem_wait_st();
     } else {
-#pragma unroll 1
-      for (int g32 = 0; g32 < 4; ++g32) {
-        float v[32];
-        tmem_ld32(tm + lane_off + TM_S + 32 * g32, v);
+      wait(BAR_MMA, mma_par);  // MMA1 done
+      tc_fence_after();
+      wait(BAR_V, par);
+      {
+        float xk[32], hi[32];
+        tmem_ld32(tm + lane_off + TM_C + 32 * grp, xk);
         tmem_wait_ld();
 #pragma unroll
-        for (int x = 0; x < 32; ++x) v[x] *= s_GC[32 * g32 + x];
-        tmem_st32(tm + lane_off + TM_S + 32 * g32, v);
+        for (int x = 0; x < 32; ++x) {
+          const int s = 32 * grp + x;
+          const float y = s < nv ? s_beta[s] * (bf_at(sm + OFF_V, s, j) - xk[x]) : 0.f;
+          hi[x] = to_tf32(y);
+          xk[x] = to_tf32(y - hi[x]);
+        }
+        tmem_st32(tm + lane_off + TM_A + 32 * grp, hi);
+        tmem_st32(tm + lane_off + TM_A + 64 + 32 * grp, xk);
+      }
+#pragma unroll 1
+      for (int g32 = 0; g32 < 2; ++g32) {  // decay: this group's 64 key channels
+        float v[32];
+        const int i0 = 64 * grp + 32 * g32;
+        tmem_ld32(tm + lane_off + TM_S + i0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) v[x] *= s_GC[i0 + x];
+        tmem_st32(tm + lane_off + TM_S + i0, v);
       }
       tmem_wait_st();
+      for (int it = tid; it < C * 16; it += 256) {  // Kbar hi | lo
+        const int s = it >> 4, c8 = it & 15;
+        uint32_t hw[4], lw[4];
+        if (s < nv) {
+          float kv[8], gg[8];
+          bf_row8(sm + OFF_K, s, c8, kv);
+          f_row8(sm + OFF_G, s, c8, gg);
+          const float4 c0v = *reinterpret_cast<const float4 *>(&s_gC[8 * c8]);
+          const float4 c1v = *reinterpret_cast<const float4 *>(&s_gC[8 * c8 + 4]);
+          const float gc[8] = {c0v.x, c0v.y, c0v.z, c0v.w, c1v.x, c1v.y, c1v.z, c1v.w};
+          const float rk = s_rk[s];
+#pragma unroll
+          for (int y = 0; y < 4; ++y) {
+            const float a0 = kv[2 * y] * rk * ex2(gc[2 * y] - gg[2 * y]);
+            const float a1 = kv[2 * y + 1] * rk * ex2(gc[2 * y + 1] - gg[2 * y + 1]);
+            hw[y] = pack_bf2(a0, a1);
+            lw[y] = pack_bf2(a0 - bf_lo(hw[y]), a1 - bf_hi(hw[y]));
+          }
+        } else {
+#pragma unroll
+          for (int y = 0; y < 4; ++y) hw[y] = lw[y] = 0u;
+        }
+        const uint32_t off = mnmaj_bf16_128(s, 8 * c8);
+        *reinterpret_cast<uint4 *>(sm + OFF_X + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4 *>(sm + OFF_X + 16384 + off) =
+            make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
     }
+    mma_par ^= 1;  // MMA1's phase (waited by groups 0 and 1)
+    fence_proxy_async();
     if (!(ok = sync())) break;
     if (tid == 0) {  // u^T = Y^T T^T, hi then lo
       for (int ks = 0; ks < 16; ++ks) {
@@ -549,37 +606,8 @@ __global__ void __launch_bounds__(NT, 1)
         mma_tf32_ts(tm + TM_B, tm + TM_A + 64 * (ks >> 3) + 8 * k8, bd, ID_64, ks > 0);
       }
       commit(mma_par);
+      if (more) issue((1u << BAR_K) | (1u << BAR_V) | (1u << BAR_G), c + 1);
     }
-    // meanwhile: Kbar = k Gamma_C / Gamma as bf16 hi | lo, MN-major [s][i], into X[0, 32K)
-    for (int it = tid; it < 64 * 16; it += NT) {
-      const int s = it >> 4, c8 = it & 15;
-      uint32_t hw[4], lw[4];
-      if (s < nv) {
-        float kv[8], gg[8];
-        bf_row8(sm + OFF_K, s, c8, kv);
-        f_row8(sm + OFF_G, s, c8, gg);
-        const float4 c0v = *reinterpret_cast<const float4 *>(&s_gC[8 * c8]);
-        const float4 c1v = *reinterpret_cast<const float4 *>(&s_gC[8 * c8 + 4]);
-        const float gc[8] = {c0v.x, c0v.y, c0v.z, c0v.w, c1v.x, c1v.y, c1v.z, c1v.w};
-        const float rk = s_rk[s];
-#pragma unroll
-        for (int y = 0; y < 4; ++y) {
-          const float a0 = kv[2 * y] * rk * ex2(gc[2 * y] - gg[2 * y]);
-          const float a1 = kv[2 * y + 1] * rk * ex2(gc[2 * y + 1] - gg[2 * y + 1]);
-          hw[y] = pack_bf2(a0, a1);
-          lw[y] = pack_bf2(a0 - bf_lo(hw[y]), a1 - bf_hi(hw[y]));
-        }
-      } else {
-#pragma unroll
-        for (int y = 0; y < 4; ++y) hw[y] = lw[y] = 0u;
-      }
-      const uint32_t off = mnmaj_bf16_128(s, 8 * c8);
-      *reinterpret_cast<uint4 *>(sm + OFF_X + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4 *>(sm + OFF_X + 16384 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    }
-    fence_proxy_async();
-    if (!(ok = sync())) break;
-    if (tid == 0 && more) issue((1u << BAR_K) | (1u << BAR_V) | (1u << BAR_G), c + 1);
     wait(BAR_MMA, mma_par);  // u ready
     mma_par ^= 1;
     tc_fence_after();
