@@ -47,6 +47,30 @@ def _peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+CSRC = os.path.join(ROOT, "hybrid_linear_attention_gb300", "csrc")
+
+
+def _profiled_traffic(summary, sources):
+    """DRAM bytes per launch from a committed ncu summary in profiles/, or None when the
+    kernel's sources changed since that capture (hash of the concatenated sources)."""
+    import hashlib
+    try:
+        h = hashlib.sha256()
+        for src in sources:
+            with open(os.path.join(CSRC, src), "rb") as f:
+                h.update(f.read())
+        want, traffic = None, None
+        with open(os.path.join(ROOT, "profiles", summary)) as f:
+            for line in f:
+                if line.startswith("source_sha256_16:"):
+                    want = line.split()[1]
+                elif line.startswith("traffic_bytes_per_launch:"):
+                    traffic = int(line.split()[1])
+        return traffic if want == h.hexdigest()[:16] else None
+    except Exception:
+        return None
+
+
 def _prefill_bytes(T, H, d, with_state_out=True):
     """Algorithmic HBM bytes of one kda_prefill launch: q, k, v, out (bf16), g (fp32),
     beta (fp32), plus the final fp32 state."""
@@ -254,7 +278,11 @@ def run_ours(args):
     from hybrid_linear_attention_gb300 import inputs, kda
 
     hbm, tflops, tflops_sus, peak_kind = _peaks()
-    wl = PrefillWorkload(dev, seed=rank)
+    # the global batch is one T=4096 sequence per rank; each rank owns its share (no
+    # collective on the data path)
+    from hybrid_linear_attention_gb300.sharding import sequence_shard
+    mine = sequence_shard([T_PREFILL] * ws, ws, rank)
+    wl = PrefillWorkload(dev, seed=mine[0])
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -313,14 +341,17 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "tokens_per_step": T_PREFILL, "heads": H, "d": D,
-                   "chunk": 64, "parallelism": f"replicas{ws}",
+                   "chunk": 64, "parallelism": f"sequence-sharded x{ws}" if ws > 1 else "single GPU",
                    "l2": "inputs larger than L2 (403 MB) and a 258 MB buffer written between "
                          "steps"},
         "breakdown_ms": {"prologue": pro, "prefill": pf},
         "prefill_kernel_tokens_per_s": ws * T_PREFILL / (pf * 1e-3),
         "roofline": {"kernel": "kda_prefill", "bound": "hbm", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_kind": f"{peak_kind} hbm_gbs", "traffic": None,
+                     "peak_kind": f"{peak_kind} hbm_gbs",
+                     "traffic": _profiled_traffic(
+                         "kda_prefill_tc_T4096_H64.md",
+                         ["kda_prefill_tc.cu", "kda_tc_ptx.cuh", "kda_common.cuh"]),
                      "algorithmic_bytes_per_launch": pf_bytes},
         "gpu_launches": int(launches),
         "gpu_launches_per_step": launches / args.steps,
@@ -397,7 +428,9 @@ def _decode_bench(dev, kda, inputs, hbm, rank, args):
                         "consecutive steps",
             "ms_per_step": ms, "tokens_per_s": n / (ms * 1e-3),
             "roofline": {"kernel": "kda_decode_step_fused", "bound": "hbm", "achieved": gbs,
-                         "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
+                         "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                         "traffic": _profiled_traffic("kda_decode_fused_N256_H64.md",
+                                                      ["kda_recurrent.cu", "kda_common.cuh"]),
                          "algorithmic_bytes_per_launch": b}}
 
 
