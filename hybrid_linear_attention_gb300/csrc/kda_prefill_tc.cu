@@ -25,7 +25,8 @@
 // column = key channel i), and is fed to the tensor core directly as the A operand.
 //   TMEM columns   [0,128) S^T   [128,256) TA   [256,384) TB   [384,512) TC
 // MMA precision: intra-chunk products in tf32 (operands rounded to nearest; beta(V - KGS)
-// split into tf32 hi + lo), the state update S += Kbar^T u as three bf16 products
+// split into tf32 hi + lo) except the band of P within a block of the diagonal, which is
+// summed in fp32 on the CUDA cores while the tensor core forms the rest; the state update S += Kbar^T u as three bf16 products
 // (hi*hi + hi*lo + lo*hi), which keeps the state at fp32-level accuracy.  Inputs arrive by
 // TMA in 128-byte-swizzled tiles; every operand is built with 16-byte vector accesses.
 #include <cuda.h>
@@ -53,7 +54,11 @@ constexpr uint32_t OFF_X = 81920;    // 64 KB: AP operand rows -> [K Gamma; Q Ga
 constexpr uint32_t OFF_T = 147456;   // 16 KB: T fp32 (plain) -> T tf32 (K-major)
 constexpr uint32_t OFF_P = 163840;   // 16 KB: P' tf32 (K-major)
 constexpr uint32_t OFF_A = 180224;   // 16 KB: A fp32 (plain)
-constexpr uint32_t SMEM_BYTES = 196608 + 1024;
+// fp32 operand rows of the exact P band, live from the AP build until the band is summed:
+constexpr uint32_t OFF_KD = OFF_T;   // 32 KB over T and P': Khat^(R(s))_s, row s
+constexpr uint32_t OFF_QD = OFF_A;   // 32 KB over A and beyond: Qtil_r, row r
+constexpr uint32_t OFF_BD = 212992;  // 4992 B: band sums (3 full blocks, 4 strict triangles)
+constexpr uint32_t SMEM_BYTES = 212992 + 5120 + 1024;
 
 constexpr uint32_t TM_S = 0, TM_A = 128, TM_B = 256, TM_C = 384, TM_COLS = 512;
 
@@ -65,6 +70,11 @@ __device__ __forceinline__ uint32_t kmaj_f32(int row, int ch) {
   const uint32_t b = (uint32_t)((ch & 31) * 4);
   return (uint32_t)(ch >> 5) * (NR * 128u) + (uint32_t)row * 128u +
          ((((b >> 4) ^ (row & 7))) << 4) + (b & 15u);
+}
+// fp32 row of 128 channels (512 bytes), 16-byte chunk c4 XOR-swizzled by the row within each
+// 128-byte group, so eight consecutive rows (or eight chunks of one row) hit distinct banks
+__device__ __forceinline__ uint32_t rowf32(int row, int c4) {
+  return (uint32_t)row * 512u + ((uint32_t)((c4 & ~7) | ((c4 & 7) ^ (row & 7))) << 4);
 }
 // K-major bf16 operand [rows][64]: a single 128-byte panel
 __device__ __forceinline__ uint32_t kmaj_bf16_64(int row, int k) {
@@ -336,7 +346,14 @@ __global__ void __launch_bounds__(NT, 1)
       }
 #pragma unroll
       for (int x = 1; x < 32; ++x) v[x] += v[x - 1];
-      if (hf == 0) s_M[i] = v[31];
+      // decay over 16-token block R-1 per channel, 2^(gam_R0 - gam_(R-1)0), at s_M[128 R + i]
+      if (hf == 0) {
+        s_M[i] = v[31];
+        s_M[128 + i] = ex2(v[15]);
+        s_M[256 + i] = ex2(v[31] - v[15]);
+      } else {
+        s_M[384 + i] = ex2(v[15]);
+      }
       asm volatile("bar.sync 2, 256;" ::: "memory");
       const float base = hf ? s_M[i] : 0.f;
 #pragma unroll
@@ -361,6 +378,7 @@ __global__ void __launch_bounds__(NT, 1)
       const int pi = grp, m = j;
       const int R = 2 * pi + (m >> 6), s = m & 63;
       const bool live = s < nv && s <= 16 * R + 15;
+      const bool band = s >= 16 * R && s <= 16 * R + 15;  // token s inside block R: keep fp32
       const float rk = s_rk[s];
       const uint32_t dst = tm + lane_off + (pi == 0 ? TM_A : TM_C);
 #pragma unroll 1
@@ -376,12 +394,20 @@ __global__ void __launch_bounds__(NT, 1)
             const float4 r1 = *reinterpret_cast<const float4 *>(&s_g0[R][32 * g32 + 8 * c8 + 4]);
             const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
-            for (int y = 0; y < 8; ++y) v[8 * c8 + y] = to_tf32(kv[y] * rk * ex2(rr[y] - gg[y]));
+            for (int y = 0; y < 8; ++y) v[8 * c8 + y] = kv[y] * rk * ex2(rr[y] - gg[y]);
           }
         } else {
 #pragma unroll
           for (int x = 0; x < 32; ++x) v[x] = 0.f;
         }
+        if (band) {
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4)
+            *reinterpret_cast<float4 *>(sm + OFF_KD + rowf32(s, 8 * g32 + c4)) =
+                make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+        }
+#pragma unroll
+        for (int x = 0; x < 32; ++x) v[x] = to_tf32(v[x]);
         tmem_st32(dst + 32 * g32, v);
       }
       tmem_wait_st();
@@ -404,12 +430,15 @@ __global__ void __launch_bounds__(NT, 1)
           for (int y = 0; y < 8; ++y) {
             const float e = ex2(gg[y] - rr[y]);
             ok8[y] = to_tf32(kv[y] * rk * e);
-            oq8[y] = to_tf32(qv[y] * rq * e);
+            oq8[y] = qv[y] * rq * e;
           }
         } else {
 #pragma unroll
           for (int y = 0; y < 8; ++y) ok8[y] = oq8[y] = 0.f;
         }
+        st_f32x8(sm + OFF_QD + rowf32(r, 2 * c8), sm + OFF_QD + rowf32(r, 2 * c8 + 1), oq8);
+#pragma unroll
+        for (int y = 0; y < 8; ++y) oq8[y] = to_tf32(oq8[y]);
         st_f32x8(sm + OFF_X + kmaj_f32<128>(rowk, 8 * c8),
                  sm + OFF_X + kmaj_f32<128>(rowk, 8 * c8 + 4), ok8);
         st_f32x8(sm + OFF_X + kmaj_f32<128>(rowk + 16, 8 * c8),
@@ -429,9 +458,82 @@ __global__ void __launch_bounds__(NT, 1)
         }
       commit(mma_par);
     }
+    // ---- exact band of P while the MMA runs.  A tf32 dot product of the two scaled rows
+    //      loses the few bits that survive where q_r.k_s nearly cancels; near the diagonal
+    //      (little decay) that error reaches the output.  P[r,s] for s in r's own block and in
+    //      the block before is summed here in fp32: Qtil_r . Khat^(R)_s, with
+    //      Khat^(R)_s = Khat^(R-1)_s * 2^(gam_R0 - gam_(R-1)0) for s in block R-1.
+    //      Items: 40 diagonal 4x4 tiles + 48 tiles of the block before, x 8 channel slices
+    //      (chunks p, p+8, p+16, p+24 of 4 channels), summed across the 8 lanes. ------------
+    {
+      float *band = reinterpret_cast<float *>(sm + OFF_BD);
+#pragma unroll 1
+      for (int item = tid; item < 704; item += NT) {
+        const int p = item & 7, tile = item >> 3;
+        int R, r0, s0;
+        const bool prev = tile >= 40;
+        if (!prev) {
+          R = tile / 10;
+          const int t10 = tile - 10 * R;
+          const int ti = t10 >= 6 ? 3 : t10 >= 3 ? 2 : t10 >= 1 ? 1 : 0;
+          r0 = 16 * R + 4 * ti;
+          s0 = 16 * R + 4 * (t10 - (ti * (ti + 1)) / 2);
+        } else {
+          const int tt = tile - 40;
+          R = 1 + (tt >> 4);
+          r0 = 16 * R + 4 * ((tt >> 2) & 3);
+          s0 = 16 * (R - 1) + 4 * (tt & 3);
+        }
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) acc[i][jj] = 0.f;
+#pragma unroll
+        for (int jx = 0; jx < 4; ++jx) {
+          const int c4 = p + 8 * jx;
+          const float4 dq = prev ? *reinterpret_cast<const float4 *>(&s_M[128 * R + 4 * c4])
+                                 : make_float4(1.f, 1.f, 1.f, 1.f);
+          float4 qf[4], kf[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            qf[i] = *reinterpret_cast<const float4 *>(sm + OFF_QD + rowf32(r0 + i, c4));
+            qf[i].x *= dq.x, qf[i].y *= dq.y, qf[i].z *= dq.z, qf[i].w *= dq.w;
+            kf[i] = *reinterpret_cast<const float4 *>(sm + OFF_KD + rowf32(s0 + i, c4));
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+              acc[i][jj] = fmaf(qf[i].w, kf[jj].w,
+                                fmaf(qf[i].z, kf[jj].z,
+                                     fmaf(qf[i].y, kf[jj].y, fmaf(qf[i].x, kf[jj].x, acc[i][jj]))));
+        }
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+              acc[i][jj] += __shfl_xor_sync(0xffffffffu, acc[i][jj], off);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int i = e >> 2, jj = e & 3;
+          if ((e >> 1) != p) continue;
+          const int r16 = r0 - 16 * R + i;
+          if (prev) {
+            band[(R - 1) * 256 + r16 * 16 + (s0 - 16 * (R - 1)) + jj] = acc[i][jj];
+          } else {
+            const int s16 = s0 - 16 * R + jj;
+            if (s16 < r16) band[768 + 120 * R + (r16 * (r16 - 1)) / 2 + s16] = acc[i][jj];
+          }
+        }
+      }
+    }
     wait(BAR_MMA, mma_par);
     mma_par ^= 1;
     tc_fence_after();
+    if (!(ok = sync())) break;  // band visible; its fp32 rows are free for A and P'
 
     // ---- P3: A (beta-scaled, strict lower, fp32) and P' (strict lower, tf32) from TMEM;
     //      then X = [K Gamma; Q Gamma] (tf32 rows) into the freed AP operand region --------
@@ -441,12 +543,17 @@ __global__ void __launch_bounds__(NT, 1)
       tmem_ld32(tm + lane_off + TM_B + 64 * pi + 32 * (m >> 6), v);
       tmem_wait_ld();
       float *Am = reinterpret_cast<float *>(sm + OFF_A);
+      const float *band = reinterpret_cast<const float *>(sm + OFF_BD);
+      const int sd = s - 16 * R, sp = s - 16 * (R - 1);  // s within block R / block R-1
 #pragma unroll
       for (int x = 0; x < 16; ++x) {
         const int r = 16 * R + x;
         const bool low = s < r;
         Am[r * 64 + s] = low ? s_beta[r] * v[x] : 0.f;
-        *reinterpret_cast<float *>(sm + OFF_P + kmaj_f32<64>(r, s)) = low ? to_tf32(v[16 + x]) : 0.f;
+        float pv = v[16 + x];
+        if (sd >= 0 && sd < x) pv = band[768 + 120 * R + (x * (x - 1)) / 2 + sd];
+        else if (R > 0 && sp >= 0 && sp < 16) pv = band[(R - 1) * 256 + x * 16 + sp];
+        *reinterpret_cast<float *>(sm + OFF_P + kmaj_f32<64>(r, s)) = low ? to_tf32(pv) : 0.f;
       }
     }
     for (int it = tid; it < C * 16; it += NT) {  // (token, 8-channel group): rows r, 64 + r

@@ -1,0 +1,158 @@
+"""GPU parity at the full workload sizes, on (sequence, head) units the oracle recomputes one by
+one.  Inputs are drawn directly on the GPU by the seeded generator; the oracle receives the
+sampled units' slices.
+
+Workloads: single-layer prefill (T=4096, H=64, d=128), the bench's prologue+prefill chain on
+the same shape, decode (256 sequences x 100 fused steps), long-context prefill with the output
+norm/gate (4 x 32768, nonzero initial state), and the packed variable-length batch (32
+sequences, ~500K tokens) with fp32 and with bf16 state storage.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hybrid_linear_attention_gb300 import inputs, kda
+from tests import _gpu
+from tests._parity import excess_over_ulp, max_err_rel_rms, out_error
+
+pytestmark = pytest.mark.gpu
+
+TOL_OUT = 1e-2
+TOL_STATE = 1e-3
+H, D = 64, 128
+
+
+def _units_ref(inp, units, *, gate=False):
+    """Oracle results for (sequence, head) units: the units' slices are packed as separate
+    one-head sequences and run in one oracle call (one host thread per unit)."""
+    cu = inp["cu_seqlens"].tolist()
+    sl = [slice(cu[n], cu[n + 1]) for n, _ in units]
+
+    def cat(name):
+        return torch.cat([inp[name][s_, h:h + 1].cpu() for s_, (_, h) in zip(sl, units)])
+
+    lens = [cu[n + 1] - cu[n] for n, _ in units]
+    args = {}
+    if "init_state" in inp:
+        args["init_state"] = torch.cat([inp["init_state"][n:n + 1, h:h + 1].cpu()
+                                        for n, h in units])
+    if gate:
+        args.update(gate=cat("gate"), norm_w=inp["norm_w"].cpu())
+    r = oracle.kda_forward(cat("q"), cat("k"), cat("v"), cat("g"), cat("beta"),
+                           inputs.cu_seqlens_from_lengths(lens), **args)
+    offs = np.concatenate([[0], np.cumsum(lens)])
+    return [(r["out"][offs[u]:offs[u + 1], 0], r["final_state"][u, 0]) for u in range(len(units))]
+
+
+def _check_units(inp, out, fin, units, *, gate=False, state_bf16=False):
+    cu = inp["cu_seqlens"].tolist()
+    worst_o, worst_s = 0.0, 0.0
+    for (n, h), (ro, rs) in zip(units, _units_ref(inp, units, gate=gate)):
+        go = out[cu[n]:cu[n + 1], h].cpu()
+        gs = fin[n, h].cpu()
+        eo = out_error(go, ro, torch.bfloat16)
+        es = excess_over_ulp(gs, rs) if state_bf16 else max_err_rel_rms(gs, rs)
+        worst_o, worst_s = max(worst_o, eo), max(worst_s, es)
+    assert worst_o <= TOL_OUT, f"output error {worst_o:.3g}"
+    assert worst_s <= TOL_STATE, f"final-state error {worst_s:.3g}"
+    return worst_o, worst_s
+
+
+def test_single_layer_prefill_T4096():
+    """T=4096, H=64, d=128; q, k, v drawn N(0,1) as the post-conv streams, zero state."""
+    inp = inputs.kda_inputs([4096], H, D, seed=100, device="cuda")
+    p = kda.params(H=H, d=D)
+    out, fin = _gpu.prefill(inp, p)
+    torch.cuda.synchronize()
+    kda.kda_check_device_error()
+    _check_units(inp, out, fin, [(0, h) for h in (0, 7, 21, 38, 50, 63)])
+
+
+def test_bench_chain_prologue_then_prefill_T4096():
+    """The chain bench.py times: raw projections ~N(0,1) -> kda_prologue (conv, SiLU, q/k L2,
+    sigmoid beta, g clamp) -> kda_prefill.  The oracle runs the same chain in fp64; the
+    bf16 storage of q, k, v between the two calls is the ABI's, so outputs are compared."""
+    T = 4096
+    pin = inputs.prologue_inputs([T], H, D, seed=101, device="cuda", conv_state=False)
+    p = kda.params(H=H, d=D)
+    q = torch.empty((T, H, D), dtype=torch.bfloat16, device="cuda")
+    k, v = torch.empty_like(q), torch.empty_like(q)
+    beta = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    g = torch.empty((T, H, D), dtype=torch.float32, device="cuda")
+    _gpu.lib()
+    kda.kda_prologue(p, pin["x"], pin["conv_w"], None, pin["cu_seqlens"], q, k, v, l2norm_qk=True,
+                     beta_logit=pin["beta_logit"], g_raw=pin["g_raw"], beta=beta, g=g)
+    out = torch.empty_like(q)
+    kda.kda_prefill(p, q, k, v, g, beta, pin["cu_seqlens"], out)
+    torch.cuda.synchronize()
+    for h in (0, 33, 63):
+        cols = np.r_[h * D:(h + 1) * D, H * D + h * D:H * D + (h + 1) * D,
+                     2 * H * D + h * D:2 * H * D + (h + 1) * D]
+        xs = pin["x"][:, cols].cpu()
+        ws = pin["conv_w"][cols].cpu()
+        pr = oracle.prologue(xs, ws, torch.tensor([0, T], dtype=torch.int32), 1, D,
+                             l2norm_qk=True, beta_logit=pin["beta_logit"][:, h:h + 1].cpu(),
+                             g_raw=pin["g_raw"][:, h:h + 1].cpu())
+        # the ABI stores the prologue's q, k, v in bf16 between the two calls: the oracle's
+        # own fp64 y is rounded to bf16 (nearest even) the same way, and the recurrence
+        # re-normalises q, k as kda_prefill does (qk_l2norm on)
+        y = torch.from_numpy(pr["y"].reshape(T, 3, 1, D)).to(torch.bfloat16)
+        r = oracle.kda_forward(y[:, 0], y[:, 1], y[:, 2],
+                               pr["g"].astype(np.float32), pr["beta"].astype(np.float32),
+                               np.array([0, T], np.int32), qk_l2norm=True)
+        assert out_error(out[:, h].cpu(), r["out"][:, 0], torch.bfloat16) <= TOL_OUT
+
+
+def test_decode_256_sequences_100_fused_steps():
+    n, K = 256, 100
+    C = 3 * H * D
+    p = kda.params(H=H, d=D)
+    _gpu.lib()
+    state0 = inputs.normal((n, H, D, D), seed=200, device="cuda", dtype=torch.float32, std=0.02)
+    cs0 = inputs.normal((n, 3, C), seed=201, device="cuda")
+    w = inputs.normal((C, 4), seed=202, device="cuda", std=0.5)
+    x = inputs.normal((K, n, C), seed=203, device="cuda")
+    g = inputs.uniform((K, n, H, D), -5.0, 0.0, seed=204, device="cuda")
+    beta = inputs.beta_draw((K, n, H), seed=205, device="cuda")
+    state, cs = state0.clone(), cs0.clone()
+    out = torch.empty((K, n, H, D), dtype=torch.bfloat16, device="cuda")
+    for t in range(K):
+        kda.kda_decode_step_fused(p, x[t], w, cs, g[t], beta[t], state, out[t])
+    torch.cuda.synchronize()
+    kda.kda_check_device_error()
+    cu = torch.tensor([0, K], dtype=torch.int32)
+    for s in (0, 97, 255):
+        pr = oracle.prologue(x[:, s].cpu(), w.cpu(), cu, H, D, conv_state=cs0[s:s + 1].cpu())
+        y = pr["y"].reshape(K, 3, H, D)
+        r = oracle.kda_forward(y[:, 0].copy(), y[:, 1].copy(), y[:, 2].copy(), g[:, s].cpu(),
+                               beta[:, s].cpu(), cu, init_state=state0[s:s + 1].cpu())
+        assert out_error(out[:, s].cpu(), r["out"], torch.bfloat16) <= TOL_OUT
+        assert max_err_rel_rms(state[s].cpu(), r["final_state"][0]) <= TOL_STATE
+        assert np.array_equal(cs[s].cpu().view(torch.int16).numpy(),
+                              pr["conv_state"][0].view(np.int16))
+
+
+def test_long_context_prefill_4x32768_with_gate():
+    lens = [32768] * 4
+    inp = inputs.kda_inputs(lens, H, D, seed=300, device="cuda", init_state="all", gate=True)
+    p = kda.params(H=H, d=D)
+    out, fin = _gpu.prefill(inp, p, gate=True)
+    torch.cuda.synchronize()
+    kda.kda_check_device_error()
+    _check_units(inp, out, fin, [(0, 0), (1, 31), (2, 47), (3, 63)], gate=True)
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+def test_varlen_packed_500k(state_dtype):
+    lens, _ = inputs.varlen_lengths(n_seqs=32, seed=0)
+    inp = inputs.kda_inputs(lens, H, D, seed=400, device="cuda", init_state="even",
+                            state_dtype=state_dtype)
+    p = kda.params(H=H, d=D, state_dtype=state_dtype)
+    out, fin = _gpu.prefill(inp, p)
+    torch.cuda.synchronize()
+    kda.kda_check_device_error()
+    order = sorted(range(len(lens)), key=lambda i: lens[i])
+    picks = [order[0], order[1], order[len(order) // 2], order[-1]]   # short, mid, longest
+    units = [(nn, (7 * nn) % H) for nn in picks]
+    _check_units(inp, out, fin, units, state_bf16=state_dtype == torch.bfloat16)
