@@ -24,9 +24,12 @@
 // order.  The fp32 state lives in tensor memory, transposed (lane = value channel j,
 // column = key channel i), and is fed to the tensor core directly as the A operand.
 //   TMEM columns   [0,128) S^T   [128,256) TA   [256,384) TB   [384,512) TC
-// MMA precision: intra-chunk products in tf32 (operands rounded to nearest; beta(V - KGS)
-// split into tf32 hi + lo) except the band of P within a block of the diagonal, which is
-// summed in fp32 on the CUDA cores while the tensor core forms the rest; the state update S += Kbar^T u as three bf16 products
+// A and P (64 x 64 each, K = 128) are formed per 16x16 block pair on the warp-level tensor
+// core (mma.sync m16n8k8 tf32), one warp per block pair: A in tf32, P in 3xtf32 (hi*hi +
+// hi*lo + lo*hi) on the diagonal blocks and the block before them, where q_r.k_s can nearly
+// cancel with little decay, and tf32 further back.
+// MMA precision elsewhere: tf32 (operands rounded to nearest; beta(V - KGS) split into tf32
+// hi + lo); the state update S += Kbar^T u as three bf16 products
 // (hi*hi + hi*lo + lo*hi), which keeps the state at fp32-level accuracy.  Inputs arrive by
 // TMA in 128-byte-swizzled tiles; every operand is built with 16-byte vector accesses.
 #include <cuda.h>
@@ -49,16 +52,13 @@ constexpr uint32_t OFF_Q = 0;        // q bf16 [64][128], two 128B-swizzled boxe
 constexpr uint32_t OFF_K = 16384;    // k
 constexpr uint32_t OFF_V = 32768;    // v
 constexpr uint32_t OFF_G = 49152;    // g -> cumulative log2-retention, fp32, 4 boxes of 32
-constexpr uint32_t OFF_X = 81920;    // 64 KB: AP operand rows -> [K Gamma; Q Gamma] ->
+constexpr uint32_t OFF_X = 81920;    // 64 KB: fp32 rows Ktil | Qtil -> [K Gamma; Q Gamma] ->
                                      //        Kbar hi | Kbar lo | u hi | u lo
-constexpr uint32_t OFF_T = 147456;   // 16 KB: T fp32 (plain) -> T tf32 (K-major)
-constexpr uint32_t OFF_P = 163840;   // 16 KB: P' tf32 (K-major)
-constexpr uint32_t OFF_A = 180224;   // 16 KB: A fp32 (plain)
-// fp32 operand rows of the exact P band, live from the AP build until the band is summed:
-constexpr uint32_t OFF_KD = OFF_T;   // 32 KB over T and P': Khat^(R(s))_s, row s
-constexpr uint32_t OFF_QD = OFF_A;   // 32 KB over A and beyond: Qtil_r, row r
-constexpr uint32_t OFF_BD = 212992;  // 4992 B: band sums (3 full blocks, 4 strict triangles)
-constexpr uint32_t SMEM_BYTES = 212992 + 5120 + 1024;
+constexpr uint32_t OFF_KH = 147456;  // 32 KB: fp32 rows Khat -> T fp32 (plain) -> T tf32
+constexpr uint32_t OFF_T = OFF_KH;
+constexpr uint32_t OFF_P = 180224;   // 16 KB: P' tf32 (K-major)
+constexpr uint32_t OFF_A = 196608;   // 16 KB: A fp32 (plain)
+constexpr uint32_t SMEM_BYTES = 212992 + 1024;
 
 constexpr uint32_t TM_S = 0, TM_A = 128, TM_B = 256, TM_C = 384, TM_COLS = 512;
 
@@ -135,6 +135,16 @@ __device__ __forceinline__ void st_f32x8(uint8_t *p0, uint8_t *p1, const float (
   *reinterpret_cast<float4 *>(p1) = make_float4(o[4], o[5], o[6], o[7]);
 }
 
+// d(16x8) += a(16x8) b(8x8) on the warp-level tensor core, tf32 operands (pre-rounded),
+// fp32 accumulate; fragments as in warp_mma16 below
+__device__ __forceinline__ void mma1688(float (&d)[4], const uint32_t (&a)[4],
+                                        const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
 // D(16x16) += A(16 x 8kk) B(8kk x 16) for row-major fp32 blocks in shared memory (row
 // strides la, lb), on the warp-level tensor-core MMA (m16n8k8, tf32 inputs, fp32
 // accumulate).  Accumulator fragment: d[nt][0..3] = rows g, g, g+8, g+8 and columns
@@ -186,7 +196,8 @@ __global__ void __launch_bounds__(NT, 1)
   __shared__ __align__(16) float s_gC[D];     // log2-retention at the chunk's last token
   __shared__ float s_GC[D];                   // Gamma_C
   __shared__ float s_red[4][C];
-  __shared__ __align__(16) float s_M[3 * 256];  // inverse scratch
+  __shared__ __align__(16) float s_M[3 * 256];  // inverse scratch; block decays in P2/P3
+  __shared__ __align__(16) float s_e0[4][D];      // 2^(gam_R0) per block and channel
   __shared__ __align__(8) uint64_t s_bar[NBAR];
   __shared__ uint32_t s_tmem, s_abort, s_pend, s_ppar[NBAR];
 
@@ -283,6 +294,9 @@ __global__ void __launch_bounds__(NT, 1)
     }
     tmem_wait_st();
   }
+  // P' blocks above the diagonal stay zero for the whole walk
+  for (int e = tid; e < C * C / 4; e += NT)
+    reinterpret_cast<float4 *>(sm + OFF_P)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (tid == 0 && nchunks > 0)
     issue((1u << BAR_Q) | (1u << BAR_K) | (1u << BAR_V) | (1u << BAR_G), 0);
   bool ok = sync();
@@ -346,14 +360,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
 #pragma unroll
       for (int x = 1; x < 32; ++x) v[x] += v[x - 1];
-      // decay over 16-token block R-1 per channel, 2^(gam_R0 - gam_(R-1)0), at s_M[128 R + i]
-      if (hf == 0) {
-        s_M[i] = v[31];
-        s_M[128 + i] = ex2(v[15]);
-        s_M[256 + i] = ex2(v[31] - v[15]);
-      } else {
-        s_M[384 + i] = ex2(v[15]);
-      }
+      if (hf == 0) s_M[i] = v[31];
       asm volatile("bar.sync 2, 256;" ::: "memory");
       const float base = hf ? s_M[i] : 0.f;
 #pragma unroll
@@ -370,218 +377,157 @@ __global__ void __launch_bounds__(NT, 1)
     }
     if (!(ok = sync())) break;
 
-    // ---- P2: AP operands.  TMEM A side (groups 0, 1 = pairs 0, 1): lane m of pair pi holds
-    //      Khat^(R)[s] = k_s 2^(gam_R0 - gam_s), R = 2pi + m/64, s = m % 64 (zero past the
-    //      block); smem B side (group 2): rows [Ktil_R; Qtil_R] x 2 blocks per pair, with
-    //      Ktil_r = k_r 2^(gam_r - gam_R0). -----------------------------------------------
-    if (grp < 2) {
-      const int pi = grp, m = j;
-      const int R = 2 * pi + (m >> 6), s = m & 63;
-      const bool live = s < nv && s <= 16 * R + 15;
-      const bool band = s >= 16 * R && s <= 16 * R + 15;  // token s inside block R: keep fp32
-      const float rk = s_rk[s];
-      const uint32_t dst = tm + lane_off + (pi == 0 ? TM_A : TM_C);
-#pragma unroll 1
-      for (int g32 = 0; g32 < 4; ++g32) {
-        float v[32];
-        if (live) {
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            float kv[8], gg[8];
-            bf_row8(sm + OFF_K, s, 4 * g32 + c8, kv);
-            f_row8(sm + OFF_G, s, 4 * g32 + c8, gg);
-            const float4 r0 = *reinterpret_cast<const float4 *>(&s_g0[R][32 * g32 + 8 * c8]);
-            const float4 r1 = *reinterpret_cast<const float4 *>(&s_g0[R][32 * g32 + 8 * c8 + 4]);
-            const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-            for (int y = 0; y < 8; ++y) v[8 * c8 + y] = kv[y] * rk * ex2(rr[y] - gg[y]);
-          }
-        } else {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) v[x] = 0.f;
-        }
-        if (band) {
-#pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4)
-            *reinterpret_cast<float4 *>(sm + OFF_KD + rowf32(s, 8 * g32 + c4)) =
-                make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
-        }
-#pragma unroll
-        for (int x = 0; x < 32; ++x) v[x] = to_tf32(v[x]);
-        tmem_st32(dst + 32 * g32, v);
-      }
-      tmem_wait_st();
-    } else {
-      // token r's rows: Ktil_r at 64 (R/2) + 32 (R&1) + r%16, Qtil_r 16 rows below
-      for (int it = tid - 256; it < C * 16; it += 128) {
-        const int r = it >> 4, c8 = it & 15;
-        const int R = r >> 4, rowk = 64 * (R >> 1) + 32 * (R & 1) + (r & 15);
-        float ok8[8], oq8[8];
-        if (r < nv) {
-          float kv[8], qv[8], gg[8];
-          bf_row8(sm + OFF_K, r, c8, kv);
-          bf_row8(sm + OFF_Q, r, c8, qv);
-          f_row8(sm + OFF_G, r, c8, gg);
-          const float4 r0 = *reinterpret_cast<const float4 *>(&s_g0[R][8 * c8]);
-          const float4 r1 = *reinterpret_cast<const float4 *>(&s_g0[R][8 * c8 + 4]);
-          const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-          const float rk = s_rk[r], rq = s_rq[r];
-#pragma unroll
-          for (int y = 0; y < 8; ++y) {
-            const float e = ex2(gg[y] - rr[y]);
-            ok8[y] = to_tf32(kv[y] * rk * e);
-            oq8[y] = qv[y] * rq * e;
-          }
-        } else {
-#pragma unroll
-          for (int y = 0; y < 8; ++y) ok8[y] = oq8[y] = 0.f;
-        }
-        st_f32x8(sm + OFF_QD + rowf32(r, 2 * c8), sm + OFF_QD + rowf32(r, 2 * c8 + 1), oq8);
-#pragma unroll
-        for (int y = 0; y < 8; ++y) oq8[y] = to_tf32(oq8[y]);
-        st_f32x8(sm + OFF_X + kmaj_f32<128>(rowk, 8 * c8),
-                 sm + OFF_X + kmaj_f32<128>(rowk, 8 * c8 + 4), ok8);
-        st_f32x8(sm + OFF_X + kmaj_f32<128>(rowk + 16, 8 * c8),
-                 sm + OFF_X + kmaj_f32<128>(rowk + 16, 8 * c8 + 4), oq8);
-      }
-    }
-    fence_proxy_async();
-    if (!(ok = sync())) break;
-    if (tid == 0) {
-#pragma unroll 1
-      for (int pi = 0; pi < 2; ++pi)
-        for (int ks = 0; ks < 16; ++ks) {
-          const uint64_t bd = sdesc_sw128(
-              sb + OFF_X + (ks >> 2) * 16384 + 64 * pi * 128 + (ks & 3) * 32, 16, 1024);
-          mma_tf32_ts(tm + TM_B + 64 * pi, tm + (pi == 0 ? TM_A : TM_C) + 8 * ks, bd, ID_64,
-                      ks > 0);
-        }
-      commit(mma_par);
-    }
-    // ---- exact band of P while the MMA runs.  A tf32 dot product of the two scaled rows
-    //      loses the few bits that survive where q_r.k_s nearly cancels; near the diagonal
-    //      (little decay) that error reaches the output.  P[r,s] for s in r's own block and in
-    //      the block before is summed here in fp32: Qtil_r . Khat^(R)_s, with
-    //      Khat^(R)_s = Khat^(R-1)_s * 2^(gam_R0 - gam_(R-1)0) for s in block R-1.
-    //      Items: 40 diagonal 4x4 tiles + 48 tiles of the block before, x 8 channel slices
-    //      (chunks p, p+8, p+16, p+24 of 4 channels), summed across the 8 lanes. ------------
-    {
-      float *band = reinterpret_cast<float *>(sm + OFF_BD);
-#pragma unroll 1
-      for (int item = tid; item < 704; item += NT) {
-        const int p = item & 7, tile = item >> 3;
-        int R, r0, s0;
-        const bool prev = tile >= 40;
-        if (!prev) {
-          R = tile / 10;
-          const int t10 = tile - 10 * R;
-          const int ti = t10 >= 6 ? 3 : t10 >= 3 ? 2 : t10 >= 1 ? 1 : 0;
-          r0 = 16 * R + 4 * ti;
-          s0 = 16 * R + 4 * (t10 - (ti * (ti + 1)) / 2);
-        } else {
-          const int tt = tile - 40;
-          R = 1 + (tt >> 4);
-          r0 = 16 * R + 4 * ((tt >> 2) & 3);
-          s0 = 16 * (R - 1) + 4 * (tt & 3);
-        }
-        float acc[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) acc[i][jj] = 0.f;
-#pragma unroll
-        for (int jx = 0; jx < 4; ++jx) {
-          const int c4 = p + 8 * jx;
-          const float4 dq = prev ? *reinterpret_cast<const float4 *>(&s_M[128 * R + 4 * c4])
-                                 : make_float4(1.f, 1.f, 1.f, 1.f);
-          float4 qf[4], kf[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            qf[i] = *reinterpret_cast<const float4 *>(sm + OFF_QD + rowf32(r0 + i, c4));
-            qf[i].x *= dq.x, qf[i].y *= dq.y, qf[i].z *= dq.z, qf[i].w *= dq.w;
-            kf[i] = *reinterpret_cast<const float4 *>(sm + OFF_KD + rowf32(s0 + i, c4));
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-              acc[i][jj] = fmaf(qf[i].w, kf[jj].w,
-                                fmaf(qf[i].z, kf[jj].z,
-                                     fmaf(qf[i].y, kf[jj].y, fmaf(qf[i].x, kf[jj].x, acc[i][jj]))));
-        }
-#pragma unroll
-        for (int off = 1; off < 8; off <<= 1)
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-              acc[i][jj] += __shfl_xor_sync(0xffffffffu, acc[i][jj], off);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int i = e >> 2, jj = e & 3;
-          if ((e >> 1) != p) continue;
-          const int r16 = r0 - 16 * R + i;
-          if (prev) {
-            band[(R - 1) * 256 + r16 * 16 + (s0 - 16 * (R - 1)) + jj] = acc[i][jj];
-          } else {
-            const int s16 = s0 - 16 * R + jj;
-            if (s16 < r16) band[768 + 120 * R + (r16 * (r16 - 1)) / 2 + s16] = acc[i][jj];
-          }
-        }
-      }
-    }
-    wait(BAR_MMA, mma_par);
-    mma_par ^= 1;
-    tc_fence_after();
-    if (!(ok = sync())) break;  // band visible; its fp32 rows are free for A and P'
-
-    // ---- P3: A (beta-scaled, strict lower, fp32) and P' (strict lower, tf32) from TMEM;
-    //      then X = [K Gamma; Q Gamma] (tf32 rows) into the freed AP operand region --------
-    if (grp < 2) {
-      const int pi = grp, m = j, R = 2 * pi + (m >> 6), s = m & 63;
-      float v[32];
-      tmem_ld32(tm + lane_off + TM_B + 64 * pi + 32 * (m >> 6), v);
-      tmem_wait_ld();
-      float *Am = reinterpret_cast<float *>(sm + OFF_A);
-      const float *band = reinterpret_cast<const float *>(sm + OFF_BD);
-      const int sd = s - 16 * R, sp = s - 16 * (R - 1);  // s within block R / block R-1
-#pragma unroll
-      for (int x = 0; x < 16; ++x) {
-        const int r = 16 * R + x;
-        const bool low = s < r;
-        Am[r * 64 + s] = low ? s_beta[r] * v[x] : 0.f;
-        float pv = v[16 + x];
-        if (sd >= 0 && sd < x) pv = band[768 + 120 * R + (x * (x - 1)) / 2 + sd];
-        else if (R > 0 && sp >= 0 && sp < 16) pv = band[(R - 1) * 256 + x * 16 + sp];
-        *reinterpret_cast<float *>(sm + OFF_P + kmaj_f32<64>(r, s)) = low ? to_tf32(pv) : 0.f;
-      }
-    }
-    for (int it = tid; it < C * 16; it += NT) {  // (token, 8-channel group): rows r, 64 + r
-      const int r = it >> 4, c8 = it & 15;
-      float ok8[8], oq8[8];
+    // ---- P2: fp32 rows, each relative to its own 16-token block R = r/16 (gam_R0 = the
+    //      log2-retention just before the block; q, k L2-normalised):
+    //        Ktil_r = k_r 2^(gam_r - gam_R0),  Qtil_r = q_r 2^(gam_r - gam_R0)   (<= 1)
+    //        Khat_r = k_r 2^(gam_R0 - gam_r)                                     (<= 2^115)
+    //      and per channel the decay between block starts, 2^(gam_R0 - gam_R'0) for R' < R,
+    //      and 2^(gam_R0) (for [K Gamma; Q Gamma] later). -----------------------------------
+    for (int it = tid; it < C * 16; it += NT) {
+      const int r = it >> 4, c8 = it & 15, R = r >> 4;
+      float kt[8], qt[8], kh[8];
       if (r < nv) {
         float kv[8], qv[8], gg[8];
         bf_row8(sm + OFF_K, r, c8, kv);
         bf_row8(sm + OFF_Q, r, c8, qv);
         f_row8(sm + OFF_G, r, c8, gg);
+        const float4 r0 = *reinterpret_cast<const float4 *>(&s_g0[R][8 * c8]);
+        const float4 r1 = *reinterpret_cast<const float4 *>(&s_g0[R][8 * c8 + 4]);
+        const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
         const float rk = s_rk[r], rq = s_rq[r];
 #pragma unroll
         for (int y = 0; y < 8; ++y) {
-          const float G = ex2(gg[y]);
-          ok8[y] = to_tf32(kv[y] * rk * G);
-          oq8[y] = to_tf32(qv[y] * rq * G);
+          const float dg = gg[y] - rr[y];
+          const float e = ex2(dg), eh = ex2(-dg);
+          kt[y] = kv[y] * rk * e;
+          qt[y] = qv[y] * rq * e;
+          kh[y] = kv[y] * rk * eh;
         }
       } else {
 #pragma unroll
-        for (int y = 0; y < 8; ++y) ok8[y] = oq8[y] = 0.f;
+        for (int y = 0; y < 8; ++y) kt[y] = qt[y] = kh[y] = 0.f;
       }
-      st_f32x8(sm + OFF_X + kmaj_f32<128>(r, 8 * c8), sm + OFF_X + kmaj_f32<128>(r, 8 * c8 + 4), ok8);
-      st_f32x8(sm + OFF_X + kmaj_f32<128>(64 + r, 8 * c8),
-               sm + OFF_X + kmaj_f32<128>(64 + r, 8 * c8 + 4), oq8);
+      st_f32x8(sm + OFF_X + rowf32(r, 2 * c8), sm + OFF_X + rowf32(r, 2 * c8 + 1), kt);
+      st_f32x8(sm + OFF_X + 32768 + rowf32(r, 2 * c8), sm + OFF_X + 32768 + rowf32(r, 2 * c8 + 1),
+               qt);
+      st_f32x8(sm + OFF_KH + rowf32(r, 2 * c8), sm + OFF_KH + rowf32(r, 2 * c8 + 1), kh);
+    }
+    for (int e = tid; e < 10 * D; e += NT) {
+      const int pr = e >> 7, i = e & 127;
+      if (pr < 6) {  // block pairs (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
+        const int R = pr < 3 ? pr + 1 : (pr == 3 ? 2 : 3);
+        const int Rp = pr < 3 ? pr : (pr == 4 ? 1 : 0);
+        s_M[pr * D + i] = ex2(s_g0[R][i] - s_g0[Rp][i]);
+      } else {
+        s_e0[pr - 6][i] = ex2(s_g0[pr - 6][i]);
+      }
+    }
+    if (!(ok = sync())) break;
+    if (tid == 0 && more) issue(1u << BAR_Q, c + 1);  // q is consumed
+
+    // ---- P3: A and P' on the warp-level tensor core, one warp per 16x16 block (R, R'),
+    //      R' <= R: warps 0-3 the diagonal blocks, 4-6 the block before, 7-9 two and three
+    //      blocks back.  Row operand Ktil_r (Qtil_r), scaled by the decay 2^(gam_R0 - gam_R'0)
+    //      off the diagonal; column operand Khat_s relative to its own block R'.  Results:
+    //      A = beta_r (.) (strict lower, fp32, plain [r][s]); P' (strict lower, tf32,
+    //      K-major). ------------------------------------------------------------------------
+    if (warp < 10) {
+      const int R = warp < 4 ? warp : warp < 7 ? warp - 3 : (warp == 7 ? 2 : 3);
+      const int Rp = warp < 4 ? warp : warp < 7 ? warp - 4 : (warp == 8 ? 1 : 0);
+      const bool diag = warp < 4, band = warp < 7;
+      const float *dec = s_M + (diag ? 0 : (warp - 4) * D);  // read off the diagonal only
+      const int g = lane >> 2, t = lane & 3;
+      const int ra = 16 * R + g, rb = ra + 8;
+      const uint8_t *KT = sm + OFF_X, *QT = sm + OFF_X + 32768, *KH = sm + OFF_KH;
+      auto at = [&](const uint8_t *base, int row, int c4) {
+        return *reinterpret_cast<const float *>(base + rowf32(row, c4) + 4 * t);
+      };
+      float accA[2][4] = {}, accP[2][4] = {}, accC[2][4] = {}, accD[2][4] = {};
+#pragma unroll 2
+      for (int ks = 0; ks < 16; ++ks) {
+        const int ca = 2 * ks, cb = 2 * ks + 1;  // channels 8ks + t and 8ks + t + 4
+        float ka[4] = {at(KT, ra, ca), at(KT, rb, ca), at(KT, ra, cb), at(KT, rb, cb)};
+        float qa[4] = {at(QT, ra, ca), at(QT, rb, ca), at(QT, ra, cb), at(QT, rb, cb)};
+        if (!diag) {
+          const float d0 = dec[8 * ks + t], d1 = dec[8 * ks + t + 4];
+          ka[0] *= d0, ka[1] *= d0, ka[2] *= d1, ka[3] *= d1;
+          qa[0] *= d0, qa[1] *= d0, qa[2] *= d1, qa[3] *= d1;
+        }
+        uint32_t ak[4], aq[4], aql[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float hi = to_tf32(qa[x]);
+          ak[x] = __float_as_uint(to_tf32(ka[x]));
+          aq[x] = __float_as_uint(hi);
+          aql[x] = __float_as_uint(to_tf32(qa[x] - hi));
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int sr = 16 * Rp + 8 * nt + g;
+          const float b0 = at(KH, sr, ca), b1 = at(KH, sr, cb);
+          const float h0 = to_tf32(b0), h1 = to_tf32(b1);
+          const uint32_t bh[2] = {__float_as_uint(h0), __float_as_uint(h1)};
+          mma1688(accA[nt], ak, bh);
+          mma1688(accP[nt], aq, bh);
+          if (band) {
+            const uint32_t bl[2] = {__float_as_uint(to_tf32(b0 - h0)),
+                                    __float_as_uint(to_tf32(b1 - h1))};
+            mma1688(accC[nt], aq, bl);
+            mma1688(accD[nt], aql, bh);
+          }
+        }
+      }
+      float *Am = reinterpret_cast<float *>(sm + OFF_A);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int r = hf ? rb : ra, s0 = 16 * Rp + 8 * nt + 2 * t;
+          const bool l0 = s0 < r, l1 = s0 + 1 < r;
+          const float br = s_beta[r];
+          *reinterpret_cast<float2 *>(&Am[r * 64 + s0]) =
+              make_float2(l0 ? br * accA[nt][2 * hf] : 0.f, l1 ? br * accA[nt][2 * hf + 1] : 0.f);
+          const float p0 = accP[nt][2 * hf] + (accC[nt][2 * hf] + accD[nt][2 * hf]);
+          const float p1 = accP[nt][2 * hf + 1] + (accC[nt][2 * hf + 1] + accD[nt][2 * hf + 1]);
+          *reinterpret_cast<float2 *>(sm + OFF_P + kmaj_f32<64>(r, s0)) =
+              make_float2(l0 ? to_tf32(p0) : 0.f, l1 ? to_tf32(p1) : 0.f);
+        }
+    }
+    if (!(ok = sync())) break;
+
+    // ---- X = [K Gamma; Q Gamma] (tf32, K-major, 128 rows) from the fp32 rows:
+    //      K Gamma_r = Ktil_r 2^(gam_R0).  Read everything, then overwrite in place. ------------
+    {
+      float xv[6][8];
+#pragma unroll
+      for (int q6 = 0; q6 < 6; ++q6) {
+        const int it = tid + NT * q6;  // (row of [Ktil; Qtil], 8-channel group)
+        if (it < 2 * C * 16) {
+          const int row = it >> 4, c8 = it & 15, r = row & 63;
+          const uint8_t *src = sm + OFF_X + (row >> 6) * 32768;
+          const float4 x0 = *reinterpret_cast<const float4 *>(src + rowf32(r, 2 * c8));
+          const float4 x1 = *reinterpret_cast<const float4 *>(src + rowf32(r, 2 * c8 + 1));
+          const float4 e0 = *reinterpret_cast<const float4 *>(&s_e0[r >> 4][8 * c8]);
+          const float4 e1 = *reinterpret_cast<const float4 *>(&s_e0[r >> 4][8 * c8 + 4]);
+          xv[q6][0] = to_tf32(x0.x * e0.x), xv[q6][1] = to_tf32(x0.y * e0.y);
+          xv[q6][2] = to_tf32(x0.z * e0.z), xv[q6][3] = to_tf32(x0.w * e0.w);
+          xv[q6][4] = to_tf32(x1.x * e1.x), xv[q6][5] = to_tf32(x1.y * e1.y);
+          xv[q6][6] = to_tf32(x1.z * e1.z), xv[q6][7] = to_tf32(x1.w * e1.w);
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int q6 = 0; q6 < 6; ++q6) {
+        const int it = tid + NT * q6;
+        if (it < 2 * C * 16) {
+          const int row = it >> 4, c8 = it & 15;
+          st_f32x8(sm + OFF_X + kmaj_f32<128>(row, 8 * c8),
+                   sm + OFF_X + kmaj_f32<128>(row, 8 * c8 + 4), xv[q6]);
+        }
+      }
     }
     fence_proxy_async();
     if (!(ok = sync())) break;
-    if (tid == 0 && more) issue(1u << BAR_Q, c + 1);  // q is consumed
 
     // ---- MMA1: X^T = S^T [K Gamma; Q Gamma]^T (A = S^T from TMEM) -> TC, in flight while
     //      the block inverse runs --------------------------------------------------------

@@ -9,8 +9,11 @@
 //     o  = scale S^T q = scale (S'^T q + u (k.q))
 // so one pass over S gives both column reductions (S'^T k and S'^T q) and the update.
 //
-// Layout of the work: one CTA per (head, sequence).  The D x D state is spread over the CTA
-// as tiles of RPT rows x 4 columns per thread (float4 along the value dimension, so a warp's
+// Layout of the work: one CTA per (head, sequence) for prefill; for decode a persistent grid
+// (as many CTAs as fit on the device) walks the (sequence, head) units in strides and asks L2
+// for the next unit's state and inputs before it works on the current one, so the state
+// stream stays queued while the CTA computes.  The D x D state is spread over the CTA as
+// tiles of RPT rows x 4 columns per thread (float4 along the value dimension, so a warp's
 // load covers whole 512-byte rows).  Column reductions over rows go through shared memory.
 #include "kda_common.cuh"
 #include "kda_internal.h"
@@ -19,6 +22,15 @@ namespace kda {
 namespace {
 
 constexpr int TT = 8;  // tokens staged per shared-memory fill
+
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+// every 128-byte line of [p, p + bytes), spread over the CTA's threads
+__device__ __forceinline__ void prefetch_span(const void *p, size_t bytes, int tid, int nt) {
+  const char *c = reinterpret_cast<const char *>(p);
+  for (size_t off = (size_t)tid * 128; off < bytes; off += (size_t)nt * 128) prefetch_l2(c + off);
+}
 
 template <int D, int NT, typename IO, typename ST, bool CONV, bool GATE>
 __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
@@ -35,170 +47,214 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
   __shared__ float s_u[D];
   __shared__ float s_ss[NW];
 
-  const int h = blockIdx.x, n = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cg = tid % CG, rg = tid / CG;
   const int H = a.H;
+  const int64_t units = (int64_t)a.n_seqs * H;
+  // prefill: this CTA's (head, sequence) only; decode: units blockIdx.x + k gridDim.x
+  const int64_t first = a.cu_seqlens ? (int64_t)blockIdx.y * H + blockIdx.x : blockIdx.x;
+  const int64_t stride = a.cu_seqlens ? units : gridDim.x;
 
-  int64_t bos, eos;
-  int slot;
-  if (a.cu_seqlens) {
-    bos = a.cu_seqlens[n];
-    eos = a.cu_seqlens[n + 1];
-    slot = n;
-  } else {
-    bos = n;
-    eos = n + 1;
-    slot = a.slot_idx ? a.slot_idx[n] : n;
-  }
-  if (eos < bos) eos = bos;  // a decreasing offset pair processes nothing
-
-  // ---- load this head's state tile into registers --------------------------------------
-  float S[RPT][4];
-  const size_t sbase = ((size_t)slot * H + h) * (size_t)D * D;
-  if (a.state_in) {
-    const ST *src = reinterpret_cast<const ST *>(a.state_in) + sbase;
-#pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-      const float4 x = load4(src + (size_t)(rg * RPT + r) * D + 4 * cg);
-      S[r][0] = x.x, S[r][1] = x.y, S[r][2] = x.z, S[r][3] = x.w;
-    }
-  } else {
-#pragma unroll
-    for (int r = 0; r < RPT; ++r) S[r][0] = S[r][1] = S[r][2] = S[r][3] = 0.f;
-  }
-
-  const IO *q = reinterpret_cast<const IO *>(a.q);
-  const IO *k = reinterpret_cast<const IO *>(a.k);
-  const IO *v = reinterpret_cast<const IO *>(a.v);
-
-  for (int64_t t0 = bos; t0 < eos; t0 += TT) {
-    const int nt = (int)((eos - t0) < TT ? (eos - t0) : TT);
-    __syncthreads();  // staging buffers free
-    if (CONV) {
-      // decode: one token; q, k, v from the width-4 causal convolution of the raw inputs
-      // and the conv tail, then the tail shifts by one (bit-exact copies).
-      const int C = 3 * H * D;
-      const IO *xr = reinterpret_cast<const IO *>(a.x_raw) + (size_t)n * C;
-      const IO *cw = reinterpret_cast<const IO *>(a.conv_w);
-      IO *cs = reinterpret_cast<IO *>(a.conv_state) + (size_t)slot * 3 * C;
-      if (tid < D) {
-#pragma unroll
-        for (int st = 0; st < 3; ++st) {
-          const int ch = st * H * D + h * D + tid;
-          const IO x0 = cs[ch], x1 = cs[C + ch], x2 = cs[2 * C + ch], xn = xr[ch];
-          const float acc = to_f(cw[4 * ch + 0]) * to_f(x0) + to_f(cw[4 * ch + 1]) * to_f(x1) +
-                            to_f(cw[4 * ch + 2]) * to_f(x2) + to_f(cw[4 * ch + 3]) * to_f(xn);
-          const float y = siluf_(acc);
-          if (st == 0) s_q[0][tid] = y;
-          else if (st == 1) s_k[0][tid] = y;
-          else s_v[0][tid] = y;
-          cs[ch] = x1;
-          cs[C + ch] = x2;
-          cs[2 * C + ch] = xn;
+  for (int64_t unit = first; unit < units; unit += stride) {
+    const int h = (int)(unit % H), n = (int)(unit / H);
+    int64_t bos, eos;
+    int slot;
+    if (a.cu_seqlens) {
+      bos = a.cu_seqlens[n];
+      eos = a.cu_seqlens[n + 1];
+      slot = n;
+    } else {
+      bos = n;
+      eos = n + 1;
+      slot = a.slot_idx ? a.slot_idx[n] : n;
+      const int64_t nx = unit + stride;  // this CTA's next unit: state and inputs into L2
+      if (nx < units) {
+        const int hn = (int)(nx % H), nn = (int)(nx / H);
+        const int sn = a.slot_idx ? a.slot_idx[nn] : nn;
+        if (a.state_in)
+          prefetch_span(reinterpret_cast<const ST *>(a.state_in) + ((size_t)sn * H + hn) * D * D,
+                        sizeof(ST) * D * D, tid, NT);
+        if (tid < 3) {
+          const size_t C3 = (size_t)3 * H * D, ch = (size_t)tid * H * D + (size_t)hn * D;
+          if (CONV) {
+            const IO *cs = reinterpret_cast<const IO *>(a.conv_state) + (size_t)sn * 3 * C3 + ch;
+            for (int r = 0; r < 3; ++r) prefetch_span(cs + r * C3, sizeof(IO) * D, 0, 1);
+            prefetch_span(reinterpret_cast<const IO *>(a.x_raw) + (size_t)nn * C3 + ch,
+                          sizeof(IO) * D, 0, 1);
+          }
+          const size_t row = ((size_t)nn * H + hn) * D;
+          if (tid == 0) prefetch_span(a.g + row, sizeof(float) * D, 0, 1);
+          if (tid == 1 && GATE) prefetch_span(reinterpret_cast<const IO *>(a.gate) + row,
+                                              sizeof(IO) * D, 0, 1);
         }
-        const size_t row = ((size_t)t0 * H + h) * D + tid;
-        s_a[0][tid] = expf(fmaxf(a.g[row], a.g_min));
+      }
+    }
+    if (eos < bos) eos = bos;  // a decreasing offset pair processes nothing
+
+    // ---- load this head's state tile into registers --------------------------------------
+    float S[RPT][4];
+    const size_t sbase = ((size_t)slot * H + h) * (size_t)D * D;
+    if (a.state_in) {
+      const ST *src = reinterpret_cast<const ST *>(a.state_in) + sbase;
+  #pragma unroll
+      for (int r = 0; r < RPT; ++r) {
+        const float4 x = load4(src + (size_t)(rg * RPT + r) * D + 4 * cg);
+        S[r][0] = x.x, S[r][1] = x.y, S[r][2] = x.z, S[r][3] = x.w;
       }
     } else {
-      for (int e = tid; e < nt * D; e += NT) {
-        const int tt = e / D, i = e % D;
-        const size_t row = ((size_t)(t0 + tt) * H + h) * D + i;
-        s_q[tt][i] = to_f(q[row]);
-        s_k[tt][i] = to_f(k[row]);
-        s_v[tt][i] = to_f(v[row]);
-        s_a[tt][i] = expf(fmaxf(a.g[row], a.g_min));
-      }
+  #pragma unroll
+      for (int r = 0; r < RPT; ++r) S[r][0] = S[r][1] = S[r][2] = S[r][3] = 0.f;
     }
-    if (tid < nt) s_beta[tid] = a.beta[(size_t)(t0 + tid) * H + h];
-    __syncthreads();
-    // L2 norms of q and k and their dot product, one warp per token
-    for (int tt = warp; tt < nt; tt += NW) {
-      float sq = 0.f, sk = 0.f, skq = 0.f;
-      for (int i = lane; i < D; i += 32) {
-        const float qq = s_q[tt][i], kk = s_k[tt][i];
-        sq += qq * qq, sk += kk * kk, skq += qq * kk;
-      }
-      sq = warp_sum(sq), sk = warp_sum(sk), skq = warp_sum(skq);
-      if (lane == 0) {
-        const float rq = a.qk_l2norm ? rsqrtf(sq + a.l2_eps) : 1.f;
-        const float rk = a.qk_l2norm ? rsqrtf(sk + a.l2_eps) : 1.f;
-        s_rq[tt] = rq, s_rk[tt] = rk, s_kq[tt] = skq * rq * rk;
-      }
-    }
-    __syncthreads();
 
-    for (int tt = 0; tt < nt; ++tt) {
-      const float rq = s_rq[tt], rk = s_rk[tt];
-      float pp[4] = {0.f, 0.f, 0.f, 0.f}, po[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int r = 0; r < RPT; ++r) {
-        const int i = rg * RPT + r;
-        const float al = s_a[tt][i], kk = s_k[tt][i] * rk, qq = s_q[tt][i] * rq;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          S[r][c] *= al;
-          pp[c] = fmaf(S[r][c], kk, pp[c]);
-          po[c] = fmaf(S[r][c], qq, po[c]);
+    const IO *q = reinterpret_cast<const IO *>(a.q);
+    const IO *k = reinterpret_cast<const IO *>(a.k);
+    const IO *v = reinterpret_cast<const IO *>(a.v);
+
+    for (int64_t t0 = bos; t0 < eos; t0 += TT) {
+      const int nt = (int)((eos - t0) < TT ? (eos - t0) : TT);
+      __syncthreads();  // staging buffers free
+      if (CONV) {
+        // decode: one token; q, k, v from the width-4 causal convolution of the raw inputs
+        // and the conv tail, then the tail shifts by one (bit-exact copies).
+        const int C = 3 * H * D;
+        const IO *xr = reinterpret_cast<const IO *>(a.x_raw) + (size_t)n * C;
+        const IO *cw = reinterpret_cast<const IO *>(a.conv_w);
+        IO *cs = reinterpret_cast<IO *>(a.conv_state) + (size_t)slot * 3 * C;
+        if (tid < D) {
+  #pragma unroll
+          for (int st = 0; st < 3; ++st) {
+            const int ch = st * H * D + h * D + tid;
+            const IO x0 = cs[ch], x1 = cs[C + ch], x2 = cs[2 * C + ch], xn = xr[ch];
+            const float acc = to_f(cw[4 * ch + 0]) * to_f(x0) + to_f(cw[4 * ch + 1]) * to_f(x1) +
+                              to_f(cw[4 * ch + 2]) * to_f(x2) + to_f(cw[4 * ch + 3]) * to_f(xn);
+            const float y = siluf_(acc);
+            if (st == 0) s_q[0][tid] = y;
+            else if (st == 1) s_k[0][tid] = y;
+            else s_v[0][tid] = y;
+            cs[ch] = x1;
+            cs[C + ch] = x2;
+            cs[2 * C + ch] = xn;
+          }
+          const size_t row = ((size_t)t0 * H + h) * D + tid;
+          s_a[0][tid] = expf(fmaxf(a.g[row], a.g_min));
+        }
+      } else {
+        for (int e = tid; e < nt * D; e += NT) {
+          const int tt = e / D, i = e % D;
+          const size_t row = ((size_t)(t0 + tt) * H + h) * D + i;
+          s_q[tt][i] = to_f(q[row]);
+          s_k[tt][i] = to_f(k[row]);
+          s_v[tt][i] = to_f(v[row]);
+          s_a[tt][i] = expf(fmaxf(a.g[row], a.g_min));
         }
       }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) s_redp[rg][4 * cg + c] = pp[c], s_redo[rg][4 * cg + c] = po[c];
+      if (tid < nt) s_beta[tid] = a.beta[(size_t)(t0 + tid) * H + h];
       __syncthreads();
-      float o = 0.f;
-      if (tid < D) {
-        float p = 0.f, o1 = 0.f;
-#pragma unroll
-        for (int g2 = 0; g2 < RG; ++g2) p += s_redp[g2][tid], o1 += s_redo[g2][tid];
-        const float u = s_beta[tt] * (s_v[tt][tid] - p);
-        s_u[tid] = u;
-        o = a.scale * fmaf(u, s_kq[tt], o1);
-      }
-      if (GATE && warp < (D + 31) / 32) {
-        const float ss = warp_sum(tid < D ? o * o : 0.f);
-        if (lane == 0) s_ss[warp] = ss;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int r = 0; r < RPT; ++r) {
-        const float kk = s_k[tt][rg * RPT + r] * rk;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) S[r][c] = fmaf(kk, s_u[4 * cg + c], S[r][c]);
-      }
-      if (tid < D) {
-        const size_t row = ((size_t)(t0 + tt) * H + h) * D + tid;
-        if (GATE) {
-          float ss = 0.f;
-#pragma unroll
-          for (int w = 0; w < (D + 31) / 32; ++w) ss += s_ss[w];
-          const float r = rsqrtf(ss / D + a.norm_eps);
-          const float w = a.norm_w ? a.norm_w[tid] : 1.f;
-          const float z = to_f(reinterpret_cast<const IO *>(a.gate)[row]);
-          o = o * r * w * sigmoidf_(z);
+      // L2 norms of q and k and their dot product, one warp per token
+      for (int tt = warp; tt < nt; tt += NW) {
+        float sq = 0.f, sk = 0.f, skq = 0.f;
+        for (int i = lane; i < D; i += 32) {
+          const float qq = s_q[tt][i], kk = s_k[tt][i];
+          sq += qq * qq, sk += kk * kk, skq += qq * kk;
         }
-        reinterpret_cast<IO *>(a.out)[row] = from_f<IO>(o);
+        sq = warp_sum(sq), sk = warp_sum(sk), skq = warp_sum(skq);
+        if (lane == 0) {
+          const float rq = a.qk_l2norm ? rsqrtf(sq + a.l2_eps) : 1.f;
+          const float rk = a.qk_l2norm ? rsqrtf(sk + a.l2_eps) : 1.f;
+          s_rq[tt] = rq, s_rk[tt] = rk, s_kq[tt] = skq * rq * rk;
+        }
+      }
+      __syncthreads();
+
+      for (int tt = 0; tt < nt; ++tt) {
+        const float rq = s_rq[tt], rk = s_rk[tt];
+        float pp[4] = {0.f, 0.f, 0.f, 0.f}, po[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+          const int i = rg * RPT + r;
+          const float al = s_a[tt][i], kk = s_k[tt][i] * rk, qq = s_q[tt][i] * rq;
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            S[r][c] *= al;
+            pp[c] = fmaf(S[r][c], kk, pp[c]);
+            po[c] = fmaf(S[r][c], qq, po[c]);
+          }
+        }
+  #pragma unroll
+        for (int c = 0; c < 4; ++c) s_redp[rg][4 * cg + c] = pp[c], s_redo[rg][4 * cg + c] = po[c];
+        __syncthreads();
+        float o = 0.f;
+        if (tid < D) {
+          float p = 0.f, o1 = 0.f;
+  #pragma unroll
+          for (int g2 = 0; g2 < RG; ++g2) p += s_redp[g2][tid], o1 += s_redo[g2][tid];
+          const float u = s_beta[tt] * (s_v[tt][tid] - p);
+          s_u[tid] = u;
+          o = a.scale * fmaf(u, s_kq[tt], o1);
+        }
+        if (GATE && warp < (D + 31) / 32) {
+          const float ss = warp_sum(tid < D ? o * o : 0.f);
+          if (lane == 0) s_ss[warp] = ss;
+        }
+        __syncthreads();
+  #pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+          const float kk = s_k[tt][rg * RPT + r] * rk;
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) S[r][c] = fmaf(kk, s_u[4 * cg + c], S[r][c]);
+        }
+        if (tid < D) {
+          const size_t row = ((size_t)(t0 + tt) * H + h) * D + tid;
+          if (GATE) {
+            float ss = 0.f;
+  #pragma unroll
+            for (int w = 0; w < (D + 31) / 32; ++w) ss += s_ss[w];
+            const float r = rsqrtf(ss / D + a.norm_eps);
+            const float w = a.norm_w ? a.norm_w[tid] : 1.f;
+            const float z = to_f(reinterpret_cast<const IO *>(a.gate)[row]);
+            o = o * r * w * sigmoidf_(z);
+          }
+          reinterpret_cast<IO *>(a.out)[row] = from_f<IO>(o);
+        }
       }
     }
-  }
 
-  if (a.state_out) {
-    ST *dst = reinterpret_cast<ST *>(a.state_out) + sbase;
-#pragma unroll
-    for (int r = 0; r < RPT; ++r)
-      store4(dst + (size_t)(rg * RPT + r) * D + 4 * cg,
-             make_float4(S[r][0], S[r][1], S[r][2], S[r][3]));
+    if (a.state_out) {
+      ST *dst = reinterpret_cast<ST *>(a.state_out) + sbase;
+  #pragma unroll
+      for (int r = 0; r < RPT; ++r)
+        store4(dst + (size_t)(rg * RPT + r) * D + 4 * cg,
+               make_float4(S[r][0], S[r][1], S[r][2], S[r][3]));
+    }
+  }  // units
+}
+
+// prefill: grid (H, N); decode: a persistent grid of the CTAs that fit at once, capped by the
+// number of (sequence, head) units
+template <typename K>
+cudaError_t launch_grid(K kernel, int nt, const RecArgs &a, cudaStream_t s) {
+  dim3 grid(a.H, a.n_seqs);
+  if (!a.cu_seqlens) {
+    int dev = 0, nsm = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, nt, 0);
+    if (e != cudaSuccess) return e;
+    const int64_t units = (int64_t)a.n_seqs * a.H;
+    const int64_t fit = (int64_t)nsm * (per_sm > 0 ? per_sm : 1);
+    grid = dim3((unsigned)(units < fit ? units : fit), 1);
   }
+  kernel<<<grid, nt, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 template <int D, int NT, typename IO, typename ST>
 cudaError_t launch_typed(const RecArgs &a, cudaStream_t s) {
-  const dim3 grid(a.H, a.n_seqs);
   const bool conv = a.x_raw != nullptr, gate = a.gate != nullptr;
-  if (conv && gate) recurrent_kernel<D, NT, IO, ST, true, true><<<grid, NT, 0, s>>>(a);
-  else if (conv) recurrent_kernel<D, NT, IO, ST, true, false><<<grid, NT, 0, s>>>(a);
-  else if (gate) recurrent_kernel<D, NT, IO, ST, false, true><<<grid, NT, 0, s>>>(a);
-  else recurrent_kernel<D, NT, IO, ST, false, false><<<grid, NT, 0, s>>>(a);
-  return cudaGetLastError();
+  if (conv && gate) return launch_grid(recurrent_kernel<D, NT, IO, ST, true, true>, NT, a, s);
+  if (conv) return launch_grid(recurrent_kernel<D, NT, IO, ST, true, false>, NT, a, s);
+  if (gate) return launch_grid(recurrent_kernel<D, NT, IO, ST, false, true>, NT, a, s);
+  return launch_grid(recurrent_kernel<D, NT, IO, ST, false, false>, NT, a, s);
 }
 
 template <int D, int NT>
