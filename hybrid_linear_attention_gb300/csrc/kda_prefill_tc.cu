@@ -24,10 +24,10 @@
 // order.  The fp32 state lives in tensor memory, transposed (lane = value channel j,
 // column = key channel i), and is fed to the tensor core directly as the A operand.
 //   TMEM columns   [0,128) S^T   [128,256) TA   [256,384) TB   [384,512) TC
-// A and P (64 x 64 each, K = 128) are formed per 16x16 block pair on the warp-level tensor
-// core (mma.sync m16n8k8 tf32), one warp per block pair: A in tf32, P in 3xtf32 (hi*hi +
-// hi*lo + lo*hi) on the diagonal blocks and the block before them, where q_r.k_s can nearly
-// cancel with little decay, and tf32 further back.
+// A and P (64 x 64 each, K = 128) come from one product on the tensor core:
+// [Ktil; Qtil] (128 rows, bf16 hi + lo in tensor memory) times the stacked Khat^(R) rows
+// (160, bf16 in shared memory), hi*hi everywhere and hi*lo + lo*hi on the band (a 16-token
+// block and the one before it), where q_r.k_s can nearly cancel with little decay.
 // MMA precision elsewhere: tf32 (operands rounded to nearest; beta(V - KGS) split into tf32
 // hi + lo); the state update S += Kbar^T u as three bf16 products
 // (hi*hi + hi*lo + lo*hi), which keeps the state at fp32-level accuracy.  Inputs arrive by
@@ -52,15 +52,21 @@ constexpr uint32_t OFF_Q = 0;        // q bf16 [64][128], two 128B-swizzled boxe
 constexpr uint32_t OFF_K = 16384;    // k
 constexpr uint32_t OFF_V = 32768;    // v
 constexpr uint32_t OFF_G = 49152;    // g -> cumulative log2-retention, fp32, 4 boxes of 32
-constexpr uint32_t OFF_X = 81920;    // 64 KB: fp32 rows Ktil | Qtil -> [K Gamma; Q Gamma] ->
-                                     //        Kbar hi | Kbar lo | u hi | u lo
-constexpr uint32_t OFF_KH = 147456;  // 32 KB: fp32 rows Khat -> T fp32 (plain) -> T tf32
-constexpr uint32_t OFF_T = OFF_KH;
-constexpr uint32_t OFF_P = 180224;   // 16 KB: P' tf32 (K-major)
-constexpr uint32_t OFF_A = 196608;   // 16 KB: A fp32 (plain)
-constexpr uint32_t SMEM_BYTES = 212992 + 1024;
+constexpr uint32_t OFF_X = 81920;    // 64 KB: [K Gamma; Q Gamma] tf32 -> Kbar hi | Kbar lo |
+                                     //        u hi | u lo
+constexpr uint32_t OFF_T = 147456;   // 16 KB: T fp32 (plain) -> T tf32 (K-major)
+constexpr uint32_t OFF_P = 163840;   // 16 KB: P' tf32 (K-major)
+constexpr uint32_t OFF_A = 180224;   // 17 KB: A fp32, rows of LDA floats
+constexpr int LDA = 68;              // A row stride: rows 16 bytes apart in the bank map
+// B operand of the A/P product (bf16, K-major), live until that product completes, over
+// T, P' and A: Khat^(R) rows, 48 far then 112 band (hi), and the band rows' lo parts
+constexpr uint32_t OFF_BH = 147456;  // 160 rows x 128 channels x 2 B = 40 KB
+constexpr uint32_t OFF_BL = 188416;  // 112 rows: 28 KB
+constexpr uint32_t SMEM_BYTES = 217088 + 1024;
 
 constexpr uint32_t TM_S = 0, TM_A = 128, TM_B = 256, TM_C = 384, TM_COLS = 512;
+// during the A/P product: [Ktil; Qtil] bf16 hi and lo (64 columns each), result 160 columns
+constexpr uint32_t TM_AH = 128, TM_AL = 192, TM_D = 256;
 
 enum { BAR_Q = 0, BAR_K, BAR_V, BAR_G, BAR_MMA, NBAR };
 
@@ -71,10 +77,21 @@ __device__ __forceinline__ uint32_t kmaj_f32(int row, int ch) {
   return (uint32_t)(ch >> 5) * (NR * 128u) + (uint32_t)row * 128u +
          ((((b >> 4) ^ (row & 7))) << 4) + (b & 15u);
 }
-// fp32 row of 128 channels (512 bytes), 16-byte chunk c4 XOR-swizzled by the row within each
-// 128-byte group, so eight consecutive rows (or eight chunks of one row) hit distinct banks
-__device__ __forceinline__ uint32_t rowf32(int row, int c4) {
-  return (uint32_t)row * 512u + ((uint32_t)((c4 & ~7) | ((c4 & 7) ^ (row & 7))) << 4);
+// K-major 128B-swizzled bf16 operand with NR rows and 128 channels: two panels of 64
+template <int NR>
+__device__ __forceinline__ uint32_t kmaj_bf16(int row, int ch) {
+  const uint32_t b = (uint32_t)((ch & 63) * 2);
+  return (uint32_t)(ch >> 6) * (NR * 128u) + (uint32_t)row * 128u +
+         ((((b >> 4) ^ (row & 7))) << 4) + (b & 15u);
+}
+// row of Khat^(R)_s in the B operand: far rows first (R = 2: s < 16; R = 3: s < 32), then
+// the band (R = 0: s < 16 at 48; R = 1: s < 32 at 64; R = 2: s in [16, 48) at 96; R = 3:
+// s in [32, 64) at 128)
+__device__ __forceinline__ int brow(int R, int s) {
+  if (R == 0) return 48 + s;
+  if (R == 1) return 64 + s;
+  if (R == 2) return s < 16 ? s : 80 + s;
+  return s < 32 ? 16 + s : 96 + s;
 }
 // K-major bf16 operand [rows][64]: a single 128-byte panel
 __device__ __forceinline__ uint32_t kmaj_bf16_64(int row, int k) {
@@ -119,8 +136,9 @@ __device__ __forceinline__ float bf_at(const uint8_t *tile, int row, int ch) {
 }
 // two fp32 -> packed bf16 pair (round to nearest even), low half = first
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
-  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
-         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+  uint32_t d;  // one conversion for the pair: the first source lands in the upper half
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(b), "f"(a));
+  return d;
 }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -135,16 +153,6 @@ __device__ __forceinline__ void st_f32x8(uint8_t *p0, uint8_t *p1, const float (
   *reinterpret_cast<float4 *>(p1) = make_float4(o[4], o[5], o[6], o[7]);
 }
 
-// d(16x8) += a(16x8) b(8x8) on the warp-level tensor core, tf32 operands (pre-rounded),
-// fp32 accumulate; fragments as in warp_mma16 below
-__device__ __forceinline__ void mma1688(float (&d)[4], const uint32_t (&a)[4],
-                                        const uint32_t (&b)[2]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
 // D(16x16) += A(16 x 8kk) B(8kk x 16) for row-major fp32 blocks in shared memory (row
 // strides la, lb), on the warp-level tensor-core MMA (m16n8k8, tf32 inputs, fp32
 // accumulate).  Accumulator fragment: d[nt][0..3] = rows g, g, g+8, g+8 and columns
@@ -196,7 +204,7 @@ __global__ void __launch_bounds__(NT, 1)
   __shared__ __align__(16) float s_gC[D];     // log2-retention at the chunk's last token
   __shared__ float s_GC[D];                   // Gamma_C
   __shared__ float s_red[4][C];
-  __shared__ __align__(16) float s_M[3 * 256];  // inverse scratch; block decays in P2/P3
+  __shared__ __align__(16) float s_M[3 * 256];  // inverse scratch; block decays P1 -> P2
   __shared__ __align__(16) float s_e0[4][D];      // 2^(gam_R0) per block and channel
   __shared__ __align__(8) uint64_t s_bar[NBAR];
   __shared__ uint32_t s_tmem, s_abort, s_pend, s_ppar[NBAR];
@@ -294,9 +302,6 @@ __global__ void __launch_bounds__(NT, 1)
     }
     tmem_wait_st();
   }
-  // P' blocks above the diagonal stay zero for the whole walk
-  for (int e = tid; e < C * C / 4; e += NT)
-    reinterpret_cast<float4 *>(sm + OFF_P)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (tid == 0 && nchunks > 0)
     issue((1u << BAR_Q) | (1u << BAR_K) | (1u << BAR_V) | (1u << BAR_G), 0);
   bool ok = sync();
@@ -304,6 +309,8 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t ID_64 = idesc(2, 128, 64, 0, 0);
   const uint32_t ID_128 = idesc(2, 128, 128, 0, 0);
   const uint32_t ID_UPD = idesc(1, 128, 128, 0, 1);
+  const uint32_t ID_AP160 = idesc(1, 128, 160, 0, 0);
+  const uint32_t ID_AP112 = idesc(1, 128, 112, 0, 0);
   uint32_t mma_par = 0;
   float beta_next = 0.f;  // beta of the next chunk, loaded one chunk ahead (threads 0..63)
   if (tid < C && tid < eos - bos) beta_next = a.beta[(size_t)(bos + tid) * H + h];
@@ -374,156 +381,193 @@ __global__ void __launch_bounds__(NT, 1)
         s_gC[i] = v[31];
         s_GC[i] = ex2(v[31]);
       }
+      asm volatile("bar.sync 2, 256;" ::: "memory");
+      // per channel: decay between block starts 2^(gam_R0 - gam_R'0) for the pairs (1,0)
+      // (2,1) (3,2) (2,0) (3,1) (3,0), and 2^(gam_R0)
+      for (int e = t; e < 10 * D; e += 256) {
+        const int pr = e >> 7, ch = e & 127;
+        if (pr < 6) {
+          const int R = pr < 3 ? pr + 1 : (pr == 3 ? 2 : 3);
+          const int Rp = pr < 3 ? pr : (pr == 4 ? 1 : 0);
+          s_M[pr * D + ch] = ex2(s_g0[R][ch] - s_g0[Rp][ch]);
+        } else {
+          s_e0[pr - 6][ch] = ex2(s_g0[pr - 6][ch]);
+        }
+      }
     }
     if (!(ok = sync())) break;
 
-    // ---- P2: fp32 rows, each relative to its own 16-token block R = r/16 (gam_R0 = the
-    //      log2-retention just before the block; q, k L2-normalised):
-    //        Ktil_r = k_r 2^(gam_r - gam_R0),  Qtil_r = q_r 2^(gam_r - gam_R0)   (<= 1)
-    //        Khat_r = k_r 2^(gam_R0 - gam_r)                                     (<= 2^115)
-    //      and per channel the decay between block starts, 2^(gam_R0 - gam_R'0) for R' < R,
-    //      and 2^(gam_R0) (for [K Gamma; Q Gamma] later). -----------------------------------
-    for (int it = tid; it < C * 16; it += NT) {
-      const int r = it >> 4, c8 = it & 15, R = r >> 4;
-      float kt[8], qt[8], kh[8];
-      if (r < nv) {
-        float kv[8], qv[8], gg[8];
-        bf_row8(sm + OFF_K, r, c8, kv);
-        bf_row8(sm + OFF_Q, r, c8, qv);
-        f_row8(sm + OFF_G, r, c8, gg);
-        const float4 r0 = *reinterpret_cast<const float4 *>(&s_g0[R][8 * c8]);
-        const float4 r1 = *reinterpret_cast<const float4 *>(&s_g0[R][8 * c8 + 4]);
+    // ---- P2: operands of A and P, and X = [K Gamma; Q Gamma].  Rows relative to their own
+    //      16-token block R = r/16 (gam_R0 = the log2-retention just before the block; q, k
+    //      L2-normalised): Ktil_r = k_r 2^(gam_r - gam_R0), Qtil_r = q_r 2^(gam_r - gam_R0)
+    //      (<= 1) form the tensor-memory A operand (lanes 0-63 and 64-127) as bf16 hi + lo,
+    //      built with X_r = Ktil_r 2^(gam_R0) (tf32, K-major) from the same values; then the
+    //      B operand, columns Khat^(R)_s = k_s 2^(gam_R0 - gam_s) for s <= 16R + 15, from
+    //      Khat^(R(s))_s times the decay between block starts: bf16 hi for all 160 rows, lo
+    //      for the 112 band rows.  All three warp groups share both. -----------------------
+    {  // tensor-memory A operand and X: lane j's row, 16-channel pieces 3 grp .. (3, 3, 2)
+      const int L = j, r = L & 63, R = r >> 4;
+      const bool isq = L >= 64, live = r < nv;
+      const uint8_t *src = sm + (isq ? OFF_Q : OFF_K);
+      const float rn = isq ? s_rq[r] : s_rk[r];
+      const int pend = grp == 2 ? 8 : 3 * grp + 3;
+#pragma unroll 1
+      for (int pc = 3 * grp; pc < pend; ++pc) {
+        float hw[8], lw[8];  // packed bf16 pairs, low half = even channel
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int c8 = 2 * pc + c2, ch = 8 * c8;
+          float x[8];
+          if (live) {
+            float vv[8], gg[8];
+            bf_row8(src, r, c8, vv);
+            f_row8(sm + OFF_G, r, c8, gg);
+            const float4 r0 = *reinterpret_cast<const float4 *>(&s_g0[R][ch]);
+            const float4 r1 = *reinterpret_cast<const float4 *>(&s_g0[R][ch + 4]);
+            const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+            for (int y = 0; y < 8; ++y) x[y] = vv[y] * rn * ex2(gg[y] - rr[y]);
+          } else {
+#pragma unroll
+            for (int y = 0; y < 8; ++y) x[y] = 0.f;
+          }
+          const float4 e0 = *reinterpret_cast<const float4 *>(&s_e0[R][ch]);
+          const float4 e1 = *reinterpret_cast<const float4 *>(&s_e0[R][ch + 4]);
+          const float xg[8] = {to_tf32(x[0] * e0.x), to_tf32(x[1] * e0.y), to_tf32(x[2] * e0.z),
+                               to_tf32(x[3] * e0.w), to_tf32(x[4] * e1.x), to_tf32(x[5] * e1.y),
+                               to_tf32(x[6] * e1.z), to_tf32(x[7] * e1.w)};
+          st_f32x8(sm + OFF_X + kmaj_f32<128>(L, ch), sm + OFF_X + kmaj_f32<128>(L, ch + 4), xg);
+#pragma unroll
+          for (int y = 0; y < 4; ++y) {
+            const uint32_t hv = pack_bf2(x[2 * y], x[2 * y + 1]);
+            hw[4 * c2 + y] = __uint_as_float(hv);
+            lw[4 * c2 + y] =
+                __uint_as_float(pack_bf2(x[2 * y] - bf_lo(hv), x[2 * y + 1] - bf_hi(hv)));
+          }
+        }
+        tmem_st8(tm + lane_off + TM_AH + 8 * pc, hw);
+        tmem_st8(tm + lane_off + TM_AL + 8 * pc, lw);
+      }
+      tmem_wait_st();
+    }
+    for (int it = tid; it < C * 16; it += NT) {  // B operand: (token s, 8-channel group)
+      const int sr = it >> 4, c8 = it & 15, Rs = sr >> 4;
+      float kh[8];
+      if (sr < nv) {
+        float kv[8], gg[8];
+        bf_row8(sm + OFF_K, sr, c8, kv);
+        f_row8(sm + OFF_G, sr, c8, gg);
+        const float4 r0 = *reinterpret_cast<const float4 *>(&s_g0[Rs][8 * c8]);
+        const float4 r1 = *reinterpret_cast<const float4 *>(&s_g0[Rs][8 * c8 + 4]);
         const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-        const float rk = s_rk[r], rq = s_rq[r];
+        const float rk = s_rk[sr];
 #pragma unroll
-        for (int y = 0; y < 8; ++y) {
-          const float dg = gg[y] - rr[y];
-          const float e = ex2(dg), eh = ex2(-dg);
-          kt[y] = kv[y] * rk * e;
-          qt[y] = qv[y] * rq * e;
-          kh[y] = kv[y] * rk * eh;
+        for (int y = 0; y < 8; ++y) kh[y] = kv[y] * rk * ex2(rr[y] - gg[y]);
+      } else {
+#pragma unroll
+        for (int y = 0; y < 8; ++y) kh[y] = 0.f;
+      }
+#pragma unroll
+      for (int R = 0; R < 4; ++R) {
+        if (R < Rs) continue;
+        float val[8];
+        if (R == Rs) {
+#pragma unroll
+          for (int y = 0; y < 8; ++y) val[y] = kh[y];
+        } else {
+          const int pr = R - Rs == 1 ? Rs : (R - Rs == 2 ? 3 + Rs : 5);
+          const float4 d0 = *reinterpret_cast<const float4 *>(&s_M[pr * D + 8 * c8]);
+          const float4 d1 = *reinterpret_cast<const float4 *>(&s_M[pr * D + 8 * c8 + 4]);
+          val[0] = kh[0] * d0.x, val[1] = kh[1] * d0.y, val[2] = kh[2] * d0.z;
+          val[3] = kh[3] * d0.w, val[4] = kh[4] * d1.x, val[5] = kh[5] * d1.y;
+          val[6] = kh[6] * d1.z, val[7] = kh[7] * d1.w;
         }
-      } else {
+        uint32_t hv[4], lv[4];
 #pragma unroll
-        for (int y = 0; y < 8; ++y) kt[y] = qt[y] = kh[y] = 0.f;
-      }
-      st_f32x8(sm + OFF_X + rowf32(r, 2 * c8), sm + OFF_X + rowf32(r, 2 * c8 + 1), kt);
-      st_f32x8(sm + OFF_X + 32768 + rowf32(r, 2 * c8), sm + OFF_X + 32768 + rowf32(r, 2 * c8 + 1),
-               qt);
-      st_f32x8(sm + OFF_KH + rowf32(r, 2 * c8), sm + OFF_KH + rowf32(r, 2 * c8 + 1), kh);
-    }
-    for (int e = tid; e < 10 * D; e += NT) {
-      const int pr = e >> 7, i = e & 127;
-      if (pr < 6) {  // block pairs (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
-        const int R = pr < 3 ? pr + 1 : (pr == 3 ? 2 : 3);
-        const int Rp = pr < 3 ? pr : (pr == 4 ? 1 : 0);
-        s_M[pr * D + i] = ex2(s_g0[R][i] - s_g0[Rp][i]);
-      } else {
-        s_e0[pr - 6][i] = ex2(s_g0[pr - 6][i]);
+        for (int y = 0; y < 4; ++y) {
+          hv[y] = pack_bf2(val[2 * y], val[2 * y + 1]);
+          lv[y] = pack_bf2(val[2 * y] - bf_lo(hv[y]), val[2 * y + 1] - bf_hi(hv[y]));
+        }
+        const int n = brow(R, sr);
+        *reinterpret_cast<uint4 *>(sm + OFF_BH + kmaj_bf16<160>(n, 8 * c8)) =
+            make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        if (R - Rs <= 1)
+          *reinterpret_cast<uint4 *>(sm + OFF_BL + kmaj_bf16<112>(n - 48, 8 * c8)) =
+              make_uint4(lv[0], lv[1], lv[2], lv[3]);
       }
     }
+    fence_proxy_async();
     if (!(ok = sync())) break;
-    if (tid == 0 && more) issue(1u << BAR_Q, c + 1);  // q is consumed
+    // D = [Ktil; Qtil] Khat^T: hi*hi over all 160 columns, hi*lo and lo*hi over the band
+    if (tid == 0) {
+      if (more) issue(1u << BAR_Q, c + 1);  // q is consumed
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t ko = (uint32_t)(ks >> 2) * (160 * 128) + (ks & 3) * 32;
+        mma_bf16_ts(tm + TM_D, tm + TM_AH + 8 * ks, sdesc_sw128(sb + OFF_BH + ko, 16, 1024),
+                    ID_AP160, ks > 0);
+      }
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t ko = (uint32_t)(ks >> 2) * (112 * 128) + (ks & 3) * 32;
+        mma_bf16_ts(tm + TM_D + 48, tm + TM_AH + 8 * ks, sdesc_sw128(sb + OFF_BL + ko, 16, 1024),
+                    ID_AP112, 1);
+      }
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t ko = (uint32_t)(ks >> 2) * (160 * 128) + 48 * 128 + (ks & 3) * 32;
+        mma_bf16_ts(tm + TM_D + 48, tm + TM_AL + 8 * ks, sdesc_sw128(sb + OFF_BH + ko, 16, 1024),
+                    ID_AP112, 1);
+      }
+      commit(mma_par);
+    }
+    wait(BAR_MMA, mma_par);
+    mma_par ^= 1;
+    tc_fence_after();
 
-    // ---- P3: A and P' on the warp-level tensor core, one warp per 16x16 block (R, R'),
-    //      R' <= R: warps 0-3 the diagonal blocks, 4-6 the block before, 7-9 two and three
-    //      blocks back.  Row operand Ktil_r (Qtil_r), scaled by the decay 2^(gam_R0 - gam_R'0)
-    //      off the diagonal; column operand Khat_s relative to its own block R'.  Results:
-    //      A = beta_r (.) (strict lower, fp32, plain [r][s]); P' (strict lower, tf32,
-    //      K-major). ------------------------------------------------------------------------
-    if (warp < 10) {
-      const int R = warp < 4 ? warp : warp < 7 ? warp - 3 : (warp == 7 ? 2 : 3);
-      const int Rp = warp < 4 ? warp : warp < 7 ? warp - 4 : (warp == 8 ? 1 : 0);
-      const bool diag = warp < 4, band = warp < 7;
-      const float *dec = s_M + (diag ? 0 : (warp - 4) * D);  // read off the diagonal only
-      const int g = lane >> 2, t = lane & 3;
-      const int ra = 16 * R + g, rb = ra + 8;
-      const uint8_t *KT = sm + OFF_X, *QT = sm + OFF_X + 32768, *KH = sm + OFF_KH;
-      auto at = [&](const uint8_t *base, int row, int c4) {
-        return *reinterpret_cast<const float *>(base + rowf32(row, c4) + 4 * t);
-      };
-      float accA[2][4] = {}, accP[2][4] = {}, accC[2][4] = {}, accD[2][4] = {};
-#pragma unroll 2
-      for (int ks = 0; ks < 16; ++ks) {
-        const int ca = 2 * ks, cb = 2 * ks + 1;  // channels 8ks + t and 8ks + t + 4
-        float ka[4] = {at(KT, ra, ca), at(KT, rb, ca), at(KT, ra, cb), at(KT, rb, cb)};
-        float qa[4] = {at(QT, ra, ca), at(QT, rb, ca), at(QT, ra, cb), at(QT, rb, cb)};
-        if (!diag) {
-          const float d0 = dec[8 * ks + t], d1 = dec[8 * ks + t + 4];
-          ka[0] *= d0, ka[1] *= d0, ka[2] *= d1, ka[3] *= d1;
-          qa[0] *= d0, qa[1] *= d0, qa[2] *= d1, qa[3] *= d1;
-        }
-        uint32_t ak[4], aq[4], aql[4];
+    // ---- P3: A (beta-scaled, strict lower, fp32 rows of LDA) and P' (strict lower, tf32,
+    //      K-major) from the product, one tensor-memory lane per row (lanes 0-63: A, 64-127:
+    //      P), in 16-column pieces that each hold one block R and 16 consecutive s; zeros in
+    //      the blocks of P' above the diagonal. ----------------------------------------------
+    {
+      const int L = j, r = L & 63, R = r >> 4;
+      const bool isp = L >= 64;
+      // pieces of this warp: rows 0-31 (R = 0, 1): piece 3 + grp; rows 32-63 (R = 2, 3):
+      // group 0 pieces 0-2, group 1 pieces 6-7, group 2 pieces 8-9
+      const bool lo_rows = (quarter & 1) == 0;
+      const int p0 = lo_rows ? 3 + grp : (grp == 0 ? 0 : 4 + 2 * grp);
+      const int np = lo_rows ? 1 : (grp == 0 ? 3 : 2);
+      float *Am = reinterpret_cast<float *>(sm + OFF_A);
+      const float br = s_beta[r];
+      for (int pc = p0; pc < p0 + np; ++pc) {
+        float v[16];
+        tmem_ld16(tm + lane_off + TM_D + 16 * pc, v);
+        tmem_wait_ld();
+        // piece -> (block, first s)
+        const int Rn = pc == 0 ? 2 : pc <= 2 ? 3 : pc == 3 ? 0 : pc <= 5 ? 1 : pc <= 7 ? 2 : 3;
+        const int s0 = pc == 0 ? 0 : pc == 1 ? 0 : pc == 2 ? 16 : pc == 3 ? 0 : pc == 4 ? 0
+                     : pc == 5 ? 16 : pc == 6 ? 16 : pc == 7 ? 32 : pc == 8 ? 32 : 48;
+        if (Rn != R) continue;
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const float hi = to_tf32(qa[x]);
-          ak[x] = __float_as_uint(to_tf32(ka[x]));
-          aq[x] = __float_as_uint(hi);
-          aql[x] = __float_as_uint(to_tf32(qa[x] - hi));
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int sr = 16 * Rp + 8 * nt + g;
-          const float b0 = at(KH, sr, ca), b1 = at(KH, sr, cb);
-          const float h0 = to_tf32(b0), h1 = to_tf32(b1);
-          const uint32_t bh[2] = {__float_as_uint(h0), __float_as_uint(h1)};
-          mma1688(accA[nt], ak, bh);
-          mma1688(accP[nt], aq, bh);
-          if (band) {
-            const uint32_t bl[2] = {__float_as_uint(to_tf32(b0 - h0)),
-                                    __float_as_uint(to_tf32(b1 - h1))};
-            mma1688(accC[nt], aq, bl);
-            mma1688(accD[nt], aql, bh);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int s = s0 + 4 * q4;
+          if (!isp) {
+            *reinterpret_cast<float4 *>(&Am[r * LDA + s]) =
+                make_float4(s < r ? br * v[4 * q4] : 0.f, s + 1 < r ? br * v[4 * q4 + 1] : 0.f,
+                            s + 2 < r ? br * v[4 * q4 + 2] : 0.f,
+                            s + 3 < r ? br * v[4 * q4 + 3] : 0.f);
+          } else {
+            *reinterpret_cast<float4 *>(sm + OFF_P + kmaj_f32<64>(r, s)) =
+                make_float4(s < r ? to_tf32(v[4 * q4]) : 0.f,
+                            s + 1 < r ? to_tf32(v[4 * q4 + 1]) : 0.f,
+                            s + 2 < r ? to_tf32(v[4 * q4 + 2]) : 0.f,
+                            s + 3 < r ? to_tf32(v[4 * q4 + 3]) : 0.f);
           }
         }
       }
-      float *Am = reinterpret_cast<float *>(sm + OFF_A);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int r = hf ? rb : ra, s0 = 16 * Rp + 8 * nt + 2 * t;
-          const bool l0 = s0 < r, l1 = s0 + 1 < r;
-          const float br = s_beta[r];
-          *reinterpret_cast<float2 *>(&Am[r * 64 + s0]) =
-              make_float2(l0 ? br * accA[nt][2 * hf] : 0.f, l1 ? br * accA[nt][2 * hf + 1] : 0.f);
-          const float p0 = accP[nt][2 * hf] + (accC[nt][2 * hf] + accD[nt][2 * hf]);
-          const float p1 = accP[nt][2 * hf + 1] + (accC[nt][2 * hf + 1] + accD[nt][2 * hf + 1]);
-          *reinterpret_cast<float2 *>(sm + OFF_P + kmaj_f32<64>(r, s0)) =
-              make_float2(l0 ? to_tf32(p0) : 0.f, l1 ? to_tf32(p1) : 0.f);
-        }
-    }
-    if (!(ok = sync())) break;
-
-    // ---- X = [K Gamma; Q Gamma] (tf32, K-major, 128 rows) from the fp32 rows:
-    //      K Gamma_r = Ktil_r 2^(gam_R0).  Read everything, then overwrite in place. ------------
-    {
-      float xv[6][8];
-#pragma unroll
-      for (int q6 = 0; q6 < 6; ++q6) {
-        const int it = tid + NT * q6;  // (row of [Ktil; Qtil], 8-channel group)
-        if (it < 2 * C * 16) {
-          const int row = it >> 4, c8 = it & 15, r = row & 63;
-          const uint8_t *src = sm + OFF_X + (row >> 6) * 32768;
-          const float4 x0 = *reinterpret_cast<const float4 *>(src + rowf32(r, 2 * c8));
-          const float4 x1 = *reinterpret_cast<const float4 *>(src + rowf32(r, 2 * c8 + 1));
-          const float4 e0 = *reinterpret_cast<const float4 *>(&s_e0[r >> 4][8 * c8]);
-          const float4 e1 = *reinterpret_cast<const float4 *>(&s_e0[r >> 4][8 * c8 + 4]);
-          xv[q6][0] = to_tf32(x0.x * e0.x), xv[q6][1] = to_tf32(x0.y * e0.y);
-          xv[q6][2] = to_tf32(x0.z * e0.z), xv[q6][3] = to_tf32(x0.w * e0.w);
-          xv[q6][4] = to_tf32(x1.x * e1.x), xv[q6][5] = to_tf32(x1.y * e1.y);
-          xv[q6][6] = to_tf32(x1.z * e1.z), xv[q6][7] = to_tf32(x1.w * e1.w);
-        }
-      }
-      __syncthreads();
-#pragma unroll
-      for (int q6 = 0; q6 < 6; ++q6) {
-        const int it = tid + NT * q6;
-        if (it < 2 * C * 16) {
-          const int row = it >> 4, c8 = it & 15;
-          st_f32x8(sm + OFF_X + kmaj_f32<128>(row, 8 * c8),
-                   sm + OFF_X + kmaj_f32<128>(row, 8 * c8 + 4), xv[q6]);
-        }
+      {  // P' blocks (R, R') with R' > R: pairs (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+        const int pr = tid >> 6, rr16 = (tid >> 2) & 15, c4 = tid & 3;
+        const int Rz = pr < 3 ? 0 : pr < 5 ? 1 : 2;
+        const int Rpz = pr < 3 ? pr + 1 : pr < 5 ? pr - 1 : 3;
+        *reinterpret_cast<float4 *>(sm + OFF_P + kmaj_f32<64>(16 * Rz + rr16, 16 * Rpz + 4 * c4)) =
+            make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
     fence_proxy_async();
@@ -556,7 +600,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int k = 0; k < 16; ++k) {
           x[k] = k < cc ? 0.f : (k == cc ? 1.f : -pacc[k]);
 #pragma unroll
-          for (int i = k + 1; i < 16; ++i) pacc[i] = fmaf(Am[(b0 + i) * 64 + b0 + k], x[k], pacc[i]);
+          for (int i = k + 1; i < 16; ++i) pacc[i] = fmaf(Am[(b0 + i) * LDA + b0 + k], x[k], pacc[i]);
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) Tm[(b0 + i) * 64 + b0 + cc] = x[i];
@@ -569,8 +613,8 @@ __global__ void __launch_bounds__(NT, 1)
           const int R = dist + wg, S = R - dist;
           float dacc[2][4] = {};
           for (int Q = S; Q < R; ++Q)
-            warp_mma16(dacc, Am + (16 * R) * 64 + 16 * Q, 64, Tm + (16 * Q) * 64 + 16 * S, 64, 2,
-                       lane);
+            warp_mma16(dacc, Am + (16 * R) * LDA + 16 * Q, LDA, Tm + (16 * Q) * 64 + 16 * S, 64,
+                       2, lane);
           warp_store16(s_M + wg * 256, 16, dacc, lane, 1.f);
           __syncwarp();
           float tacc[2][4] = {};
