@@ -8,8 +8,8 @@
 //
 // Kernels:
 //   prologue_kernel     packed prefill: conv + SiLU (+ per-head L2 of q, k) for a tile of
-//                       tokens x one (stream, head) group of d channels; also the gate
-//                       activations beta = sigmoid(logit), g = max(g_raw, g_min).
+//                       tokens x (stream, head) rows, 16-byte vectors, one read per input.
+//   gate_act_kernel     the gate activations beta = sigmoid(logit), g = max(g_raw, g_min).
 //   conv_tail_kernel    afterwards, the new tail of every sequence (separate launch, so the
 //                       in-place update never races with the reads of the old tail).
 //   conv_update_kernel  decode: one new token per sequence, tail shifted in place.
@@ -19,105 +19,159 @@
 namespace kda {
 namespace {
 
-constexpr int PT = 16;  // tokens per prologue tile
+constexpr int TT = 64;    // tokens per prologue tile
+constexpr int PNT = 256;  // threads per prologue CTA
+constexpr int UNR = 4;    // tokens loaded ahead
 
+// eight consecutive channels as fp32 (16-byte bf16 vector, or two fp32 vectors)
+__device__ __forceinline__ void load8(const bf16 *p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4 *>(p);
+  v[0] = __uint_as_float(u.x << 16), v[1] = __uint_as_float(u.x & 0xffff0000u);
+  v[2] = __uint_as_float(u.y << 16), v[3] = __uint_as_float(u.y & 0xffff0000u);
+  v[4] = __uint_as_float(u.z << 16), v[5] = __uint_as_float(u.z & 0xffff0000u);
+  v[6] = __uint_as_float(u.w << 16), v[7] = __uint_as_float(u.w & 0xffff0000u);
+}
+__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4 *>(p);
+  const float4 b = *reinterpret_cast<const float4 *>(p + 4);
+  v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+}
+// x * sigmoid(x) with the special-function unit's 2^x and reciprocal (relative error ~1e-7)
+__device__ __forceinline__ float silu_fast(float x) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-1.4426950408889634f * x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return x * r;
+}
+__device__ __forceinline__ uint32_t bf2(float a, float b) {
+  uint32_t d;  // round to nearest even; the first source lands in the upper half
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(b), "f"(a));
+  return d;
+}
+__device__ __forceinline__ void store8(bf16 *p, const float (&v)[8]) {
+  *reinterpret_cast<uint4 *>(p) =
+      make_uint4(bf2(v[0], v[1]), bf2(v[2], v[3]), bf2(v[4], v[5]), bf2(v[6], v[7]));
+}
+__device__ __forceinline__ void store8(float *p, const float (&v)[8]) {
+  *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4 *>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// One CTA: a tile of TT tokens x PNT/(D/8) rows of D channels (a row = one head of one of the
+// q, k, v streams); D/8 threads per row, eight channels each.  Every thread walks the tile's
+// tokens in order with the last three raw inputs of its channels in registers (each input
+// is read once); at a sequence start inside the tile the window restarts from that
+// sequence's conv tail (zeros without one).  The per-token L2 norm of q and k is a shuffle
+// reduction over the row's D/8 lanes.
 template <int D, typename IO>
-__global__ void __launch_bounds__(D / 2 < 32 ? 32 : D / 2)
-    prologue_kernel(const ProArgs a) {
-  constexpr int NT = D / 2 < 32 ? 32 : D / 2;
-  constexpr int NW = NT / 32;
-  __shared__ int64_t s_bos[PT];
-  __shared__ int s_seq[PT];
-  __shared__ float s_ss[NW][PT];
-  __shared__ float s_r[PT];
-
+__global__ void __launch_bounds__(PNT, 2) prologue_kernel(const ProArgs a) {
+  constexpr int TPH = D / 8;
+  constexpr int NU = PNT / TPH;
   const int H = a.H, C = 3 * H * D;
-  const int grp = blockIdx.y;                   // stream * H + head
-  const int stream = grp / H, h = grp % H;
-  const int64_t t0 = (int64_t)blockIdx.x * PT;
-  const int nt = (int)((a.T - t0) < PT ? (a.T - t0) : PT);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int c0 = stream * H * D + h * D + 2 * tid;  // this thread's first channel
-  const bool act = 2 * tid < D;
-
-  if (tid < nt) {
-    const int n = seq_of_token(a.cu_seqlens, a.n_seqs, t0 + tid);
-    s_seq[tid] = n;
-    s_bos[tid] = a.cu_seqlens[n];
-  }
-  __syncthreads();
-
+  const int tid = threadIdx.x, sub = tid % TPH;
+  const int u = blockIdx.y * NU + tid / TPH;  // stream * H + head
+  const bool act = u < 3 * H;
+  const int stream = act ? u / H : 0, h = act ? u % H : 0;
+  const int64_t c0 = (int64_t)stream * H * D + (int64_t)h * D + 8 * sub;
+  const int64_t t0 = (int64_t)blockIdx.x * TT;
+  const int64_t t1 = (t0 + TT) < a.T ? (t0 + TT) : a.T;
   const IO *x = reinterpret_cast<const IO *>(a.x);
   const IO *cs = reinterpret_cast<const IO *>(a.conv_state);
-  float w[2][4];
-  if (act) {
-    const IO *cw = reinterpret_cast<const IO *>(a.conv_w);
-#pragma unroll
-    for (int e = 0; e < 2; ++e)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) w[e][j] = to_f(cw[4 * (c0 + e) + j]);
-  }
-
-  float y[PT][2];
-#pragma unroll
-  for (int tt = 0; tt < PT; ++tt) {
-    y[tt][0] = y[tt][1] = 0.f;
-    if (tt < nt && act) {
-      const int64_t t = t0 + tt, bos = s_bos[tt];
-      float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int64_t src = t - 3 + j;
-        float2 xv = make_float2(0.f, 0.f);
-        if (src >= bos) xv = load2(x + src * C + c0);
-        else if (cs) xv = load2(cs + ((int64_t)s_seq[tt] * 3 + 3 + (src - bos)) * C + c0);
-        acc0 = fmaf(w[0][j], xv.x, acc0);
-        acc1 = fmaf(w[1][j], xv.y, acc1);
-      }
-      y[tt][0] = siluf_(acc0);
-      y[tt][1] = siluf_(acc1);
-    }
-  }
-
-  if (a.l2norm_qk && stream < 2) {  // per-token L2 over the head's D channels
-#pragma unroll
-    for (int tt = 0; tt < PT; ++tt) {
-      const float ss = warp_sum(y[tt][0] * y[tt][0] + y[tt][1] * y[tt][1]);
-      if (lane == 0) s_ss[warp][tt] = ss;
-    }
-    __syncthreads();
-    if (tid < PT) {
-      float ss = 0.f;
-#pragma unroll
-      for (int w2 = 0; w2 < NW; ++w2) ss += s_ss[w2][tid];
-      s_r[tid] = rsqrtf(ss + a.l2_eps);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int tt = 0; tt < PT; ++tt) y[tt][0] *= s_r[tt], y[tt][1] *= s_r[tt];
-  }
-
   IO *dst = reinterpret_cast<IO *>(stream == 0 ? a.q : stream == 1 ? a.k : a.v);
-  if (act) {
+  const bool norm = a.l2norm_qk && stream < 2;
+
+  float w[8][4];
+  {
+    const IO *cw = reinterpret_cast<const IO *>(a.conv_w) + 4 * c0;
+    float t8[8];
 #pragma unroll
-    for (int tt = 0; tt < PT; ++tt)
-      if (tt < nt) store2(dst + ((t0 + tt) * H + h) * D + 2 * tid, make_float2(y[tt][0], y[tt][1]));
+    for (int q = 0; q < 4; ++q) {  // 32 consecutive weights: channel e, tap j at 4e + j
+      if (act) load8(cw + 8 * q, t8);
+      else
+#pragma unroll
+        for (int y = 0; y < 8; ++y) t8[y] = 0.f;
+#pragma unroll
+      for (int y = 0; y < 8; ++y) w[(8 * q + y) >> 2][y & 3] = t8[y];
+    }
+  }
+  int n = seq_of_token(a.cu_seqlens, a.n_seqs, t0);
+  int64_t bos = a.cu_seqlens[n], eos = a.cu_seqlens[n + 1];
+  float win[3][8];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const int64_t src = t0 - 3 + k;
+    if (act && src >= bos) load8(x + src * C + c0, win[k]);
+    else if (act && cs) load8(cs + ((int64_t)n * 3 + 3 + (src - bos)) * C + c0, win[k]);
+    else
+#pragma unroll
+      for (int y = 0; y < 8; ++y) win[k][y] = 0.f;
   }
 
-  if (stream == 0) {  // gate activations for this head's tokens
-    if (a.g_raw && act) {
-#pragma unroll 4
-      for (int tt = 0; tt < nt; ++tt) {
-        const size_t row = ((size_t)(t0 + tt) * H + h) * D + 2 * tid;
-        const float2 gr = load2(a.g_raw + row);
-        store2(a.g + row, make_float2(fmaxf(gr.x, a.g_min), fmaxf(gr.y, a.g_min)));
-      }
+  for (int64_t tb = t0; tb < t1; tb += UNR) {
+    float xv[UNR][8];
+#pragma unroll
+    for (int i = 0; i < UNR; ++i) {
+      if (act && tb + i < t1) load8(x + (tb + i) * C + c0, xv[i]);
+      else
+#pragma unroll
+        for (int y = 0; y < 8; ++y) xv[i][y] = 0.f;
     }
-    if (a.beta_logit && tid < nt) {
-      const size_t i = (size_t)(t0 + tid) * H + h;
-      a.beta[i] = sigmoidf_(a.beta_logit[i]);
+#pragma unroll
+    for (int i = 0; i < UNR; ++i) {
+      const int64_t t = tb + i;
+      if (t >= t1) break;
+      if (t == eos) {  // next non-empty sequence starts here: its conv tail is the history
+        do {
+          ++n;
+          bos = a.cu_seqlens[n];
+          eos = a.cu_seqlens[n + 1];
+        } while (eos <= t);
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          if (act && cs) load8(cs + ((int64_t)n * 3 + k) * C + c0, win[k]);
+          else
+#pragma unroll
+            for (int y = 0; y < 8; ++y) win[k][y] = 0.f;
+        }
+      }
+      float yv[8], ss = 0.f;
+#pragma unroll
+      for (int y = 0; y < 8; ++y) {
+        float acc = w[y][0] * win[0][y];
+        acc = fmaf(w[y][1], win[1][y], acc);
+        acc = fmaf(w[y][2], win[2][y], acc);
+        acc = fmaf(w[y][3], xv[i][y], acc);
+        yv[y] = silu_fast(acc);
+        ss = fmaf(yv[y], yv[y], ss);
+        win[0][y] = win[1][y], win[1][y] = win[2][y], win[2][y] = xv[i][y];
+      }
+#pragma unroll
+      for (int off = TPH / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      if (norm) {
+        const float r = rsqrtf(ss + a.l2_eps);
+#pragma unroll
+        for (int y = 0; y < 8; ++y) yv[y] *= r;
+      }
+      if (act) store8(dst + (t * H + h) * D + 8 * sub, yv);
     }
   }
+}
+
+// Gate activations, elementwise: g = max(g_raw, g_min) (four at a time), beta = sigmoid.
+template <int D>
+__global__ void gate_act_kernel(const ProArgs a) {
+  const int64_t n4 = a.T * a.H * (int64_t)D / 4, nb = a.T * a.H;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n4; e += stride) {
+    if (a.g_raw) {
+      const float4 v = reinterpret_cast<const float4 *>(a.g_raw)[e];
+      reinterpret_cast<float4 *>(a.g)[e] = make_float4(fmaxf(v.x, a.g_min), fmaxf(v.y, a.g_min),
+                                                       fmaxf(v.z, a.g_min), fmaxf(v.w, a.g_min));
+    }
+    if (a.beta_logit && e < nb) a.beta[e] = sigmoidf_(a.beta_logit[e]);
+  }
+  for (int64_t e = n4 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nb; e += stride)
+    if (a.beta_logit) a.beta[e] = sigmoidf_(a.beta_logit[e]);
 }
 
 // New tail of sequence n: the last three raw inputs, reaching into the old tail when the
@@ -161,12 +215,24 @@ __global__ void conv_update_kernel(const ConvArgs a) {
 
 template <int D, typename IO>
 cudaError_t launch_pro(const ProArgs &a, cudaStream_t s) {
-  constexpr int NT = D / 2 < 32 ? 32 : D / 2;
   if (a.T > 0) {
-    const dim3 grid((unsigned)((a.T + PT - 1) / PT), 3 * a.H);
-    prologue_kernel<D, IO><<<grid, NT, 0, s>>>(a);
+    constexpr int NU = PNT / (D / 8);
+    const dim3 grid((unsigned)((a.T + TT - 1) / TT), (unsigned)((3 * a.H + NU - 1) / NU));
+    prologue_kernel<D, IO><<<grid, PNT, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (a.g_raw || a.beta_logit) {
+      int dev = 0, nsm = 0;
+      e = cudaGetDevice(&dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      const int64_t work = a.T * a.H * (int64_t)D / 4;
+      const int64_t blocks = (work + 255) / 256;
+      const int64_t cap = (int64_t)nsm * 8;
+      gate_act_kernel<D><<<(unsigned)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap), 256, 0, s>>>(a);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
   }
   if (a.conv_state && a.n_seqs > 0) {
     const int C = 3 * a.H * D;
