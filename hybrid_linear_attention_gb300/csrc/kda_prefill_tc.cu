@@ -192,7 +192,7 @@ __device__ __forceinline__ void warp_store16(float *D, int ld, const float (&d)[
 }
 
 struct Maps {
-  CUtensorMap q, k, v, g;
+  CUtensorMap q, k, v, g, out;
 };
 
 template <typename ST, bool GATE>
@@ -395,6 +395,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
     }
+    if (tid == 0) bulk_wait_read0();  // the previous chunk's output tile has left X
     if (!(ok = sync())) break;
 
     // ---- P2: operands of A and P, and X = [K Gamma; Q Gamma].  Rows relative to their own
@@ -758,15 +759,21 @@ __global__ void __launch_bounds__(NT, 1)
     mma_par ^= 1;
     tc_fence_after();
 
-    // ---- P8: outputs o_r = scale (O'_r + (q_r.k_r) u_r), norm and gate, store ------------
+    // ---- P8: outputs o_r = scale (O'_r + (q_r.k_r) u_r), norm and gate, store.  A full
+    //      chunk goes out as one bulk tensor store of the [64 tokens][128] bf16 tile, staged
+    //      in the X region (free once the update has read it); a partial last chunk, whose
+    //      box would run into the next sequence, is stored element by element. ---------------
     if (grp < 2) {
-      float o[32], u[32];
-      tmem_ld32(tm + lane_off + TM_C + 64 + 32 * grp, o);
-      tmem_ld32(tm + lane_off + TM_A + 32 * grp, u);
-      tmem_wait_ld();
-#pragma unroll
-      for (int x = 0; x < 32; ++x) o[x] = a.scale * fmaf(s_pd[32 * grp + x], u[x], o[x]);
+      const bool tile = nv == C;
+      bf16 *stage = reinterpret_cast<bf16 *>(sm + OFF_X);
+      bf16 *out = reinterpret_cast<bf16 *>(a.out);
       if (GATE) {
+        float o[32], u[32];
+        tmem_ld32(tm + lane_off + TM_C + 64 + 32 * grp, o);
+        tmem_ld32(tm + lane_off + TM_A + 32 * grp, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) o[x] = a.scale * fmaf(s_pd[32 * grp + x], u[x], o[x]);
         float sq[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) sq[x] = o[x] * o[x];
@@ -782,28 +789,59 @@ __global__ void __launch_bounds__(NT, 1)
           }
         }
         s_red[quarter][32 * grp + lane] = sq[0];
-      }
-      // named barrier over the 256 threads of groups 0 and 1
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      const float w = GATE ? (a.norm_w ? a.norm_w[j] : 1.f) : 1.f;
-      bf16 *out = reinterpret_cast<bf16 *>(a.out);
-      const bf16 *gate = reinterpret_cast<const bf16 *>(a.gate);
+        // named barrier over the 256 threads of groups 0 and 1
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        const float w = a.norm_w ? a.norm_w[j] : 1.f;
+        const bf16 *gate = reinterpret_cast<const bf16 *>(a.gate);
 #pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        const int r = 32 * grp + x;
-        if (r < nv) {
-          const size_t row = ((size_t)(t0 + r) * H + h) * D + j;
-          float val = o[x];
-          if (GATE) {
+        for (int x = 0; x < 32; ++x) {
+          const int r = 32 * grp + x;
+          if (r < nv) {
+            const size_t row = ((size_t)(t0 + r) * H + h) * D + j;
             const float ss = s_red[0][r] + s_red[1][r] + s_red[2][r] + s_red[3][r];
-            val = val * rsqrtf(ss * (1.f / D) + a.norm_eps) * w * sigmoidf_(__bfloat162float(gate[row]));
+            const float val = o[x] * rsqrtf(ss * (1.f / D) + a.norm_eps) * w *
+                              sigmoidf_(__bfloat162float(gate[row]));
+            if (tile) stage[r * D + j] = __float2bfloat16_rn(val);
+            else out[row] = __float2bfloat16_rn(val);
           }
-          out[row] = __float2bfloat16_rn(val);
+        }
+      } else {
+#pragma unroll 1
+        for (int sl = 0; sl < 4; ++sl) {  // 8 rows at a time: a short loop body
+          float o8[8], u8[8];
+          tmem_ld8(tm + lane_off + TM_C + 64 + 32 * grp + 8 * sl, o8);
+          tmem_ld8(tm + lane_off + TM_A + 32 * grp + 8 * sl, u8);
+          tmem_wait_ld();
+#pragma unroll
+          for (int y = 0; y < 8; y += 2) {  // two rows per packed conversion
+            const int r = 32 * grp + 8 * sl + y;
+            const uint32_t pr = pack_bf2(a.scale * fmaf(s_pd[r], u8[y], o8[y]),
+                                         a.scale * fmaf(s_pd[r + 1], u8[y + 1], o8[y + 1]));
+            const uint16_t v0 = (uint16_t)(pr & 0xffffu), v1 = (uint16_t)(pr >> 16);
+            if (tile) {
+              reinterpret_cast<uint16_t *>(stage)[r * D + j] = v0;
+              reinterpret_cast<uint16_t *>(stage)[(r + 1) * D + j] = v1;
+            } else {
+              uint16_t *o16 = reinterpret_cast<uint16_t *>(out);
+              if (r < nv) o16[((size_t)(t0 + r) * H + h) * D + j] = v0;
+              if (r + 1 < nv) o16[((size_t)(t0 + r + 1) * H + h) * D + j] = v1;
+            }
+          }
+        }
+      }
+      if (tile) {
+        fence_proxy_async();
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (tid == 0) {
+          tma_store_3d(&maps.out, 0, h, (int)t0, sb + OFF_X);
+          bulk_commit();
         }
       }
     }
     if (!(ok = sync())) break;
   }
+
+  if (tid == 0) bulk_wait0();  // output tiles written before the shared memory is released
 
   // ---- final state: S[i][j] = S^T[j][i] ------------------------------------------------
   if (ok && a.final_state && grp < 2) {
@@ -859,6 +897,19 @@ bool make_map(CUtensorMap *m, const void *ptr, bool f32, int64_t T, int H) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// output [T, H, 128] bf16: plain (unswizzled) boxes of 64 tokens x 128 channels
+bool make_out_map(CUtensorMap *m, void *ptr, int64_t T, int H) {
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)C};
+  cuuint32_t es[3] = {1, 1, 1};
+  auto fn = encode_fn();
+  if (!fn) return false;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename ST, bool GATE>
 cudaError_t launch_typed(const TcArgs &a, const Maps &maps, cudaStream_t s) {
   static bool attr_set[64] = {false};
@@ -895,7 +946,8 @@ cudaError_t launch_prefill_tc(const TcArgs &a, int64_t total_tokens, bool st_bf1
     if (!make_map(&maps.q, a.q, false, total_tokens, a.H) ||
         !make_map(&maps.k, a.k, false, total_tokens, a.H) ||
         !make_map(&maps.v, a.v, false, total_tokens, a.H) ||
-        !make_map(&maps.g, a.g, true, total_tokens, a.H))
+        !make_map(&maps.g, a.g, true, total_tokens, a.H) ||
+        !make_out_map(&maps.out, a.out, total_tokens, a.H))
       return cudaErrorInvalidValue;
   }
   const bool gate = a.gate != nullptr;
