@@ -199,7 +199,7 @@ template <typename ST, bool GATE>
 __global__ void __launch_bounds__(NT, 1)
     prefill_tc_kernel(const TcArgs a, const __grid_constant__ Maps maps) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ float s_beta[C], s_rq[C], s_rk[C], s_pd[C];
+  __shared__ float s_beta[C], s_rq[C], s_rk[C], s_pd[2][C];  // s_pd by chunk parity
   __shared__ __align__(16) float s_g0[4][D];  // log2-retention just before each 16-block
   __shared__ __align__(16) float s_gC[D];     // log2-retention at the chunk's last token
   __shared__ float s_GC[D];                   // Gamma_C
@@ -265,19 +265,19 @@ __global__ void __launch_bounds__(NT, 1)
     }
     for (int b = 0; b < NBAR; ++b)
       if (mask & (1u << b)) s_ppar[b] = (uint32_t)(c & 1);
-    s_pend |= mask;
+    atomicOr(&s_pend, mask);
   };
   auto commit = [&](uint32_t parity) {
     mma_commit(bar(BAR_MMA));
     s_ppar[BAR_MMA] = parity;
-    s_pend |= 1u << BAR_MMA;
+    atomicOr(&s_pend, 1u << BAR_MMA);
   };
   auto wait = [&](int b, uint32_t parity) {
     if (!mbar_wait(bar(b), parity)) {
       s_abort = 1;
       if (a.err) atomicOr(a.err, ERR_MBAR_TIMEOUT);
-    } else if (tid == 0) {
-      s_pend &= ~(1u << b);
+    } else if (tid == 0 || tid == 256) {
+      atomicAnd(&s_pend, ~(1u << b));
     }
   };
   auto sync = [&]() {
@@ -306,36 +306,25 @@ __global__ void __launch_bounds__(NT, 1)
     issue((1u << BAR_Q) | (1u << BAR_K) | (1u << BAR_V) | (1u << BAR_G), 0);
   bool ok = sync();
 
-  const uint32_t ID_64 = idesc(2, 128, 64, 0, 0);
-  const uint32_t ID_128 = idesc(2, 128, 128, 0, 0);
-  const uint32_t ID_UPD = idesc(1, 128, 128, 0, 1);
-  const uint32_t ID_AP160 = idesc(1, 128, 160, 0, 0);
-  const uint32_t ID_AP112 = idesc(1, 128, 112, 0, 0);
-  uint32_t mma_par = 0;
-  float beta_next = 0.f;  // beta of the next chunk, loaded one chunk ahead (threads 0..63)
-  if (tid < C && tid < eos - bos) beta_next = a.beta[(size_t)(bos + tid) * H + h];
-
-  for (int c = 0; c < nchunks && ok; ++c) {
-    const int64_t t0 = bos + (int64_t)c * C;
-    const int nv = (int)((eos - t0) < C ? (eos - t0) : C);
-    const uint32_t par = (uint32_t)(c & 1);
-    const bool more = c + 1 < nchunks;
-
-    if (tid < C) {
-      s_beta[tid] = tid < nv ? beta_next : 0.f;
-      const int64_t tn = t0 + C + tid;
-      beta_next = (more && tn < eos) ? a.beta[(size_t)tn * H + h] : 0.f;
-    }
-    wait(BAR_Q, par);
-    wait(BAR_K, par);
-    wait(BAR_G, par);
-
-    // ---- P1: row norms and q.k (threads 0..127, two per row); log2-retention prefix sums
-    //      per channel (threads 128..255) --------------------------------------------------
-    if (tid < 128) {
-      const int r = tid >> 1, hf = tid & 1;
+  // ---- P1 of chunk cc, by warp group 2 (128 threads): beta; row norms and q.k (two threads
+  //      per row); per channel (one thread each) the prefix sums of the clamped
+  //      log2-retention, written back over g, with its value before each 16-token block,
+  //      at the chunk end and Gamma_C; and per channel the decay between block starts
+  //      2^(gam_R0 - gam_R'0) for the pairs (1,0) (2,1) (3,2) (2,0) (3,1) (3,0), and 2^(gam_R0).
+  //      It runs before the walk for chunk 0 and during the output phase of chunk cc - 1.
+  auto p1 = [&](int cc) {
+    const int t = tid - 256;
+    const int64_t tc = bos + (int64_t)cc * C;
+    const int nvc = (int)((eos - tc) < C ? (eos - tc) : C);
+    const uint32_t pc = (uint32_t)(cc & 1);
+    if (t < C) s_beta[t] = t < nvc ? a.beta[(size_t)(tc + t) * H + h] : 0.f;
+    wait(BAR_Q, pc);
+    wait(BAR_K, pc);
+    wait(BAR_G, pc);
+    {
+      const int r = t >> 1, hf = t & 1;
       float sq = 0.f, sk = 0.f, sqk = 0.f;
-      if (r < nv) {
+      if (r < nvc) {
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
           float qv[8], kv[8];
@@ -350,52 +339,62 @@ __global__ void __launch_bounds__(NT, 1)
       sk += __shfl_xor_sync(0xffffffffu, sk, 1);
       sqk += __shfl_xor_sync(0xffffffffu, sqk, 1);
       if (hf == 0) {
-        const float rq = r < nv ? (a.qk_l2norm ? rsqrtf(sq + a.l2_eps) : 1.f) : 0.f;
-        const float rk = r < nv ? (a.qk_l2norm ? rsqrtf(sk + a.l2_eps) : 1.f) : 0.f;
-        s_rq[r] = rq, s_rk[r] = rk, s_pd[r] = sqk * rq * rk;
-      }
-    } else {
-      // prefix sums of the clamped log2-retention per channel: two threads per channel
-      // (rows 0..31 and 32..63), the upper half offset by the lower half's total
-      const int t = tid - 128, i = t & 127, hf = t >> 7, r0 = 32 * hf;
-      float v[32];
-#pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        const int r = r0 + x;
-        const float gv = *reinterpret_cast<const float *>(sm + OFF_G + swz<4>(r, i));
-        v[x] = r < nv ? fmaxf(gv, a.g_min) * LOG2E : 0.f;
-      }
-#pragma unroll
-      for (int x = 1; x < 32; ++x) v[x] += v[x - 1];
-      if (hf == 0) s_M[i] = v[31];
-      asm volatile("bar.sync 2, 256;" ::: "memory");
-      const float base = hf ? s_M[i] : 0.f;
-#pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        v[x] += base;
-        *reinterpret_cast<float *>(sm + OFF_G + swz<4>(r0 + x, i)) = v[x];
-      }
-      s_g0[2 * hf][i] = base;
-      s_g0[2 * hf + 1][i] = v[15];
-      if (hf) {
-        s_gC[i] = v[31];
-        s_GC[i] = ex2(v[31]);
-      }
-      asm volatile("bar.sync 2, 256;" ::: "memory");
-      // per channel: decay between block starts 2^(gam_R0 - gam_R'0) for the pairs (1,0)
-      // (2,1) (3,2) (2,0) (3,1) (3,0), and 2^(gam_R0)
-      for (int e = t; e < 10 * D; e += 256) {
-        const int pr = e >> 7, ch = e & 127;
-        if (pr < 6) {
-          const int R = pr < 3 ? pr + 1 : (pr == 3 ? 2 : 3);
-          const int Rp = pr < 3 ? pr : (pr == 4 ? 1 : 0);
-          s_M[pr * D + ch] = ex2(s_g0[R][ch] - s_g0[Rp][ch]);
-        } else {
-          s_e0[pr - 6][ch] = ex2(s_g0[pr - 6][ch]);
-        }
+        const float rq = r < nvc ? (a.qk_l2norm ? rsqrtf(sq + a.l2_eps) : 1.f) : 0.f;
+        const float rk = r < nvc ? (a.qk_l2norm ? rsqrtf(sk + a.l2_eps) : 1.f) : 0.f;
+        s_rq[r] = rq, s_rk[r] = rk, s_pd[pc][r] = sqk * rq * rk;
       }
     }
-    if (tid == 0) bulk_wait_read0();  // the previous chunk's output tile has left X
+    {
+      const int i = t;
+      float run = 0.f;
+#pragma unroll 1
+      for (int blk = 0; blk < 4; ++blk) {  // 16 rows at a time, running sum carried over
+        s_g0[blk][i] = run;
+        float v[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const int r = 16 * blk + x;
+          const float gv = *reinterpret_cast<const float *>(sm + OFF_G + swz<4>(r, i));
+          v[x] = r < nvc ? fmaxf(gv, a.g_min) * LOG2E : 0.f;
+        }
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          run += v[x];
+          *reinterpret_cast<float *>(sm + OFF_G + swz<4>(16 * blk + x, i)) = run;
+        }
+      }
+      float g0[4];
+#pragma unroll
+      for (int R = 0; R < 4; ++R) {
+        g0[R] = s_g0[R][i];
+        s_e0[R][i] = ex2(g0[R]);
+      }
+      s_gC[i] = run;
+      s_GC[i] = ex2(run);
+      s_M[0 * D + i] = ex2(g0[1] - g0[0]);
+      s_M[1 * D + i] = ex2(g0[2] - g0[1]);
+      s_M[2 * D + i] = ex2(g0[3] - g0[2]);
+      s_M[3 * D + i] = ex2(g0[2] - g0[0]);
+      s_M[4 * D + i] = ex2(g0[3] - g0[1]);
+      s_M[5 * D + i] = ex2(g0[3] - g0[0]);
+    }
+  };
+
+  const uint32_t ID_64 = idesc(2, 128, 64, 0, 0);
+  const uint32_t ID_128 = idesc(2, 128, 128, 0, 0);
+  const uint32_t ID_UPD = idesc(1, 128, 128, 0, 1);
+  const uint32_t ID_AP160 = idesc(1, 128, 160, 0, 0);
+  const uint32_t ID_AP112 = idesc(1, 128, 112, 0, 0);
+  uint32_t mma_par = 0;
+  if (ok && nchunks > 0 && grp == 2) p1(0);
+  ok = sync();
+
+  for (int c = 0; c < nchunks && ok; ++c) {
+    const int64_t t0 = bos + (int64_t)c * C;
+    const int nv = (int)((eos - t0) < C ? (eos - t0) : C);
+    const uint32_t par = (uint32_t)(c & 1);
+    const bool more = c + 1 < nchunks;
+
     if (!(ok = sync())) break;
 
     // ---- P2: operands of A and P, and X = [K Gamma; Q Gamma].  Rows relative to their own
@@ -502,6 +501,10 @@ __global__ void __launch_bounds__(NT, 1)
     // D = [Ktil; Qtil] Khat^T: hi*hi over all 160 columns, hi*lo and lo*hi over the band
     if (tid == 0) {
       if (more) issue(1u << BAR_Q, c + 1);  // q is consumed
+      if (c > 0) {  // V is free once the previous output tile has been read out of it
+        bulk_wait_read0();
+        issue(1u << BAR_V, c);
+      }
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t ko = (uint32_t)(ks >> 2) * (160 * 128) + (ks & 3) * 32;
         mma_bf16_ts(tm + TM_D, tm + TM_AH + 8 * ks, sdesc_sw128(sb + OFF_BH + ko, 16, 1024),
@@ -704,7 +707,7 @@ __global__ void __launch_bounds__(NT, 1)
         mma_tf32_ts(tm + TM_B, tm + TM_A + 64 * (ks >> 3) + 8 * k8, bd, ID_64, ks > 0);
       }
       commit(mma_par);
-      if (more) issue((1u << BAR_K) | (1u << BAR_V) | (1u << BAR_G), c + 1);
+      if (more) issue((1u << BAR_K) | (1u << BAR_G), c + 1);
     }
     wait(BAR_MMA, mma_par);  // u ready
     mma_par ^= 1;
@@ -761,11 +764,12 @@ __global__ void __launch_bounds__(NT, 1)
 
     // ---- P8: outputs o_r = scale (O'_r + (q_r.k_r) u_r), norm and gate, store.  A full
     //      chunk goes out as one bulk tensor store of the [64 tokens][128] bf16 tile, staged
-    //      in the X region (free once the update has read it); a partial last chunk, whose
-    //      box would run into the next sequence, is stored element by element. ---------------
+    //      in the V region (free since the Y pass; the next V load waits for the store to
+    //      have read it); a partial last chunk, whose box would run into the next sequence,
+    //      is stored element by element.  Meanwhile warp group 2 runs P1 of the next chunk. ----
     if (grp < 2) {
       const bool tile = nv == C;
-      bf16 *stage = reinterpret_cast<bf16 *>(sm + OFF_X);
+      bf16 *stage = reinterpret_cast<bf16 *>(sm + OFF_V);  // V was consumed by the Y pass
       bf16 *out = reinterpret_cast<bf16 *>(a.out);
       if (GATE) {
         float o[32], u[32];
@@ -773,7 +777,7 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_ld32(tm + lane_off + TM_A + 32 * grp, u);
         tmem_wait_ld();
 #pragma unroll
-        for (int x = 0; x < 32; ++x) o[x] = a.scale * fmaf(s_pd[32 * grp + x], u[x], o[x]);
+        for (int x = 0; x < 32; ++x) o[x] = a.scale * fmaf(s_pd[par][32 * grp + x], u[x], o[x]);
         float sq[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) sq[x] = o[x] * o[x];
@@ -815,8 +819,8 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
           for (int y = 0; y < 8; y += 2) {  // two rows per packed conversion
             const int r = 32 * grp + 8 * sl + y;
-            const uint32_t pr = pack_bf2(a.scale * fmaf(s_pd[r], u8[y], o8[y]),
-                                         a.scale * fmaf(s_pd[r + 1], u8[y + 1], o8[y + 1]));
+            const uint32_t pr = pack_bf2(a.scale * fmaf(s_pd[par][r], u8[y], o8[y]),
+                                         a.scale * fmaf(s_pd[par][r + 1], u8[y + 1], o8[y + 1]));
             const uint16_t v0 = (uint16_t)(pr & 0xffffu), v1 = (uint16_t)(pr >> 16);
             if (tile) {
               reinterpret_cast<uint16_t *>(stage)[r * D + j] = v0;
@@ -833,11 +837,12 @@ __global__ void __launch_bounds__(NT, 1)
         fence_proxy_async();
         asm volatile("bar.sync 1, 256;" ::: "memory");
         if (tid == 0) {
-          tma_store_3d(&maps.out, 0, h, (int)t0, sb + OFF_X);
+          tma_store_3d(&maps.out, 0, h, (int)t0, sb + OFF_V);
           bulk_commit();
         }
       }
     }
+    if (grp == 2 && more) p1(c + 1);  // overlapped with the output phase
     if (!(ok = sync())) break;
   }
 
