@@ -205,7 +205,6 @@ __global__ void __launch_bounds__(NT, 1)
   __shared__ float s_GC[D];                   // Gamma_C
   __shared__ float s_red[4][C];
   __shared__ __align__(16) float s_M[3 * 256];  // inverse scratch; block decays P1 -> P2
-  __shared__ __align__(16) float s_e0[4][D];      // 2^(gam_R0) per block and channel
   __shared__ __align__(8) uint64_t s_bar[NBAR];
   __shared__ uint32_t s_tmem, s_abort, s_pend, s_ppar[NBAR];
 
@@ -310,7 +309,7 @@ __global__ void __launch_bounds__(NT, 1)
   //      per row); per channel (one thread each) the prefix sums of the clamped
   //      log2-retention, written back over g, with its value before each 16-token block,
   //      at the chunk end and Gamma_C; and per channel the decay between block starts
-  //      2^(gam_R0 - gam_R'0) for the pairs (1,0) (2,1) (3,2) (2,0) (3,1) (3,0), and 2^(gam_R0).
+  //      2^(gam_R0 - gam_R'0) for the pairs (1,0) (2,1) (3,2) (2,0) (3,1) (3,0).
   //      It runs before the walk for chunk 0 and during the output phase of chunk cc - 1.
   auto p1 = [&](int cc) {
     const int t = tid - 256;
@@ -365,10 +364,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
       float g0[4];
 #pragma unroll
-      for (int R = 0; R < 4; ++R) {
-        g0[R] = s_g0[R][i];
-        s_e0[R][i] = ex2(g0[R]);
-      }
+      for (int R = 0; R < 4; ++R) g0[R] = s_g0[R][i];
       s_gC[i] = run;
       s_GC[i] = ex2(run);
       s_M[0 * D + i] = ex2(g0[1] - g0[0]);
@@ -400,8 +396,8 @@ __global__ void __launch_bounds__(NT, 1)
     // ---- P2: operands of A and P, and X = [K Gamma; Q Gamma].  Rows relative to their own
     //      16-token block R = r/16 (gam_R0 = the log2-retention just before the block; q, k
     //      L2-normalised): Ktil_r = k_r 2^(gam_r - gam_R0), Qtil_r = q_r 2^(gam_r - gam_R0)
-    //      (<= 1) form the tensor-memory A operand (lanes 0-63 and 64-127) as bf16 hi + lo,
-    //      built with X_r = Ktil_r 2^(gam_R0) (tf32, K-major) from the same values; then the
+    //      (<= 1) form the tensor-memory A operand (lanes 0-63 and 64-127) as bf16 hi + lo;
+    //      then the
     //      B operand, columns Khat^(R)_s = k_s 2^(gam_R0 - gam_s) for s <= 16R + 15, from
     //      Khat^(R(s))_s times the decay between block starts: bf16 hi for all 160 rows, lo
     //      for the 112 band rows.  All three warp groups share both. -----------------------
@@ -431,12 +427,6 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int y = 0; y < 8; ++y) x[y] = 0.f;
           }
-          const float4 e0 = *reinterpret_cast<const float4 *>(&s_e0[R][ch]);
-          const float4 e1 = *reinterpret_cast<const float4 *>(&s_e0[R][ch + 4]);
-          const float xg[8] = {to_tf32(x[0] * e0.x), to_tf32(x[1] * e0.y), to_tf32(x[2] * e0.z),
-                               to_tf32(x[3] * e0.w), to_tf32(x[4] * e1.x), to_tf32(x[5] * e1.y),
-                               to_tf32(x[6] * e1.z), to_tf32(x[7] * e1.w)};
-          st_f32x8(sm + OFF_X + kmaj_f32<128>(L, ch), sm + OFF_X + kmaj_f32<128>(L, ch + 4), xg);
 #pragma unroll
           for (int y = 0; y < 4; ++y) {
             const uint32_t hv = pack_bf2(x[2 * y], x[2 * y + 1]);
@@ -500,7 +490,6 @@ __global__ void __launch_bounds__(NT, 1)
     if (!(ok = sync())) break;
     // D = [Ktil; Qtil] Khat^T: hi*hi over all 160 columns, hi*lo and lo*hi over the band
     if (tid == 0) {
-      if (more) issue(1u << BAR_Q, c + 1);  // q is consumed
       if (c > 0) {  // V is free once the previous output tile has been read out of it
         bulk_wait_read0();
         issue(1u << BAR_V, c);
@@ -521,6 +510,30 @@ __global__ void __launch_bounds__(NT, 1)
                     ID_AP112, 1);
       }
       commit(mma_par);
+    }
+    // X = [K Gamma; Q Gamma] (tf32, K-major, 128 rows) while the product runs
+    for (int it = tid; it < C * 16; it += NT) {  // (token, 8-channel group): rows r, 64 + r
+      const int r = it >> 4, c8 = it & 15;
+      float ok8[8], oq8[8];
+      if (r < nv) {
+        float kv[8], qv[8], gg[8];
+        bf_row8(sm + OFF_K, r, c8, kv);
+        bf_row8(sm + OFF_Q, r, c8, qv);
+        f_row8(sm + OFF_G, r, c8, gg);
+        const float rk = s_rk[r], rq = s_rq[r];
+#pragma unroll
+        for (int y = 0; y < 8; ++y) {
+          const float G = ex2(gg[y]);
+          ok8[y] = to_tf32(kv[y] * rk * G);
+          oq8[y] = to_tf32(qv[y] * rq * G);
+        }
+      } else {
+#pragma unroll
+        for (int y = 0; y < 8; ++y) ok8[y] = oq8[y] = 0.f;
+      }
+      st_f32x8(sm + OFF_X + kmaj_f32<128>(r, 8 * c8), sm + OFF_X + kmaj_f32<128>(r, 8 * c8 + 4), ok8);
+      st_f32x8(sm + OFF_X + kmaj_f32<128>(64 + r, 8 * c8),
+               sm + OFF_X + kmaj_f32<128>(64 + r, 8 * c8 + 4), oq8);
     }
     wait(BAR_MMA, mma_par);
     mma_par ^= 1;
@@ -576,6 +589,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
     fence_proxy_async();
     if (!(ok = sync())) break;
+    if (tid == 0 && more) issue(1u << BAR_Q, c + 1);  // q is consumed
 
     // ---- MMA1: X^T = S^T [K Gamma; Q Gamma]^T (A = S^T from TMEM) -> TC, in flight while
     //      the block inverse runs --------------------------------------------------------
@@ -758,6 +772,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
       commit(mma_par);
     }
+    if (grp == 2 && more) p1(c + 1);  // overlapped with the update and the output phase
     wait(BAR_MMA, mma_par);
     mma_par ^= 1;
     tc_fence_after();
@@ -842,7 +857,6 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
     }
-    if (grp == 2 && more) p1(c + 1);  // overlapped with the output phase
     if (!(ok = sync())) break;
   }
 
