@@ -602,9 +602,8 @@ __global__ void __launch_bounds__(NT, 1)
     }
 
     // ---- P4 (warp group 2): T = (I + A)^-1 by 16x16 blocks, fp32, then tf32 K-major
-    //      [r][s] in the T region.  Meanwhile groups 0 and 1 wait for MMA1 and build
-    //      Y^T = beta (V - K Gamma S)^T (tf32 hi + lo in TA), decay S^T by Gamma_C, and
-    //      build Kbar = k Gamma_C / Gamma (bf16 hi | lo, MN-major) into X[0, 32K). ---------
+    //      [r][s] in the T region.  Meanwhile groups 0 and 1 wait for MMA1, build
+    //      Y^T = beta (V - K Gamma S)^T (tf32 hi + lo in TA) and decay S^T by Gamma_C. -----
     if (grp == 2) {
       const int t = tid - 256, wg = t >> 5;
       const float *Am = reinterpret_cast<const float *>(sm + OFF_A);
@@ -683,33 +682,6 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_st32(tm + lane_off + TM_S + i0, v);
       }
       tmem_wait_st();
-      for (int it = tid; it < C * 16; it += 256) {  // Kbar hi | lo
-        const int s = it >> 4, c8 = it & 15;
-        uint32_t hw[4], lw[4];
-        if (s < nv) {
-          float kv[8], gg[8];
-          bf_row8(sm + OFF_K, s, c8, kv);
-          f_row8(sm + OFF_G, s, c8, gg);
-          const float4 c0v = *reinterpret_cast<const float4 *>(&s_gC[8 * c8]);
-          const float4 c1v = *reinterpret_cast<const float4 *>(&s_gC[8 * c8 + 4]);
-          const float gc[8] = {c0v.x, c0v.y, c0v.z, c0v.w, c1v.x, c1v.y, c1v.z, c1v.w};
-          const float rk = s_rk[s];
-#pragma unroll
-          for (int y = 0; y < 4; ++y) {
-            const float a0 = kv[2 * y] * rk * ex2(gc[2 * y] - gg[2 * y]);
-            const float a1 = kv[2 * y + 1] * rk * ex2(gc[2 * y + 1] - gg[2 * y + 1]);
-            hw[y] = pack_bf2(a0, a1);
-            lw[y] = pack_bf2(a0 - bf_lo(hw[y]), a1 - bf_hi(hw[y]));
-          }
-        } else {
-#pragma unroll
-          for (int y = 0; y < 4; ++y) hw[y] = lw[y] = 0u;
-        }
-        const uint32_t off = mnmaj_bf16_128(s, 8 * c8);
-        *reinterpret_cast<uint4 *>(sm + OFF_X + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4 *>(sm + OFF_X + 16384 + off) =
-            make_uint4(lw[0], lw[1], lw[2], lw[3]);
-      }
     }
     mma_par ^= 1;  // MMA1's phase (waited by groups 0 and 1)
     fence_proxy_async();
@@ -721,8 +693,39 @@ __global__ void __launch_bounds__(NT, 1)
         mma_tf32_ts(tm + TM_B, tm + TM_A + 64 * (ks >> 3) + 8 * k8, bd, ID_64, ks > 0);
       }
       commit(mma_par);
-      if (more) issue((1u << BAR_K) | (1u << BAR_G), c + 1);
     }
+    // Kbar = k Gamma_C / Gamma (bf16 hi | lo, MN-major) into X[0, 32K) while u is formed;
+    // then k and g of the next chunk may be loaded
+    for (int it = tid; it < C * 16; it += NT) {  // Kbar hi | lo
+      const int s = it >> 4, c8 = it & 15;
+      uint32_t hw[4], lw[4];
+      if (s < nv) {
+        float kv[8], gg[8];
+        bf_row8(sm + OFF_K, s, c8, kv);
+        f_row8(sm + OFF_G, s, c8, gg);
+        const float4 c0v = *reinterpret_cast<const float4 *>(&s_gC[8 * c8]);
+        const float4 c1v = *reinterpret_cast<const float4 *>(&s_gC[8 * c8 + 4]);
+        const float gc[8] = {c0v.x, c0v.y, c0v.z, c0v.w, c1v.x, c1v.y, c1v.z, c1v.w};
+        const float rk = s_rk[s];
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          const float a0 = kv[2 * y] * rk * ex2(gc[2 * y] - gg[2 * y]);
+          const float a1 = kv[2 * y + 1] * rk * ex2(gc[2 * y + 1] - gg[2 * y + 1]);
+          hw[y] = pack_bf2(a0, a1);
+          lw[y] = pack_bf2(a0 - bf_lo(hw[y]), a1 - bf_hi(hw[y]));
+        }
+      } else {
+#pragma unroll
+        for (int y = 0; y < 4; ++y) hw[y] = lw[y] = 0u;
+      }
+      const uint32_t off = mnmaj_bf16_128(s, 8 * c8);
+      *reinterpret_cast<uint4 *>(sm + OFF_X + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4 *>(sm + OFF_X + 16384 + off) =
+          make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    fence_proxy_async();
+    if (!(ok = sync())) break;
+    if (tid == 0 && more) issue((1u << BAR_K) | (1u << BAR_G), c + 1);
     wait(BAR_MMA, mma_par);  // u ready
     mma_par ^= 1;
     tc_fence_after();
