@@ -94,28 +94,39 @@ def _decode_bytes(n, H, d):
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) while the timed region runs."""
+    """nvidia-smi samples every 50 ms; the summary keeps the samples whose timestamps fall
+    inside the timed window (window() marks its start and end)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         time.sleep(0.3)
         return self
+
+    def window(self, start):
+        import datetime
+        if start:
+            self.t0 = datetime.datetime.now()
+        else:
+            self.t1 = datetime.datetime.now()
+            time.sleep(0.1)  # the sample in flight at the end
 
     def __exit__(self, *exc):
         if self.proc:
@@ -126,27 +137,35 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        import datetime
         rows = []
         try:
             for line in open(self.path):
                 p = [x.strip() for x in line.split(",")]
-                if len(p) >= 9:
+                if len(p) >= 10:
+                    try:
+                        p[0] = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f")
+                    except ValueError:
+                        continue
                     rows.append(p)
         except Exception:
             pass
+        if self.t0 and self.t1:
+            inside = [r for r in rows if self.t0 <= r[0] <= self.t1]
+            rows = inside or [r for r in rows if r[0] >= self.t0]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
-            for name, val in zip(names, r[5:9]):
+            for name, val in zip(names, r[6:10]):
                 if val.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
-                "samples": len(rows)}
+                "samples": len(rows), "period_ms": 50}
 
 
 def _dist():
@@ -300,6 +319,7 @@ def run_ours(args):
     _barrier(dist)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.window(True)
         wall0 = time.perf_counter()
         for _ in range(args.steps):
             flush.zero_()
@@ -315,6 +335,7 @@ def run_ours(args):
             step_ms.append(e0.elapsed_time(e2))
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
+        clk.window(False)
     _barrier(dist)
     launches = kda.kda_launch_count() - launches0
     kda.kda_check_device_error()
@@ -437,7 +458,7 @@ def _decode_bench(dev, kda, inputs, hbm, rank, args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
