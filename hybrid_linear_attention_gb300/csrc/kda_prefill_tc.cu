@@ -33,6 +33,8 @@
 // (hi*hi + hi*lo + lo*hi), which keeps the state at fp32-level accuracy.  Inputs arrive by
 // TMA in 128-byte-swizzled tiles; every operand is built with 16-byte vector accesses.
 #include <cuda.h>
+#include <cstdlib>
+#include <cstring>
 #include <cudaTypedefs.h>
 
 #include "kda_common.cuh"
@@ -68,7 +70,15 @@ constexpr uint32_t TM_S = 0, TM_A = 128, TM_B = 256, TM_C = 384, TM_COLS = 512;
 // during the A/P product: [Ktil; Qtil] bf16 hi and lo (64 columns each), result 160 columns
 constexpr uint32_t TM_AH = 128, TM_AL = 192, TM_D = 256;
 
-enum { BAR_Q = 0, BAR_K, BAR_V, BAR_G, BAR_MMA, NBAR };
+// TMA loads and tensor-core completion; in a cluster pair, the consumer's FULL (landing
+// buffer 0 / 1 holds T and P') and the producer's EMPTY (buffer 0 / 1 may be rewritten)
+enum { BAR_Q = 0, BAR_K, BAR_V, BAR_G, BAR_MMA, BAR_F0, BAR_F1, BAR_E0, BAR_E1, NBAR };
+// consumer landing buffers b = 0, 1: T then P' (16 KB each, tf32 K-major); buffer 0 is the
+// fused kernel's own T and P' region
+__host__ __device__ constexpr uint32_t off_lt(int b) { return 147456u + 32768u * (uint32_t)b; }
+__host__ __device__ constexpr uint32_t off_lp(int b) { return off_lt(b) + 16384u; }
+static_assert(off_lt(0) == OFF_T && off_lp(0) == OFF_P, "landing buffer 0 = T, P' regions");
+static_assert(off_lp(1) + 16384u <= 217088u, "landing buffers inside the shared memory map");
 
 // K-major 128B-swizzled tf32 operand with NR rows: panels of 32 channels, NR*128 bytes each
 template <int NR>
@@ -195,7 +205,9 @@ struct Maps {
   CUtensorMap q, k, v, g, out;
 };
 
-template <typename ST, bool GATE>
+// PAIR: a cluster of two CTAs per (head, sequence), rank 0 the consumer (state walk), rank 1
+// the producer (A, P', T); otherwise one CTA does both.
+template <typename ST, bool GATE, bool PAIR>
 __global__ void __launch_bounds__(NT, 1)
     prefill_tc_kernel(const TcArgs a, const __grid_constant__ Maps maps) {
   extern __shared__ uint8_t smem_raw[];
@@ -213,7 +225,8 @@ __global__ void __launch_bounds__(NT, 1)
   uint8_t *sm = smem_raw + pad;
   const uint32_t sb = raw_u32 + pad;
 
-  const int h = blockIdx.x, n = blockIdx.y;
+  const int h = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x, n = blockIdx.y;
+  const bool producer = PAIR && cluster_rank() == 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.H;
   const int64_t bos = a.cu_seqlens[n];
@@ -236,6 +249,7 @@ __global__ void __launch_bounds__(NT, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (PAIR) cluster_sync();  // both CTAs' barriers initialised before any remote arrive
   const uint32_t tm = s_tmem;
 
   // thread 0: TMA loads of chunk c into the buffers in `mask`
@@ -287,7 +301,7 @@ __global__ void __launch_bounds__(NT, 1)
   };
 
   // ---- initial state: S^T[j][i] = S0[i][j] (warp groups 0 and 1: 64 key channels each)
-  if (grp < 2) {
+  if (grp < 2 && !producer) {
     const ST *s0 = a.init_state
                        ? reinterpret_cast<const ST *>(a.init_state) + ((size_t)n * H + h) * D * D
                        : nullptr;
@@ -302,7 +316,7 @@ __global__ void __launch_bounds__(NT, 1)
     tmem_wait_st();
   }
   if (tid == 0 && nchunks > 0)
-    issue((1u << BAR_Q) | (1u << BAR_K) | (1u << BAR_V) | (1u << BAR_G), 0);
+    issue((1u << BAR_Q) | (1u << BAR_K) | (producer ? 0u : (1u << BAR_V)) | (1u << BAR_G), 0);
   bool ok = sync();
 
   // ---- P1 of chunk cc, by warp group 2 (128 threads): beta; row norms and q.k (two threads
@@ -385,14 +399,8 @@ __global__ void __launch_bounds__(NT, 1)
   if (ok && nchunks > 0 && grp == 2) p1(0);
   ok = sync();
 
-  for (int c = 0; c < nchunks && ok; ++c) {
-    const int64_t t0 = bos + (int64_t)c * C;
-    const int nv = (int)((eos - t0) < C ? (eos - t0) : C);
-    const uint32_t par = (uint32_t)(c & 1);
-    const bool more = c + 1 < nchunks;
-
-    if (!(ok = sync())) break;
-
+  // ---- phases of one chunk (t0: first token, nv: valid tokens, par: chunk parity) -----
+  auto ap_operands = [&](int nv) {
     // ---- P2: operands of A and P, and X = [K Gamma; Q Gamma].  Rows relative to their own
     //      16-token block R = r/16 (gam_R0 = the log2-retention just before the block; q, k
     //      L2-normalised): Ktil_r = k_r 2^(gam_r - gam_R0), Qtil_r = q_r 2^(gam_r - gam_R0)
@@ -486,14 +494,10 @@ __global__ void __launch_bounds__(NT, 1)
               make_uint4(lv[0], lv[1], lv[2], lv[3]);
       }
     }
-    fence_proxy_async();
-    if (!(ok = sync())) break;
-    // D = [Ktil; Qtil] Khat^T: hi*hi over all 160 columns, hi*lo and lo*hi over the band
-    if (tid == 0) {
-      if (c > 0) {  // V is free once the previous output tile has been read out of it
-        bulk_wait_read0();
-        issue(1u << BAR_V, c);
-      }
+  };
+  // thread 0: D = [Ktil; Qtil] Khat^T: hi*hi over all 160 columns, hi*lo and lo*hi over
+  // the band
+  auto ap_issue = [&]() {
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t ko = (uint32_t)(ks >> 2) * (160 * 128) + (ks & 3) * 32;
         mma_bf16_ts(tm + TM_D, tm + TM_AH + 8 * ks, sdesc_sw128(sb + OFF_BH + ko, 16, 1024),
@@ -510,8 +514,9 @@ __global__ void __launch_bounds__(NT, 1)
                     ID_AP112, 1);
       }
       commit(mma_par);
-    }
-    // X = [K Gamma; Q Gamma] (tf32, K-major, 128 rows) while the product runs
+  };
+  // X = [K Gamma; Q Gamma] (tf32, K-major, 128 rows)
+  auto x_rows = [&](int nv) {
     for (int it = tid; it < C * 16; it += NT) {  // (token, 8-channel group): rows r, 64 + r
       const int r = it >> 4, c8 = it & 15;
       float ok8[8], oq8[8];
@@ -535,10 +540,8 @@ __global__ void __launch_bounds__(NT, 1)
       st_f32x8(sm + OFF_X + kmaj_f32<128>(64 + r, 8 * c8),
                sm + OFF_X + kmaj_f32<128>(64 + r, 8 * c8 + 4), oq8);
     }
-    wait(BAR_MMA, mma_par);
-    mma_par ^= 1;
-    tc_fence_after();
-
+  };
+  auto extract = [&](int nv, uint8_t *pbase) {
     // ---- P3: A (beta-scaled, strict lower, fp32 rows of LDA) and P' (strict lower, tf32,
     //      K-major) from the product, one tensor-memory lane per row (lanes 0-63: A, 64-127:
     //      P), in 16-column pieces that each hold one block R and 16 consecutive s; zeros in
@@ -571,7 +574,7 @@ __global__ void __launch_bounds__(NT, 1)
                             s + 2 < r ? br * v[4 * q4 + 2] : 0.f,
                             s + 3 < r ? br * v[4 * q4 + 3] : 0.f);
           } else {
-            *reinterpret_cast<float4 *>(sm + OFF_P + kmaj_f32<64>(r, s)) =
+            *reinterpret_cast<float4 *>(pbase + kmaj_f32<64>(r, s)) =
                 make_float4(s < r ? to_tf32(v[4 * q4]) : 0.f,
                             s + 1 < r ? to_tf32(v[4 * q4 + 1]) : 0.f,
                             s + 2 < r ? to_tf32(v[4 * q4 + 2]) : 0.f,
@@ -583,28 +586,22 @@ __global__ void __launch_bounds__(NT, 1)
         const int pr = tid >> 6, rr16 = (tid >> 2) & 15, c4 = tid & 3;
         const int Rz = pr < 3 ? 0 : pr < 5 ? 1 : 2;
         const int Rpz = pr < 3 ? pr + 1 : pr < 5 ? pr - 1 : 3;
-        *reinterpret_cast<float4 *>(sm + OFF_P + kmaj_f32<64>(16 * Rz + rr16, 16 * Rpz + 4 * c4)) =
+        *reinterpret_cast<float4 *>(pbase + kmaj_f32<64>(16 * Rz + rr16, 16 * Rpz + 4 * c4)) =
             make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    fence_proxy_async();
-    if (!(ok = sync())) break;
-    if (tid == 0 && more) issue(1u << BAR_Q, c + 1);  // q is consumed
-
-    // ---- MMA1: X^T = S^T [K Gamma; Q Gamma]^T (A = S^T from TMEM) -> TC, in flight while
-    //      the block inverse runs --------------------------------------------------------
-    if (tid == 0) {
+  };
+  // ---- MMA1: X^T = S^T [K Gamma; Q Gamma]^T (A = S^T from TMEM) -> TC (thread 0)
+  auto mma1_issue = [&]() {
       for (int ks = 0; ks < 16; ++ks) {
         const uint64_t bd = sdesc_sw128(sb + OFF_X + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
         mma_tf32_ts(tm + TM_C, tm + TM_S + 8 * ks, bd, ID_128, ks > 0);
       }
       commit(mma_par);
-    }
-
-    // ---- P4 (warp group 2): T = (I + A)^-1 by 16x16 blocks, fp32, then tf32 K-major
-    //      [r][s] in the T region.  Meanwhile groups 0 and 1 wait for MMA1, build
-    //      Y^T = beta (V - K Gamma S)^T (tf32 hi + lo in TA) and decay S^T by Gamma_C. -----
-    if (grp == 2) {
+  };
+  // ---- T = (I + A)^-1 by 16x16 blocks on warp group 2, fp32, then tf32 K-major [r][s]
+  //      at tbase
+  auto inverse = [&](uint8_t *tbase) {
       const int t = tid - 256, wg = t >> 5;
       const float *Am = reinterpret_cast<const float *>(sm + OFF_A);
       float *Tm = reinterpret_cast<float *>(sm + OFF_T);
@@ -651,9 +648,12 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
       for (int q = 0; q < 32; ++q) {
         const int e = t + 128 * q;
-        *reinterpret_cast<float *>(sm + OFF_T + kmaj_f32<64>(e >> 6, e & 63)) = tv[q];
+        *reinterpret_cast<float *>(tbase + kmaj_f32<64>(e >> 6, e & 63)) = tv[q];
       }
-    } else {
+  };
+  // ---- groups 0 and 1: wait for MMA1, Y^T = beta (V - K Gamma S)^T (tf32 hi + lo in TA),
+  //      decay S^T by Gamma_C
+  auto y_decay = [&](int nv, uint32_t par) {
       wait(BAR_MMA, mma_par);  // MMA1 done
       tc_fence_after();
       wait(BAR_V, par);
@@ -682,18 +682,17 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_st32(tm + lane_off + TM_S + i0, v);
       }
       tmem_wait_st();
-    }
-    mma_par ^= 1;  // MMA1's phase (waited by groups 0 and 1)
-    fence_proxy_async();
-    if (!(ok = sync())) break;
-    if (tid == 0) {  // u^T = Y^T T^T, hi then lo
+  };
+  // thread 0: u^T = Y^T T^T, hi then lo (T at shared offset t_off)
+  auto mmau_issue = [&](uint32_t t_off) {
       for (int ks = 0; ks < 16; ++ks) {
         const int k8 = ks & 7;
-        const uint64_t bd = sdesc_sw128(sb + OFF_T + (k8 >> 2) * 8192 + (k8 & 3) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(sb + t_off + (k8 >> 2) * 8192 + (k8 & 3) * 32, 16, 1024);
         mma_tf32_ts(tm + TM_B, tm + TM_A + 64 * (ks >> 3) + 8 * k8, bd, ID_64, ks > 0);
       }
       commit(mma_par);
-    }
+  };
+  auto kbar = [&](int nv) {
     // Kbar = k Gamma_C / Gamma (bf16 hi | lo, MN-major) into X[0, 32K) while u is formed;
     // then k and g of the next chunk may be loaded
     for (int it = tid; it < C * 16; it += NT) {  // Kbar hi | lo
@@ -723,13 +722,8 @@ __global__ void __launch_bounds__(NT, 1)
       *reinterpret_cast<uint4 *>(sm + OFF_X + 16384 + off) =
           make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
-    fence_proxy_async();
-    if (!(ok = sync())) break;
-    if (tid == 0 && more) issue((1u << BAR_K) | (1u << BAR_G), c + 1);
-    wait(BAR_MMA, mma_par);  // u ready
-    mma_par ^= 1;
-    tc_fence_after();
-
+  };
+  auto p6 = [&]() {
     // ---- P6: u (fp32 -> TA[0,64), tf32 -> TA[64,128)) and u hi | lo (bf16, K-major
     //      [j][s]) into X[32K, 64K) ---------------------------------------------------------
     if (grp < 2) {
@@ -755,13 +749,12 @@ __global__ void __launch_bounds__(NT, 1)
       }
       tmem_wait_st();
     }
-    fence_proxy_async();
-    if (!(ok = sync())) break;
-
-    // ---- P7: O += P' u (tf32); S^T += u^T Kbar as hi*hi + hi*lo + lo*hi (bf16) ---------
-    if (tid == 0) {
+  };
+  // ---- P7 (thread 0): O += P' u (tf32, P' at shared offset p_off); S^T += u^T Kbar as
+  //      hi*hi + hi*lo + lo*hi (bf16)
+  auto p7_issue = [&](uint32_t p_off) {
       for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t bd = sdesc_sw128(sb + OFF_P + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(sb + p_off + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
         mma_tf32_ts(tm + TM_C + 64, tm + TM_A + 64 + 8 * ks, bd, ID_64, 1);
       }
       for (int term = 0; term < 3; ++term) {
@@ -774,12 +767,8 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       commit(mma_par);
-    }
-    if (grp == 2 && more) p1(c + 1);  // overlapped with the update and the output phase
-    wait(BAR_MMA, mma_par);
-    mma_par ^= 1;
-    tc_fence_after();
-
+  };
+  auto p8 = [&](int nv, int64_t t0, uint32_t par) {
     // ---- P8: outputs o_r = scale (O'_r + (q_r.k_r) u_r), norm and gate, store.  A full
     //      chunk goes out as one bulk tensor store of the [64 tokens][128] bf16 tile, staged
     //      in the V region (free since the Y pass; the next V load waits for the store to
@@ -860,13 +849,153 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
     }
-    if (!(ok = sync())) break;
+  };
+
+  if (!PAIR) {
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int64_t t0 = bos + (int64_t)c * C;
+      const int nv = (int)((eos - t0) < C ? (eos - t0) : C);
+      const uint32_t par = (uint32_t)(c & 1);
+      const bool more = c + 1 < nchunks;
+      ap_operands(nv);
+      fence_proxy_async();
+      if (!(ok = sync())) break;
+      if (tid == 0) {
+        if (c > 0) {  // V is free once the previous output tile has been read out of it
+          bulk_wait_read0();
+          issue(1u << BAR_V, c);
+        }
+        ap_issue();
+      }
+      x_rows(nv);  // while the product runs
+      wait(BAR_MMA, mma_par);
+      mma_par ^= 1;
+      tc_fence_after();
+      extract(nv, sm + OFF_P);
+      fence_proxy_async();
+      if (!(ok = sync())) break;
+      if (tid == 0) {
+        if (more) issue(1u << BAR_Q, c + 1);  // q is consumed
+        mma1_issue();
+      }
+      if (grp == 2) inverse(sm + OFF_T);  // in flight with MMA1 and the Y / decay work
+      else y_decay(nv, par);
+      mma_par ^= 1;  // MMA1's phase (waited by groups 0 and 1)
+      fence_proxy_async();
+      if (!(ok = sync())) break;
+      if (tid == 0) mmau_issue(OFF_T);
+      kbar(nv);  // while u is formed; then k and g of the next chunk may be loaded
+      fence_proxy_async();
+      if (!(ok = sync())) break;
+      if (tid == 0 && more) issue((1u << BAR_K) | (1u << BAR_G), c + 1);
+      wait(BAR_MMA, mma_par);  // u ready
+      mma_par ^= 1;
+      tc_fence_after();
+      p6();
+      fence_proxy_async();
+      if (!(ok = sync())) break;
+      if (tid == 0) p7_issue(OFF_P);
+      if (grp == 2 && more) p1(c + 1);  // overlapped with the update and the output phase
+      wait(BAR_MMA, mma_par);
+      mma_par ^= 1;
+      tc_fence_after();
+      p8(nv, t0, par);
+      if (!(ok = sync())) break;
+    }
+  } else if (!producer) {
+    // ---- consumer of a cluster pair: the state walk; T and P' of chunk c arrive from the
+    //      producer in landing buffer c & 1 (FULL), which is handed back after the update
+    //      (EMPTY) ---------------------------------------------------------------------------
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int64_t t0 = bos + (int64_t)c * C;
+      const int nv = (int)((eos - t0) < C ? (eos - t0) : C);
+      const uint32_t par = (uint32_t)(c & 1);
+      const bool more = c + 1 < nchunks;
+      const int b = c & 1;
+      if (tid == 0 && c > 0) {  // V is free once the previous output tile has been read
+        bulk_wait_read0();
+        issue(1u << BAR_V, c);
+      }
+      x_rows(nv);
+      fence_proxy_async();
+      if (!(ok = sync())) break;
+      if (tid == 0) {
+        if (more) issue(1u << BAR_Q, c + 1);  // q is consumed
+        mma1_issue();
+      }
+      if (grp < 2) y_decay(nv, par);
+      mma_par ^= 1;
+      fence_proxy_async();
+      if (!(ok = sync())) break;
+      if (tid == 0) {
+        if (mbar_wait_cluster(bar(BAR_F0 + b), (uint32_t)((c >> 1) & 1))) {
+          fence_proxy_async();
+          mmau_issue(off_lt(b));
+        } else {
+          s_abort = 1;
+          if (a.err) atomicOr(a.err, ERR_MBAR_TIMEOUT);
+        }
+      }
+      kbar(nv);
+      fence_proxy_async();
+      if (!(ok = sync())) break;
+      if (tid == 0 && more) issue((1u << BAR_K) | (1u << BAR_G), c + 1);
+      wait(BAR_MMA, mma_par);  // u ready
+      mma_par ^= 1;
+      tc_fence_after();
+      p6();
+      fence_proxy_async();
+      if (!(ok = sync())) break;
+      if (tid == 0) p7_issue(off_lp(b));
+      if (grp == 2 && more) p1(c + 1);
+      wait(BAR_MMA, mma_par);
+      mma_par ^= 1;
+      tc_fence_after();
+      if (tid == 0) mbar_arrive_remote(bar(BAR_E0 + b), 1);  // landing buffer b is free
+      p8(nv, t0, par);
+      if (!(ok = sync())) break;
+    }
+  } else {
+    // ---- producer of a cluster pair: A and P' of each chunk, the inverse T, written into the
+    //      consumer's landing buffer c & 1 -------------------------------------------------
+    uint8_t *peer = reinterpret_cast<uint8_t *>(map_rank(sm, 0));
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int64_t t0 = bos + (int64_t)c * C;
+      const int nv = (int)((eos - t0) < C ? (eos - t0) : C);
+      const bool more = c + 1 < nchunks;
+      const int b = c & 1;
+      if (c > 0) {
+        if (grp == 2) p1(c);
+        if (!(ok = sync())) break;
+      }
+      ap_operands(nv);
+      fence_proxy_async();
+      if (!(ok = sync())) break;
+      if (tid == 0) {
+        if (more) issue((1u << BAR_Q) | (1u << BAR_K) | (1u << BAR_G), c + 1);
+        ap_issue();
+      }
+      wait(BAR_MMA, mma_par);
+      mma_par ^= 1;
+      tc_fence_after();
+      if (c >= 2 && !mbar_wait_cluster(bar(BAR_E0 + b), (uint32_t)(((c - 2) >> 1) & 1))) {
+        s_abort = 1;
+        if (a.err) atomicOr(a.err, ERR_MBAR_TIMEOUT);
+      }
+      if (!(ok = sync())) break;
+      extract(nv, peer + off_lp(b));
+      if (!(ok = sync())) break;
+      if (grp == 2) inverse(peer + off_lt(b));
+      fence_cluster();
+      if (!(ok = sync())) break;
+      if (tid == 0) mbar_arrive_remote(bar(BAR_F0 + b), 0);  // T and P' of chunk c landed
+    }
   }
 
   if (tid == 0) bulk_wait0();  // output tiles written before the shared memory is released
 
   // ---- final state: S[i][j] = S^T[j][i] ------------------------------------------------
-  if (ok && a.final_state && grp < 2) {
+  if (ok && a.final_state && grp < 2 && !producer) {
     ST *dst = reinterpret_cast<ST *>(a.final_state) + ((size_t)n * H + h) * D * D;
 #pragma unroll 1
     for (int g32 = 0; g32 < 2; ++g32) {
@@ -885,6 +1014,7 @@ __global__ void __launch_bounds__(NT, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // neither CTA leaves while the other may still write to it
   if (warp == 0) tmem_dealloc(tm, TM_COLS);
 }
 
@@ -932,19 +1062,49 @@ bool make_out_map(CUtensorMap *m, void *ptr, int64_t T, int H) {
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename ST, bool GATE>
+template <typename ST, bool GATE, bool PAIR>
 cudaError_t launch_typed(const TcArgs &a, const Maps &maps, cudaStream_t s) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<ST, GATE>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<ST, GATE, PAIR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  prefill_tc_kernel<ST, GATE><<<dim3(a.H, a.n_seqs), NT, SMEM_BYTES, s>>>(a, maps);
-  return cudaGetLastError();
+  if (!PAIR) {
+    prefill_tc_kernel<ST, GATE, PAIR><<<dim3(a.H, a.n_seqs), NT, SMEM_BYTES, s>>>(a, maps);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(2 * a.H, a.n_seqs);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<ST, GATE, PAIR>, a, maps);
+}
+
+// A cluster pair per (head, sequence) when the pairs fit on the device at once (small
+// batches: otherwise the SMs are better spent on more units); KDA_PREFILL_PAIR=0 / 1
+// forces one form (tests run both).
+bool use_pair(const TcArgs &a) {
+  const char *env = getenv("KDA_PREFILL_PAIR");
+  if (env && env[0] == '0') return false;
+  if (env && env[0] == '1') return true;
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return false;
+  return (int64_t)a.n_seqs * a.H * 2 <= nsm;
 }
 
 }  // namespace
@@ -973,9 +1133,18 @@ cudaError_t launch_prefill_tc(const TcArgs &a, int64_t total_tokens, bool st_bf1
       return cudaErrorInvalidValue;
   }
   const bool gate = a.gate != nullptr;
+  if (use_pair(a)) {
+    if (st_bf16)
+      return gate ? launch_typed<bf16, true, true>(a, maps, s)
+                  : launch_typed<bf16, false, true>(a, maps, s);
+    return gate ? launch_typed<float, true, true>(a, maps, s)
+                : launch_typed<float, false, true>(a, maps, s);
+  }
   if (st_bf16)
-    return gate ? launch_typed<bf16, true>(a, maps, s) : launch_typed<bf16, false>(a, maps, s);
-  return gate ? launch_typed<float, true>(a, maps, s) : launch_typed<float, false>(a, maps, s);
+    return gate ? launch_typed<bf16, true, false>(a, maps, s)
+                : launch_typed<bf16, false, false>(a, maps, s);
+  return gate ? launch_typed<float, true, false>(a, maps, s)
+              : launch_typed<float, false, false>(a, maps, s);
 }
 
 }  // namespace kda

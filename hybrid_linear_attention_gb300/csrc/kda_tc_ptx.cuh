@@ -38,7 +38,50 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 // Bounded wait: returns false when the phase did not complete within the iteration limit
 // (each try_wait already suspends for a while in hardware).
+// cluster scope: a wait that also acquires what other CTAs of the cluster released
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 constexpr long kWaitLimit = 1L << 24;
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+  for (long it = 0; it < kWaitLimit; ++it)
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+  return false;
+}
+// this CTA's rank in its cluster
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// generic address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ void *map_rank(const void *p, uint32_t rank) {
+  uint64_t d;
+  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(d) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+  return reinterpret_cast<void *>(d);
+}
+// arrive (release, cluster scope) on the mbarrier at the same offset in CTA `rank`
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
+  uint32_t rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(bar), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rb)
+               : "memory");
+}
+__device__ __forceinline__ void fence_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   for (long it = 0; it < kWaitLimit; ++it)
     if (mbar_try_wait(bar, parity)) return true;
