@@ -324,9 +324,9 @@ __global__ void __launch_bounds__(NT, 1)
   //      log2-retention, written back over g, with its value before each 16-token block,
   //      at the chunk end and Gamma_C; and per channel the decay between block starts
   //      2^(gam_R0 - gam_R'0) for the pairs (1,0) (2,1) (3,2) (2,0) (3,1) (3,0).
-  //      It runs before the walk for chunk 0 and during the output phase of chunk cc - 1.
-  auto p1 = [&](int cc) {
-    const int t = tid - 256;
+  //      It runs before the walk for chunk 0 and during the output phase of chunk cc - 1
+  //      (t: the thread's index in the 128 running it).
+  auto p1 = [&](int cc, int t) {
     const int64_t tc = bos + (int64_t)cc * C;
     const int nvc = (int)((eos - tc) < C ? (eos - tc) : C);
     const uint32_t pc = (uint32_t)(cc & 1);
@@ -396,11 +396,11 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t ID_AP160 = idesc(1, 128, 160, 0, 0);
   const uint32_t ID_AP112 = idesc(1, 128, 112, 0, 0);
   uint32_t mma_par = 0;
-  if (ok && nchunks > 0 && grp == 2) p1(0);
+  if (ok && nchunks > 0 && grp == 2) p1(0, tid - 256);
   ok = sync();
 
   // ---- phases of one chunk (t0: first token, nv: valid tokens, par: chunk parity) -----
-  auto ap_operands = [&](int nv) {
+  auto ap_operands = [&](int nv, int nthr) {
     // ---- P2: operands of A and P, and X = [K Gamma; Q Gamma].  Rows relative to their own
     //      16-token block R = r/16 (gam_R0 = the log2-retention just before the block; q, k
     //      L2-normalised): Ktil_r = k_r 2^(gam_r - gam_R0), Qtil_r = q_r 2^(gam_r - gam_R0)
@@ -414,9 +414,10 @@ __global__ void __launch_bounds__(NT, 1)
       const bool isq = L >= 64, live = r < nv;
       const uint8_t *src = sm + (isq ? OFF_Q : OFF_K);
       const float rn = isq ? s_rq[r] : s_rk[r];
-      const int pend = grp == 2 ? 8 : 3 * grp + 3;
+      const int pbeg = nthr == NT ? 3 * grp : 4 * grp;
+      const int pend = nthr == NT ? (grp == 2 ? 8 : 3 * grp + 3) : (tid < nthr ? 4 * grp + 4 : 0);
 #pragma unroll 1
-      for (int pc = 3 * grp; pc < pend; ++pc) {
+      for (int pc = pbeg; pc < pend; ++pc) {
         float hw[8], lw[8];  // packed bf16 pairs, low half = even channel
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
@@ -448,7 +449,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
       tmem_wait_st();
     }
-    for (int it = tid; it < C * 16; it += NT) {  // B operand: (token s, 8-channel group)
+    for (int it = tid; it < C * 16 && tid < nthr; it += nthr) {  // B: (token s, 8-channel group)
       const int sr = it >> 4, c8 = it & 15, Rs = sr >> 4;
       float kh[8];
       if (sr < nv) {
@@ -541,7 +542,7 @@ __global__ void __launch_bounds__(NT, 1)
                sm + OFF_X + kmaj_f32<128>(64 + r, 8 * c8 + 4), oq8);
     }
   };
-  auto extract = [&](int nv, uint8_t *pbase) {
+  auto extract = [&](int nv, uint8_t *pbase, float *Am) {
     // ---- P3: A (beta-scaled, strict lower, fp32 rows of LDA) and P' (strict lower, tf32,
     //      K-major) from the product, one tensor-memory lane per row (lanes 0-63: A, 64-127:
     //      P), in 16-column pieces that each hold one block R and 16 consecutive s; zeros in
@@ -554,7 +555,6 @@ __global__ void __launch_bounds__(NT, 1)
       const bool lo_rows = (quarter & 1) == 0;
       const int p0 = lo_rows ? 3 + grp : (grp == 0 ? 0 : 4 + 2 * grp);
       const int np = lo_rows ? 1 : (grp == 0 ? 3 : 2);
-      float *Am = reinterpret_cast<float *>(sm + OFF_A);
       const float br = s_beta[r];
       for (int pc = p0; pc < p0 + np; ++pc) {
         float v[16];
@@ -601,10 +601,8 @@ __global__ void __launch_bounds__(NT, 1)
   };
   // ---- T = (I + A)^-1 by 16x16 blocks on warp group 2, fp32, then tf32 K-major [r][s]
   //      at tbase
-  auto inverse = [&](uint8_t *tbase) {
+  auto inverse = [&](uint8_t *tbase, const float *Am, float *Tm, float *scr) {
       const int t = tid - 256, wg = t >> 5;
-      const float *Am = reinterpret_cast<const float *>(sm + OFF_A);
-      float *Tm = reinterpret_cast<float *>(sm + OFF_T);
       if (t < 64) {  // diagonal blocks: right-looking substitution, one column per thread
         const int R = t >> 4, cc = t & 15, b0 = 16 * R;
         float x[16], pacc[16];
@@ -629,10 +627,10 @@ __global__ void __launch_bounds__(NT, 1)
           for (int Q = S; Q < R; ++Q)
             warp_mma16(dacc, Am + (16 * R) * LDA + 16 * Q, LDA, Tm + (16 * Q) * 64 + 16 * S, 64,
                        2, lane);
-          warp_store16(s_M + wg * 256, 16, dacc, lane, 1.f);
+          warp_store16(scr + wg * 256, 16, dacc, lane, 1.f);
           __syncwarp();
           float tacc[2][4] = {};
-          warp_mma16(tacc, Tm + (16 * R) * 64 + 16 * R, 64, s_M + wg * 256, 16, 2, lane);
+          warp_mma16(tacc, Tm + (16 * R) * 64 + 16 * R, 64, scr + wg * 256, 16, 2, lane);
           warp_store16(Tm + (16 * R) * 64 + 16 * S, 64, tacc, lane, -1.f);
         }
         asm volatile("bar.sync 3, 128;" ::: "memory");
@@ -857,7 +855,7 @@ __global__ void __launch_bounds__(NT, 1)
       const int nv = (int)((eos - t0) < C ? (eos - t0) : C);
       const uint32_t par = (uint32_t)(c & 1);
       const bool more = c + 1 < nchunks;
-      ap_operands(nv);
+      ap_operands(nv, NT);
       fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0) {
@@ -871,14 +869,16 @@ __global__ void __launch_bounds__(NT, 1)
       wait(BAR_MMA, mma_par);
       mma_par ^= 1;
       tc_fence_after();
-      extract(nv, sm + OFF_P);
+      extract(nv, sm + OFF_P, reinterpret_cast<float *>(sm + OFF_A));
       fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0) {
         if (more) issue(1u << BAR_Q, c + 1);  // q is consumed
         mma1_issue();
       }
-      if (grp == 2) inverse(sm + OFF_T);  // in flight with MMA1 and the Y / decay work
+      if (grp == 2)  // in flight with MMA1 and the Y / decay work
+        inverse(sm + OFF_T, reinterpret_cast<const float *>(sm + OFF_A),
+                reinterpret_cast<float *>(sm + OFF_T), s_M);
       else y_decay(nv, par);
       mma_par ^= 1;  // MMA1's phase (waited by groups 0 and 1)
       fence_proxy_async();
@@ -895,7 +895,7 @@ __global__ void __launch_bounds__(NT, 1)
       fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0) p7_issue(OFF_P);
-      if (grp == 2 && more) p1(c + 1);  // overlapped with the update and the output phase
+      if (grp == 2 && more) p1(c + 1, tid - 256);  // overlapped with the update and the output phase
       wait(BAR_MMA, mma_par);
       mma_par ^= 1;
       tc_fence_after();
@@ -947,7 +947,7 @@ __global__ void __launch_bounds__(NT, 1)
       fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0) p7_issue(off_lp(b));
-      if (grp == 2 && more) p1(c + 1);
+      if (grp == 2 && more) p1(c + 1, tid - 256);
       wait(BAR_MMA, mma_par);
       mma_par ^= 1;
       tc_fence_after();
@@ -959,18 +959,22 @@ __global__ void __launch_bounds__(NT, 1)
     // ---- producer of a cluster pair: A and P' of each chunk, the inverse T, written into the
     //      consumer's landing buffer c & 1 -------------------------------------------------
     uint8_t *peer = reinterpret_cast<uint8_t *>(map_rank(sm, 0));
+    // the producer loads no v and builds no X: A, the fp32 T and the inverse's block scratch
+    // live there, clear of the operand regions, so the next chunk's operands can be built
+    // while the inverse runs
+    float *pA = reinterpret_cast<float *>(sm + OFF_X);
+    float *pS = reinterpret_cast<float *>(sm + OFF_X + 20480);
+    float *pT = reinterpret_cast<float *>(sm + OFF_V);
+    if (ok && nchunks > 0) {
+      ap_operands((int)((eos - bos) < C ? (eos - bos) : C), NT);
+      fence_proxy_async();
+    }
+    ok = sync() && ok;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int64_t t0 = bos + (int64_t)c * C;
       const int nv = (int)((eos - t0) < C ? (eos - t0) : C);
       const bool more = c + 1 < nchunks;
       const int b = c & 1;
-      if (c > 0) {
-        if (grp == 2) p1(c);
-        if (!(ok = sync())) break;
-      }
-      ap_operands(nv);
-      fence_proxy_async();
-      if (!(ok = sync())) break;
       if (tid == 0) {
         if (more) issue((1u << BAR_Q) | (1u << BAR_K) | (1u << BAR_G), c + 1);
         ap_issue();
@@ -983,10 +987,19 @@ __global__ void __launch_bounds__(NT, 1)
         if (a.err) atomicOr(a.err, ERR_MBAR_TIMEOUT);
       }
       if (!(ok = sync())) break;
-      extract(nv, peer + off_lp(b));
+      extract(nv, peer + off_lp(b), pA);
       if (!(ok = sync())) break;
-      if (grp == 2) inverse(peer + off_lt(b));
+      if (grp == 2) {
+        inverse(peer + off_lt(b), pA, pT, pS);
+      } else if (more) {  // P1 and the operands of chunk c + 1 on groups 0 and 1
+        const int64_t t1 = t0 + C;
+        const int nv1 = (int)((eos - t1) < C ? (eos - t1) : C);
+        if (grp == 0) p1(c + 1, tid);
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        ap_operands(nv1, 256);
+      }
       fence_cluster();
+      fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0) mbar_arrive_remote(bar(BAR_F0 + b), 0);  // T and P' of chunk c landed
     }
