@@ -91,6 +91,7 @@ const char *kda_status_string(kda_status s) {
     case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA launch or runtime error";
     case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace too small";
     case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device wait ran out";
+    case KDA_ERR_BAD_INDEX: return "KDA_ERR_BAD_INDEX: a device-side index was out of range";
   }
   return "unknown kda_status";
 }
@@ -190,6 +191,7 @@ kda_status kda_prefill(const kda_params *p, const void *q, const void *k, const 
   }
   kda::RecArgs a = base_args(p);
   a.n_seqs = n_seqs;
+  a.n_slots = n_seqs;
   a.q = q, a.k = k, a.v = v, a.g = g, a.beta = beta;
   a.cu_seqlens = cu_seqlens;
   a.state_in = init_state;
@@ -226,6 +228,7 @@ kda_status kda_decode_step(const kda_params *p, const void *q, const void *k, co
     return KDA_ERR_INVALID_ARG;
   kda::RecArgs a = base_args(p);
   a.n_seqs = n_seqs;
+  a.n_slots = n_slots;
   a.q = q, a.k = k, a.v = v, a.g = g, a.beta = beta;
   a.slot_idx = slot_idx;
   a.state_in = state;
@@ -251,6 +254,7 @@ kda_status kda_decode_step_fused(const kda_params *p, const void *x_raw, const v
     return KDA_ERR_INVALID_ARG;
   kda::RecArgs a = base_args(p);
   a.n_seqs = n_seqs;
+  a.n_slots = n_slots;
   a.x_raw = x_raw;
   a.conv_w = conv_w;
   a.conv_state = conv_state;
@@ -284,8 +288,58 @@ kda_status kda_conv_state_update(const kda_params *p, const void *x_new, const v
   a.conv_w = conv_w;
   a.conv_state = conv_state;
   a.slot_idx = slot_idx;
+  a.n_slots = n_slots;
+  a.err = device_error_ptr();
   a.y = y;
   return finish(kda::launch_conv_update(a, p->io_dtype == KDA_BF16, stream), 1);
+}
+
+kda_status kda_decode_multi(const kda_params *p, const void *q, const void *k, const void *v,
+                            const float *g, const float *beta, void *state, int n_slots,
+                            const int32_t *slot_idx, int n_seqs, int K, const void *gate_logit,
+                            const float *norm_w, void *out, void *step_states, int commit_final,
+                            cudaStream_t stream) {
+  if (K < 1 || K > 64) return KDA_ERR_INVALID_ARG;
+  if ((int64_t)n_seqs * K > 65535 * 64) return KDA_ERR_UNSUPPORTED;
+  kda_status st = decode_common(p, g, beta, state, n_slots, slot_idx, n_seqs, gate_logit,
+                                norm_w, out);
+  if (st != KDA_OK || n_seqs == 0) return st;
+  if (!q || !k || !v || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      !opt_aligned16(step_states))
+    return KDA_ERR_INVALID_ARG;
+  if (!step_states && !commit_final) return KDA_ERR_INVALID_ARG;  // nothing would be kept
+  kda::RecArgs a = base_args(p);
+  a.n_seqs = n_seqs;
+  a.n_slots = n_slots;
+  a.tokens_per_seq = K;
+  a.q = q, a.k = k, a.v = v, a.g = g, a.beta = beta;
+  a.slot_idx = slot_idx;
+  a.state_in = state;
+  a.state_out = commit_final ? state : nullptr;
+  a.step_states = step_states;
+  a.gate = gate_logit;
+  a.norm_w = norm_w;
+  a.out = out;
+  return finish(kda::launch_recurrent(a, p->d_k, p->io_dtype == KDA_BF16,
+                                      p->state_dtype == KDA_BF16, stream),
+                1);
+}
+
+kda_status kda_state_accept(const kda_params *p, const void *step_states, int n_seqs, int K,
+                            const int32_t *accept_len, void *state, int n_slots,
+                            const int32_t *slot_idx, cudaStream_t stream) {
+  kda_status st = check_params(p);
+  if (st != KDA_OK) return st;
+  if (n_seqs < 0 || n_seqs > 65535 || K < 1 || K > 64 || n_slots < 0) return KDA_ERR_INVALID_ARG;
+  if (n_seqs == 0) return KDA_OK;
+  if (!step_states || !accept_len || !state) return KDA_ERR_INVALID_ARG;
+  if (!slot_idx && n_slots < n_seqs) return KDA_ERR_INVALID_ARG;
+  if (!aligned16(step_states) || !aligned16(state) || !opt_aligned16(slot_idx))
+    return KDA_ERR_INVALID_ARG;
+  return finish(kda::launch_state_accept(step_states, state, accept_len, slot_idx, n_slots,
+                                         n_seqs, K, p->H, p->d_k, p->state_dtype == KDA_BF16,
+                                         device_error_ptr(), stream),
+                1);
 }
 
 kda_status kda_check_device_error(cudaStream_t stream) {
@@ -299,7 +353,7 @@ kda_status kda_check_device_error(cudaStream_t stream) {
     const int zero = 0;
     if (cudaMemcpy(ptr, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
       return KDA_ERR_CUDA;
-    return KDA_ERR_TIMEOUT;
+    return (host & kda::ERR_MBAR_TIMEOUT) ? KDA_ERR_TIMEOUT : KDA_ERR_BAD_INDEX;
   }
   return KDA_OK;
 }

@@ -1,6 +1,8 @@
 // kda_common.cuh -- small device helpers shared by the KDA kernels (sm_103a only).
 #pragma once
 
+#include "kda_internal.h"
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -11,7 +13,7 @@ namespace kda {
 typedef __nv_bfloat16 bf16;
 
 // Sticky device error bits (written by kernels whose bounded waits ran out).
-enum : int { ERR_MBAR_TIMEOUT = 1, ERR_BAD_SEQLEN = 2 };
+// device error flag bits (ERR_*): kda_internal.h
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }

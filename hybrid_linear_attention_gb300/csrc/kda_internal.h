@@ -7,6 +7,9 @@
 
 namespace kda {
 
+// bits of the library's sticky device error flag
+enum : int { ERR_MBAR_TIMEOUT = 1, ERR_BAD_SEQLEN = 2, ERR_BAD_INDEX = 4 };
+
 // Token-serial recurrence (decode, and the exact-fp32 prefill path).
 struct RecArgs {
   int H, n_seqs;
@@ -19,6 +22,9 @@ struct RecArgs {
   void *conv_state;            // [slots, 3, 3HD] io, updated in place
   const int32_t *cu_seqlens;   // prefill: [N + 1]; nullptr for decode (seq n = token n)
   const int32_t *slot_idx;     // decode: state/conv slot of each sequence, or nullptr
+  int n_slots;                 // slots in the state pool (slot indices are checked against it)
+  int tokens_per_seq;          // decode: tokens per sequence (rows n*K .. n*K+K-1); 0 = one
+  void *step_states;           // decode: [N*K, H, D, D] state after each token, or nullptr
   const void *state_in;        // [N or slots, H, D, D] state dtype, or nullptr (zeros)
   void *state_out;             // same layout, or nullptr; may equal state_in
   const void *gate;            // [T, H, D] io or nullptr
@@ -43,7 +49,8 @@ struct ProArgs {
 };
 
 struct ConvArgs {
-  int n_seqs, channels;
+  int n_seqs, channels, n_slots;
+  int *err;
   const void *x_new;           // [N, C]
   const void *conv_w;          // [C, 4]
   void *conv_state;            // [slots, 3, C]
@@ -53,6 +60,10 @@ struct ConvArgs {
 
 cudaError_t launch_recurrent(const RecArgs &a, int D, bool io_bf16, bool st_bf16,
                              cudaStream_t s);
+// pool[slot(n)] <- step_states[n*K + accept[n] - 1] for accept[n] in 1..K (0: unchanged)
+cudaError_t launch_state_accept(const void *step_states, void *pool, const int32_t *accept,
+                                const int32_t *slot_idx, int n_slots, int n_seqs, int K, int H,
+                                int D, bool st_bf16, int *err, cudaStream_t s);
 cudaError_t launch_prologue(const ProArgs &a, int D, bool io_bf16, cudaStream_t s);
 cudaError_t launch_conv_update(const ConvArgs &a, bool io_bf16, cudaStream_t s);
 

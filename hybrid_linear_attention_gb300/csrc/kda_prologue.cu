@@ -201,6 +201,10 @@ __global__ void conv_update_kernel(const ConvArgs a) {
   if (c >= a.channels) return;
   const int C = a.channels;
   const int slot = a.slot_idx ? a.slot_idx[n] : n;
+  if (slot < 0 || slot >= a.n_slots) {  // an index outside the pool: flagged, skipped
+    if (c == 0 && a.err) atomicOr(a.err, ERR_BAD_INDEX);
+    return;
+  }
   IO *st = reinterpret_cast<IO *>(a.conv_state) + (int64_t)slot * 3 * C + c;
   const IO *cw = reinterpret_cast<const IO *>(a.conv_w) + 4 * (int64_t)c;
   const IO x0 = st[0], x1 = st[C], x2 = st[2 * C];

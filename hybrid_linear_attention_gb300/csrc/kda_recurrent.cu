@@ -9,6 +9,13 @@
 //     o  = scale S^T q = scale (S'^T q + u (k.q))
 // so one pass over S gives both column reductions (S'^T k and S'^T q) and the update.
 //
+// Decode takes one token per sequence, or K tokens (the draft of a speculative step, with the
+// state after each token kept for rollback: "Ling-3.1-flash: Grouped Routing and Two
+// Different MLA Caches", section "KDA replaces a token list with a recurrent matrix", counts
+// speculative rollback state among the per-sequence costs; "Ling-3.1-flash: What 63
+// Linear-Attention Layers Do to the KV Budget", section "Where the hybrid makes serving
+// harder", reports the MTP acceptance lengths).
+//
 // Layout of the work: one CTA per (head, sequence) for prefill; for decode a persistent grid
 // (as many CTAs as fit on the device) walks the (sequence, head) units in strides and asks L2
 // for the next unit's state and inputs before it works on the current one, so the state
@@ -64,25 +71,26 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
       eos = a.cu_seqlens[n + 1];
       slot = n;
     } else {
-      bos = n;
-      eos = n + 1;
+      const int K = a.tokens_per_seq > 0 ? a.tokens_per_seq : 1;
+      bos = (int64_t)n * K;
+      eos = bos + K;
       slot = a.slot_idx ? a.slot_idx[n] : n;
       const int64_t nx = unit + stride;  // this CTA's next unit: state and inputs into L2
       if (nx < units) {
         const int hn = (int)(nx % H), nn = (int)(nx / H);
         const int sn = a.slot_idx ? a.slot_idx[nn] : nn;
-        if (a.state_in)
+        if (a.state_in && sn >= 0 && sn < a.n_slots)
           prefetch_span(reinterpret_cast<const ST *>(a.state_in) + ((size_t)sn * H + hn) * D * D,
                         sizeof(ST) * D * D, tid, NT);
         if (tid < 3) {
           const size_t C3 = (size_t)3 * H * D, ch = (size_t)tid * H * D + (size_t)hn * D;
-          if (CONV) {
+          if (CONV && sn >= 0 && sn < a.n_slots) {
             const IO *cs = reinterpret_cast<const IO *>(a.conv_state) + (size_t)sn * 3 * C3 + ch;
             for (int r = 0; r < 3; ++r) prefetch_span(cs + r * C3, sizeof(IO) * D, 0, 1);
             prefetch_span(reinterpret_cast<const IO *>(a.x_raw) + (size_t)nn * C3 + ch,
                           sizeof(IO) * D, 0, 1);
           }
-          const size_t row = ((size_t)nn * H + hn) * D;
+          const size_t row = ((size_t)nn * K * H + hn) * D;
           if (tid == 0) prefetch_span(a.g + row, sizeof(float) * D, 0, 1);
           if (tid == 1 && GATE) prefetch_span(reinterpret_cast<const IO *>(a.gate) + row,
                                               sizeof(IO) * D, 0, 1);
@@ -90,19 +98,23 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
       }
     }
     if (eos < bos) eos = bos;  // a decreasing offset pair processes nothing
+    if (slot < 0 || slot >= a.n_slots) {  // an index outside the pool: flagged, unit skipped
+      if (tid == 0 && a.err) atomicOr(a.err, ERR_BAD_INDEX);
+      continue;
+    }
 
     // ---- load this head's state tile into registers --------------------------------------
     float S[RPT][4];
     const size_t sbase = ((size_t)slot * H + h) * (size_t)D * D;
     if (a.state_in) {
       const ST *src = reinterpret_cast<const ST *>(a.state_in) + sbase;
-  #pragma unroll
+#pragma unroll
       for (int r = 0; r < RPT; ++r) {
         const float4 x = load4(src + (size_t)(rg * RPT + r) * D + 4 * cg);
         S[r][0] = x.x, S[r][1] = x.y, S[r][2] = x.z, S[r][3] = x.w;
       }
     } else {
-  #pragma unroll
+#pragma unroll
       for (int r = 0; r < RPT; ++r) S[r][0] = S[r][1] = S[r][2] = S[r][3] = 0.f;
     }
 
@@ -121,7 +133,7 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
         const IO *cw = reinterpret_cast<const IO *>(a.conv_w);
         IO *cs = reinterpret_cast<IO *>(a.conv_state) + (size_t)slot * 3 * C;
         if (tid < D) {
-  #pragma unroll
+#pragma unroll
           for (int st = 0; st < 3; ++st) {
             const int ch = st * H * D + h * D + tid;
             const IO x0 = cs[ch], x1 = cs[C + ch], x2 = cs[2 * C + ch], xn = xr[ch];
@@ -169,24 +181,24 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
       for (int tt = 0; tt < nt; ++tt) {
         const float rq = s_rq[tt], rk = s_rk[tt];
         float pp[4] = {0.f, 0.f, 0.f, 0.f}, po[4] = {0.f, 0.f, 0.f, 0.f};
-  #pragma unroll
+#pragma unroll
         for (int r = 0; r < RPT; ++r) {
           const int i = rg * RPT + r;
           const float al = s_a[tt][i], kk = s_k[tt][i] * rk, qq = s_q[tt][i] * rq;
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < 4; ++c) {
             S[r][c] *= al;
             pp[c] = fmaf(S[r][c], kk, pp[c]);
             po[c] = fmaf(S[r][c], qq, po[c]);
           }
         }
-  #pragma unroll
+#pragma unroll
         for (int c = 0; c < 4; ++c) s_redp[rg][4 * cg + c] = pp[c], s_redo[rg][4 * cg + c] = po[c];
         __syncthreads();
         float o = 0.f;
         if (tid < D) {
           float p = 0.f, o1 = 0.f;
-  #pragma unroll
+#pragma unroll
           for (int g2 = 0; g2 < RG; ++g2) p += s_redp[g2][tid], o1 += s_redo[g2][tid];
           const float u = s_beta[tt] * (s_v[tt][tid] - p);
           s_u[tid] = u;
@@ -197,17 +209,24 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
           if (lane == 0) s_ss[warp] = ss;
         }
         __syncthreads();
-  #pragma unroll
+#pragma unroll
         for (int r = 0; r < RPT; ++r) {
           const float kk = s_k[tt][rg * RPT + r] * rk;
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < 4; ++c) S[r][c] = fmaf(kk, s_u[4 * cg + c], S[r][c]);
+        }
+        if (a.step_states) {  // the state after this token (speculative rollback points)
+          ST *dst = reinterpret_cast<ST *>(a.step_states) + ((size_t)(t0 + tt) * H + h) * D * D;
+#pragma unroll
+          for (int r = 0; r < RPT; ++r)
+            store4(dst + (size_t)(rg * RPT + r) * D + 4 * cg,
+                   make_float4(S[r][0], S[r][1], S[r][2], S[r][3]));
         }
         if (tid < D) {
           const size_t row = ((size_t)(t0 + tt) * H + h) * D + tid;
           if (GATE) {
             float ss = 0.f;
-  #pragma unroll
+#pragma unroll
             for (int w = 0; w < (D + 31) / 32; ++w) ss += s_ss[w];
             const float r = rsqrtf(ss / D + a.norm_eps);
             const float w = a.norm_w ? a.norm_w[tid] : 1.f;
@@ -221,7 +240,7 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
 
     if (a.state_out) {
       ST *dst = reinterpret_cast<ST *>(a.state_out) + sbase;
-  #pragma unroll
+#pragma unroll
       for (int r = 0; r < RPT; ++r)
         store4(dst + (size_t)(rg * RPT + r) * D + 4 * cg,
                make_float4(S[r][0], S[r][1], S[r][2], S[r][3]));
@@ -264,7 +283,37 @@ cudaError_t launch_d(const RecArgs &a, bool io_bf16, bool st_bf16, cudaStream_t 
   return st_bf16 ? launch_typed<D, NT, float, bf16>(a, s) : launch_typed<D, NT, float, float>(a, s);
 }
 
+// Commit accepted speculative steps: for sequence n and head h, pool[slot(n), h] <-
+// step_states[n*K + accept[n] - 1, h] when 1 <= accept[n] <= K; 0 keeps the pool state.
+// Raw 16-byte copies (bit-exact).  Indices outside their range are flagged and skipped.
+__global__ void state_accept_kernel(const uint4 *step, uint4 *pool, const int32_t *accept,
+                                    const int32_t *slot_idx, int n_slots, int K, int H,
+                                    int vec_per_head, int *err) {
+  const int h = blockIdx.x, n = blockIdx.y;
+  const int acc = accept[n];
+  const int slot = slot_idx ? slot_idx[n] : n;
+  if (acc < 0 || acc > K || slot < 0 || slot >= n_slots) {
+    if (threadIdx.x == 0 && err) atomicOr(err, ERR_BAD_INDEX);
+    return;
+  }
+  if (acc == 0) return;
+  const uint4 *src = step + (((size_t)n * K + acc - 1) * H + h) * vec_per_head;
+  uint4 *dst = pool + ((size_t)slot * H + h) * vec_per_head;
+  for (int e = threadIdx.x; e < vec_per_head; e += blockDim.x) dst[e] = src[e];
+}
+
 }  // namespace
+
+cudaError_t launch_state_accept(const void *step_states, void *pool, const int32_t *accept,
+                                const int32_t *slot_idx, int n_slots, int n_seqs, int K, int H,
+                                int D, bool st_bf16, int *err, cudaStream_t s) {
+  if (n_seqs == 0) return cudaSuccess;
+  const int vec = D * D * (st_bf16 ? 2 : 4) / 16;
+  state_accept_kernel<<<dim3(H, n_seqs), 256, 0, s>>>(
+      reinterpret_cast<const uint4 *>(step_states), reinterpret_cast<uint4 *>(pool), accept,
+      slot_idx, n_slots, K, H, vec, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_recurrent(const RecArgs &a, int D, bool io_bf16, bool st_bf16,
                              cudaStream_t s) {

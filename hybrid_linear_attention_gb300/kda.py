@@ -26,7 +26,8 @@ _TORCH_OF = {KDA_F32: torch.float32, KDA_BF16: torch.bfloat16}
 EXPORTS = (
     "kda_params_default", "kda_status_string", "kda_state_bytes", "kda_prefill_workspace_size",
     "kda_prologue", "kda_prefill", "kda_decode_step", "kda_conv_state_update",
-    "kda_decode_step_fused", "kda_check_device_error", "kda_launch_count",
+    "kda_decode_step_fused", "kda_decode_multi", "kda_state_accept", "kda_check_device_error",
+    "kda_launch_count",
 )
 
 
@@ -84,6 +85,9 @@ def load():
                                              _vp]),
             "kda_decode_step_fused": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32,
                                              _vp, _vp, _vp, _vp]),
+            "kda_decode_multi": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
+                                        _vp, _vp, _vp, _vp, _i32, _vp]),
+            "kda_state_accept": (_i32, [_P, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp]),
             "kda_check_device_error": (_i32, [_vp]),
             "kda_launch_count": (ctypes.c_uint64, []),
         }
@@ -208,6 +212,31 @@ def kda_decode_step_fused(p, x_raw, conv_w, conv_state, g, beta, state, out, *, 
         _ptr(gate_logit, io, "gate_logit"), _ptr(norm_w, torch.float32, "norm_w"),
         _ptr(out, io, "out"), _stream(stream))
     _check(st, "kda_decode_step_fused")
+
+
+def kda_decode_multi(p, q, k, v, g, beta, state, out, K, *, slot_idx=None, gate_logit=None,
+                     norm_w=None, step_states=None, commit_final=False, stream=None):
+    """K tokens per sequence: q, k, v, g, beta, out, gate_logit have n_seqs * K rows."""
+    io, sd = p.io_torch, p.state_torch
+    if q.shape[0] % K:
+        raise ValueError("rows must be n_seqs * K")
+    st = load().kda_decode_multi(
+        ctypes.byref(p), _ptr(q, io, "q"), _ptr(k, io, "k"), _ptr(v, io, "v"),
+        _ptr(g, torch.float32, "g"), _ptr(beta, torch.float32, "beta"),
+        _ptr(state, sd, "state"), state.shape[0], _ptr(slot_idx, torch.int32, "slot_idx"),
+        q.shape[0] // K, K, _ptr(gate_logit, io, "gate_logit"),
+        _ptr(norm_w, torch.float32, "norm_w"), _ptr(out, io, "out"),
+        _ptr(step_states, sd, "step_states"), 1 if commit_final else 0, _stream(stream))
+    _check(st, "kda_decode_multi")
+
+
+def kda_state_accept(p, step_states, accept_len, state, K, *, slot_idx=None, stream=None):
+    sd = p.state_torch
+    st = load().kda_state_accept(
+        ctypes.byref(p), _ptr(step_states, sd, "step_states"), accept_len.shape[0], K,
+        _ptr(accept_len, torch.int32, "accept_len"), _ptr(state, sd, "state"), state.shape[0],
+        _ptr(slot_idx, torch.int32, "slot_idx"), _stream(stream))
+    _check(st, "kda_state_accept")
 
 
 def kda_conv_state_update(p, x_new, conv_w, conv_state, y, *, slot_idx=None, stream=None):

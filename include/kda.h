@@ -57,7 +57,8 @@ typedef enum {
   KDA_ERR_UNSUPPORTED = -2,
   KDA_ERR_CUDA = -3,
   KDA_ERR_WORKSPACE = -4,
-  KDA_ERR_TIMEOUT = -5
+  KDA_ERR_TIMEOUT = -5,
+  KDA_ERR_BAD_INDEX = -6
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -145,7 +146,8 @@ kda_status kda_prefill(const kda_params* p, const void* q, const void* k, const 
  *   g           [n_seqs, H, d] fp32 log-retention; beta [n_seqs, H] fp32.
  *   state       [n_slots, H, d, d] state_dtype pool, updated in place.
  *   slot_idx    [n_seqs] int32 (device): sequence n uses state slot slot_idx[n]; NULL means
- *               slot n.  Slots must be distinct and in [0, n_slots).
+ *               slot n.  Slots must be distinct; a slot outside [0, n_slots) is skipped and
+ *               reported by kda_check_device_error (KDA_ERR_BAD_INDEX).
  *   gate_logit  [n_seqs, H, d] io_dtype or NULL; norm_w [d] fp32 or NULL.
  *   out         [n_seqs, H, d] io_dtype.
  * Each head's state is read from HBM once and written once.
@@ -179,9 +181,49 @@ kda_status kda_decode_step_fused(const kda_params* p, const void* x_raw, const v
                                  const void* gate_logit, const float* norm_w, void* out,
                                  cudaStream_t stream);
 
+/*
+ * kda_decode_multi -- K tokens for each of n_seqs sequences (a speculative draft), from the
+ * state in its pool slot, keeping the state after every token for rollback.  The pages
+ * count speculative rollback state among the per-sequence costs of a KDA layer
+ * ("Ling-3.1-flash: Grouped Routing and Two Different MLA Caches", section "KDA replaces a
+ * token list with a recurrent matrix") and report MTP acceptance lengths of 2.1-2.6 tokens
+ * ("Ling-3.1-flash: What 63 Linear-Attention Layers Do to the KV Budget", section "Where the
+ * hybrid makes serving harder").  No counterpart interface is printed on the pages.
+ *
+ *   q, k, v, gate_logit, out [n_seqs * K, H, d] io_dtype, sequence-major (row n*K + i is
+ *               token i of sequence n); g [n_seqs * K, H, d] fp32; beta [n_seqs * K, H] fp32.
+ *   state       [n_slots, H, d, d] state_dtype pool: read; written with the state after all
+ *               K tokens only when commit_final is nonzero.
+ *   slot_idx    as in kda_decode_step.
+ *   K           1..64.
+ *   step_states [n_seqs * K, H, d, d] state_dtype or NULL: the state after token i of
+ *               sequence n at row n*K + i.  At least one of step_states / commit_final.
+ * Token by token the result equals K calls of kda_decode_step.  Slot indices outside
+ * [0, n_slots) are skipped and reported by kda_check_device_error (KDA_ERR_BAD_INDEX).
+ */
+kda_status kda_decode_multi(const kda_params* p, const void* q, const void* k, const void* v,
+                            const float* g, const float* beta, void* state, int n_slots,
+                            const int32_t* slot_idx, int n_seqs, int K, const void* gate_logit,
+                            const float* norm_w, void* out, void* step_states, int commit_final,
+                            cudaStream_t stream);
+
+/*
+ * kda_state_accept -- commit the accepted part of a speculative step: for every sequence n
+ * and head, state[slot(n)] <- step_states[n*K + accept_len[n] - 1] when
+ * 1 <= accept_len[n] <= K; accept_len[n] == 0 leaves the pool state as it was.  Bit-exact
+ * copies.
+ *   step_states [n_seqs * K, H, d, d] from kda_decode_multi; accept_len [n_seqs] int32
+ *   (device); state, n_slots, slot_idx as in kda_decode_step.  Out-of-range accept lengths
+ *   or slots are skipped and reported by kda_check_device_error (KDA_ERR_BAD_INDEX).
+ * No counterpart interface is printed on the pages.
+ */
+kda_status kda_state_accept(const kda_params* p, const void* step_states, int n_seqs, int K,
+                            const int32_t* accept_len, void* state, int n_slots,
+                            const int32_t* slot_idx, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the library's sticky device error flag
- * (set when a bounded device wait ran out).  Returns KDA_OK, KDA_ERR_TIMEOUT or
- * KDA_ERR_CUDA. */
+ * (set when a bounded device wait ran out, or a device-side index was out of range).
+ * Returns KDA_OK, KDA_ERR_TIMEOUT, KDA_ERR_BAD_INDEX or KDA_ERR_CUDA. */
 kda_status kda_check_device_error(cudaStream_t stream);
 
 /* Number of kernels the library launched since load (host-side counter, for benchmarks). */

@@ -115,3 +115,28 @@ def test_workspace_query(lib):
     assert kda.kda_prefill_workspace_size(p, 32, 500_000) == 0
     bad = kda.params(d=64)
     assert kda.kda_prefill_workspace_size(bad, 1, 10) == 0
+
+
+def test_multi_decode_and_accept_reject_bad_arguments_on_host(lib):
+    p = kda.params(H=2, d=128)
+    buf = ctypes.c_void_p(16)  # never dereferenced: every call fails validation first
+    vp = lambda: buf
+    # K outside 1..64
+    for K in (0, 65):
+        st = lib.kda_decode_multi(ctypes.byref(p), vp(), vp(), vp(), vp(), vp(), vp(), 4, None,
+                                  2, K, None, None, vp(), vp(), 1, None)
+        assert st == -1
+    # neither step states nor a committed final state: nothing would be kept
+    st = lib.kda_decode_multi(ctypes.byref(p), vp(), vp(), vp(), vp(), vp(), vp(), 4, None, 2, 3,
+                              None, None, vp(), None, 0, None)
+    assert st == -1
+    # misaligned step states
+    st = lib.kda_decode_multi(ctypes.byref(p), vp(), vp(), vp(), vp(), vp(), vp(), 4, None, 2, 3,
+                              None, None, vp(), ctypes.c_void_p(24), 1, None)
+    assert st == -1
+    # accept: too few slots without an index, bad K, null pointers
+    assert lib.kda_state_accept(ctypes.byref(p), vp(), 5, 3, vp(), vp(), 4, None, None) == -1
+    assert lib.kda_state_accept(ctypes.byref(p), vp(), 2, 0, vp(), vp(), 4, None, None) == -1
+    assert lib.kda_state_accept(ctypes.byref(p), None, 2, 3, vp(), vp(), 4, None, None) == -1
+    assert lib.kda_state_accept(ctypes.byref(p), vp(), 0, 3, None, None, 0, None, None) == 0
+    assert lib.kda_status_string(-6).decode().startswith("KDA_ERR_BAD_INDEX")
