@@ -348,9 +348,10 @@ def run_ours(args):
     e2e_line = _e2e(wl, flush, args, dist) if not args.no_e2e else None
 
     # ---- decode: 256 sequences x 100 fused steps --------------------------------------
-    dec = None
+    dec = dmulti = None
     if not args.no_decode:
         dec = _decode_bench(dev, kda, inputs, hbm, rank, args)
+        dmulti = _decode_multi_bench(dev, kda, inputs, hbm, rank)
 
     if rank != 0:
         return
@@ -383,6 +384,8 @@ def run_ours(args):
         line["e2e"] = e2e_line
     if dec:
         line["decode"] = dec
+    if dmulti:
+        line["decode_multi"] = dmulti
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = _cpu_baseline()
     print(json.dumps(line), flush=True)
@@ -453,6 +456,51 @@ def _decode_bench(dev, kda, inputs, hbm, rank, args):
                          "traffic": _profiled_traffic("kda_decode_fused_N256_H64.md",
                                                       ["kda_recurrent.cu", "kda_common.cuh"]),
                          "algorithmic_bytes_per_launch": b}}
+
+
+def _decode_multi_bench(dev, kda, inputs, hbm, rank):
+    """Speculative draft: 256 sequences x K=3 tokens, state after every token kept (fp32),
+    then the commit of the accepted steps."""
+    n, K, reps = N_DECODE, 3, 20
+    p = kda.params(H=H, d=D)
+    rows = n * K
+    pool = inputs.normal((n, H, D, D), seed=400 + rank, device=dev, dtype=torch.float32,
+                         std=0.02)
+    q = inputs.normal((rows, H, D), seed=401 + rank, device=dev)
+    k = inputs.normal((rows, H, D), seed=402 + rank, device=dev)
+    v = inputs.normal((rows, H, D), seed=403 + rank, device=dev)
+    g = inputs.uniform((rows, H, D), -5.0, 0.0, seed=404 + rank, device=dev)
+    beta = inputs.beta_draw((rows, H), seed=405 + rank, device=dev)
+    out = torch.empty((rows, H, D), dtype=torch.bfloat16, device=dev)
+    steps = torch.empty((rows, H, D, D), dtype=torch.float32, device=dev)
+    acc = (torch.arange(n, device=dev, dtype=torch.int32) % (K + 1)).contiguous()
+    for _ in range(3):
+        kda.kda_decode_multi(p, q, k, v, g, beta, pool, out, K, step_states=steps)
+    torch.cuda.synchronize()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    e0.record()
+    for _ in range(reps):
+        kda.kda_decode_multi(p, q, k, v, g, beta, pool, out, K, step_states=steps)
+    e1.record()
+    for _ in range(reps):
+        kda.kda_state_accept(p, steps, acc, pool, K)
+    e2.record()
+    e2.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    ms_acc = e1.elapsed_time(e2) / reps
+    st = n * H * D * D * 4
+    b = st * (1 + K) + rows * H * (3 * D * 2 + D * 4 + 4 + D * 2)
+    acc_bytes = 2 * st * int((acc > 0).sum().item()) // n
+    gbs = b / (ms * 1e-3) / 1e9
+    return {"metric": "KDA speculative draft GB/s", "value": gbs, "unit": "GB/s",
+            "workload": "256 sequences x K=3 draft tokens, H=64, d=128, fp32 state pool (1 GiB) "
+                        "read once, fp32 state after every token written (3 GiB)",
+            "ms_per_call": ms, "tokens_per_s": rows / (ms * 1e-3),
+            "roofline": {"kernel": "kda_decode_multi", "bound": "hbm", "achieved": gbs,
+                         "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                         "algorithmic_bytes_per_launch": b},
+            "accept": {"ms_per_call": ms_acc, "bytes": acc_bytes,
+                       "gbs": acc_bytes / (ms_acc * 1e-3) / 1e9}}
 
 
 def main():
