@@ -92,6 +92,8 @@ const char *kda_status_string(kda_status s) {
     case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace too small";
     case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device wait ran out";
     case KDA_ERR_BAD_INDEX: return "KDA_ERR_BAD_INDEX: a device-side index was out of range";
+    case KDA_ERR_BAD_SEQLENS:
+      return "KDA_ERR_BAD_SEQLENS: device-side sequence offsets outside the token rows";
   }
   return "unknown kda_status";
 }
@@ -142,17 +144,19 @@ kda_status kda_prologue(const kda_params *p, const void *x_raw, const void *conv
   a.g_raw = g_raw;
   a.q = q, a.k = k, a.v = v;
   a.beta = beta, a.g = g;
+  a.err = device_error_ptr();
   const int n_launch = (total_tokens > 0 ? 1 + ((g_raw || beta_logit) ? 1 : 0) : 0) +
                        (conv_state ? 1 : 0);
   return finish(kda::launch_prologue(a, p->d_k, p->io_dtype == KDA_BF16, stream), n_launch);
 }
 
-kda_status kda_prefill(const kda_params *p, const void *q, const void *k, const void *v,
-                       const float *g, const float *beta, const void *init_state,
-                       const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
-                       const void *gate_logit, const float *norm_w, void *out,
-                       void *final_state, void *workspace, size_t ws_bytes,
-                       cudaStream_t stream) {
+static kda_status prefill_impl(const kda_params *p, const void *q, const void *k, const void *v,
+                               const float *g, const float *beta, const void *init_state,
+                               const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
+                               const void *gate_logit, const float *norm_w, void *out,
+                               void *final_state, const int32_t *ckpt_cu,
+                               const int32_t *ckpt_pos, int n_ckpt, void *ckpt_states,
+                               void *workspace, size_t ws_bytes, cudaStream_t stream) {
   kda_status st = check_params(p);
   if (st != KDA_OK) return st;
   if (n_seqs < 0 || total_tokens < 0 || n_seqs > 65535) return KDA_ERR_INVALID_ARG;
@@ -167,6 +171,11 @@ kda_status kda_prefill(const kda_params *p, const void *q, const void *k, const 
       !opt_aligned16(gate_logit) || !opt_aligned16(norm_w) || !opt_aligned16(out) ||
       !opt_aligned16(final_state))
     return KDA_ERR_INVALID_ARG;
+  if (n_ckpt < 0) return KDA_ERR_INVALID_ARG;
+  if (n_ckpt > 0 && (!ckpt_cu || !ckpt_pos || !ckpt_states || !aligned16(ckpt_states) ||
+                     !aligned16(ckpt_cu) || !aligned16(ckpt_pos)))
+    return KDA_ERR_INVALID_ARG;
+  if (n_ckpt == 0) ckpt_cu = nullptr;
 
   const bool io_bf16 = p->io_dtype == KDA_BF16, st_bf16 = p->state_dtype == KDA_BF16;
   if (kda::prefill_tc_supported(p->d_k, io_bf16)) {
@@ -186,6 +195,8 @@ kda_status kda_prefill(const kda_params *p, const void *q, const void *k, const 
     t.gate = gate_logit;
     t.norm_w = norm_w;
     t.out = out;
+    t.ckpt_cu = ckpt_cu, t.ckpt_pos = ckpt_pos, t.ckpt_states = ckpt_states;
+    t.total = total_tokens, t.n_ckpt = n_ckpt;
     t.err = device_error_ptr();
     return finish(kda::launch_prefill_tc(t, total_tokens, st_bf16, stream), 1);
   }
@@ -199,7 +210,55 @@ kda_status kda_prefill(const kda_params *p, const void *q, const void *k, const 
   a.gate = gate_logit;
   a.norm_w = norm_w;
   a.out = out;
+  a.ckpt_cu = ckpt_cu, a.ckpt_pos = ckpt_pos, a.ckpt_states = ckpt_states;
+  a.total = total_tokens, a.n_ckpt = n_ckpt;
   return finish(kda::launch_recurrent(a, p->d_k, io_bf16, st_bf16, stream), 1);
+}
+
+kda_status kda_prefill(const kda_params *p, const void *q, const void *k, const void *v,
+                       const float *g, const float *beta, const void *init_state,
+                       const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
+                       const void *gate_logit, const float *norm_w, void *out,
+                       void *final_state, void *workspace, size_t ws_bytes,
+                       cudaStream_t stream) {
+  return prefill_impl(p, q, k, v, g, beta, init_state, cu_seqlens, n_seqs, total_tokens,
+                      gate_logit, norm_w, out, final_state, nullptr, nullptr, 0, nullptr,
+                      workspace, ws_bytes, stream);
+}
+
+kda_status kda_prefill_checkpointed(const kda_params *p, const void *q, const void *k,
+                                    const void *v, const float *g, const float *beta,
+                                    const void *init_state, const int32_t *cu_seqlens,
+                                    int n_seqs, int64_t total_tokens, const void *gate_logit,
+                                    const float *norm_w, void *out, void *final_state,
+                                    const int32_t *ckpt_cu, const int32_t *ckpt_pos,
+                                    int n_ckpt, void *ckpt_states, void *workspace,
+                                    size_t ws_bytes, cudaStream_t stream) {
+  if (n_ckpt < 1) return KDA_ERR_INVALID_ARG;
+  return prefill_impl(p, q, k, v, g, beta, init_state, cu_seqlens, n_seqs, total_tokens,
+                      gate_logit, norm_w, out, final_state, ckpt_cu, ckpt_pos, n_ckpt,
+                      ckpt_states, workspace, ws_bytes, stream);
+}
+
+kda_status kda_conv_tail_checkpoints(const kda_params *p, const void *x_raw,
+                                     const void *conv_state, const int32_t *cu_seqlens,
+                                     int n_seqs, int64_t total_tokens, const int32_t *ckpt_cu,
+                                     const int32_t *ckpt_pos, int n_ckpt, void *conv_ckpt,
+                                     cudaStream_t stream) {
+  kda_status st = check_params(p);
+  if (st != KDA_OK) return st;
+  if (n_seqs < 1 || n_seqs > 65535 || n_ckpt < 0 || n_ckpt > 65535) return KDA_ERR_INVALID_ARG;
+  if (n_ckpt == 0) return KDA_OK;
+  if (!x_raw || !cu_seqlens || !ckpt_cu || !ckpt_pos || !conv_ckpt) return KDA_ERR_INVALID_ARG;
+  if (!aligned16(x_raw) || !opt_aligned16(conv_state) || !aligned16(cu_seqlens) ||
+      !aligned16(ckpt_cu) || !aligned16(ckpt_pos) || !aligned16(conv_ckpt))
+    return KDA_ERR_INVALID_ARG;
+  const int channels = 3 * p->H * p->d_k;
+  if (total_tokens < 0) return KDA_ERR_INVALID_ARG;
+  return finish(kda::launch_conv_ckpt(x_raw, conv_state, cu_seqlens, n_seqs, total_tokens,
+                                      ckpt_cu, ckpt_pos, n_ckpt, channels, conv_ckpt,
+                                      p->io_dtype == KDA_BF16, device_error_ptr(), stream),
+                1);
 }
 
 static kda_status decode_common(const kda_params *p, const float *g, const float *beta,
@@ -312,6 +371,7 @@ kda_status kda_decode_multi(const kda_params *p, const void *q, const void *k, c
   a.n_seqs = n_seqs;
   a.n_slots = n_slots;
   a.tokens_per_seq = K;
+  a.total = (int64_t)n_seqs * K;
   a.q = q, a.k = k, a.v = v, a.g = g, a.beta = beta;
   a.slot_idx = slot_idx;
   a.state_in = state;
@@ -353,7 +413,8 @@ kda_status kda_check_device_error(cudaStream_t stream) {
     const int zero = 0;
     if (cudaMemcpy(ptr, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
       return KDA_ERR_CUDA;
-    return (host & kda::ERR_MBAR_TIMEOUT) ? KDA_ERR_TIMEOUT : KDA_ERR_BAD_INDEX;
+    if (host & kda::ERR_MBAR_TIMEOUT) return KDA_ERR_TIMEOUT;
+    return (host & kda::ERR_BAD_INDEX) ? KDA_ERR_BAD_INDEX : KDA_ERR_BAD_SEQLENS;
   }
   return KDA_OK;
 }

@@ -23,8 +23,13 @@ struct RecArgs {
   const int32_t *cu_seqlens;   // prefill: [N + 1]; nullptr for decode (seq n = token n)
   const int32_t *slot_idx;     // decode: state/conv slot of each sequence, or nullptr
   int n_slots;                 // slots in the state pool (slot indices are checked against it)
+  int64_t total;               // rows of q, k, v, g, out (sequence offsets are checked against it)
+  int n_ckpt;                  // checkpoints (checkpoint ranges are checked against it)
   int tokens_per_seq;          // decode: tokens per sequence (rows n*K .. n*K+K-1); 0 = one
   void *step_states;           // decode: [N*K, H, D, D] state after each token, or nullptr
+  const int32_t *ckpt_cu;      // prefill: checkpoints of sequence n are ckpt_cu[n] .. [n+1]
+  const int32_t *ckpt_pos;     // tokens of the sequence before each checkpoint
+  void *ckpt_states;           // [n_ckpt, H, D, D] state dtype
   const void *state_in;        // [N or slots, H, D, D] state dtype, or nullptr (zeros)
   void *state_out;             // same layout, or nullptr; may equal state_in
   const void *gate;            // [T, H, D] io or nullptr
@@ -46,6 +51,7 @@ struct ProArgs {
   const float *g_raw;          // [T, H, D] or nullptr
   void *q, *k, *v;             // [T, H, D]
   float *beta, *g;
+  int *err;
 };
 
 struct ConvArgs {
@@ -65,6 +71,11 @@ cudaError_t launch_state_accept(const void *step_states, void *pool, const int32
                                 const int32_t *slot_idx, int n_slots, int n_seqs, int K, int H,
                                 int D, bool st_bf16, int *err, cudaStream_t s);
 cudaError_t launch_prologue(const ProArgs &a, int D, bool io_bf16, cudaStream_t s);
+// out[k] <- the three raw inputs before checkpoint k (conv tail at that position)
+cudaError_t launch_conv_ckpt(const void *x, const void *conv_state, const int32_t *cu,
+                             int n_seqs, int64_t T, const int32_t *ckpt_cu,
+                             const int32_t *ckpt_pos, int n_ckpt, int channels, void *out,
+                             bool io_bf16, int *err, cudaStream_t s);
 cudaError_t launch_conv_update(const ConvArgs &a, bool io_bf16, cudaStream_t s);
 
 }  // namespace kda

@@ -229,9 +229,12 @@ __global__ void __launch_bounds__(NT, 1)
   const bool producer = PAIR && cluster_rank() == 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.H;
-  const int64_t bos = a.cu_seqlens[n];
+  int64_t bos = a.cu_seqlens[n];
   int64_t eos = a.cu_seqlens[n + 1];
-  if (eos < bos) eos = bos;
+  if (bos < 0 || eos > a.total || eos < bos) {  // offsets outside the rows: flagged, empty
+    if (threadIdx.x == 0 && a.err) atomicOr(a.err, ERR_BAD_SEQLEN);
+    bos = eos = 0;
+  }
   const int nchunks = (int)((eos - bos + C - 1) / C);
   const int quarter = warp & 3, grp = warp >> 2;   // TMEM lane quarter; warp group 0..2
   const int j = 32 * quarter + lane;               // this thread's TMEM lane
@@ -398,6 +401,36 @@ __global__ void __launch_bounds__(NT, 1)
   uint32_t mma_par = 0;
   if (ok && nchunks > 0 && grp == 2) p1(0, tid - 256);
   ok = sync();
+
+  // ---- prefix-state checkpoints: after chunk c (cnt tokens of the sequence done), warp group
+  //      2 writes S for every checkpoint placed there ("Ling-3.1-flash: What 63 Linear-
+  //      Attention Layers Do to the KV Budget", section "Where the hybrid makes serving
+  //      harder": a recurrent state can only be reused where a snapshot was saved).  A
+  //      checkpoint passed over (not on a chunk edge or the sequence end) is flagged. ------
+  int kc = a.ckpt_cu ? a.ckpt_cu[n] : 0;
+  int kend = a.ckpt_cu ? a.ckpt_cu[n + 1] : 0;
+  if (kc < 0 || kend > a.n_ckpt || kend < kc) {  // a range outside the checkpoints: flagged
+    if (tid == 0 && a.err) atomicOr(a.err, ERR_BAD_INDEX);
+    kc = kend = 0;
+  }
+  auto ckpt_write = [&](int64_t cnt) {
+    for (; kc < kend && a.ckpt_pos[kc] <= cnt; ++kc) {
+      if (a.ckpt_pos[kc] < cnt) {
+        if (tid == 256 && a.err) atomicOr(a.err, ERR_BAD_INDEX);
+        continue;
+      }
+      if (grp != 2) continue;
+      ST *dst = reinterpret_cast<ST *>(a.ckpt_states) + ((size_t)kc * H + h) * D * D;
+#pragma unroll 1
+      for (int g32 = 0; g32 < 4; ++g32) {
+        float v[32];
+        tmem_ld32(tm + lane_off + TM_S + 32 * g32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) dst[(size_t)(32 * g32 + x) * D + j] = from_f<ST>(v[x]);
+      }
+    }
+  };
 
   // ---- phases of one chunk (t0: first token, nv: valid tokens, par: chunk parity) -----
   auto ap_operands = [&](int nv, int nthr) {
@@ -900,6 +933,7 @@ __global__ void __launch_bounds__(NT, 1)
       mma_par ^= 1;
       tc_fence_after();
       p8(nv, t0, par);
+      ckpt_write((int64_t)c * C + nv);
       if (!(ok = sync())) break;
     }
   } else if (!producer) {
@@ -953,6 +987,7 @@ __global__ void __launch_bounds__(NT, 1)
       tc_fence_after();
       if (tid == 0) mbar_arrive_remote(bar(BAR_E0 + b), 1);  // landing buffer b is free
       p8(nv, t0, par);
+      ckpt_write((int64_t)c * C + nv);
       if (!(ok = sync())) break;
     }
   } else {
@@ -1005,6 +1040,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
   }
 
+  if (ok && !producer && kc < kend && tid == 0 && a.err) atomicOr(a.err, ERR_BAD_INDEX);
   if (tid == 0) bulk_wait0();  // output tiles written before the shared memory is released
 
   // ---- final state: S[i][j] = S^T[j][i] ------------------------------------------------

@@ -19,6 +19,11 @@ struct TcArgs {
   const void *gate;            // [T, H, 128] bf16 or nullptr
   const float *norm_w;         // [128] or nullptr
   void *out;                   // [T, H, 128] bf16
+  int64_t total;               // rows of q, k, v, g, out (sequence offsets are checked against it)
+  int n_ckpt;                  // checkpoints (checkpoint ranges are checked against it)
+  const int32_t *ckpt_cu;      // checkpoints of sequence n: ckpt_cu[n] .. ckpt_cu[n+1], or null
+  const int32_t *ckpt_pos;     // tokens of the sequence before each checkpoint
+  void *ckpt_states;           // [n_ckpt, H, 128, 128] state dtype
   int *err;
 };
 

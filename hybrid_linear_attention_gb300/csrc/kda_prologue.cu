@@ -96,12 +96,14 @@ __global__ void __launch_bounds__(PNT, 2) prologue_kernel(const ProArgs a) {
   }
   int n = seq_of_token(a.cu_seqlens, a.n_seqs, t0);
   int64_t bos = a.cu_seqlens[n], eos = a.cu_seqlens[n + 1];
+  if ((bos > t0 || eos <= t0) && threadIdx.x == 0 && a.err) atomicOr(a.err, ERR_BAD_SEQLEN);
   float win[3][8];
 #pragma unroll
   for (int k = 0; k < 3; ++k) {
     const int64_t src = t0 - 3 + k;
-    if (act && src >= bos) load8(x + src * C + c0, win[k]);
-    else if (act && cs) load8(cs + ((int64_t)n * 3 + 3 + (src - bos)) * C + c0, win[k]);
+    if (act && src >= bos && src >= 0) load8(x + src * C + c0, win[k]);
+    else if (act && cs && src >= bos - 3)
+      load8(cs + ((int64_t)n * 3 + 3 + (src - bos)) * C + c0, win[k]);
     else
 #pragma unroll
       for (int y = 0; y < 8; ++y) win[k][y] = 0.f;
@@ -125,7 +127,7 @@ __global__ void __launch_bounds__(PNT, 2) prologue_kernel(const ProArgs a) {
           ++n;
           bos = a.cu_seqlens[n];
           eos = a.cu_seqlens[n + 1];
-        } while (eos <= t);
+        } while (eos <= t && n + 1 < a.n_seqs);
 #pragma unroll
         for (int k = 0; k < 3; ++k) {
           if (act && cs) load8(cs + ((int64_t)n * 3 + k) * C + c0, win[k]);
@@ -177,11 +179,16 @@ __global__ void gate_act_kernel(const ProArgs a) {
 // New tail of sequence n: the last three raw inputs, reaching into the old tail when the
 // sequence is shorter than three; a length-0 sequence keeps its tail.  Raw element copies.
 template <typename E>
-__global__ void conv_tail_kernel(const E *x, E *cs, const int32_t *cu, int C) {
+__global__ void conv_tail_kernel(const E *x, E *cs, const int32_t *cu, int C, int64_t T,
+                                 int *err) {
   const int n = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= C) return;
   const int64_t bos = cu[n], eos = cu[n + 1];
+  if (bos < 0 || eos > T) {  // offsets outside the rows: flagged, tail kept
+    if (c == 0 && err) atomicOr(err, ERR_BAD_SEQLEN);
+    return;
+  }
   if (eos <= bos) return;
   E *st = cs + (int64_t)n * 3 * C + c;
   E nv[3];
@@ -192,6 +199,38 @@ __global__ void conv_tail_kernel(const E *x, E *cs, const int32_t *cu, int C) {
   }
 #pragma unroll
   for (int r = 0; r < 3; ++r) st[r * C] = nv[r];
+}
+
+// Conv tail at checkpoint k of sequence n (pos tokens in): the three raw inputs before it,
+// oldest first, reaching into the sequence's prior tail (zeros without one) when pos < 3.
+// Raw element copies.  A position outside 1..length is flagged and skipped.
+template <typename E>
+__global__ void conv_ckpt_kernel(const E *x, const E *cs, const int32_t *cu, int n_seqs,
+                                 const int32_t *ckpt_cu, const int32_t *ckpt_pos, int C,
+                                 int64_t T, E *out, int *err) {
+  const int kk = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= C) return;
+  int lo = 0, hi = n_seqs;  // sequence n with ckpt_cu[n] <= kk < ckpt_cu[n + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (ckpt_cu[mid] <= kk) lo = mid; else hi = mid;
+  }
+  const int n = lo;
+  const int64_t bos = cu[n], len = (int64_t)cu[n + 1] - bos, pos = ckpt_pos[kk];
+  if (bos < 0 || bos + len > T || pos < 1 || pos > len) {
+    if (c == 0 && err) atomicOr(err, ERR_BAD_INDEX);
+    return;
+  }
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    const int64_t src = pos - 3 + r;  // position within the sequence
+    E val;
+    if (src >= 0) val = x[(bos + src) * C + c];
+    else if (cs) val = cs[((int64_t)n * 3 + 3 + src) * C + c];
+    else val = E(0);
+    out[((int64_t)kk * 3 + r) * C + c] = val;
+  }
 }
 
 template <typename IO>
@@ -244,11 +283,11 @@ cudaError_t launch_pro(const ProArgs &a, cudaStream_t s) {
     if (sizeof(IO) == 2)
       conv_tail_kernel<uint16_t><<<grid, 256, 0, s>>>(
           reinterpret_cast<const uint16_t *>(a.x), reinterpret_cast<uint16_t *>(a.conv_state),
-          a.cu_seqlens, C);
+          a.cu_seqlens, C, a.T, a.err);
     else
       conv_tail_kernel<uint32_t><<<grid, 256, 0, s>>>(
           reinterpret_cast<const uint32_t *>(a.x), reinterpret_cast<uint32_t *>(a.conv_state),
-          a.cu_seqlens, C);
+          a.cu_seqlens, C, a.T, a.err);
     return cudaGetLastError();
   }
   return cudaSuccess;
@@ -260,6 +299,23 @@ cudaError_t launch_prologue(const ProArgs &a, int D, bool io_bf16, cudaStream_t 
   if (D == 128) return io_bf16 ? launch_pro<128, bf16>(a, s) : launch_pro<128, float>(a, s);
   if (D == 16) return io_bf16 ? launch_pro<16, bf16>(a, s) : launch_pro<16, float>(a, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_conv_ckpt(const void *x, const void *conv_state, const int32_t *cu,
+                             int n_seqs, int64_t T, const int32_t *ckpt_cu,
+                             const int32_t *ckpt_pos, int n_ckpt, int channels, void *out,
+                             bool io_bf16, int *err, cudaStream_t s) {
+  if (n_ckpt == 0) return cudaSuccess;
+  const dim3 grid((channels + 255) / 256, n_ckpt);
+  if (io_bf16)
+    conv_ckpt_kernel<uint16_t><<<grid, 256, 0, s>>>(
+        reinterpret_cast<const uint16_t *>(x), reinterpret_cast<const uint16_t *>(conv_state),
+        cu, n_seqs, ckpt_cu, ckpt_pos, channels, T, reinterpret_cast<uint16_t *>(out), err);
+  else
+    conv_ckpt_kernel<uint32_t><<<grid, 256, 0, s>>>(
+        reinterpret_cast<const uint32_t *>(x), reinterpret_cast<const uint32_t *>(conv_state),
+        cu, n_seqs, ckpt_cu, ckpt_pos, channels, T, reinterpret_cast<uint32_t *>(out), err);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_conv_update(const ConvArgs &a, bool io_bf16, cudaStream_t s) {

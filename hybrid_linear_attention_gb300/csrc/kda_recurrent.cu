@@ -70,6 +70,10 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
       bos = a.cu_seqlens[n];
       eos = a.cu_seqlens[n + 1];
       slot = n;
+      if (bos < 0 || eos > a.total || eos < bos) {  // offsets outside the rows: flagged, empty
+        if (tid == 0 && a.err) atomicOr(a.err, ERR_BAD_SEQLEN);
+        bos = eos = 0;
+      }
     } else {
       const int K = a.tokens_per_seq > 0 ? a.tokens_per_seq : 1;
       bos = (int64_t)n * K;
@@ -121,6 +125,13 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
     const IO *q = reinterpret_cast<const IO *>(a.q);
     const IO *k = reinterpret_cast<const IO *>(a.k);
     const IO *v = reinterpret_cast<const IO *>(a.v);
+    // prefix-state checkpoints of this sequence (prefill only): next one and the end
+    int kc = a.ckpt_cu ? a.ckpt_cu[n] : 0;
+    int kend = a.ckpt_cu ? a.ckpt_cu[n + 1] : 0;
+    if (kc < 0 || kend > a.n_ckpt || kend < kc) {  // a range outside the checkpoints: flagged
+      if (tid == 0 && a.err) atomicOr(a.err, ERR_BAD_INDEX);
+      kc = kend = 0;
+    }
 
     for (int64_t t0 = bos; t0 < eos; t0 += TT) {
       const int nt = (int)((eos - t0) < TT ? (eos - t0) : TT);
@@ -215,6 +226,18 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) S[r][c] = fmaf(kk, s_u[4 * cg + c], S[r][c]);
         }
+        // checkpoints placed after this token; one placed before (out of order) is flagged
+        for (const int64_t done = t0 + tt + 1 - bos; kc < kend && a.ckpt_pos[kc] <= done; ++kc) {
+          if (a.ckpt_pos[kc] < done) {
+            if (tid == 0 && a.err) atomicOr(a.err, ERR_BAD_INDEX);
+            continue;
+          }
+          ST *dst = reinterpret_cast<ST *>(a.ckpt_states) + ((size_t)kc * H + h) * D * D;
+#pragma unroll
+          for (int r = 0; r < RPT; ++r)
+            store4(dst + (size_t)(rg * RPT + r) * D + 4 * cg,
+                   make_float4(S[r][0], S[r][1], S[r][2], S[r][3]));
+        }
         if (a.step_states) {  // the state after this token (speculative rollback points)
           ST *dst = reinterpret_cast<ST *>(a.step_states) + ((size_t)(t0 + tt) * H + h) * D * D;
 #pragma unroll
@@ -238,6 +261,7 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
       }
     }
 
+    if (kc < kend && tid == 0 && a.err) atomicOr(a.err, ERR_BAD_INDEX);  // beyond the end
     if (a.state_out) {
       ST *dst = reinterpret_cast<ST *>(a.state_out) + sbase;
 #pragma unroll

@@ -18,14 +18,15 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libkda.so")
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_WORKSPACE, \
-    KDA_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+    KDA_ERR_TIMEOUT, KDA_ERR_BAD_INDEX, KDA_ERR_BAD_SEQLENS = 0, -1, -2, -3, -4, -5, -6, -7
 KDA_F32, KDA_BF16 = 0, 1
 
 _TORCH_OF = {KDA_F32: torch.float32, KDA_BF16: torch.bfloat16}
 
 EXPORTS = (
     "kda_params_default", "kda_status_string", "kda_state_bytes", "kda_prefill_workspace_size",
-    "kda_prologue", "kda_prefill", "kda_decode_step", "kda_conv_state_update",
+    "kda_prologue", "kda_prefill", "kda_prefill_checkpointed", "kda_conv_tail_checkpoints",
+    "kda_decode_step", "kda_conv_state_update",
     "kda_decode_step_fused", "kda_decode_multi", "kda_state_accept", "kda_check_device_error",
     "kda_launch_count",
 )
@@ -79,6 +80,11 @@ def load():
                                     _vp, _vp, _vp, _vp, _vp, _vp]),
             "kda_prefill": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp,
                                    _vp, _vp, _vp, _sz, _vp]),
+            "kda_prefill_checkpointed": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                                _i64, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp,
+                                                _vp, _sz, _vp]),
+            "kda_conv_tail_checkpoints": (_i32, [_P, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _i32,
+                                                 _vp, _vp]),
             "kda_decode_step": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _vp,
                                        _vp, _vp, _vp]),
             "kda_conv_state_update": (_i32, [_P, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _vp,
@@ -187,6 +193,35 @@ def kda_prefill(p, q, k, v, g, beta, cu_seqlens, out, *, init_state=None, final_
         _ptr(final_state, sd, "final_state"), _ptr(workspace, None, "workspace"), ws_bytes,
         _stream(stream))
     _check(st, "kda_prefill")
+
+
+def kda_prefill_checkpointed(p, q, k, v, g, beta, cu_seqlens, out, ckpt_cu, ckpt_pos,
+                             ckpt_states, *, init_state=None, final_state=None, gate_logit=None,
+                             norm_w=None, workspace=None, stream=None):
+    io, sd = p.io_torch, p.state_torch
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().kda_prefill_checkpointed(
+        ctypes.byref(p), _ptr(q, io, "q"), _ptr(k, io, "k"), _ptr(v, io, "v"),
+        _ptr(g, torch.float32, "g"), _ptr(beta, torch.float32, "beta"),
+        _ptr(init_state, sd, "init_state"), _ptr(cu_seqlens, torch.int32, "cu_seqlens"),
+        cu_seqlens.numel() - 1, q.shape[0], _ptr(gate_logit, io, "gate_logit"),
+        _ptr(norm_w, torch.float32, "norm_w"), _ptr(out, io, "out"),
+        _ptr(final_state, sd, "final_state"), _ptr(ckpt_cu, torch.int32, "ckpt_cu"),
+        _ptr(ckpt_pos, torch.int32, "ckpt_pos"), ckpt_pos.numel(),
+        _ptr(ckpt_states, sd, "ckpt_states"), _ptr(workspace, None, "workspace"), ws_bytes,
+        _stream(stream))
+    _check(st, "kda_prefill_checkpointed")
+
+
+def kda_conv_tail_checkpoints(p, x_raw, conv_state, cu_seqlens, ckpt_cu, ckpt_pos, conv_ckpt, *,
+                              stream=None):
+    io = p.io_torch
+    st = load().kda_conv_tail_checkpoints(
+        ctypes.byref(p), _ptr(x_raw, io, "x_raw"), _ptr(conv_state, io, "conv_state"),
+        _ptr(cu_seqlens, torch.int32, "cu_seqlens"), cu_seqlens.numel() - 1, x_raw.shape[0],
+        _ptr(ckpt_cu, torch.int32, "ckpt_cu"), _ptr(ckpt_pos, torch.int32, "ckpt_pos"),
+        ckpt_pos.numel(), _ptr(conv_ckpt, io, "conv_ckpt"), _stream(stream))
+    _check(st, "kda_conv_tail_checkpoints")
 
 
 def kda_decode_step(p, q, k, v, g, beta, state, out, *, slot_idx=None, gate_logit=None,

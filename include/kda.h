@@ -34,9 +34,12 @@
  *    sets a sticky device flag read by kda_check_device_error().
  *  - Packed sequences: token t of the batch lives at row t of every [T_tot, ...] tensor;
  *    sequence n owns rows [cu_seqlens[n], cu_seqlens[n+1]).  cu_seqlens is a device int32
- *    array of n_seqs + 1 non-decreasing offsets starting at 0 (the library does not read it
- *    on the host; a decreasing array yields unspecified results for those sequences but no
- *    out-of-bounds access as long as every entry lies in [0, total_tokens]).
+ *    array of n_seqs + 1 non-decreasing offsets starting at 0.  The library does not read
+ *    it on the host; the kernels check every sequence's offsets against [0, total_tokens]
+ *    and treat one that falls outside (or runs backwards) as empty, setting the sticky flag
+ *    (KDA_ERR_BAD_SEQLENS).  Offsets that are in range but not non-decreasing across
+ *    sequences give unspecified values for those rows, never an access outside the
+ *    buffers.
  *  - Supported: d_k == d_v == d in {16, 128}; any H >= 1; sequences of any length >= 0.
  */
 #ifndef KDA_H_
@@ -58,7 +61,8 @@ typedef enum {
   KDA_ERR_CUDA = -3,
   KDA_ERR_WORKSPACE = -4,
   KDA_ERR_TIMEOUT = -5,
-  KDA_ERR_BAD_INDEX = -6
+  KDA_ERR_BAD_INDEX = -6,
+  KDA_ERR_BAD_SEQLENS = -7
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -124,7 +128,10 @@ kda_status kda_prologue(const kda_params* p, const void* x_raw, const void* conv
  *   g           [T_tot, H, d_k] fp32 log-retention (clamped at p->g_min inside).
  *   beta        [T_tot, H] fp32 write strength in (0, 1).
  *   init_state  [n_seqs, H, d_k, d_v] state_dtype, or NULL for zeros.
- *   cu_seqlens  [n_seqs + 1] int32 (device).
+ *   cu_seqlens  [n_seqs + 1] int32 (device): cu_seqlens[0] = 0, non-decreasing,
+ *               cu_seqlens[n_seqs] = total_tokens.  A sequence whose offsets fall outside
+ *               [0, total_tokens] (or run backwards) is treated as empty and reported by
+ *               kda_check_device_error (KDA_ERR_BAD_SEQLENS).
  *   gate_logit  [T_tot, H, d_v] io_dtype, or NULL: no output norm/gate (plain read).
  *   norm_w      [d_v] fp32 output-norm weight, or NULL for ones (used only with a gate).
  *   out         [T_tot, H, d_v] io_dtype.
@@ -138,6 +145,58 @@ kda_status kda_prefill(const kda_params* p, const void* q, const void* k, const 
                        const void* gate_logit, const float* norm_w, void* out,
                        void* final_state, void* workspace, size_t ws_bytes,
                        cudaStream_t stream);
+
+/*
+ * kda_prefill_checkpointed -- kda_prefill that also saves the state at caller-given token
+ * boundaries inside the sequences (prefix-state checkpoints: a recurrent state can be
+ * reused only where a snapshot of it was saved, "Ling-3.1-flash: What 63 Linear-Attention
+ * Layers Do to the KV Budget", section "Where the hybrid makes serving harder").
+ *
+ *   ckpt_cu     [n_seqs + 1] int32 (device): checkpoints of sequence n are
+ *               ckpt_cu[n] .. ckpt_cu[n+1]-1, non-decreasing, ckpt_cu[n_seqs] = n_ckpt.
+ *   ckpt_pos    [n_ckpt] int32 (device): tokens of its sequence before the checkpoint,
+ *               strictly increasing within a sequence, each in [1, length] and a multiple
+ *               of 64 (the chunk) or the sequence length.  A fork at another position is
+ *               taken by ending a sequence there and passing its final state on as the
+ *               next part's init_state.
+ *   ckpt_states [n_ckpt, H, d_k, d_v] state_dtype: the state after ckpt_pos[j] tokens of
+ *               its sequence, the same value a kda_prefill of that prefix leaves in
+ *               final_state.
+ *   Other arguments as kda_prefill.  n_ckpt >= 1 (KDA_ERR_INVALID_ARG otherwise).  Ranges
+ *   or positions that break these rules are skipped and reported by
+ *   kda_check_device_error (KDA_ERR_BAD_INDEX); the outputs and final states are unaffected.
+ */
+kda_status kda_prefill_checkpointed(const kda_params* p, const void* q, const void* k,
+                                    const void* v, const float* g, const float* beta,
+                                    const void* init_state, const int32_t* cu_seqlens,
+                                    int n_seqs, int64_t total_tokens, const void* gate_logit,
+                                    const float* norm_w, void* out, void* final_state,
+                                    const int32_t* ckpt_cu, const int32_t* ckpt_pos,
+                                    int n_ckpt, void* ckpt_states, void* workspace,
+                                    size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * kda_conv_tail_checkpoints -- the short-convolution half of a prefix checkpoint: for every
+ * checkpoint j (ckpt_cu / ckpt_pos as in kda_prefill_checkpointed, any position in
+ * [1, length] allowed), the three raw inputs before position ckpt_pos[j] of its sequence,
+ * oldest first, i.e. the conv_state a kda_prologue of that prefix would leave.  Reuse at
+ * a token boundary needs both halves ("Ling-3.1-flash: Grouped Routing and Two Different
+ * MLA Caches", section "Two cache budgets for one checkpoint": prefix reuse restores every
+ * recurrent state at the same boundary).
+ *
+ *   x_raw       [T_tot, 3*H*d] io_dtype, as kda_prologue.
+ *   conv_state  [n_seqs, 3, 3*H*d] io_dtype or NULL: the tails before the sequences (the
+ *               values kda_prologue reads, so call this first when kda_prologue updates
+ *               them in place); taps before a sequence start read it (zeros if NULL).
+ *   conv_ckpt   [n_ckpt, 3, 3*H*d] io_dtype output.  Bit-exact copies.
+ * n_ckpt = 0 is a no-op.  A position outside [1, length] is skipped and reported
+ * (KDA_ERR_BAD_INDEX).
+ */
+kda_status kda_conv_tail_checkpoints(const kda_params* p, const void* x_raw,
+                                     const void* conv_state, const int32_t* cu_seqlens,
+                                     int n_seqs, int64_t total_tokens, const int32_t* ckpt_cu,
+                                     const int32_t* ckpt_pos, int n_ckpt, void* conv_ckpt,
+                                     cudaStream_t stream);
 
 /*
  * kda_decode_step -- one token for each of n_seqs sequences, state updated in place.
@@ -222,8 +281,9 @@ kda_status kda_state_accept(const kda_params* p, const void* step_states, int n_
                             const int32_t* slot_idx, cudaStream_t stream);
 
 /* Synchronises `stream`, then reads and clears the library's sticky device error flag
- * (set when a bounded device wait ran out, or a device-side index was out of range).
- * Returns KDA_OK, KDA_ERR_TIMEOUT, KDA_ERR_BAD_INDEX or KDA_ERR_CUDA. */
+ * (set when a bounded device wait ran out, a device-side index was out of range, or a
+ * sequence's offsets fell outside the token rows).  Returns KDA_OK, KDA_ERR_TIMEOUT,
+ * KDA_ERR_BAD_INDEX, KDA_ERR_BAD_SEQLENS (in that order of precedence) or KDA_ERR_CUDA. */
 kda_status kda_check_device_error(cudaStream_t stream);
 
 /* Number of kernels the library launched since load (host-side counter, for benchmarks). */

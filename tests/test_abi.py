@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, -5):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert kda.status_string(code).startswith("KDA_")
 
 
@@ -140,3 +140,30 @@ def test_multi_decode_and_accept_reject_bad_arguments_on_host(lib):
     assert lib.kda_state_accept(ctypes.byref(p), None, 2, 3, vp(), vp(), 4, None, None) == -1
     assert lib.kda_state_accept(ctypes.byref(p), vp(), 0, 3, None, None, 0, None, None) == 0
     assert lib.kda_status_string(-6).decode().startswith("KDA_ERR_BAD_INDEX")
+
+
+def test_checkpoint_calls_reject_bad_arguments_on_host(lib):
+    p = kda.params(H=2, d=128)
+    P = ctypes.byref(p)
+    buf = ctypes.c_void_p(16)  # never dereferenced: every call fails validation first
+
+    def prefill_ck(n_ckpt=2, cu=buf, pos=buf, states=buf):
+        return lib.kda_prefill_checkpointed(P, buf, buf, buf, buf, buf, None, buf, 1, 64, None,
+                                            None, buf, None, cu, pos, n_ckpt, states, None, 0,
+                                            None)
+    assert prefill_ck(n_ckpt=0) == kda.KDA_ERR_INVALID_ARG        # at least one checkpoint
+    assert prefill_ck(n_ckpt=-3) == kda.KDA_ERR_INVALID_ARG
+    assert prefill_ck(cu=None) == kda.KDA_ERR_INVALID_ARG
+    assert prefill_ck(pos=None) == kda.KDA_ERR_INVALID_ARG
+    assert prefill_ck(states=None) == kda.KDA_ERR_INVALID_ARG
+    assert prefill_ck(states=ctypes.c_void_p(24)) == kda.KDA_ERR_INVALID_ARG  # misaligned
+
+    def conv_ck(n_seqs=1, n_ckpt=2, x=buf, out=buf):
+        return lib.kda_conv_tail_checkpoints(P, x, None, buf, n_seqs, 64, buf, buf, n_ckpt, out,
+                                             None)
+    assert conv_ck(n_ckpt=0) == kda.KDA_OK                            # nothing to do
+    assert conv_ck(n_seqs=0) == kda.KDA_ERR_INVALID_ARG
+    assert conv_ck(n_ckpt=-1) == kda.KDA_ERR_INVALID_ARG
+    assert conv_ck(n_ckpt=70000) == kda.KDA_ERR_INVALID_ARG           # grid limit
+    assert conv_ck(x=None) == kda.KDA_ERR_INVALID_ARG
+    assert conv_ck(out=ctypes.c_void_p(40)) == kda.KDA_ERR_INVALID_ARG
