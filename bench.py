@@ -3,7 +3,10 @@
 Main line (value): prefill tokens/s per layer on the single-layer, Ling-shaped workload
 (B=1, T=4096, H=64, d=128, bf16 I/O, fp32 state, zero initial state, chunk 64).  One step is
 the whole prefill hot path over that batch: kda_prologue (width-4 causal conv + SiLU over the
-raw q|k|v projections, q/k L2 norm, beta = sigmoid, g clamp) then kda_prefill.
+raw q|k|v projections, beta = sigmoid) then kda_prefill (q/k L2 norm, g clamp at -5, the
+chunked recurrence).  Each activation runs once, inside the kernel that consumes it: the
+prefill reads the raw log-retention and normalises q and k itself, so the prologue writes
+neither a clamped copy of g nor normalised q, k.
 Also reported: the prefill kernel alone, the decode workload (256 sequences x 1 token,
 H=64, d=128, fp32 state pool ~N(0,0.02), fused conv + decode, 100 consecutive steps) as
 state GB/s, the roofline of the dominant kernel against MEASURED_PEAKS.json, an end-to-end
@@ -79,10 +82,10 @@ def _prefill_bytes(T, H, d, with_state_out=True):
 
 
 def _prologue_bytes(T, H, d):
-    """kda_prologue: read raw x (3Hd bf16) + g_raw (Hd fp32) + beta logits; write q, k, v
-    (bf16), g (fp32), beta (fp32)."""
+    """kda_prologue as the step runs it: read raw x (3Hd bf16) + beta logits; write q, k, v
+    (bf16) and beta (fp32)."""
     C = 3 * H * d
-    return T * (C * 2 * 2 + H * d * 4 * 2 + H * 4 * 2)
+    return T * (C * 2 * 2 + H * 4 * 2)
 
 
 def _decode_bytes(n, H, d):
@@ -206,12 +209,12 @@ def _oracle_prefill_sample(heads, seed=0):
     pin = inputs.prologue_inputs([T_PREFILL], heads, D, seed=seed, conv_state=False)
     threads = os.cpu_count() or 1
     t0 = time.perf_counter()
-    pr = oracle.prologue(pin["x"], pin["conv_w"], pin["cu_seqlens"], heads, D, l2norm_qk=True,
-                         beta_logit=pin["beta_logit"], g_raw=pin["g_raw"])
+    pr = oracle.prologue(pin["x"], pin["conv_w"], pin["cu_seqlens"], heads, D,
+                         beta_logit=pin["beta_logit"])
     y = pr["y"].reshape(T_PREFILL, 3, heads, D)
     oracle.kda_forward(np.ascontiguousarray(y[:, 0]), np.ascontiguousarray(y[:, 1]),
-                       np.ascontiguousarray(y[:, 2]), pr["g"].astype(np.float32),
-                       pr["beta"].astype(np.float32), pin["cu_seqlens"], qk_l2norm=False,
+                       np.ascontiguousarray(y[:, 2]), pin["g_raw"],
+                       pr["beta"].astype(np.float32), pin["cu_seqlens"], qk_l2norm=True,
                        n_threads=threads)
     return time.perf_counter() - t0, threads
 
@@ -273,17 +276,18 @@ class PrefillWorkload:
         self.q = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
         self.k, self.v = torch.empty_like(self.q), torch.empty_like(self.q)
         self.beta = torch.empty((T, H), dtype=torch.float32, device=dev)
-        self.g = torch.empty((T, H, D), dtype=torch.float32, device=dev)
         self.out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
         self.fin = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
 
     def prologue(self, stream=None):
         self.kda.kda_prologue(self.p, self.x, self.w, None, self.cu, self.q, self.k, self.v,
-                              l2norm_qk=True, beta_logit=self.beta_logit, g_raw=self.g_raw,
-                              beta=self.beta, g=self.g, stream=stream)
+                              l2norm_qk=False, beta_logit=self.beta_logit, beta=self.beta,
+                              stream=stream)
 
     def prefill(self, stream=None):
-        self.kda.kda_prefill(self.p, self.q, self.k, self.v, self.g, self.beta, self.cu,
+        # the raw log-retention goes straight in: the kernel clamps it at g_min (and the
+        # params' qk_l2norm normalises q, k) as it loads them
+        self.kda.kda_prefill(self.p, self.q, self.k, self.v, self.g_raw, self.beta, self.cu,
                              self.out, final_state=self.fin, stream=stream)
 
 

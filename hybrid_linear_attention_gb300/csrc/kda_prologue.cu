@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(PNT, 2) prologue_kernel(const ProArgs a) {
 // Gate activations, elementwise: g = max(g_raw, g_min) (four at a time), beta = sigmoid.
 template <int D>
 __global__ void gate_act_kernel(const ProArgs a) {
-  const int64_t n4 = a.T * a.H * (int64_t)D / 4, nb = a.T * a.H;
+  // without g_raw only the T * H gates are walked
+  const int64_t n4 = a.g_raw ? a.T * a.H * (int64_t)D / 4 : 0, nb = a.T * a.H;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n4; e += stride) {
     if (a.g_raw) {
@@ -269,7 +270,7 @@ cudaError_t launch_pro(const ProArgs &a, cudaStream_t s) {
       e = cudaGetDevice(&dev);
       if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
       if (e != cudaSuccess) return e;
-      const int64_t work = a.T * a.H * (int64_t)D / 4;
+      const int64_t work = a.g_raw ? a.T * a.H * (int64_t)D / 4 : a.T * a.H;
       const int64_t blocks = (work + 255) / 256;
       const int64_t cap = (int64_t)nsm * 8;
       gate_act_kernel<D><<<(unsigned)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap), 256, 0, s>>>(a);

@@ -70,21 +70,21 @@ def test_single_layer_prefill_T4096():
 
 
 def test_bench_chain_prologue_then_prefill_T4096():
-    """The chain bench.py times: raw projections ~N(0,1) -> kda_prologue (conv, SiLU, q/k L2,
-    sigmoid beta, g clamp) -> kda_prefill.  The oracle runs the same chain in fp64; the
-    bf16 storage of q, k, v between the two calls is the ABI's, so outputs are compared."""
+    """The chain bench.py times: raw projections ~N(0,1) -> kda_prologue (conv, SiLU, sigmoid
+    beta) -> kda_prefill fed the raw log-retention (clamped at -5 inside) with q/k L2 norm on.
+    The oracle runs the same chain in fp64; the bf16 storage of q, k, v between the two calls
+    is the ABI's, so outputs are compared."""
     T = 4096
     pin = inputs.prologue_inputs([T], H, D, seed=101, device="cuda", conv_state=False)
     p = kda.params(H=H, d=D)
     q = torch.empty((T, H, D), dtype=torch.bfloat16, device="cuda")
     k, v = torch.empty_like(q), torch.empty_like(q)
     beta = torch.empty((T, H), dtype=torch.float32, device="cuda")
-    g = torch.empty((T, H, D), dtype=torch.float32, device="cuda")
     _gpu.lib()
-    kda.kda_prologue(p, pin["x"], pin["conv_w"], None, pin["cu_seqlens"], q, k, v, l2norm_qk=True,
-                     beta_logit=pin["beta_logit"], g_raw=pin["g_raw"], beta=beta, g=g)
+    kda.kda_prologue(p, pin["x"], pin["conv_w"], None, pin["cu_seqlens"], q, k, v,
+                     beta_logit=pin["beta_logit"], beta=beta)
     out = torch.empty_like(q)
-    kda.kda_prefill(p, q, k, v, g, beta, pin["cu_seqlens"], out)
+    kda.kda_prefill(p, q, k, v, pin["g_raw"], beta, pin["cu_seqlens"], out)
     torch.cuda.synchronize()
     for h in (0, 33, 63):
         cols = np.r_[h * D:(h + 1) * D, H * D + h * D:H * D + (h + 1) * D,
@@ -92,15 +92,14 @@ def test_bench_chain_prologue_then_prefill_T4096():
         xs = pin["x"][:, cols].cpu()
         ws = pin["conv_w"][cols].cpu()
         pr = oracle.prologue(xs, ws, torch.tensor([0, T], dtype=torch.int32), 1, D,
-                             l2norm_qk=True, beta_logit=pin["beta_logit"][:, h:h + 1].cpu(),
-                             g_raw=pin["g_raw"][:, h:h + 1].cpu())
+                             beta_logit=pin["beta_logit"][:, h:h + 1].cpu())
         # the ABI stores the prologue's q, k, v in bf16 between the two calls: the oracle's
-        # own fp64 y is rounded to bf16 (nearest even) the same way, and the recurrence
-        # re-normalises q, k as kda_prefill does (qk_l2norm on)
+        # own fp64 y is rounded to bf16 (nearest even) the same way; the recurrence
+        # normalises q, k and clamps the raw log-retention as kda_prefill does
         y = torch.from_numpy(pr["y"].reshape(T, 3, 1, D)).to(torch.bfloat16)
-        r = oracle.kda_forward(y[:, 0], y[:, 1], y[:, 2],
-                               pr["g"].astype(np.float32), pr["beta"].astype(np.float32),
-                               np.array([0, T], np.int32), qk_l2norm=True)
+        r = oracle.kda_forward(y[:, 0], y[:, 1], y[:, 2], pin["g_raw"][:, h:h + 1].cpu(),
+                               pr["beta"].astype(np.float32), np.array([0, T], np.int32),
+                               qk_l2norm=True)
         assert out_error(out[:, h].cpu(), r["out"][:, 0], torch.bfloat16) <= TOL_OUT
 
 
