@@ -7,8 +7,9 @@
 // sequence's first token read that sequence's conv tail (three raw inputs, oldest first).
 //
 // Kernels:
-//   prologue_kernel     packed prefill: conv + SiLU (+ per-head L2 of q, k) for a tile of
-//                       tokens x (stream, head) rows, 16-byte vectors, one read per input.
+//   prologue_kernel     packed prefill: conv + SiLU (+ per-head L2 of q, k) for a share of
+//                       the tokens x (stream, head) rows, 16-byte vectors, one read per
+//                       input, the next tokens' inputs always in flight.
 //   gate_act_kernel     the gate activations beta = sigmoid(logit), g = max(g_raw, g_min).
 //   conv_tail_kernel    afterwards, the new tail of every sequence (separate launch, so the
 //                       in-place update never races with the reads of the old tail).
@@ -19,9 +20,8 @@
 namespace kda {
 namespace {
 
-constexpr int TT = 64;    // tokens per prologue tile
-constexpr int PNT = 256;  // threads per prologue CTA
-constexpr int UNR = 4;    // tokens loaded ahead
+constexpr int PNT = 256;     // threads per prologue CTA
+constexpr int MIN_TOK = 16;  // fewest tokens a prologue CTA walks
 
 // eight consecutive channels as fp32 (16-byte bf16 vector, or two fp32 vectors)
 __device__ __forceinline__ void load8(const bf16 *p, float (&v)[8]) {
@@ -56,8 +56,59 @@ __device__ __forceinline__ void store8(float *p, const float (&v)[8]) {
   *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
   *reinterpret_cast<float4 *>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
 }
+// eight consecutive channels as loaded, converted to fp32 only when used (a bf16 vector is
+// four registers, so a deep prefetch ring stays small)
+template <typename IO> struct Raw;
+template <> struct Raw<bf16> { uint4 u; };
+template <> struct Raw<float> { float4 a, b; };
+__device__ __forceinline__ Raw<bf16> load_raw(const bf16 *p) {
+  return Raw<bf16>{*reinterpret_cast<const uint4 *>(p)};
+}
+__device__ __forceinline__ Raw<float> load_raw(const float *p) {
+  return Raw<float>{*reinterpret_cast<const float4 *>(p), *reinterpret_cast<const float4 *>(p + 4)};
+}
+__device__ __forceinline__ void unpack8(const Raw<bf16> &r, float (&v)[8]) {
+  v[0] = __uint_as_float(r.u.x << 16), v[1] = __uint_as_float(r.u.x & 0xffff0000u);
+  v[2] = __uint_as_float(r.u.y << 16), v[3] = __uint_as_float(r.u.y & 0xffff0000u);
+  v[4] = __uint_as_float(r.u.z << 16), v[5] = __uint_as_float(r.u.z & 0xffff0000u);
+  v[6] = __uint_as_float(r.u.w << 16), v[7] = __uint_as_float(r.u.w & 0xffff0000u);
+}
+__device__ __forceinline__ void unpack8(const Raw<float> &r, float (&v)[8]) {
+  v[0] = r.a.x, v[1] = r.a.y, v[2] = r.a.z, v[3] = r.a.w;
+  v[4] = r.b.x, v[5] = r.b.y, v[6] = r.b.z, v[7] = r.b.w;
+}
 
-// One CTA: a tile of TT tokens x PNT/(D/8) rows of D channels (a row = one head of one of the
+// Conv weights of eight consecutive channels (channel e, tap j at 4e + j): bf16 pairs kept as
+// loaded and widened on use (16 registers), fp32 as is.
+template <typename IO> struct ConvW;
+template <> struct ConvW<bf16> {
+  uint32_t p[8][2];  // channel y: taps (0, 1) and (2, 3), tap 0 / 2 in the low half
+  __device__ __forceinline__ void load(const bf16 *cw, bool act) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = act ? *reinterpret_cast<const uint4 *>(cw + 8 * q) : make_uint4(0, 0, 0, 0);
+      p[2 * q][0] = u.x, p[2 * q][1] = u.y, p[2 * q + 1][0] = u.z, p[2 * q + 1][1] = u.w;
+    }
+  }
+  __device__ __forceinline__ float tap(int y, int j) const {
+    const uint32_t v = p[y][j >> 1];
+    return __uint_as_float((j & 1) ? (v & 0xffff0000u) : (v << 16));
+  }
+};
+template <> struct ConvW<float> {
+  float w[8][4];
+  __device__ __forceinline__ void load(const float *cw, bool act) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 u = act ? *reinterpret_cast<const float4 *>(cw + 4 * q)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      w[q][0] = u.x, w[q][1] = u.y, w[q][2] = u.z, w[q][3] = u.w;
+    }
+  }
+  __device__ __forceinline__ float tap(int y, int j) const { return w[y][j]; }
+};
+
+// One CTA: a share of the tokens x PNT/(D/8) rows of D channels (a row = one head of one of the
 // q, k, v streams); D/8 threads per row, eight channels each.  Every thread walks the tile's
 // tokens in order with the last three raw inputs of its channels in registers (each input
 // is read once); at a sequence start inside the tile the window restarts from that
@@ -73,27 +124,16 @@ __global__ void __launch_bounds__(PNT, 2) prologue_kernel(const ProArgs a) {
   const bool act = u < 3 * H;
   const int stream = act ? u / H : 0, h = act ? u % H : 0;
   const int64_t c0 = (int64_t)stream * H * D + (int64_t)h * D + 8 * sub;
-  const int64_t t0 = (int64_t)blockIdx.x * TT;
-  const int64_t t1 = (t0 + TT) < a.T ? (t0 + TT) : a.T;
+  // a contiguous, balanced share of the tokens (gridDim.x shares of T)
+  const int64_t t0 = a.T * blockIdx.x / gridDim.x;
+  const int64_t t1 = a.T * (blockIdx.x + 1) / gridDim.x;
   const IO *x = reinterpret_cast<const IO *>(a.x);
   const IO *cs = reinterpret_cast<const IO *>(a.conv_state);
   IO *dst = reinterpret_cast<IO *>(stream == 0 ? a.q : stream == 1 ? a.k : a.v);
   const bool norm = a.l2norm_qk && stream < 2;
 
-  float w[8][4];
-  {
-    const IO *cw = reinterpret_cast<const IO *>(a.conv_w) + 4 * c0;
-    float t8[8];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {  // 32 consecutive weights: channel e, tap j at 4e + j
-      if (act) load8(cw + 8 * q, t8);
-      else
-#pragma unroll
-        for (int y = 0; y < 8; ++y) t8[y] = 0.f;
-#pragma unroll
-      for (int y = 0; y < 8; ++y) w[(8 * q + y) >> 2][y & 3] = t8[y];
-    }
-  }
+  ConvW<IO> w;  // the four taps of this thread's eight channels
+  w.load(reinterpret_cast<const IO *>(a.conv_w) + 4 * c0, act);
   int n = seq_of_token(a.cu_seqlens, a.n_seqs, t0);
   int64_t bos = a.cu_seqlens[n], eos = a.cu_seqlens[n + 1];
   if ((bos > t0 || eos <= t0) && threadIdx.x == 0 && a.err) atomicOr(a.err, ERR_BAD_SEQLEN);
@@ -109,19 +149,24 @@ __global__ void __launch_bounds__(PNT, 2) prologue_kernel(const ProArgs a) {
       for (int y = 0; y < 8; ++y) win[k][y] = 0.f;
   }
 
-  for (int64_t tb = t0; tb < t1; tb += UNR) {
-    float xv[UNR][8];
+  // rolling prefetch: the raw inputs of the next PF tokens stay in flight while a token is
+  // convolved (slot i of the ring holds token tb + i, refilled with token tb + i + PF)
+  constexpr int PF = sizeof(IO) == 2 ? 6 : 2;
+  Raw<IO> xr[PF];
 #pragma unroll
-    for (int i = 0; i < UNR; ++i) {
-      if (act && tb + i < t1) load8(x + (tb + i) * C + c0, xv[i]);
-      else
+  for (int i = 0; i < PF; ++i)
+    if (act && t0 + i < t1) xr[i] = load_raw(x + (t0 + i) * C + c0);
+  const IO *xn = x + (t0 + PF) * C + c0;              // token t + PF of this thread's channels
+  IO *dp = dst + (t0 * H + h) * (int64_t)D + 8 * sub;  // output row of token t
+  for (int64_t tb = t0; tb < t1; tb += PF) {
 #pragma unroll
-        for (int y = 0; y < 8; ++y) xv[i][y] = 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < UNR; ++i) {
+    for (int i = 0; i < PF; ++i) {
       const int64_t t = tb + i;
       if (t >= t1) break;
+      float xv[8];
+      unpack8(xr[i], xv);
+      if (act && t + PF < t1) xr[i] = load_raw(xn);
+      xn += C;
       if (t == eos) {  // next non-empty sequence starts here: its conv tail is the history
         do {
           ++n;
@@ -139,14 +184,15 @@ __global__ void __launch_bounds__(PNT, 2) prologue_kernel(const ProArgs a) {
       float yv[8], ss = 0.f;
 #pragma unroll
       for (int y = 0; y < 8; ++y) {
-        float acc = w[y][0] * win[0][y];
-        acc = fmaf(w[y][1], win[1][y], acc);
-        acc = fmaf(w[y][2], win[2][y], acc);
-        acc = fmaf(w[y][3], xv[i][y], acc);
+        float acc = w.tap(y, 0) * win[0][y];
+        acc = fmaf(w.tap(y, 1), win[1][y], acc);
+        acc = fmaf(w.tap(y, 2), win[2][y], acc);
+        acc = fmaf(w.tap(y, 3), xv[y], acc);
         yv[y] = silu_fast(acc);
         ss = fmaf(yv[y], yv[y], ss);
-        win[0][y] = win[1][y], win[1][y] = win[2][y], win[2][y] = xv[i][y];
+        win[0][y] = win[1][y], win[1][y] = win[2][y], win[2][y] = xv[y];
       }
+      // every lane takes part in the shuffle (a warp may hold rows of different streams)
 #pragma unroll
       for (int off = TPH / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
       if (norm) {
@@ -154,7 +200,8 @@ __global__ void __launch_bounds__(PNT, 2) prologue_kernel(const ProArgs a) {
 #pragma unroll
         for (int y = 0; y < 8; ++y) yv[y] *= r;
       }
-      if (act) store8(dst + (t * H + h) * D + 8 * sub, yv);
+      if (act) store8(dp, yv);
+      dp += (int64_t)H * D;
     }
   }
 }
@@ -260,16 +307,24 @@ __global__ void conv_update_kernel(const ConvArgs a) {
 template <int D, typename IO>
 cudaError_t launch_pro(const ProArgs &a, cudaStream_t s) {
   if (a.T > 0) {
+    int dev = 0, nsm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // rows of D channels (one head of one stream) in groups of NU; the tokens are split into
+    // as many contiguous shares as fill one wave at two CTAs per SM (at least MIN_TOK tokens
+    // a share), so every CTA walks the same number of tokens and no partial wave is left
     constexpr int NU = PNT / (D / 8);
-    const dim3 grid((unsigned)((a.T + TT - 1) / TT), (unsigned)((3 * a.H + NU - 1) / NU));
+    const int64_t groups = (3 * a.H + NU - 1) / NU;
+    int64_t shares = 2 * (int64_t)nsm / groups;
+    const int64_t most = (a.T + MIN_TOK - 1) / MIN_TOK;
+    if (shares > most) shares = most;
+    if (shares < 1) shares = 1;
+    const dim3 grid((unsigned)shares, (unsigned)groups);
     prologue_kernel<D, IO><<<grid, PNT, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (a.g_raw || a.beta_logit) {
-      int dev = 0, nsm = 0;
-      e = cudaGetDevice(&dev);
-      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-      if (e != cudaSuccess) return e;
       const int64_t work = a.g_raw ? a.T * a.H * (int64_t)D / 4 : a.T * a.H;
       const int64_t blocks = (work + 255) / 256;
       const int64_t cap = (int64_t)nsm * 8;
