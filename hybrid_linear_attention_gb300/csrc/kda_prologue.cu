@@ -78,22 +78,24 @@ __device__ __forceinline__ void unpack8(const Raw<float> &r, float (&v)[8]) {
   v[4] = r.b.x, v[5] = r.b.y, v[6] = r.b.z, v[7] = r.b.w;
 }
 
-// Conv weights of eight consecutive channels (channel e, tap j at 4e + j): bf16 pairs kept as
-// loaded and widened on use (16 registers), fp32 as is.
+// Conv weights of eight consecutive channels (channel e, tap j at 4e + j), widened to fp32 once
+// (kept packed, they cost an unpack per tap and token: measured slower).
 template <typename IO> struct ConvW;
 template <> struct ConvW<bf16> {
-  uint32_t p[8][2];  // channel y: taps (0, 1) and (2, 3), tap 0 / 2 in the low half
+  float w[8][4];
   __device__ __forceinline__ void load(const bf16 *cw, bool act) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const uint4 u = act ? *reinterpret_cast<const uint4 *>(cw + 8 * q) : make_uint4(0, 0, 0, 0);
-      p[2 * q][0] = u.x, p[2 * q][1] = u.y, p[2 * q + 1][0] = u.z, p[2 * q + 1][1] = u.w;
+      const uint32_t p[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        w[2 * q + (e >> 1)][2 * (e & 1)] = __uint_as_float(p[e] << 16);
+        w[2 * q + (e >> 1)][2 * (e & 1) + 1] = __uint_as_float(p[e] & 0xffff0000u);
+      }
     }
   }
-  __device__ __forceinline__ float tap(int y, int j) const {
-    const uint32_t v = p[y][j >> 1];
-    return __uint_as_float((j & 1) ? (v & 0xffff0000u) : (v << 16));
-  }
+  __device__ __forceinline__ float tap(int y, int j) const { return w[y][j]; }
 };
 template <> struct ConvW<float> {
   float w[8][4];
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(PNT, 2) prologue_kernel(const ProArgs a) {
             for (int y = 0; y < 8; ++y) win[k][y] = 0.f;
         }
       }
-      float yv[8], ss = 0.f;
+      float yv[8];
 #pragma unroll
       for (int y = 0; y < 8; ++y) {
         float acc = w.tap(y, 0) * win[0][y];
@@ -189,16 +191,20 @@ __global__ void __launch_bounds__(PNT, 2) prologue_kernel(const ProArgs a) {
         acc = fmaf(w.tap(y, 2), win[2][y], acc);
         acc = fmaf(w.tap(y, 3), xv[y], acc);
         yv[y] = silu_fast(acc);
-        ss = fmaf(yv[y], yv[y], ss);
         win[0][y] = win[1][y], win[1][y] = win[2][y], win[2][y] = xv[y];
       }
-      // every lane takes part in the shuffle (a warp may hold rows of different streams)
+      if (a.l2norm_qk) {  // the same for the whole grid: every lane of a warp takes part in
+                          // the shuffle (a warp may hold rows of different streams)
+        float ss = 0.f;
 #pragma unroll
-      for (int off = TPH / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-      if (norm) {
-        const float r = rsqrtf(ss + a.l2_eps);
+        for (int y = 0; y < 8; ++y) ss = fmaf(yv[y], yv[y], ss);
 #pragma unroll
-        for (int y = 0; y < 8; ++y) yv[y] *= r;
+        for (int off = TPH / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (norm) {
+          const float r = rsqrtf(ss + a.l2_eps);
+#pragma unroll
+          for (int y = 0; y < 8; ++y) yv[y] *= r;
+        }
       }
       if (act) store8(dp, yv);
       dp += (int64_t)H * D;
