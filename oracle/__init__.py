@@ -251,3 +251,80 @@ def state_bytes(H, dk, dv, elem_bytes):
 def conv_tail_bytes(H, d, width, elem_bytes):
     """Bytes of one layer's short-convolution tail for one sequence."""
     return int(_load().oracle_conv_tail_bytes(H, d, width, elem_bytes))
+
+
+# ---------------------------------------------------------------------------------------
+# FP8 output quantisation
+# ---------------------------------------------------------------------------------------
+# The checkpoint stores block-FP8 E4M3 weights in 128 x 128 scaling blocks and quantises
+# activations dynamically ("Ling-3.1-flash: Grouped Routing and Two Different MLA Caches",
+# section "Production boundaries"); the serving setup fuses the quantisation of the KDA output
+# feeding o_proj into the KDA kernel ("Ling-3.1-flash: What 63 Linear-Attention Layers Do to
+# the KV Budget", section "Fitting it on a node").  Reading: one group per (token, head), the
+# 128 value channels that meet one 128-row block of o_proj's weight; fp32 scale =
+# max(amax, 1e-10) / 448; code = E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+# no infinities, largest finite 448) of x / scale, rounded to nearest even and saturated.
+
+FP8_MAX = 448.0
+FP8_EPS = 1e-10
+
+
+def fp8_e4m3_encode(y):
+    """E4M3 codes (uint8) of the values y, rounded to the nearest representable value (ties
+    to the even code) and saturated at +-448; NaN maps to 0x7F.  Works in the precision of
+    y's dtype: the scaling by powers of two below is exact."""
+    y = np.asarray(y)
+    a = np.abs(y)
+    sign = np.signbit(y).astype(np.uint8) << 7
+    code = np.zeros(a.shape, dtype=np.int64)
+    # subnormals and zero: multiples of 2^-9 below 2^-6 (an exact 2^-6 rounds up into the
+    # first normal binade, code 8 = exponent field 1, mantissa 0: the same value)
+    sub = a < 2.0 ** -6
+    code[sub] = np.round(a[sub] * 2.0 ** 9).astype(np.int64)
+    nrm = ~sub & np.isfinite(a)
+    e = np.floor(np.log2(np.where(nrm, a, 1.0))).astype(np.int64)
+    # guard log2 rounding at binade edges
+    e = np.where(nrm & (np.ldexp(np.ones_like(a), e) > a), e - 1, e)
+    e = np.where(nrm & (np.ldexp(np.ones_like(a), e + 1) <= a), e + 1, e)
+    m = np.round(np.ldexp(np.where(nrm, a, 1.0), -e) * 8.0).astype(np.int64) - 8  # 0 .. 8
+    carry = m == 8
+    e = np.where(carry, e + 1, e)
+    m = np.where(carry, 0, m)
+    code = np.where(nrm, ((e + 7) << 3) | m, code)
+    code = np.where(nrm & (e + 7 > 15), 0x7F, code)
+    code = np.minimum(code, 0x7E)  # above 448 (including the NaN slot 0x7F): saturate
+    code = np.where(np.isinf(a), 0x7E, code)
+    out = (code.astype(np.uint8) | sign).astype(np.uint8)
+    return np.where(np.isnan(y), np.uint8(0x7F), out)
+
+
+def fp8_e4m3_decode(codes):
+    """fp64 values of E4M3 codes (0x7F / 0xFF decode to NaN)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    s = np.where(c & 0x80, -1.0, 1.0)
+    ef, m = (c >> 3) & 0xF, c & 0x7
+    val = np.where(ef == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(ef.astype(np.float64) - 7))
+    val = np.where((ef == 15) & (m == 7), np.nan, val)
+    return s * val
+
+
+def fp8_quantize_groups(x, group=128, dtype=np.float64):
+    """Dynamic FP8 quantisation of the last axis of x in groups of `group` channels:
+    returns (codes uint8 with x's shape, scales with x.shape[:-1] + (n_groups,)).  `dtype`
+    is the precision the scale and the division are taken in (float32 reproduces a device
+    that divides in IEEE fp32)."""
+    x = np.asarray(x).astype(dtype)
+    shp = x.shape
+    xg = x.reshape(shp[:-1] + (shp[-1] // group, group))
+    amax = np.abs(xg).max(axis=-1)
+    scale = (np.maximum(amax, dtype(FP8_EPS)) / dtype(FP8_MAX)).astype(dtype)
+    codes = fp8_e4m3_encode((xg / scale[..., None]).astype(dtype))
+    return codes.reshape(shp), scale
+
+
+def fp8_dequantize_groups(codes, scales, group=128):
+    """fp64 values of grouped codes: code value x the group's scale."""
+    c = np.asarray(codes)
+    shp = c.shape
+    v = fp8_e4m3_decode(c).reshape(shp[:-1] + (shp[-1] // group, group))
+    return (v * np.asarray(scales, dtype=np.float64)[..., None]).reshape(shp)

@@ -430,3 +430,71 @@ def test_prologue_l2_and_gate_activations():
     assert np.array_equal(y[:, 2], plain[:, 2])          # v is not normalised
     np.testing.assert_allclose(r["beta"], expit(_f64(p["beta_logit"])), rtol=1e-15)
     np.testing.assert_array_equal(r["g"], np.maximum(_f64(p["g_raw"] - 1.0), -5.0))
+
+
+# ---------------------------------------------------------------------------------------
+# FP8 E4M3 output quantisation
+# ---------------------------------------------------------------------------------------
+
+def test_fp8_e4m3_codes_pinned_by_the_format():
+    """Codes fixed by the E4M3 layout (sign, 4 exponent bits with bias 7, 3 mantissa bits,
+    no infinities, largest finite 448): exact values, ties to the even code, subnormals,
+    saturation."""
+    table = [
+        (0.0, 0x00), (-0.0, 0x80), (1.0, 0x38), (-1.0, 0xB8), (0.5, 0x30), (448.0, 0x7E),
+        (-448.0, 0xFE), (240.0, 0x77), (2.0 ** -6, 0x08), (2.0 ** -9, 0x01),
+        (7 * 2.0 ** -9, 0x07),
+        (1.0625, 0x38),          # halfway 1 | 1.125: even mantissa 0
+        (1.1875, 0x3A),          # halfway 1.125 | 1.25: even mantissa 2
+        (2.0 ** -10, 0x00),      # halfway 0 | 2^-9: even code 0
+        (3 * 2.0 ** -10, 0x02),  # halfway 2^-9 | 2^-8: even code 2
+        (15 * 2.0 ** -10, 0x08), # halfway 7*2^-9 | 2^-6: rounds up into the normal binade
+        (464.0, 0x7E), (480.0, 0x7E), (1e6, 0x7E), (-1e6, 0xFE), (np.inf, 0x7E),
+    ]
+    x = np.array([v for v, _ in table])
+    got = oracle.fp8_e4m3_encode(x)
+    assert [int(c) for c in got] == [c for _, c in table]
+    assert oracle.fp8_e4m3_encode(np.array([np.nan]))[0] == 0x7F
+
+
+def test_fp8_e4m3_matches_the_library_conversion():
+    """In range, the encoder is the round-to-nearest-even conversion torch implements for
+    float8_e4m3fn (fp64 and fp32 inputs)."""
+    rng = np.random.default_rng(60)
+    x = rng.standard_normal(100000) * np.exp2(rng.uniform(-12, 9, 100000))
+    x = x[np.abs(x) <= 448.0]
+    for arr in (x, x.astype(np.float32)):
+        want = torch.from_numpy(arr).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(oracle.fp8_e4m3_encode(arr), want)
+
+
+def test_fp8_e4m3_every_code_round_trips():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = oracle.fp8_e4m3_decode(codes)
+    assert np.array_equal(oracle.fp8_e4m3_encode(vals), codes)
+    assert np.isnan(oracle.fp8_e4m3_decode(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+    pos = np.sort(vals[vals > 0])
+    assert pos[0] == 2.0 ** -9 and pos[-1] == 448.0 and len(np.unique(pos)) == 126
+
+
+def test_fp8_group_quantisation_bounds():
+    """Each group's largest magnitude lands on +-448 (code 0x7E / 0xFE); every value comes
+    back within half a step of its binade (2^-4 relative in the normal range, 2^-10 of the
+    scale in the subnormal one)."""
+    rng = np.random.default_rng(61)
+    x = rng.standard_normal((37, 3, 256)) * np.exp2(rng.uniform(-6, 6, (37, 3, 1)))
+    codes, scales = oracle.fp8_quantize_groups(x, 128)
+    assert scales.shape == (37, 3, 2)
+    xg = x.reshape(37, 3, 2, 128)
+    np.testing.assert_allclose(scales, np.abs(xg).max(-1) / 448.0, rtol=1e-15)
+    cg = codes.reshape(37, 3, 2, 128)
+    top = np.abs(xg).argmax(-1)
+    assert np.isin(np.take_along_axis(cg, top[..., None], -1), [0x7E, 0xFE]).all()
+    deq = oracle.fp8_dequantize_groups(codes, scales, 128).reshape(xg.shape)
+    y = np.abs(xg) / scales[..., None]
+    half = np.where(y >= 2.0 ** -6, np.exp2(np.floor(np.log2(np.maximum(y, 2.0 ** -6))) - 4),
+                    2.0 ** -10)
+    assert (np.abs(deq - xg) <= half * scales[..., None] * (1 + 1e-12)).all()
+    # an all-zero group keeps a positive scale and zero codes
+    z_codes, z_scales = oracle.fp8_quantize_groups(np.zeros((2, 128)), 128)
+    assert (z_codes == 0).all() and (z_scales > 0).all()
