@@ -300,14 +300,16 @@ kda_status kda_decode_step(const kda_params *p, const void *q, const void *k, co
                 1);
 }
 
-kda_status kda_decode_step_fused(const kda_params *p, const void *x_raw, const void *conv_w,
-                                 void *conv_state, const float *g, const float *beta,
-                                 void *state, int n_slots, const int32_t *slot_idx, int n_seqs,
-                                 const void *gate_logit, const float *norm_w, void *out,
-                                 cudaStream_t stream) {
+static kda_status decode_fused_impl(const kda_params *p, const void *x_raw, const void *conv_w,
+                                    void *conv_state, const float *g, const float *beta,
+                                    void *state, int n_slots, const int32_t *slot_idx,
+                                    int n_seqs, const void *gate_logit, const float *norm_w,
+                                    void *out, uint8_t *out_q, float *out_scale,
+                                    cudaStream_t stream) {
   kda_status st = decode_common(p, g, beta, state, n_slots, slot_idx, n_seqs, gate_logit,
-                                norm_w, out);
+                                norm_w, out_q ? static_cast<void *>(out_q) : out);
   if (st != KDA_OK || n_seqs == 0) return st;
+  if (out_q && (!out_scale || !aligned16(out_scale))) return KDA_ERR_INVALID_ARG;
   if (!x_raw || !conv_w || !conv_state || !aligned16(x_raw) || !aligned16(conv_w) ||
       !aligned16(conv_state))
     return KDA_ERR_INVALID_ARG;
@@ -324,9 +326,29 @@ kda_status kda_decode_step_fused(const kda_params *p, const void *x_raw, const v
   a.gate = gate_logit;
   a.norm_w = norm_w;
   a.out = out;
+  a.out_q = out_q, a.out_scale = out_scale;
   return finish(kda::launch_recurrent(a, p->d_k, p->io_dtype == KDA_BF16,
                                       p->state_dtype == KDA_BF16, stream),
                 1);
+}
+
+kda_status kda_decode_step_fused(const kda_params *p, const void *x_raw, const void *conv_w,
+                                 void *conv_state, const float *g, const float *beta,
+                                 void *state, int n_slots, const int32_t *slot_idx, int n_seqs,
+                                 const void *gate_logit, const float *norm_w, void *out,
+                                 cudaStream_t stream) {
+  return decode_fused_impl(p, x_raw, conv_w, conv_state, g, beta, state, n_slots, slot_idx,
+                           n_seqs, gate_logit, norm_w, out, nullptr, nullptr, stream);
+}
+
+kda_status kda_decode_step_fused_fp8(const kda_params *p, const void *x_raw,
+                                     const void *conv_w, void *conv_state, const float *g,
+                                     const float *beta, void *state, int n_slots,
+                                     const int32_t *slot_idx, int n_seqs,
+                                     const void *gate_logit, const float *norm_w,
+                                     uint8_t *out_q, float *out_scale, cudaStream_t stream) {
+  return decode_fused_impl(p, x_raw, conv_w, conv_state, g, beta, state, n_slots, slot_idx,
+                           n_seqs, gate_logit, norm_w, nullptr, out_q, out_scale, stream);
 }
 
 kda_status kda_conv_state_update(const kda_params *p, const void *x_new, const void *conv_w,

@@ -34,7 +34,9 @@ struct RecArgs {
   void *state_out;             // same layout, or nullptr; may equal state_in
   const void *gate;            // [T, H, D] io or nullptr
   const float *norm_w;         // [D] or nullptr
-  void *out;                   // [T, H, D] io
+  void *out;                   // [T, H, D] io (unused when out_q is set)
+  uint8_t *out_q;              // [T, H, D] FP8 E4M3 codes of the output, or nullptr
+  float *out_scale;            // [T, H] fp32 scale of each (token, head) group
   int *err;
 };
 

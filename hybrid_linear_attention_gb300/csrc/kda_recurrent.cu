@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
   __shared__ float s_beta[TT], s_rq[TT], s_rk[TT], s_kq[TT];
   __shared__ float s_redp[RG][D], s_redo[RG][D];
   __shared__ float s_u[D];
-  __shared__ float s_ss[NW];
+  __shared__ float s_ss[NW], s_amax[NW];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cg = tid % CG, rg = tid / CG;
@@ -245,8 +245,8 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
             store4(dst + (size_t)(rg * RPT + r) * D + 4 * cg,
                    make_float4(S[r][0], S[r][1], S[r][2], S[r][3]));
         }
+        const size_t row = ((size_t)(t0 + tt) * H + h) * D + tid;
         if (tid < D) {
-          const size_t row = ((size_t)(t0 + tt) * H + h) * D + tid;
           if (GATE) {
             float ss = 0.f;
 #pragma unroll
@@ -256,7 +256,21 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
             const float z = to_f(reinterpret_cast<const IO *>(a.gate)[row]);
             o = o * r * w * sigmoidf_(z);
           }
-          reinterpret_cast<IO *>(a.out)[row] = from_f<IO>(o);
+          if (!a.out_q) reinterpret_cast<IO *>(a.out)[row] = from_f<IO>(o);
+        }
+        if (a.out_q) {  // the same for the whole grid, so every thread meets the barrier
+          // FP8 output: the group's amax over its D values (warp max, then across warps)
+          const float m = warp_max(tid < D ? fabsf(o) : 0.f);
+          if (lane == 0 && warp < (D + 31) / 32) s_amax[warp] = m;
+          __syncthreads();
+          if (tid < D) {
+            float amax = 0.f;
+#pragma unroll
+            for (int w = 0; w < (D + 31) / 32; ++w) amax = fmaxf(amax, s_amax[w]);
+            const float sc = fp8_scale(amax);
+            a.out_q[row] = fp8_code(o, sc);
+            if (tid == 0) a.out_scale[(size_t)(t0 + tt) * H + h] = sc;
+          }
         }
       }
     }

@@ -27,7 +27,7 @@ EXPORTS = (
     "kda_params_default", "kda_status_string", "kda_state_bytes", "kda_prefill_workspace_size",
     "kda_prologue", "kda_prefill", "kda_prefill_checkpointed", "kda_conv_tail_checkpoints",
     "kda_decode_step", "kda_conv_state_update",
-    "kda_decode_step_fused", "kda_decode_multi", "kda_state_accept", "kda_check_device_error",
+    "kda_decode_step_fused", "kda_decode_step_fused_fp8", "kda_decode_multi", "kda_state_accept", "kda_check_device_error",
     "kda_launch_count",
 )
 
@@ -91,6 +91,8 @@ def load():
                                              _vp]),
             "kda_decode_step_fused": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32,
                                              _vp, _vp, _vp, _vp]),
+            "kda_decode_step_fused_fp8": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp,
+                                                 _i32, _vp, _vp, _vp, _vp, _vp]),
             "kda_decode_multi": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
                                         _vp, _vp, _vp, _vp, _i32, _vp]),
             "kda_state_accept": (_i32, [_P, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp]),
@@ -247,6 +249,21 @@ def kda_decode_step_fused(p, x_raw, conv_w, conv_state, g, beta, state, out, *, 
         _ptr(gate_logit, io, "gate_logit"), _ptr(norm_w, torch.float32, "norm_w"),
         _ptr(out, io, "out"), _stream(stream))
     _check(st, "kda_decode_step_fused")
+
+
+def kda_decode_step_fused_fp8(p, x_raw, conv_w, conv_state, g, beta, state, out_q, out_scale, *,
+                              slot_idx=None, gate_logit=None, norm_w=None, stream=None):
+    """out_q [n_seqs, H, d] uint8 E4M3 codes, out_scale [n_seqs, H] fp32."""
+    io, sd = p.io_torch, p.state_torch
+    st = load().kda_decode_step_fused_fp8(
+        ctypes.byref(p), _ptr(x_raw, io, "x_raw"), _ptr(conv_w, io, "conv_w"),
+        _ptr(conv_state, io, "conv_state"), _ptr(g, torch.float32, "g"),
+        _ptr(beta, torch.float32, "beta"), _ptr(state, sd, "state"), state.shape[0],
+        _ptr(slot_idx, torch.int32, "slot_idx"), x_raw.shape[0],
+        _ptr(gate_logit, io, "gate_logit"), _ptr(norm_w, torch.float32, "norm_w"),
+        _ptr(out_q, torch.uint8, "out_q"), _ptr(out_scale, torch.float32, "out_scale"),
+        _stream(stream))
+    _check(st, "kda_decode_step_fused_fp8")
 
 
 def kda_decode_multi(p, q, k, v, g, beta, state, out, K, *, slot_idx=None, gate_logit=None,

@@ -241,6 +241,29 @@ kda_status kda_decode_step_fused(const kda_params* p, const void* x_raw, const v
                                  cudaStream_t stream);
 
 /*
+ * kda_decode_step_fused_fp8 -- kda_decode_step_fused whose output leaves the kernel already
+ * quantised for a block-FP8 o_proj.  The checkpoint's weights are E4M3 in 128 x 128 scaling
+ * blocks with dynamic activation quantisation ("Ling-3.1-flash: Grouped Routing and Two
+ * Different MLA Caches", section "Production boundaries"), and the serving setup fuses this
+ * quantisation into the KDA kernel for decode ("Ling-3.1-flash: What 63 Linear-Attention
+ * Layers Do to the KV Budget", section "Fitting it on a node").  One group = the d values of
+ * one (sequence, head): the 128 input channels that meet one weight block.
+ *
+ *   out_q      [n_seqs, H, d] uint8: E4M3 codes (1 sign, 4 exponent bits with bias 7,
+ *              3 mantissa bits, no infinities) of o / scale, rounded to nearest even and
+ *              saturated at +-448.
+ *   out_scale  [n_seqs, H] fp32: scale = max(amax, 1e-10) / 448, amax = max |o| over the
+ *              group (o after the output norm and gate when gate logits are given).
+ *   Both divisions are IEEE fp32 round-to-nearest.  Other arguments as kda_decode_step_fused.
+ */
+kda_status kda_decode_step_fused_fp8(const kda_params* p, const void* x_raw,
+                                     const void* conv_w, void* conv_state, const float* g,
+                                     const float* beta, void* state, int n_slots,
+                                     const int32_t* slot_idx, int n_seqs,
+                                     const void* gate_logit, const float* norm_w,
+                                     uint8_t* out_q, float* out_scale, cudaStream_t stream);
+
+/*
  * kda_decode_multi -- K tokens for each of n_seqs sequences (a speculative draft), from the
  * state in its pool slot, keeping the state after every token for rollback.  The pages
  * count speculative rollback state among the per-sequence costs of a KDA layer

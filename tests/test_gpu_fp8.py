@@ -1,0 +1,132 @@
+"""GPU parity: the FP8 (E4M3) output quantisation fused into the KDA epilogue.
+
+Two checks.  (1) Bit-exact quantiser: with fp32 I/O the kernel's unquantised output is its
+own fp32 value, so the oracle's quantiser run in fp32 on that output must give the same codes
+and scales bit for bit (the decision is taken in the same precision on both sides).  (2) The
+dequantised output against the fp64 oracle: within half an E4M3 step of the value (2^-4
+relative in the normal range, 2^-10 of the scale below it) plus the output tolerance.
+The quantised launch leaves the state and conv tail updates bit-identical to the plain one.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hybrid_linear_attention_gb300 import inputs, kda
+from tests import _gpu
+from tests._parity import rms, to64
+from tests.test_gpu_core import _decode_reference
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-4, torch.bfloat16: 1e-2}
+
+
+def _setup(H, d, n, slots_n, K, io, gate, seed):
+    C = 3 * H * d
+    S0 = inputs.normal((slots_n, H, d, d), seed=seed, dtype=torch.float32, std=0.02)
+    cs0 = inputs.normal((slots_n, 3, C), seed=seed + 1, dtype=io)
+    w = inputs.normal((C, 4), seed=seed + 2, std=0.5, dtype=io)
+    steps = [inputs.decode_inputs(n, H, d, seed=seed + 10 + t, io_dtype=io, gate=gate)
+             for t in range(K)]
+    norm_w = inputs.normal((d,), seed=seed + 3, dtype=torch.float32) if gate else None
+    return S0, cs0, w, steps, norm_w
+
+
+def _run(p, S0, cs0, w, steps, norm_w, slots, gate, fp8):
+    n, H, d = steps[0]["g"].shape
+    state, cs = S0.cuda().clone(), cs0.cuda().clone()
+    slot_t = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    outs = []
+    for st in steps:
+        common = dict(slot_idx=slot_t, gate_logit=st["gate"].cuda() if gate else None,
+                      norm_w=norm_w.cuda() if gate else None)
+        if fp8:
+            q = torch.empty((n, H, d), dtype=torch.uint8, device="cuda")
+            sc = torch.empty((n, H), dtype=torch.float32, device="cuda")
+            kda.kda_decode_step_fused_fp8(p, st["x"].cuda(), w.cuda(), cs, st["g"].cuda(),
+                                          st["beta"].cuda(), state, q, sc, **common)
+            outs.append((q, sc))
+        else:
+            out = torch.empty((n, H, d), dtype=p.io_torch, device="cuda")
+            kda.kda_decode_step_fused(p, st["x"].cuda(), w.cuda(), cs, st["g"].cuda(),
+                                      st["beta"].cuda(), state, out, **common)
+            outs.append(out)
+    torch.cuda.synchronize()
+    kda.kda_check_device_error()
+    return outs, state, cs
+
+
+@pytest.mark.parametrize("gate", [False, True])
+@pytest.mark.parametrize("d", [128, 16])
+def test_fp8_codes_are_the_quantisation_of_the_fp32_output(gate, d):
+    H, n, slots_n, K = 3, 5, 7, 3
+    slots = [6, 0, 3, 2, 5]
+    io = torch.float32
+    p = kda.params(H=H, d=d, io_dtype=io)
+    _gpu.lib()
+    S0, cs0, w, steps, norm_w = _setup(H, d, n, slots_n, K, io, gate, seed=700)
+    plain, st_a, cs_a = _run(p, S0, cs0, w, steps, norm_w, slots, gate, fp8=False)
+    quant, st_b, cs_b = _run(p, S0, cs0, w, steps, norm_w, slots, gate, fp8=True)
+    # the state and conv-tail updates do not depend on the output format
+    assert torch.equal(st_a, st_b) and torch.equal(cs_a, cs_b)
+    for o32, (q, sc) in zip(plain, quant):
+        want_q, want_sc = oracle.fp8_quantize_groups(o32.cpu().numpy(), d, dtype=np.float32)
+        assert np.array_equal(sc.cpu().numpy(), want_sc[..., 0])
+        assert np.array_equal(q.cpu().numpy(), want_q)
+
+
+@pytest.mark.parametrize("io", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("gate", [False, True])
+def test_fp8_decode_matches_the_oracle(io, gate):
+    H, d, n, slots_n, K = 4, 128, 6, 9, 4
+    slots = [8, 2, 0, 5, 3, 7]
+    p = kda.params(H=H, d=d, io_dtype=io)
+    _gpu.lib()
+    S0, cs0, w, steps, norm_w = _setup(H, d, n, slots_n, K, io, gate, seed=720)
+    quant, state, cs = _run(p, S0, cs0, w, steps, norm_w, slots, gate, fp8=True)
+    x_steps = torch.stack([st["x"] for st in steps])
+    g_steps = torch.stack([st["g"] for st in steps])
+    b_steps = torch.stack([st["beta"] for st in steps])
+    gate_steps = torch.stack([st["gate"] for st in steps]) if gate else None
+    ref_out, ref_fin, _ = _decode_reference(x_steps, w, cs0, S0, g_steps, b_steps, H, d, slots,
+                                            gate_steps, norm_w)
+    for t, (q, sc) in enumerate(quant):
+        ref = ref_out[t]                                     # [n, H, d] fp64
+        sc64 = to64(sc)
+        deq = oracle.fp8_dequantize_groups(q.cpu().numpy(), sc64[..., None], d)
+        # the scale is the group's amax / 448 up to the output error
+        np.testing.assert_allclose(sc64, np.abs(ref).max(-1) / 448.0,
+                                   rtol=0, atol=TOL[io] * rms(ref) / 448.0 * 4)
+        # half a step of the binade the value or its code lies in (a value just below a
+        # binade edge may round up into the next, coarser one)
+        y = np.maximum(np.abs(ref), np.abs(deq)) / sc64[..., None]
+        half = np.where(y >= 2.0 ** -6, np.exp2(np.floor(np.log2(np.maximum(y, 2.0 ** -6))) - 4),
+                        2.0 ** -10) * sc64[..., None]
+        excess = np.maximum(np.abs(deq - ref) - half * (1 + 2 ** -6), 0.0)
+        assert excess.max() <= TOL[io] * rms(ref), f"step {t}: {excess.max() / rms(ref):.3g}"
+    st_cpu = state.cpu()
+    for s in slots:
+        np.testing.assert_allclose(to64(st_cpu[s]), ref_fin[s], rtol=0,
+                                   atol=1e-3 * rms(ref_fin[s]))
+
+
+def test_fp8_decode_rejects_missing_scales():
+    H, d, n = 2, 128, 2
+    p = kda.params(H=H, d=d)
+    _gpu.lib()
+    C = 3 * H * d
+    x = torch.zeros((n, C), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((C, 4), dtype=torch.bfloat16, device="cuda")
+    cs = torch.zeros((n, 3, C), dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros((n, H, d), device="cuda")
+    b = torch.zeros((n, H), device="cuda")
+    state = torch.zeros((n, H, d, d), device="cuda")
+    q = torch.empty((n, H, d), dtype=torch.uint8, device="cuda")
+    lib = kda.load()
+    st = lib.kda_decode_step_fused_fp8(
+        ctypes.byref(p), x.data_ptr(), w.data_ptr(), cs.data_ptr(), g.data_ptr(),
+        b.data_ptr(), state.data_ptr(), n, None, n, None, None, q.data_ptr(), None, None)
+    assert st == kda.KDA_ERR_INVALID_ARG
