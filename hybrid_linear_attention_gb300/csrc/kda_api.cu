@@ -154,9 +154,10 @@ static kda_status prefill_impl(const kda_params *p, const void *q, const void *k
                                const float *g, const float *beta, const void *init_state,
                                const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
                                const void *gate_logit, const float *norm_w, void *out,
-                               void *final_state, const int32_t *ckpt_cu,
-                               const int32_t *ckpt_pos, int n_ckpt, void *ckpt_states,
-                               void *workspace, size_t ws_bytes, cudaStream_t stream) {
+                               uint8_t *out_q, float *out_scale, void *final_state,
+                               const int32_t *ckpt_cu, const int32_t *ckpt_pos, int n_ckpt,
+                               void *ckpt_states, void *workspace, size_t ws_bytes,
+                               cudaStream_t stream) {
   kda_status st = check_params(p);
   if (st != KDA_OK) return st;
   if (n_seqs < 0 || total_tokens < 0 || n_seqs > 65535) return KDA_ERR_INVALID_ARG;
@@ -165,7 +166,10 @@ static kda_status prefill_impl(const kda_params *p, const void *q, const void *k
   (void)workspace;
   if (n_seqs == 0) return KDA_OK;
   if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
-  if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !(out_q ? out_scale : out)))
+    return KDA_ERR_INVALID_ARG;
+  if (total_tokens > 0 && out_q && (!aligned16(out_q) || !aligned16(out_scale)))
+    return KDA_ERR_INVALID_ARG;
   if (!opt_aligned16(q) || !opt_aligned16(k) || !opt_aligned16(v) || !opt_aligned16(g) ||
       !opt_aligned16(beta) || !opt_aligned16(init_state) || !aligned16(cu_seqlens) ||
       !opt_aligned16(gate_logit) || !opt_aligned16(norm_w) || !opt_aligned16(out) ||
@@ -196,6 +200,7 @@ static kda_status prefill_impl(const kda_params *p, const void *q, const void *k
     t.norm_w = norm_w;
     t.out = out;
     t.ckpt_cu = ckpt_cu, t.ckpt_pos = ckpt_pos, t.ckpt_states = ckpt_states;
+    t.out_q = out_q, t.out_scale = out_scale;
     t.total = total_tokens, t.n_ckpt = n_ckpt;
     t.err = device_error_ptr();
     return finish(kda::launch_prefill_tc(t, total_tokens, st_bf16, stream), 1);
@@ -212,6 +217,7 @@ static kda_status prefill_impl(const kda_params *p, const void *q, const void *k
   a.out = out;
   a.ckpt_cu = ckpt_cu, a.ckpt_pos = ckpt_pos, a.ckpt_states = ckpt_states;
   a.total = total_tokens, a.n_ckpt = n_ckpt;
+  a.out_q = out_q, a.out_scale = out_scale;
   return finish(kda::launch_recurrent(a, p->d_k, io_bf16, st_bf16, stream), 1);
 }
 
@@ -222,8 +228,20 @@ kda_status kda_prefill(const kda_params *p, const void *q, const void *k, const 
                        void *final_state, void *workspace, size_t ws_bytes,
                        cudaStream_t stream) {
   return prefill_impl(p, q, k, v, g, beta, init_state, cu_seqlens, n_seqs, total_tokens,
-                      gate_logit, norm_w, out, final_state, nullptr, nullptr, 0, nullptr,
-                      workspace, ws_bytes, stream);
+                      gate_logit, norm_w, out, nullptr, nullptr, final_state, nullptr, nullptr, 0,
+                      nullptr, workspace, ws_bytes, stream);
+}
+
+kda_status kda_prefill_fp8(const kda_params *p, const void *q, const void *k, const void *v,
+                           const float *g, const float *beta, const void *init_state,
+                           const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
+                           const void *gate_logit, const float *norm_w, uint8_t *out_q,
+                           float *out_scale, void *final_state, void *workspace,
+                           size_t ws_bytes, cudaStream_t stream) {
+  if (total_tokens > 0 && !out_q) return KDA_ERR_INVALID_ARG;
+  return prefill_impl(p, q, k, v, g, beta, init_state, cu_seqlens, n_seqs, total_tokens,
+                      gate_logit, norm_w, nullptr, out_q, out_scale, final_state, nullptr,
+                      nullptr, 0, nullptr, workspace, ws_bytes, stream);
 }
 
 kda_status kda_prefill_checkpointed(const kda_params *p, const void *q, const void *k,
@@ -236,8 +254,8 @@ kda_status kda_prefill_checkpointed(const kda_params *p, const void *q, const vo
                                     size_t ws_bytes, cudaStream_t stream) {
   if (n_ckpt < 1) return KDA_ERR_INVALID_ARG;
   return prefill_impl(p, q, k, v, g, beta, init_state, cu_seqlens, n_seqs, total_tokens,
-                      gate_logit, norm_w, out, final_state, ckpt_cu, ckpt_pos, n_ckpt,
-                      ckpt_states, workspace, ws_bytes, stream);
+                      gate_logit, norm_w, out, nullptr, nullptr, final_state, ckpt_cu, ckpt_pos,
+                      n_ckpt, ckpt_states, workspace, ws_bytes, stream);
 }
 
 kda_status kda_conv_tail_checkpoints(const kda_params *p, const void *x_raw,

@@ -207,7 +207,7 @@ struct Maps {
 
 // PAIR: a cluster of two CTAs per (head, sequence), rank 0 the consumer (state walk), rank 1
 // the producer (A, P', T); otherwise one CTA does both.
-template <typename ST, bool GATE, bool PAIR>
+template <typename ST, bool GATE, bool PAIR, bool QUANT>
 __global__ void __launch_bounds__(NT, 1)
     prefill_tc_kernel(const TcArgs a, const __grid_constant__ Maps maps) {
   extern __shared__ uint8_t smem_raw[];
@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(NT, 1)
   __shared__ __align__(16) float s_gC[D];     // log2-retention at the chunk's last token
   __shared__ float s_GC[D];                   // Gamma_C
   __shared__ float s_red[4][C];
+  __shared__ float s_amx[4][C];  // FP8 output: each row's amax by TMEM lane quarter
   __shared__ __align__(16) float s_M[3 * 256];  // inverse scratch; block decays P1 -> P2
   __shared__ __align__(8) uint64_t s_bar[NBAR];
   __shared__ uint32_t s_tmem, s_abort, s_pend, s_ppar[NBAR];
@@ -809,7 +810,87 @@ __global__ void __launch_bounds__(NT, 1)
       const bool tile = nv == C;
       bf16 *stage = reinterpret_cast<bf16 *>(sm + OFF_V);  // V was consumed by the Y pass
       bf16 *out = reinterpret_cast<bf16 *>(a.out);
-      if (GATE) {
+      if (QUANT) {
+        // FP8 output (E4M3 codes, one fp32 scale per token): a row's scale needs all of its
+        // 128 values, so this thread holds its channel's 32 rows at once and a second
+        // transpose-reduce over the warp, then over the four lane quarters, gives each
+        // row's amax
+        float o[32];
+        {
+          float u[32];
+          tmem_ld32(tm + lane_off + TM_C + 64 + 32 * grp, o);
+          tmem_ld32(tm + lane_off + TM_A + 32 * grp, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 32; ++x)
+            o[x] = a.scale * fmaf(s_pd[par][32 * grp + x], u[x], o[x]);
+        }
+        if (GATE) {
+          float sq[32];
+#pragma unroll
+          for (int x = 0; x < 32; ++x) sq[x] = o[x] * o[x];
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) {
+            const bool up = (lane & off) != 0;
+#pragma unroll
+            for (int x = 0; x < off; ++x) {
+              const float send = up ? sq[x] : sq[x + off];
+              const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+              sq[x] = (up ? sq[x + off] : sq[x]) + recv;
+            }
+          }
+          s_red[quarter][32 * grp + lane] = sq[0];
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+          const float w = a.norm_w ? a.norm_w[j] : 1.f;
+          const bf16 *gate = reinterpret_cast<const bf16 *>(a.gate);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const int r = 32 * grp + x;
+            if (r < nv) {
+              const size_t row = ((size_t)(t0 + r) * H + h) * D + j;
+              const float ss = s_red[0][r] + s_red[1][r] + s_red[2][r] + s_red[3][r];
+              o[x] = o[x] * rsqrtf(ss * (1.f / D) + a.norm_eps) * w *
+                     sigmoidf_(__bfloat162float(gate[row]));
+            }
+          }
+        }
+#pragma unroll
+        for (int x = 0; x < 32; ++x)
+          if (32 * grp + x >= nv) o[x] = 0.f;
+        float mx[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) mx[x] = fabsf(o[x]);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {  // mx[0] ends as row (32 grp + lane)
+          const bool up = (lane & off) != 0;
+#pragma unroll
+          for (int x = 0; x < off; ++x) {
+            const float send = up ? mx[x] : mx[x + off];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+            mx[x] = fmaxf(up ? mx[x + off] : mx[x], recv);
+          }
+        }
+        s_amx[quarter][32 * grp + lane] = mx[0];
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        uint8_t *stage8 = sm + OFF_V;
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const int r = 32 * grp + x;
+          if (r < nv) {
+            const float sc = fp8_scale(fmaxf(fmaxf(s_amx[0][r], s_amx[1][r]),
+                                             fmaxf(s_amx[2][r], s_amx[3][r])));
+            const uint8_t code = fp8_code(o[x], sc);
+            if (tile) stage8[r * D + j] = code;
+            else a.out_q[((size_t)(t0 + r) * H + h) * D + j] = code;
+          }
+        }
+        if (quarter == 0) {
+          const int r = 32 * grp + lane;
+          if (r < nv)
+            a.out_scale[(size_t)(t0 + r) * H + h] = fp8_scale(
+                fmaxf(fmaxf(s_amx[0][r], s_amx[1][r]), fmaxf(s_amx[2][r], s_amx[3][r])));
+        }
+      } else if (GATE) {
         float o[32], u[32];
         tmem_ld32(tm + lane_off + TM_C + 64 + 32 * grp, o);
         tmem_ld32(tm + lane_off + TM_A + 32 * grp, u);
@@ -1098,32 +1179,35 @@ bool make_map(CUtensorMap *m, const void *ptr, bool f32, int64_t T, int H) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// output [T, H, 128] bf16: plain (unswizzled) boxes of 64 tokens x 128 channels
-bool make_out_map(CUtensorMap *m, void *ptr, int64_t T, int H) {
+// output [T, H, 128] bf16 (or FP8 codes, one byte each): plain (unswizzled) boxes of 64
+// tokens x 128 channels
+bool make_out_map(CUtensorMap *m, void *ptr, int64_t T, int H, bool fp8) {
+  const int esz = fp8 ? 1 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint64_t strides[2] = {(cuuint64_t)D * esz, (cuuint64_t)H * D * esz};
   cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)C};
   cuuint32_t es[3] = {1, 1, 1};
   auto fn = encode_fn();
   if (!fn) return false;
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, es,
+  return fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr,
+            dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename ST, bool GATE, bool PAIR>
+template <typename ST, bool GATE, bool PAIR, bool QUANT>
 cudaError_t launch_typed(const TcArgs &a, const Maps &maps, cudaStream_t s) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<ST, GATE, PAIR>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<ST, GATE, PAIR, QUANT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   if (!PAIR) {
-    prefill_tc_kernel<ST, GATE, PAIR><<<dim3(a.H, a.n_seqs), NT, SMEM_BYTES, s>>>(a, maps);
+    prefill_tc_kernel<ST, GATE, PAIR, QUANT><<<dim3(a.H, a.n_seqs), NT, SMEM_BYTES, s>>>(a, maps);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg;
@@ -1139,7 +1223,7 @@ cudaError_t launch_typed(const TcArgs &a, const Maps &maps, cudaStream_t s) {
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<ST, GATE, PAIR>, a, maps);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<ST, GATE, PAIR, QUANT>, a, maps);
 }
 
 // A cluster pair per (head, sequence) when the pairs fit on the device at once (small
@@ -1154,6 +1238,23 @@ bool use_pair(const TcArgs &a) {
   if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return false;
   return (int64_t)a.n_seqs * a.H * 2 <= nsm;
+}
+
+template <bool QUANT>
+cudaError_t dispatch(const TcArgs &a, const Maps &maps, bool st_bf16, bool gate, bool pair,
+                     cudaStream_t s) {
+  if (pair) {
+    if (st_bf16)
+      return gate ? launch_typed<bf16, true, true, QUANT>(a, maps, s)
+                  : launch_typed<bf16, false, true, QUANT>(a, maps, s);
+    return gate ? launch_typed<float, true, true, QUANT>(a, maps, s)
+                : launch_typed<float, false, true, QUANT>(a, maps, s);
+  }
+  if (st_bf16)
+    return gate ? launch_typed<bf16, true, false, QUANT>(a, maps, s)
+                : launch_typed<bf16, false, false, QUANT>(a, maps, s);
+  return gate ? launch_typed<float, true, false, QUANT>(a, maps, s)
+              : launch_typed<float, false, false, QUANT>(a, maps, s);
 }
 
 }  // namespace
@@ -1178,22 +1279,13 @@ cudaError_t launch_prefill_tc(const TcArgs &a, int64_t total_tokens, bool st_bf1
         !make_map(&maps.k, a.k, false, total_tokens, a.H) ||
         !make_map(&maps.v, a.v, false, total_tokens, a.H) ||
         !make_map(&maps.g, a.g, true, total_tokens, a.H) ||
-        !make_out_map(&maps.out, a.out, total_tokens, a.H))
+        !make_out_map(&maps.out, a.out_q ? static_cast<void *>(a.out_q) : a.out, total_tokens,
+                      a.H, a.out_q != nullptr))
       return cudaErrorInvalidValue;
   }
-  const bool gate = a.gate != nullptr;
-  if (use_pair(a)) {
-    if (st_bf16)
-      return gate ? launch_typed<bf16, true, true>(a, maps, s)
-                  : launch_typed<bf16, false, true>(a, maps, s);
-    return gate ? launch_typed<float, true, true>(a, maps, s)
-                : launch_typed<float, false, true>(a, maps, s);
-  }
-  if (st_bf16)
-    return gate ? launch_typed<bf16, true, false>(a, maps, s)
-                : launch_typed<bf16, false, false>(a, maps, s);
-  return gate ? launch_typed<float, true, false>(a, maps, s)
-              : launch_typed<float, false, false>(a, maps, s);
+  const bool gate = a.gate != nullptr, pair = use_pair(a);
+  if (a.out_q) return dispatch<true>(a, maps, st_bf16, gate, pair, s);
+  return dispatch<false>(a, maps, st_bf16, gate, pair, s);
 }
 
 }  // namespace kda

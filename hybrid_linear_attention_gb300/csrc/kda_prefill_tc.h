@@ -19,6 +19,8 @@ struct TcArgs {
   const void *gate;            // [T, H, 128] bf16 or nullptr
   const float *norm_w;         // [128] or nullptr
   void *out;                   // [T, H, 128] bf16
+  uint8_t *out_q;              // FP8 E4M3 output codes [T, H, D] (instead of out), or nullptr
+  float *out_scale;            // [T, H] fp32 scale of each (token, head) group
   int64_t total;               // rows of q, k, v, g, out (sequence offsets are checked against it)
   int n_ckpt;                  // checkpoints (checkpoint ranges are checked against it)
   const int32_t *ckpt_cu;      // checkpoints of sequence n: ckpt_cu[n] .. ckpt_cu[n+1], or null

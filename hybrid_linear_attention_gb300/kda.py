@@ -25,7 +25,8 @@ _TORCH_OF = {KDA_F32: torch.float32, KDA_BF16: torch.bfloat16}
 
 EXPORTS = (
     "kda_params_default", "kda_status_string", "kda_state_bytes", "kda_prefill_workspace_size",
-    "kda_prologue", "kda_prefill", "kda_prefill_checkpointed", "kda_conv_tail_checkpoints",
+    "kda_prologue", "kda_prefill", "kda_prefill_fp8", "kda_prefill_checkpointed",
+    "kda_conv_tail_checkpoints",
     "kda_decode_step", "kda_conv_state_update",
     "kda_decode_step_fused", "kda_decode_step_fused_fp8", "kda_decode_multi", "kda_state_accept", "kda_check_device_error",
     "kda_launch_count",
@@ -80,6 +81,8 @@ def load():
                                     _vp, _vp, _vp, _vp, _vp, _vp]),
             "kda_prefill": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp,
                                    _vp, _vp, _vp, _sz, _vp]),
+            "kda_prefill_fp8": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _vp,
+                                       _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
             "kda_prefill_checkpointed": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
                                                 _i64, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp,
                                                 _vp, _sz, _vp]),
@@ -195,6 +198,22 @@ def kda_prefill(p, q, k, v, g, beta, cu_seqlens, out, *, init_state=None, final_
         _ptr(final_state, sd, "final_state"), _ptr(workspace, None, "workspace"), ws_bytes,
         _stream(stream))
     _check(st, "kda_prefill")
+
+
+def kda_prefill_fp8(p, q, k, v, g, beta, cu_seqlens, out_q, out_scale, *, init_state=None,
+                    final_state=None, gate_logit=None, norm_w=None, workspace=None, stream=None):
+    """out_q [T, H, d] uint8 E4M3 codes, out_scale [T, H] fp32 (one group per token, head)."""
+    io, sd = p.io_torch, p.state_torch
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().kda_prefill_fp8(
+        ctypes.byref(p), _ptr(q, io, "q"), _ptr(k, io, "k"), _ptr(v, io, "v"),
+        _ptr(g, torch.float32, "g"), _ptr(beta, torch.float32, "beta"),
+        _ptr(init_state, sd, "init_state"), _ptr(cu_seqlens, torch.int32, "cu_seqlens"),
+        cu_seqlens.numel() - 1, q.shape[0], _ptr(gate_logit, io, "gate_logit"),
+        _ptr(norm_w, torch.float32, "norm_w"), _ptr(out_q, torch.uint8, "out_q"),
+        _ptr(out_scale, torch.float32, "out_scale"), _ptr(final_state, sd, "final_state"),
+        _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream))
+    _check(st, "kda_prefill_fp8")
 
 
 def kda_prefill_checkpointed(p, q, k, v, g, beta, cu_seqlens, out, ckpt_cu, ckpt_pos,

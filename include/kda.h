@@ -147,6 +147,23 @@ kda_status kda_prefill(const kda_params* p, const void* q, const void* k, const 
                        cudaStream_t stream);
 
 /*
+ * kda_prefill_fp8 -- kda_prefill whose output leaves the kernel quantised for a block-FP8
+ * o_proj, as kda_decode_step_fused_fp8 does for decode (same pages, same reading): one group
+ * per (token, head).
+ *
+ *   out_q      [T_tot, H, d_v] uint8 E4M3 codes of o / scale (nearest even, saturated).
+ *   out_scale  [T_tot, H] fp32: max(amax, 1e-10) / 448 over the group's d_v values (after
+ *              the output norm and gate when gate logits are given).
+ *   Other arguments as kda_prefill.
+ */
+kda_status kda_prefill_fp8(const kda_params* p, const void* q, const void* k, const void* v,
+                           const float* g, const float* beta, const void* init_state,
+                           const int32_t* cu_seqlens, int n_seqs, int64_t total_tokens,
+                           const void* gate_logit, const float* norm_w, uint8_t* out_q,
+                           float* out_scale, void* final_state, void* workspace,
+                           size_t ws_bytes, cudaStream_t stream);
+
+/*
  * kda_prefill_checkpointed -- kda_prefill that also saves the state at caller-given token
  * boundaries inside the sequences (prefix-state checkpoints: a recurrent state can be
  * reused only where a snapshot of it was saved, "Ling-3.1-flash: What 63 Linear-Attention

@@ -167,3 +167,21 @@ def test_checkpoint_calls_reject_bad_arguments_on_host(lib):
     assert conv_ck(n_ckpt=70000) == kda.KDA_ERR_INVALID_ARG           # grid limit
     assert conv_ck(x=None) == kda.KDA_ERR_INVALID_ARG
     assert conv_ck(out=ctypes.c_void_p(40)) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_fp8_calls_reject_bad_arguments_on_host(lib):
+    p = kda.params(H=2, d=128)
+    P = ctypes.byref(p)
+    buf = ctypes.c_void_p(16)  # never dereferenced: every call fails validation first
+    # prefill: codes without scales, misaligned scales, no codes at all
+    assert lib.kda_prefill_fp8(P, buf, buf, buf, buf, buf, None, buf, 1, 64, None, None, buf,
+                               None, None, None, 0, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_prefill_fp8(P, buf, buf, buf, buf, buf, None, buf, 1, 64, None, None, buf,
+                               ctypes.c_void_p(20), None, None, 0, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_prefill_fp8(P, buf, buf, buf, buf, buf, None, buf, 1, 64, None, None, None,
+                               buf, None, None, 0, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_prefill_fp8(P, None, None, None, None, None, None, buf, 0, 0, None, None,
+                               None, None, None, None, 0, None) == kda.KDA_OK
+    # decode: codes without scales
+    assert lib.kda_decode_step_fused_fp8(P, buf, buf, buf, buf, buf, buf, 2, None, 2, None, None,
+                                         buf, None, None) == kda.KDA_ERR_INVALID_ARG

@@ -130,3 +130,89 @@ def test_fp8_decode_rejects_missing_scales():
         ctypes.byref(p), x.data_ptr(), w.data_ptr(), cs.data_ptr(), g.data_ptr(),
         b.data_ptr(), state.data_ptr(), n, None, n, None, None, q.data_ptr(), None, None)
     assert st == kda.KDA_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------------------------------
+# Prefill
+# ---------------------------------------------------------------------------------------
+
+def _prefill_fp8(inp, p, gate):
+    c = _gpu.cuda
+    T, H, d = inp["q"].shape
+    N = inp["cu_seqlens"].numel() - 1
+    q8 = torch.zeros((T, H, d), dtype=torch.uint8, device="cuda")
+    sc = torch.zeros((T, H), dtype=torch.float32, device="cuda")
+    fin = torch.empty((N, H, d, d), dtype=p.state_torch, device="cuda")
+    kda.kda_prefill_fp8(p, c(inp["q"]), c(inp["k"]), c(inp["v"]), c(inp["g"]), c(inp["beta"]),
+                        c(inp["cu_seqlens"]), q8, sc, init_state=c(inp.get("init_state")),
+                        final_state=fin, gate_logit=c(inp["gate"]) if gate else None,
+                        norm_w=c(inp.get("norm_w")) if gate else None)
+    torch.cuda.synchronize()
+    kda.kda_check_device_error()
+    return q8, sc, fin
+
+
+def _check_against_oracle(q8, sc, inp, p, gate, tol):
+    ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                             inp["cu_seqlens"], init_state=inp.get("init_state"),
+                             gate=inp.get("gate") if gate else None,
+                             norm_w=inp.get("norm_w") if gate else None)["out"]
+    d = ref.shape[-1]
+    sc64 = to64(sc)
+    deq = oracle.fp8_dequantize_groups(q8.cpu().numpy(), sc64[..., None], d)
+    y = np.maximum(np.abs(ref), np.abs(deq)) / sc64[..., None]
+    half = np.where(y >= 2.0 ** -6, np.exp2(np.floor(np.log2(np.maximum(y, 2.0 ** -6))) - 4),
+                    2.0 ** -10) * sc64[..., None]
+    excess = np.maximum(np.abs(deq - ref) - half * (1 + 2 ** -6), 0.0)
+    assert excess.max() <= tol * rms(ref), f"{excess.max() / rms(ref):.3g}"
+    np.testing.assert_allclose(sc64, np.abs(ref).max(-1) / 448.0, rtol=0,
+                               atol=4 * tol * rms(ref) / 448.0)
+    return ref
+
+
+@pytest.mark.parametrize("path", ["fused", "pair"])
+@pytest.mark.parametrize("gate", [False, True])
+def test_fp8_prefill_chunked_matches_the_oracle(path, gate, monkeypatch):
+    """The chunked tensor-core kernel's FP8 epilogue over ragged sequences (full 64-token
+    tiles go out by bulk store, ragged tails element by element), both kernel forms."""
+    monkeypatch.setenv("KDA_PREFILL_PAIR", "1" if path == "pair" else "0")
+    lens = [0, 1, 63, 64, 65, 130, 256]
+    inp = inputs.kda_inputs(lens, 2, 128, seed=740, init_state="even", gate=True)
+    inp["norm_w"] = inputs.normal((128,), seed=741, dtype=torch.float32)
+    p = kda.params(H=2, d=128)
+    _gpu.lib()
+    q8, sc, fin = _prefill_fp8(inp, p, gate)
+    _check_against_oracle(q8, sc, inp, p, gate, TOL[torch.bfloat16])
+    # the same kernel's bf16 output: the codes dequantise to it within half a step and one
+    # bf16 ulp (both come from the same fp32 value), and the final states are identical
+    out, fin0 = _gpu.prefill(inp, p, gate=gate)
+    torch.cuda.synchronize()
+    assert torch.equal(fin, fin0)
+    o = to64(out)
+    sc64 = to64(sc)
+    deq = oracle.fp8_dequantize_groups(q8.cpu().numpy(), sc64[..., None], 128)
+    y = np.maximum(np.abs(o), np.abs(deq)) / sc64[..., None]
+    half = np.where(y >= 2.0 ** -6, np.exp2(np.floor(np.log2(np.maximum(y, 2.0 ** -6))) - 4),
+                    2.0 ** -10) * sc64[..., None]
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(o), 1e-30))) - 7)
+    assert (np.abs(deq - o) <= half * (1 + 2 ** -6) + ulp).all()
+
+
+@pytest.mark.parametrize("gate", [False, True])
+def test_fp8_prefill_codes_are_the_quantisation_of_the_fp32_output(gate):
+    """fp32 I/O runs the token-serial kernel: its fp32 output quantised by the oracle in
+    fp32 gives the kernel's codes and scales bit for bit."""
+    lens = [5, 0, 70, 33]
+    inp = inputs.kda_inputs(lens, 3, 128, seed=750, io_dtype=torch.float32, init_state="all",
+                            gate=True)
+    inp["norm_w"] = inputs.normal((128,), seed=751, dtype=torch.float32)
+    p = kda.params(H=3, d=128, io_dtype=torch.float32)
+    _gpu.lib()
+    q8, sc, fin = _prefill_fp8(inp, p, gate)
+    out, fin0 = _gpu.prefill(inp, p, gate=gate)
+    torch.cuda.synchronize()
+    assert torch.equal(fin, fin0)
+    want_q, want_sc = oracle.fp8_quantize_groups(out.cpu().numpy(), 128, dtype=np.float32)
+    assert np.array_equal(sc.cpu().numpy(), want_sc[..., 0])
+    assert np.array_equal(q8.cpu().numpy(), want_q)
+    _check_against_oracle(q8, sc, inp, p, gate, TOL[torch.float32])
