@@ -261,9 +261,11 @@ def conv_tail_bytes(H, d, width, elem_bytes):
 # section "Production boundaries"); the serving setup fuses the quantisation of the KDA output
 # feeding o_proj into the KDA kernel ("Ling-3.1-flash: What 63 Linear-Attention Layers Do to
 # the KV Budget", section "Fitting it on a node").  Reading: one group per (token, head), the
-# 128 value channels that meet one 128-row block of o_proj's weight; fp32 scale =
-# max(amax, 1e-10) / 448; code = E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
-# no infinities, largest finite 448) of x / scale, rounded to nearest even and saturated.
+# 128 value channels that meet one 128-row block of o_proj's weight; with a = max(amax, 1e-10),
+# fp32 scale = a / 448 (what o_proj multiplies back) and code = E4M3 (1 sign, 4 exponent bits
+# with bias 7, 3 mantissa bits, no infinities, largest finite 448) of x * (448 / a), rounded to
+# nearest even and saturated: the multiply-by-reciprocal form of block quantisation, so a
+# group costs one division and each value one product.
 
 FP8_MAX = 448.0
 FP8_EPS = 1e-10
@@ -311,14 +313,15 @@ def fp8_e4m3_decode(codes):
 def fp8_quantize_groups(x, group=128, dtype=np.float64):
     """Dynamic FP8 quantisation of the last axis of x in groups of `group` channels:
     returns (codes uint8 with x's shape, scales with x.shape[:-1] + (n_groups,)).  `dtype`
-    is the precision the scale and the division are taken in (float32 reproduces a device
-    that divides in IEEE fp32)."""
+    is the precision the scale, the reciprocal and the product are taken in (float32
+    reproduces a device that rounds each of them in IEEE fp32)."""
     x = np.asarray(x).astype(dtype)
     shp = x.shape
     xg = x.reshape(shp[:-1] + (shp[-1] // group, group))
-    amax = np.abs(xg).max(axis=-1)
-    scale = (np.maximum(amax, dtype(FP8_EPS)) / dtype(FP8_MAX)).astype(dtype)
-    codes = fp8_e4m3_encode((xg / scale[..., None]).astype(dtype))
+    a = np.maximum(np.abs(xg).max(axis=-1), dtype(FP8_EPS)).astype(dtype)
+    scale = (a / dtype(FP8_MAX)).astype(dtype)
+    inv = (dtype(FP8_MAX) / a).astype(dtype)
+    codes = fp8_e4m3_encode((xg * inv[..., None]).astype(dtype))
     return codes.reshape(shp), scale
 
 
