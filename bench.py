@@ -277,6 +277,8 @@ class PrefillWorkload:
         self.k, self.v = torch.empty_like(self.q), torch.empty_like(self.q)
         self.beta = torch.empty((T, H), dtype=torch.float32, device=dev)
         self.out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+        self.out_q = torch.empty((T, H, D), dtype=torch.uint8, device=dev)
+        self.out_scale = torch.empty((T, H), dtype=torch.float32, device=dev)
         self.fin = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
 
     def prologue(self, stream=None):
@@ -289,6 +291,11 @@ class PrefillWorkload:
         # params' qk_l2norm normalises q, k) as it loads them
         self.kda.kda_prefill(self.p, self.q, self.k, self.v, self.g_raw, self.beta, self.cu,
                              self.out, final_state=self.fin, stream=stream)
+
+    def prefill_fp8(self, stream=None):
+        # the same recurrence with the output quantised to FP8 in the epilogue
+        self.kda.kda_prefill_fp8(self.p, self.q, self.k, self.v, self.g_raw, self.beta, self.cu,
+                                 self.out_q, self.out_scale, final_state=self.fin, stream=stream)
 
 
 def run_ours(args):
@@ -348,6 +355,20 @@ def run_ours(args):
     pro = _max_over_ranks(dist, sum(pro_ms) / len(pro_ms))
     value = ws * T_PREFILL / (ms * 1e-3)
 
+    # ---- the prefill with FP8 output (codes + one scale per token and head) ------------
+    pf8_ms = []
+    for i in range(3 + min(args.steps, 50)):
+        flush.zero_()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        wl.prefill_fp8()
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 3:
+            pf8_ms.append(e0.elapsed_time(e1))
+    kda.kda_check_device_error()
+    pf8 = _max_over_ranks(dist, sum(pf8_ms) / len(pf8_ms))
+
     # ---- end to end through the same API with host buffers ---------------------------
     e2e_line = _e2e(wl, flush, args, dist) if not args.no_e2e else None
 
@@ -371,6 +392,7 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (403 MB) and a 258 MB buffer written between "
                          "steps"},
         "breakdown_ms": {"prologue": pro, "prefill": pf},
+        "prefill_fp8_output_ms": pf8,
         "prefill_kernel_tokens_per_s": ws * T_PREFILL / (pf * 1e-3),
         "roofline": {"kernel": "kda_prefill", "bound": "hbm", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
@@ -450,7 +472,24 @@ def _decode_bench(dev, kda, inputs, hbm, rank, args):
     ms = e0.elapsed_time(e1) / K
     b = _decode_bytes(n, H, D)
     gbs = b / (ms * 1e-3) / 1e9
-    return {"metric": "KDA decode state GB/s", "value": gbs, "unit": "GB/s",
+    # the same steps with the output quantised to FP8 in the epilogue (codes + one fp32
+    # scale per sequence and head instead of bf16 values)
+    q8 = torch.empty((K, n, H, D), dtype=torch.uint8, device=dev)
+    sc8 = torch.empty((K, n, H), dtype=torch.float32, device=dev)
+    for t in range(3):
+        kda.kda_decode_step_fused_fp8(p, x[t], w, cs, g[t], beta[t], state, q8[t], sc8[t])
+    torch.cuda.synchronize()
+    e0.record()
+    for t in range(K):
+        kda.kda_decode_step_fused_fp8(p, x[t], w, cs, g[t], beta[t], state, q8[t], sc8[t])
+    e1.record()
+    e1.synchronize()
+    ms8 = e0.elapsed_time(e1) / K
+    b8 = b - n * H * D * 2 + n * H * D + n * H * 4
+    fp8 = {"kernel": "kda_decode_step_fused_fp8", "ms_per_step": ms8,
+           "achieved_gbs": b8 / (ms8 * 1e-3) / 1e9, "frac": b8 / (ms8 * 1e-3) / 1e9 / hbm,
+           "algorithmic_bytes_per_launch": b8}
+    return {"metric": "KDA decode state GB/s", "value": gbs, "unit": "GB/s", "fp8_output": fp8,
             "workload": "256 sequences x 1 token, H=64, d=128, fp32 state pool [256,64,128,128]"
                         " ~N(0,0.02) (1 GiB, > L2), bf16 conv tails, fused conv+decode, 100 "
                         "consecutive steps",

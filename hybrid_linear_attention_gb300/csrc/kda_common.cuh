@@ -82,15 +82,19 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // Dynamic FP8 quantisation of one output group (the d_v values of one token and head, which
-// meet one 128-row block of o_proj's block-FP8 weight): fp32 scale = max(amax, 1e-10) / 448
-// and code = E4M3 of x / scale, rounded to nearest even and saturated at +-448.  Both
-// divisions are IEEE round-to-nearest, so the codes are a function of the fp32 values alone.
+// meet one 128-row block of o_proj's block-FP8 weight): with a = max(amax, 1e-10), the fp32
+// scale o_proj multiplies back is a / 448, and code = E4M3 of x * (448 / a), rounded to
+// nearest even and saturated at +-448.  The divisions (once per group) and the product are
+// IEEE round-to-nearest, so the codes are a function of the fp32 values alone.
 constexpr float FP8_MAX = 448.f, FP8_EPS = 1e-10f;
 __device__ __forceinline__ float fp8_scale(float amax) {
   return __fdiv_rn(fmaxf(amax, FP8_EPS), FP8_MAX);
 }
-__device__ __forceinline__ uint8_t fp8_code(float x, float scale) {
-  return (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3);
+__device__ __forceinline__ float fp8_inv_scale(float amax) {
+  return __fdiv_rn(FP8_MAX, fmaxf(amax, FP8_EPS));
+}
+__device__ __forceinline__ uint8_t fp8_code(float x, float inv_scale) {
+  return (uint8_t)__nv_cvt_float_to_fp8(__fmul_rn(x, inv_scale), __NV_SATFINITE, __NV_E4M3);
 }
 
 // Sequence containing packed token t: the largest n with cu[n] <= t (empty sequences

@@ -72,7 +72,7 @@ constexpr uint32_t TM_AH = 128, TM_AL = 192, TM_D = 256;
 
 // TMA loads and tensor-core completion; in a cluster pair, the consumer's FULL (landing
 // buffer 0 / 1 holds T and P') and the producer's EMPTY (buffer 0 / 1 may be rewritten)
-enum { BAR_Q = 0, BAR_K, BAR_V, BAR_G, BAR_MMA, BAR_F0, BAR_F1, BAR_E0, BAR_E1, NBAR };
+enum { BAR_Q = 0, BAR_K, BAR_V, BAR_G, BAR_MMA, BAR_F0, BAR_F1, BAR_E0, BAR_E1, BAR_GT, NBAR };
 // consumer landing buffers b = 0, 1: T then P' (16 KB each, tf32 K-major); buffer 0 is the
 // fused kernel's own T and P' region
 __host__ __device__ constexpr uint32_t off_lt(int b) { return 147456u + 32768u * (uint32_t)b; }
@@ -158,6 +158,13 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// sigmoid(x) = 1 / (1 + 2^(-x log2 e)) with the special-function unit's 2^x and reciprocal:
+// branch-free (relative error ~1e-7, far below the bf16 output's rounding)
+__device__ __forceinline__ float sigmoid_sfu(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + ex2(-1.4426950408889634f * x)));
+  return r;
+}
 __device__ __forceinline__ void st_f32x8(uint8_t *p0, uint8_t *p1, const float (&o)[8]) {
   *reinterpret_cast<float4 *>(p0) = make_float4(o[0], o[1], o[2], o[3]);
   *reinterpret_cast<float4 *>(p1) = make_float4(o[4], o[5], o[6], o[7]);
@@ -202,7 +209,7 @@ __device__ __forceinline__ void warp_store16(float *D, int ld, const float (&d)[
 }
 
 struct Maps {
-  CUtensorMap q, k, v, g, out;
+  CUtensorMap q, k, v, g, out, gate;
 };
 
 // PAIR: a cluster of two CTAs per (head, sequence), rank 0 the consumer (state walk), rank 1
@@ -217,6 +224,8 @@ __global__ void __launch_bounds__(NT, 1)
   __shared__ float s_GC[D];                   // Gamma_C
   __shared__ float s_red[4][C];
   __shared__ float s_amx[4][C];  // FP8 output: each row's amax by TMEM lane quarter
+  __shared__ float s_inv[C];     // FP8 output: each row's 448 / amax
+  __shared__ float s_nrm[C];     // gated output: each row's 1 / RMS
   __shared__ __align__(16) float s_M[3 * 256];  // inverse scratch; block decays P1 -> P2
   __shared__ __align__(8) uint64_t s_bar[NBAR];
   __shared__ uint32_t s_tmem, s_abort, s_pend, s_ppar[NBAR];
@@ -279,6 +288,10 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_expect_tx(bar(BAR_G), 32768);
       for (int bx = 0; bx < 4; ++bx)
         tma_load_3d(sb + OFF_G + 8192 * bx, &maps.g, 32 * bx, h, t0, bar(BAR_G));
+    }
+    if (mask & (1u << BAR_GT)) {  // gate logits [64 tokens][128] bf16, plain, into V's region
+      mbar_expect_tx(bar(BAR_GT), 16384);
+      tma_load_3d(sb + OFF_V, &maps.gate, 0, h, t0, bar(BAR_GT));
     }
     for (int b = 0; b < NBAR; ++b)
       if (mask & (1u << b)) s_ppar[b] = (uint32_t)(c & 1);
@@ -810,122 +823,144 @@ __global__ void __launch_bounds__(NT, 1)
       const bool tile = nv == C;
       bf16 *stage = reinterpret_cast<bf16 *>(sm + OFF_V);  // V was consumed by the Y pass
       bf16 *out = reinterpret_cast<bf16 *>(a.out);
-      if (QUANT) {
-        // FP8 output (E4M3 codes, one fp32 scale per token): a row's scale needs all of its
-        // 128 values, so this thread holds its channel's 32 rows at once and a second
-        // transpose-reduce over the warp, then over the four lane quarters, gives each
-        // row's amax
-        float o[32];
-        {
-          float u[32];
-          tmem_ld32(tm + lane_off + TM_C + 64 + 32 * grp, o);
-          tmem_ld32(tm + lane_off + TM_A + 32 * grp, u);
-          tmem_wait_ld();
-#pragma unroll
-          for (int x = 0; x < 32; ++x)
-            o[x] = a.scale * fmaf(s_pd[par][32 * grp + x], u[x], o[x]);
-        }
-        if (GATE) {
-          float sq[32];
-#pragma unroll
-          for (int x = 0; x < 32; ++x) sq[x] = o[x] * o[x];
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) {
-            const bool up = (lane & off) != 0;
-#pragma unroll
-            for (int x = 0; x < off; ++x) {
-              const float send = up ? sq[x] : sq[x + off];
-              const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-              sq[x] = (up ? sq[x + off] : sq[x]) + recv;
-            }
-          }
-          s_red[quarter][32 * grp + lane] = sq[0];
-          asm volatile("bar.sync 1, 256;" ::: "memory");
-          const float w = a.norm_w ? a.norm_w[j] : 1.f;
-          const bf16 *gate = reinterpret_cast<const bf16 *>(a.gate);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            const int r = 32 * grp + x;
-            if (r < nv) {
-              const size_t row = ((size_t)(t0 + r) * H + h) * D + j;
-              const float ss = s_red[0][r] + s_red[1][r] + s_red[2][r] + s_red[3][r];
-              o[x] = o[x] * rsqrtf(ss * (1.f / D) + a.norm_eps) * w *
-                     sigmoidf_(__bfloat162float(gate[row]));
-            }
-          }
-        }
-#pragma unroll
-        for (int x = 0; x < 32; ++x)
-          if (32 * grp + x >= nv) o[x] = 0.f;
-        float mx[32];
-#pragma unroll
-        for (int x = 0; x < 32; ++x) mx[x] = fabsf(o[x]);
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {  // mx[0] ends as row (32 grp + lane)
-          const bool up = (lane & off) != 0;
-#pragma unroll
-          for (int x = 0; x < off; ++x) {
-            const float send = up ? mx[x] : mx[x + off];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-            mx[x] = fmaxf(up ? mx[x + off] : mx[x], recv);
-          }
-        }
-        s_amx[quarter][32 * grp + lane] = mx[0];
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        uint8_t *stage8 = sm + OFF_V;
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const int r = 32 * grp + x;
-          if (r < nv) {
-            const float sc = fp8_scale(fmaxf(fmaxf(s_amx[0][r], s_amx[1][r]),
-                                             fmaxf(s_amx[2][r], s_amx[3][r])));
-            const uint8_t code = fp8_code(o[x], sc);
-            if (tile) stage8[r * D + j] = code;
-            else a.out_q[((size_t)(t0 + r) * H + h) * D + j] = code;
-          }
-        }
-        if (quarter == 0) {
-          const int r = 32 * grp + lane;
-          if (r < nv)
-            a.out_scale[(size_t)(t0 + r) * H + h] = fp8_scale(
-                fmaxf(fmaxf(s_amx[0][r], s_amx[1][r]), fmaxf(s_amx[2][r], s_amx[3][r])));
-        }
-      } else if (GATE) {
-        float o[32], u[32];
-        tmem_ld32(tm + lane_off + TM_C + 64 + 32 * grp, o);
-        tmem_ld32(tm + lane_off + TM_A + 32 * grp, u);
-        tmem_wait_ld();
-#pragma unroll
-        for (int x = 0; x < 32; ++x) o[x] = a.scale * fmaf(s_pd[par][32 * grp + x], u[x], o[x]);
-        float sq[32];
-#pragma unroll
-        for (int x = 0; x < 32; ++x) sq[x] = o[x] * o[x];
-        // transpose-reduce over the warp's 32 lanes: sq[0] ends as row (32 grp + lane)
+      // Per-row statistics (sum of squares for the norm, amax for FP8) need all 128 values of
+      // a row: this thread holds its channel's 32 rows at once and a transpose-reduce over the
+      // warp leaves row 32 grp + lane in each lane (31 shuffles for 32 rows); the four lane
+      // quarters meet in shared memory, and one lane per row turns them into factors.  Values
+      // are then written 8 rows at a time, o re-read from tensor memory, so the unrolled code
+      // stays short: the whole kernel is larger than the instruction cache, and unrolled
+      // length costs time (measured).
+      auto transpose_reduce = [&](float (&v)[32], bool is_max) {
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) {
           const bool up = (lane & off) != 0;
 #pragma unroll
           for (int x = 0; x < off; ++x) {
-            const float send = up ? sq[x] : sq[x + off];
+            const float send = up ? v[x] : v[x + off];
             const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-            sq[x] = (up ? sq[x + off] : sq[x]) + recv;
+            const float keep = up ? v[x + off] : v[x];
+            v[x] = is_max ? fmaxf(keep, recv) : keep + recv;
           }
         }
-        s_red[quarter][32 * grp + lane] = sq[0];
-        // named barrier over the 256 threads of groups 0 and 1
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        const float w = a.norm_w ? a.norm_w[j] : 1.f;
-        const bf16 *gate = reinterpret_cast<const bf16 *>(a.gate);
+      };
+      auto load_o = [&](float (&o)[32]) {  // o of rows 32 grp + x, this thread's channel
+        float u[32];
+        tmem_ld32(tm + lane_off + TM_C + 64 + 32 * grp, o);
+        tmem_ld32(tm + lane_off + TM_A + 32 * grp, u);
+        tmem_wait_ld();
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const int r = 32 * grp + x;
-          if (r < nv) {
-            const size_t row = ((size_t)(t0 + r) * H + h) * D + j;
-            const float ss = s_red[0][r] + s_red[1][r] + s_red[2][r] + s_red[3][r];
-            const float val = o[x] * rsqrtf(ss * (1.f / D) + a.norm_eps) * w *
-                              sigmoidf_(__bfloat162float(gate[row]));
-            if (tile) stage[r * D + j] = __float2bfloat16_rn(val);
-            else out[row] = __float2bfloat16_rn(val);
+        for (int x = 0; x < 32; ++x) o[x] = a.scale * fmaf(s_pd[par][32 * grp + x], u[x], o[x]);
+      };
+      auto o_slice = [&](int sl, float (&v)[8]) {  // o of rows 32 grp + 8 sl + y, this channel
+        float u8[8];
+        tmem_ld8(tm + lane_off + TM_C + 64 + 32 * grp + 8 * sl, v);
+        tmem_ld8(tm + lane_off + TM_A + 32 * grp + 8 * sl, u8);
+        tmem_wait_ld();
+#pragma unroll
+        for (int y = 0; y < 8; ++y) v[y] = a.scale * fmaf(s_pd[par][32 * grp + 8 * sl + y], u8[y], v[y]);
+      };
+      const float w = GATE ? (a.norm_w ? a.norm_w[j] : 1.f) : 1.f;
+      if (GATE) {
+        wait(BAR_GT, par);  // the gate tile, loaded into the stage region after the Y pass
+        {
+          float sq[32];
+          load_o(sq);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) sq[x] *= sq[x];
+          transpose_reduce(sq, false);
+          s_red[quarter][32 * grp + lane] = sq[0];
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (quarter == 0) {  // the row's norm factor
+          const int r = 32 * grp + lane;
+          s_nrm[r] = rsqrtf((s_red[0][r] + s_red[1][r] + s_red[2][r] + s_red[3][r]) * (1.f / D) +
+                            a.norm_eps);
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+      }
+      if (QUANT) {
+        // FP8 output (E4M3 codes, one fp32 scale per token): each row's amax of its final
+        // values, then one lane per row computes the scale (to HBM) and 448 / amax (to all)
+        auto row_factors = [&]() {
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+          if (quarter == 0) {
+            const int r = 32 * grp + lane;
+            const float amax =
+                fmaxf(fmaxf(s_amx[0][r], s_amx[1][r]), fmaxf(s_amx[2][r], s_amx[3][r]));
+            s_inv[r] = fp8_inv_scale(amax);
+            if (r < nv) a.out_scale[(size_t)(t0 + r) * H + h] = fp8_scale(amax);
+          }
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+        };
+        uint8_t *stage8 = sm + OFF_V;
+        if (!GATE) {
+          {
+            float mx[32];
+            load_o(mx);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) mx[x] = 32 * grp + x < nv ? fabsf(mx[x]) : 0.f;
+            transpose_reduce(mx, true);
+            s_amx[quarter][32 * grp + lane] = mx[0];
+          }
+          row_factors();
+#pragma unroll 1
+          for (int sl = 0; sl < 4; ++sl) {  // codes, 8 rows at a time
+            float v[8];
+            o_slice(sl, v);
+#pragma unroll
+            for (int y = 0; y < 8; ++y) {
+              const int r = 32 * grp + 8 * sl + y;
+              const uint8_t code = fp8_code(v[y], s_inv[r]);
+              if (tile) stage8[r * D + j] = code;
+              else if (r < nv) a.out_q[((size_t)(t0 + r) * H + h) * D + j] = code;
+            }
+          }
+        } else {
+          // the codes overwrite gate logits of other rows (one byte per value in the same
+          // region), so every logit is read first: the 32 gated values stay in registers
+          float o[32];
+#pragma unroll
+          for (int sl = 0; sl < 4; ++sl) {
+            float v[8];
+            o_slice(sl, v);
+#pragma unroll
+            for (int y = 0; y < 8; ++y) {
+              const int r = 32 * grp + 8 * sl + y;
+              o[8 * sl + y] = v[y] * s_nrm[r] * w * sigmoid_sfu(__bfloat162float(stage[r * D + j]));
+            }
+          }
+          {
+            float mx[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x) mx[x] = 32 * grp + x < nv ? fabsf(o[x]) : 0.f;
+            transpose_reduce(mx, true);
+            s_amx[quarter][32 * grp + lane] = mx[0];
+          }
+          row_factors();  // its first barrier: every gate logit has been read
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const int r = 32 * grp + x;
+            const uint8_t code = fp8_code(o[x], s_inv[r]);
+            if (tile) stage8[r * D + j] = code;
+            else if (r < nv) a.out_q[((size_t)(t0 + r) * H + h) * D + j] = code;
+          }
+        }
+      } else if (GATE) {
+#pragma unroll 1
+        for (int sl = 0; sl < 4; ++sl) {  // 8 rows at a time, o re-read: a short loop body
+          float o8[8], u8[8];
+          tmem_ld8(tm + lane_off + TM_C + 64 + 32 * grp + 8 * sl, o8);
+          tmem_ld8(tm + lane_off + TM_A + 32 * grp + 8 * sl, u8);
+          tmem_wait_ld();
+#pragma unroll
+          for (int y = 0; y < 8; ++y) {
+            const int r = 32 * grp + 8 * sl + y;
+            if (r < nv) {  // each thread overwrites the gate logit it has just read
+              const float val = a.scale * fmaf(s_pd[par][r], u8[y], o8[y]) * s_nrm[r] * w *
+                                sigmoid_sfu(__bfloat162float(stage[r * D + j]));
+              if (tile) stage[r * D + j] = __float2bfloat16_rn(val);
+              else out[((size_t)(t0 + r) * H + h) * D + j] = __float2bfloat16_rn(val);
+            }
           }
         }
       } else {
@@ -997,7 +1032,10 @@ __global__ void __launch_bounds__(NT, 1)
       mma_par ^= 1;  // MMA1's phase (waited by groups 0 and 1)
       fence_proxy_async();
       if (!(ok = sync())) break;
-      if (tid == 0) mmau_issue(OFF_T);
+      if (tid == 0) {
+        mmau_issue(OFF_T);
+        if (GATE) issue(1u << BAR_GT, c);  // V is consumed: the gate tile takes its place
+      }
       kbar(nv);  // while u is formed; then k and g of the next chunk may be loaded
       fence_proxy_async();
       if (!(ok = sync())) break;
@@ -1043,6 +1081,7 @@ __global__ void __launch_bounds__(NT, 1)
       fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0) {
+        if (GATE) issue(1u << BAR_GT, c);  // V is consumed: the gate tile takes its place
         if (mbar_wait_cluster(bar(BAR_F0 + b), (uint32_t)((c >> 1) & 1))) {
           fence_proxy_async();
           mmau_issue(off_lt(b));
@@ -1281,6 +1320,9 @@ cudaError_t launch_prefill_tc(const TcArgs &a, int64_t total_tokens, bool st_bf1
         !make_map(&maps.g, a.g, true, total_tokens, a.H) ||
         !make_out_map(&maps.out, a.out_q ? static_cast<void *>(a.out_q) : a.out, total_tokens,
                       a.H, a.out_q != nullptr))
+      return cudaErrorInvalidValue;
+    // gate logits [T, H, 128] bf16: the same plain boxes as the output
+    if (a.gate && !make_out_map(&maps.gate, const_cast<void *>(a.gate), total_tokens, a.H, false))
       return cudaErrorInvalidValue;
   }
   const bool gate = a.gate != nullptr, pair = use_pair(a);

@@ -267,9 +267,8 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
             float amax = 0.f;
 #pragma unroll
             for (int w = 0; w < (D + 31) / 32; ++w) amax = fmaxf(amax, s_amax[w]);
-            const float sc = fp8_scale(amax);
-            a.out_q[row] = fp8_code(o, sc);
-            if (tid == 0) a.out_scale[(size_t)(t0 + tt) * H + h] = sc;
+            a.out_q[row] = fp8_code(o, fp8_inv_scale(amax));
+            if (tid == 0) a.out_scale[(size_t)(t0 + tt) * H + h] = fp8_scale(amax);
           }
         }
       }

@@ -151,9 +151,10 @@ kda_status kda_prefill(const kda_params* p, const void* q, const void* k, const 
  * o_proj, as kda_decode_step_fused_fp8 does for decode (same pages, same reading): one group
  * per (token, head).
  *
- *   out_q      [T_tot, H, d_v] uint8 E4M3 codes of o / scale (nearest even, saturated).
- *   out_scale  [T_tot, H] fp32: max(amax, 1e-10) / 448 over the group's d_v values (after
- *              the output norm and gate when gate logits are given).
+ *   out_q      [T_tot, H, d_v] uint8 E4M3 codes of o * (448 / a) (nearest even, saturated),
+ *              a = max(amax, 1e-10) over the group's d_v values (after the output norm and
+ *              gate when gate logits are given).
+ *   out_scale  [T_tot, H] fp32: a / 448.
  *   Other arguments as kda_prefill.
  */
 kda_status kda_prefill_fp8(const kda_params* p, const void* q, const void* k, const void* v,
@@ -267,11 +268,12 @@ kda_status kda_decode_step_fused(const kda_params* p, const void* x_raw, const v
  * one (sequence, head): the 128 input channels that meet one weight block.
  *
  *   out_q      [n_seqs, H, d] uint8: E4M3 codes (1 sign, 4 exponent bits with bias 7,
- *              3 mantissa bits, no infinities) of o / scale, rounded to nearest even and
- *              saturated at +-448.
- *   out_scale  [n_seqs, H] fp32: scale = max(amax, 1e-10) / 448, amax = max |o| over the
- *              group (o after the output norm and gate when gate logits are given).
- *   Both divisions are IEEE fp32 round-to-nearest.  Other arguments as kda_decode_step_fused.
+ *              3 mantissa bits, no infinities) of o * (448 / a), rounded to nearest even
+ *              and saturated at +-448; a = max(amax, 1e-10), amax = max |o| over the group
+ *              (o after the output norm and gate when gate logits are given).
+ *   out_scale  [n_seqs, H] fp32: scale = a / 448 (value = code * scale).
+ *   The divisions and the product are IEEE fp32 round-to-nearest.  Other arguments as
+ *   kda_decode_step_fused.
  */
 kda_status kda_decode_step_fused_fp8(const kda_params* p, const void* x_raw,
                                      const void* conv_w, void* conv_state, const float* g,
