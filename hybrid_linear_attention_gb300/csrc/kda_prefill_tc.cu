@@ -302,13 +302,10 @@ __global__ void __launch_bounds__(NT, 1)
     s_ppar[BAR_MMA] = parity;
     atomicOr(&s_pend, 1u << BAR_MMA);
   };
+  // a bounded wait; one that runs out only raises the CTA's abort flag (reported once, at
+  // exit): waits are inlined at every phase boundary, and the chunk loop's code size costs time
   auto wait = [&](int b, uint32_t parity) {
-    if (!mbar_wait(bar(b), parity)) {
-      s_abort = 1;
-      if (a.err) atomicOr(a.err, ERR_MBAR_TIMEOUT);
-    } else if (tid == 0 || tid == 256) {
-      atomicAnd(&s_pend, ~(1u << b));
-    }
+    if (!mbar_wait(bar(b), parity)) s_abort = 1;
   };
   auto sync = [&]() {
     tc_fence_before();
@@ -1087,7 +1084,6 @@ __global__ void __launch_bounds__(NT, 1)
           mmau_issue(off_lt(b));
         } else {
           s_abort = 1;
-          if (a.err) atomicOr(a.err, ERR_MBAR_TIMEOUT);
         }
       }
       kbar(nv);
@@ -1137,10 +1133,8 @@ __global__ void __launch_bounds__(NT, 1)
       wait(BAR_MMA, mma_par);
       mma_par ^= 1;
       tc_fence_after();
-      if (c >= 2 && !mbar_wait_cluster(bar(BAR_E0 + b), (uint32_t)(((c - 2) >> 1) & 1))) {
+      if (c >= 2 && !mbar_wait_cluster(bar(BAR_E0 + b), (uint32_t)(((c - 2) >> 1) & 1)))
         s_abort = 1;
-        if (a.err) atomicOr(a.err, ERR_MBAR_TIMEOUT);
-      }
       if (!(ok = sync())) break;
       extract(nv, peer + off_lp(b), pA);
       if (!(ok = sync())) break;
@@ -1177,7 +1171,10 @@ __global__ void __launch_bounds__(NT, 1)
     }
   }
   if (!ok && tid == 0) {
-    // drain: let loads and MMAs still in flight land (bounded) before the CTA exits
+    if (s_abort && a.err) atomicOr(a.err, ERR_MBAR_TIMEOUT);  // a bounded wait ran out
+    // drain: let loads and MMAs still in flight land (bounded) before the CTA exits.  s_pend
+    // marks every barrier that was ever armed and s_ppar the parity of its latest phase, whose
+    // wait returns at once when that phase has completed
     for (int b = 0; b < NBAR; ++b)
       if (s_pend & (1u << b)) mbar_wait(bar(b), s_ppar[b]);
   }
