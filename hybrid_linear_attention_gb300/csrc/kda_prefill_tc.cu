@@ -352,8 +352,8 @@ __global__ void __launch_bounds__(NT, 1)
       const int r = t >> 1, hf = t & 1;
       float sq = 0.f, sk = 0.f, sqk = 0.f;
       if (r < nvc) {
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
+#pragma unroll 2
+        for (int c8 = 0; c8 < 8; ++c8) {  // two at a time: p1 is inlined at three places
           float qv[8], kv[8];
           bf_row8(sm + OFF_Q, r, 8 * hf + c8, qv);
           bf_row8(sm + OFF_K, r, 8 * hf + c8, kv);
@@ -377,17 +377,20 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll 1
       for (int blk = 0; blk < 4; ++blk) {  // 16 rows at a time, running sum carried over
         s_g0[blk][i] = run;
-        float v[16];
+#pragma unroll 1
+        for (int x0 = 0; x0 < 16; x0 += 8) {  // 8 loads in flight, then the 8 sums
+          float v[8];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int r = 16 * blk + x;
-          const float gv = *reinterpret_cast<const float *>(sm + OFF_G + swz<4>(r, i));
-          v[x] = r < nvc ? fmaxf(gv, a.g_min) * LOG2E : 0.f;
-        }
+          for (int x = 0; x < 8; ++x) {
+            const int r = 16 * blk + x0 + x;
+            const float gv = *reinterpret_cast<const float *>(sm + OFF_G + swz<4>(r, i));
+            v[x] = r < nvc ? fmaxf(gv, a.g_min) * LOG2E : 0.f;
+          }
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          run += v[x];
-          *reinterpret_cast<float *>(sm + OFF_G + swz<4>(16 * blk + x, i)) = run;
+          for (int x = 0; x < 8; ++x) {
+            run += v[x];
+            *reinterpret_cast<float *>(sm + OFF_G + swz<4>(16 * blk + x0 + x, i)) = run;
+          }
         }
       }
       float g0[4];
