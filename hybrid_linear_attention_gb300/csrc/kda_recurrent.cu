@@ -39,7 +39,7 @@ __device__ __forceinline__ void prefetch_span(const void *p, size_t bytes, int t
   for (size_t off = (size_t)tid * 128; off < bytes; off += (size_t)nt * 128) prefetch_l2(c + off);
 }
 
-template <int D, int NT, typename IO, typename ST, bool CONV, bool GATE>
+template <int D, int NT, typename IO, typename ST, bool CONV, bool GATE, bool QUANT>
 __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
   constexpr int CG = D / 4;        // column groups of four
   constexpr int RG = NT / CG;      // row groups
@@ -256,9 +256,9 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
             const float z = to_f(reinterpret_cast<const IO *>(a.gate)[row]);
             o = o * r * w * sigmoidf_(z);
           }
-          if (!a.out_q) reinterpret_cast<IO *>(a.out)[row] = from_f<IO>(o);
+          if (!QUANT) reinterpret_cast<IO *>(a.out)[row] = from_f<IO>(o);
         }
-        if (a.out_q) {  // the same for the whole grid, so every thread meets the barrier
+        if (QUANT) {
           // FP8 output: the group's amax over its D values (warp max, then across warps)
           const float m = warp_max(tid < D ? fabsf(o) : 0.f);
           if (lane == 0 && warp < (D + 31) / 32) s_amax[warp] = m;
@@ -307,10 +307,16 @@ cudaError_t launch_grid(K kernel, int nt, const RecArgs &a, cudaStream_t s) {
 template <int D, int NT, typename IO, typename ST>
 cudaError_t launch_typed(const RecArgs &a, cudaStream_t s) {
   const bool conv = a.x_raw != nullptr, gate = a.gate != nullptr;
-  if (conv && gate) return launch_grid(recurrent_kernel<D, NT, IO, ST, true, true>, NT, a, s);
-  if (conv) return launch_grid(recurrent_kernel<D, NT, IO, ST, true, false>, NT, a, s);
-  if (gate) return launch_grid(recurrent_kernel<D, NT, IO, ST, false, true>, NT, a, s);
-  return launch_grid(recurrent_kernel<D, NT, IO, ST, false, false>, NT, a, s);
+  if (a.out_q) {  // FP8 output epilogue (its own instantiations: the bf16 path is untouched)
+    if (conv && gate) return launch_grid(recurrent_kernel<D, NT, IO, ST, true, true, true>, NT, a, s);
+    if (conv) return launch_grid(recurrent_kernel<D, NT, IO, ST, true, false, true>, NT, a, s);
+    if (gate) return launch_grid(recurrent_kernel<D, NT, IO, ST, false, true, true>, NT, a, s);
+    return launch_grid(recurrent_kernel<D, NT, IO, ST, false, false, true>, NT, a, s);
+  }
+  if (conv && gate) return launch_grid(recurrent_kernel<D, NT, IO, ST, true, true, false>, NT, a, s);
+  if (conv) return launch_grid(recurrent_kernel<D, NT, IO, ST, true, false, false>, NT, a, s);
+  if (gate) return launch_grid(recurrent_kernel<D, NT, IO, ST, false, true, false>, NT, a, s);
+  return launch_grid(recurrent_kernel<D, NT, IO, ST, false, false, false>, NT, a, s);
 }
 
 template <int D, int NT>
