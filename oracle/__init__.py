@@ -4,10 +4,11 @@ TEST INFRASTRUCTURE ONLY: the test suite, the package smoke check and the benchm
 CPU-baseline leg may import this package; the product path never does.  It shares no code
 with the CUDA library and never imports it.
 
-``kda_oracle.c`` holds the arithmetic (plain C, fp64, token by token).  This module only
-builds it with gcc and marshals numpy arrays into it.  Every function returns fp64 results
-computed from the exact stored values of its inputs (fp32 arrays, or bf16 given as the
-``torch.bfloat16`` / raw uint16 bit patterns).
+``kda_oracle.c`` holds the KDA arithmetic (plain C, fp64, token by token); this module
+builds it with gcc and marshals numpy arrays into it.  The FP8 output quantiser and the
+absorbed gated-MLA decode are written here in plain numpy (fp64, position by position).
+Every function returns results computed from the exact stored values of its inputs (fp32
+arrays, or bf16 given as the ``torch.bfloat16`` / raw uint16 bit patterns).
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py`` (closed forms,
 invariants, brute force and library routines); none is "parity unpinned".
@@ -331,3 +332,94 @@ def fp8_dequantize_groups(codes, scales, group=128):
     shp = c.shape
     v = fp8_e4m3_decode(c).reshape(shp[:-1] + (shp[-1] // group, group))
     return (v * np.asarray(scales, dtype=np.float64)[..., None]).reshape(shp)
+
+
+# ---------------------------------------------------------------------------------------
+# Absorbed gated-MLA decode (the other token mixer of the hybrid)
+# ---------------------------------------------------------------------------------------
+# "Ling-3.1-flash: Grouped Routing and Two Different MLA Caches", sections "MLA's expanded
+# reference path" and "Why weight absorption keeps the same attention function".  Per head
+# i, the cached latent c_t (512) and shared rotated positional key r_t (64) of every cached
+# position t; key up-projection W_K,i and value up-projection W_V,i, each 128 x 512; query
+# parts q_i^N (128) and q_i^R (64, already rotated); score scale 1/sqrt(192); one sigmoid
+# gate per head on the head's 128-wide output.  Plain fp64, position by position.
+
+def _f64(x):
+    a, _ = _as_np(x)
+    if a is None:
+        return None
+    if a.dtype == np.uint16:  # bf16 bit patterns
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def _softmax(s):
+    e = np.exp(s - s.max())
+    return e / e.sum()
+
+
+def mla_decode_expanded(q_nope, q_rope, c, r, lengths, w_uk, w_uv, gate_logit,
+                        scale=192 ** -0.5):
+    """The expanded reference path: keys [W_K,i c_t ; r_t] (192 wide) and values W_V,i c_t
+    (128 wide) for every cached position t < lengths[b]; softmax of scale * q . k; the
+    weighted value sum times sigmoid(gate).  q_nope [B,H,128], q_rope [B,H,64], c [B,L,512],
+    r [B,L,64], w_uk / w_uv [H,128,512], gate_logit [B,H].  Returns [B,H,128] fp64."""
+    qn, qr, cc, rr = _f64(q_nope), _f64(q_rope), _f64(c), _f64(r)
+    wk, wv, gl = _f64(w_uk), _f64(w_uv), _f64(gate_logit)
+    B, H, dv = qn.shape[0], qn.shape[1], wv.shape[1]
+    out = np.zeros((B, H, dv))
+    for b in range(B):
+        L = int(lengths[b])
+        for i in range(H):
+            keys = np.concatenate([cc[b, :L] @ wk[i].T, rr[b, :L]], axis=1)   # [L, 192]
+            vals = cc[b, :L] @ wv[i].T                                       # [L, 128]
+            q = np.concatenate([qn[b, i], qr[b, i]])
+            p = _softmax(scale * (keys @ q))
+            out[b, i] = (p @ vals) / (1.0 + np.exp(-gl[b, i]))
+    return out
+
+
+def mla_absorb(q_nope, q_rope, w_uk):
+    """The absorbed query: [W_K,i^T q_i^N ; q_i^R], 576 wide per head.  Returns [B,H,576]."""
+    qn, qr, wk = _f64(q_nope), _f64(q_rope), _f64(w_uk)
+    qt = np.einsum("bhn,hnl->bhl", qn, wk)
+    return np.concatenate([qt, qr], axis=2)
+
+
+def mla_latent_attention(q_cat, cache, lengths, scale=192 ** -0.5):
+    """The absorbed attention over the shared 576-wide cached key [c_t ; r_t], with the
+    latent c_t itself as the value: per head, z = sum_t softmax_t(scale q . [c_t; r_t]) c_t.
+    q_cat [B,H,576], cache [B,L,576].  Returns (z [B,H,512], lse [B,H]) in fp64, lse the
+    natural log-sum-exp of the scaled scores."""
+    q, kv = _f64(q_cat), _f64(cache)
+    B, H = q.shape[0], q.shape[1]
+    dl = kv.shape[2] - 64
+    z = np.zeros((B, H, dl))
+    lse = np.full((B, H), -np.inf)
+    for b in range(B):
+        L = int(lengths[b])
+        if L == 0:
+            continue
+        for i in range(H):
+            s = scale * (kv[b, :L] @ q[b, i])
+            m = s.max()
+            e = np.exp(s - m)
+            z[b, i] = (e @ kv[b, :L, :dl]) / e.sum()
+            lse[b, i] = m + np.log(e.sum())
+    return z, lse
+
+
+def mla_up_gate(z, w_uv, gate_logit):
+    """The value up-projection after the latent sum, then the head's sigmoid gate:
+    o_i = W_V,i z_i * sigmoid(gate_i).  z [B,H,512], w_uv [H,128,512], gate_logit [B,H]."""
+    zz, wv, gl = _f64(z), _f64(w_uv), _f64(gate_logit)
+    return np.einsum("bhl,hvl->bhv", zz, wv) / (1.0 + np.exp(-gl))[..., None]
+
+
+def mla_decode_absorbed(q_nope, q_rope, c, r, lengths, w_uk, w_uv, gate_logit,
+                        scale=192 ** -0.5):
+    """The absorbed path: absorb the key up-projection into the query, attend over the
+    576-wide cache with the latent as the value, project after the sum, gate."""
+    cache = np.concatenate([_f64(c), _f64(r)], axis=2)
+    z, _ = mla_latent_attention(mla_absorb(q_nope, q_rope, w_uk), cache, lengths, scale)
+    return mla_up_gate(z, w_uv, gate_logit)

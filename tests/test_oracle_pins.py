@@ -498,3 +498,66 @@ def test_fp8_group_quantisation_bounds():
     # an all-zero group keeps a positive scale and zero codes
     z_codes, z_scales = oracle.fp8_quantize_groups(np.zeros((2, 128)), 128)
     assert (z_codes == 0).all() and (z_scales > 0).all()
+
+
+# ---------------------------------------------------------------------------------------
+# Absorbed gated-MLA decode
+# ---------------------------------------------------------------------------------------
+
+def _mla_case(B, H, L, seed, lengths=None):
+    g = torch.Generator().manual_seed(seed)
+    bf = lambda *s, std=1.0: (torch.randn(*s, generator=g) * std).to(torch.bfloat16)
+    return dict(q_nope=bf(B, H, 128), q_rope=bf(B, H, 64), c=bf(B, L, 512), r=bf(B, L, 64),
+                w_uk=bf(H, 128, 512, std=0.05), w_uv=bf(H, 128, 512, std=0.05),
+                gate=bf(B, H), lengths=np.array(lengths if lengths is not None else [L] * B))
+
+
+def test_mla_absorbed_path_equals_the_expanded_one():
+    """The pages' identity: moving W_K,i into the query and W_V,i after the latent sum gives
+    the same attention function as expanding every cached position."""
+    m = _mla_case(4, 6, 23, seed=70, lengths=[23, 1, 7, 16])
+    args = (m["q_nope"], m["q_rope"], m["c"], m["r"], m["lengths"], m["w_uk"], m["w_uv"],
+            m["gate"])
+    e, a = oracle.mla_decode_expanded(*args), oracle.mla_decode_absorbed(*args)
+    np.testing.assert_allclose(a, e, rtol=0, atol=1e-12 * np.abs(e).max())
+
+
+def test_mla_one_cached_position_returns_its_value():
+    m = _mla_case(2, 3, 5, seed=71, lengths=[1, 1])
+    out = oracle.mla_decode_absorbed(m["q_nope"], m["q_rope"], m["c"], m["r"], m["lengths"],
+                                     m["w_uk"], m["w_uv"], m["gate"])
+    c0 = m["c"][:, 0].double().numpy()
+    wv = m["w_uv"].double().numpy()
+    sig = expit(m["gate"].double().numpy())
+    want = np.einsum("hvl,bl->bhv", wv, c0) * sig[..., None]
+    np.testing.assert_allclose(out, want, rtol=1e-13, atol=1e-15)
+
+
+def test_mla_zero_query_averages_the_values():
+    m = _mla_case(2, 2, 6, seed=72, lengths=[6, 3])
+    z = torch.zeros_like(m["q_nope"]), torch.zeros_like(m["q_rope"])
+    out = oracle.mla_decode_expanded(z[0], z[1], m["c"], m["r"], m["lengths"], m["w_uk"],
+                                     m["w_uv"], m["gate"])
+    wv = m["w_uv"].double().numpy()
+    sig = expit(m["gate"].double().numpy())
+    for b, L in enumerate(m["lengths"]):
+        mean_c = m["c"][b, :L].double().numpy().mean(0)
+        np.testing.assert_allclose(out[b], (wv @ mean_c) * sig[b][:, None], rtol=1e-12)
+
+
+def test_mla_latent_attention_brute_force_and_lse():
+    """The attention core against scalar loops, and its log-sum-exp against scipy's."""
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(73)
+    q = rng.standard_normal((1, 2, 576))
+    kv = rng.standard_normal((1, 3, 576))
+    z, lse = oracle.mla_latent_attention(q, kv, np.array([3]), scale=0.05)
+    for i in range(2):
+        s = [0.05 * sum(q[0, i, d] * kv[0, t, d] for d in range(576)) for t in range(3)]
+        w = [np.exp(x - max(s)) for x in s]
+        for dd in (0, 7, 511):
+            want = sum(w[t] * kv[0, t, dd] for t in range(3)) / sum(w)
+            assert abs(z[0, i, dd] - want) <= 1e-12 * max(1.0, abs(want))
+        assert abs(lse[0, i] - logsumexp(s)) <= 1e-12 * abs(lse[0, i])
+    z0, l0 = oracle.mla_latent_attention(q, kv, np.array([0]))
+    assert not z0.any() and np.isneginf(l0).all()
