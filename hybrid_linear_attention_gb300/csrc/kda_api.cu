@@ -1,6 +1,7 @@
 // kda_api.cu -- the C ABI (include/kda.h): host-side validation, then kernel launches.
 // Nothing here allocates device memory; every buffer belongs to the caller.
 #include "../../include/kda.h"
+#include "../../include/mla.h"
 
 #include <atomic>
 #include <cstdint>
@@ -440,6 +441,58 @@ kda_status kda_state_accept(const kda_params *p, const void *step_states, int n_
                                          n_seqs, K, p->H, p->d_k, p->state_dtype == KDA_BF16,
                                          device_error_ptr(), stream),
                 1);
+}
+
+// ---- absorbed gated-MLA decode ----------------------------------------------------------
+
+static kda_status mla_common(const void *cache, int64_t cache_len, const int32_t *lengths,
+                             int n_seqs, float scale, float *z) {
+  if (n_seqs < 0 || n_seqs > 65535 || !(scale > 0.f) || !(scale < 1e30f))
+    return KDA_ERR_INVALID_ARG;
+  if (n_seqs == 0) return KDA_OK;
+  if (cache_len < 1 || cache_len > (int64_t)1 << 30 || !cache || !lengths || !z)
+    return KDA_ERR_INVALID_ARG;
+  if (!aligned16(cache) || !aligned16(lengths) || !aligned16(z)) return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
+kda_status mla_decode_latent(const void *q_cat, const void *cache, int64_t cache_len,
+                             const int32_t *lengths, int n_seqs, float scale, float *z,
+                             cudaStream_t stream) {
+  kda_status st = mla_common(cache, cache_len, lengths, n_seqs, scale, z);
+  if (st != KDA_OK || n_seqs == 0) return st;
+  if (!q_cat || !aligned16(q_cat)) return KDA_ERR_INVALID_ARG;
+  if (!kda::mla_latent_supported()) return KDA_ERR_UNSUPPORTED;
+  kda::MlaArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.B = n_seqs, a.L_max = cache_len, a.scale_log2 = scale * 1.4426950408889634f;
+  a.q_cat = const_cast<void *>(q_cat), a.cache = cache, a.lengths = lengths, a.z = z;
+  a.err = device_error_ptr();
+  return finish(kda::launch_mla_latent(a, stream), 1);
+}
+
+kda_status mla_decode(const void *q_nope, const void *q_rope, const void *w_uk,
+                      const void *w_uv, const void *cache, int64_t cache_len,
+                      const int32_t *lengths, int n_seqs, const void *gate_logit, float scale,
+                      void *q_cat, float *z, void *out, cudaStream_t stream) {
+  kda_status st = mla_common(cache, cache_len, lengths, n_seqs, scale, z);
+  if (st != KDA_OK || n_seqs == 0) return st;
+  if (!q_nope || !q_rope || !w_uk || !w_uv || !gate_logit || !q_cat || !out)
+    return KDA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(w_uv) ||
+      !aligned16(gate_logit) || !aligned16(q_cat) || !aligned16(out))
+    return KDA_ERR_INVALID_ARG;
+  if (!kda::mla_latent_supported()) return KDA_ERR_UNSUPPORTED;
+  kda::MlaArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.B = n_seqs, a.L_max = cache_len, a.scale_log2 = scale * 1.4426950408889634f;
+  a.q_nope = q_nope, a.q_rope = q_rope, a.w_uk = w_uk, a.w_uv = w_uv, a.gate = gate_logit;
+  a.q_cat = q_cat, a.cache = cache, a.lengths = lengths, a.z = z, a.out = out;
+  a.err = device_error_ptr();
+  cudaError_t e = kda::launch_mla_absorb(a, stream);
+  if (e == cudaSuccess) e = kda::launch_mla_latent(a, stream);
+  if (e == cudaSuccess) e = kda::launch_mla_up_gate(a, stream);
+  return finish(e, 3);
 }
 
 kda_status kda_check_device_error(cudaStream_t stream) {

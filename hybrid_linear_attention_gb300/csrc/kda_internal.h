@@ -40,6 +40,23 @@ struct RecArgs {
   int *err;
 };
 
+// Absorbed gated-MLA decode, the pages' shapes: 64 heads, latent 512 + positional key 64,
+// 128-wide non-positional query and value per head.
+struct MlaArgs {
+  int B;                       // sequences (one query token each)
+  int64_t L_max;               // cache rows per sequence
+  float scale_log2;            // score scale x log2(e)
+  const void *q_nope, *q_rope; // [B, 64, 128], [B, 64, 64] bf16
+  const void *w_uk, *w_uv;     // [64, 128, 512] bf16 each
+  const void *gate;            // [B, 64] bf16 gate logits
+  void *q_cat;                 // [B, 64, 576] bf16 absorbed query (written, then read)
+  const void *cache;           // [B, L_max, 576] bf16: latent | positional key per row
+  const int32_t *lengths;      // [B] cached positions of each sequence
+  float *z;                    // [B, 64, 512] fp32 attention output (latent)
+  void *out;                   // [B, 64, 128] bf16 gated head outputs
+  int *err;
+};
+
 struct ProArgs {
   int H, n_seqs;
   int64_t T;
@@ -74,6 +91,10 @@ cudaError_t launch_state_accept(const void *step_states, void *pool, const int32
                                 int D, bool st_bf16, int *err, cudaStream_t s);
 cudaError_t launch_prologue(const ProArgs &a, int D, bool io_bf16, cudaStream_t s);
 // out[k] <- the three raw inputs before checkpoint k (conv tail at that position)
+bool mla_latent_supported();
+cudaError_t launch_mla_absorb(const MlaArgs &a, cudaStream_t s);
+cudaError_t launch_mla_latent(const MlaArgs &a, cudaStream_t s);
+cudaError_t launch_mla_up_gate(const MlaArgs &a, cudaStream_t s);
 cudaError_t launch_conv_ckpt(const void *x, const void *conv_state, const int32_t *cu,
                              int n_seqs, int64_t T, const int32_t *ckpt_cu,
                              const int32_t *ckpt_pos, int n_ckpt, int channels, void *out,

@@ -1,0 +1,452 @@
+// mla_decode.cu -- absorbed gated-MLA decode over the 576-wide latent cache.
+//
+// "Ling-3.1-flash: Grouped Routing and Two Different MLA Caches", sections "MLA's expanded
+// reference path" and "Why weight absorption keeps the same attention function": each cached
+// position keeps its 512-wide normalised latent c_t and the 64-wide rotated positional key r_t
+// shared by the 64 heads.  With the key up-projection W_K,i moved into the query
+// (q~_i = W_K,i^T q_i^N) the score of head i is scale * [q~_i ; q_i^R] . [c_t ; r_t] over the
+// same 576-wide key for every head; the latent itself is the attention value, and the value
+// up-projection W_V,i comes after the weighted sum; a per-head sigmoid gate scales the head's
+// 128-wide output.
+//
+// Kernels:
+//   mla_absorb_kernel   q_cat = [W_K,i^T q_i^N ; q_i^R] (bf16), a CTA per (head, 8 sequences).
+//   mla_latent_kernel   per sequence, all 64 heads: S^T = C Q^T over 128-position tiles of the
+//                       cache (tcgen05, C K-major, Q K-major, fp32 in TMEM), online softmax on
+//                       the CUDA cores, Z^T += C^T P^T with the same C tile read MN-major and P
+//                       written MN-major over the tile's positional block (tcgen05, 4 M-slices
+//                       of 128 latent channels); Z rescaled in TMEM when a head's max moves.
+//   mla_up_gate_kernel  o_i = W_V,i z_i * sigmoid(gate_i), a CTA per (head, 8 sequences).
+#include "kda_common.cuh"
+#include "kda_internal.h"
+#include "kda_tc_ptx.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+namespace kda {
+namespace {
+
+using namespace tc;
+
+constexpr int MH = 64;        // heads
+constexpr int ML = 512;       // latent width
+constexpr int MR = 64;        // positional-key width
+constexpr int MK = ML + MR;   // cached key width
+constexpr int MV = 128;       // per-head value width after the up-projection
+constexpr int MN = 128;       // per-head non-positional query width
+constexpr int TP = 128;       // cached positions per tile
+constexpr int KB = MK / 64;   // 64-element key blocks (128 bytes of bf16)
+constexpr int MLA_NT = 128;   // threads of the latent kernel (four warps = four TMEM lane quarters)
+
+// shared memory of the latent kernel (1024-byte aligned base):
+//   Q: [KB][64 heads][128 B] K-major, 72 KB; C: [KB][128 positions][128 B], 144 KB, whose last
+//   (positional) block becomes P = softmax weights [128 positions][64 heads] bf16 once the
+//   score product has read it
+constexpr uint32_t M_OFF_Q = 0;
+constexpr uint32_t M_OFF_C = KB * MH * 128;
+constexpr uint32_t M_OFF_P = M_OFF_C + (KB - 1) * TP * 128;
+constexpr uint32_t M_SMEM = M_OFF_C + KB * TP * 128 + 1024;
+constexpr uint32_t M_TM_S = 0;    // S^T: 128 lanes (positions) x 64 columns (heads)
+constexpr uint32_t M_TM_Z = 256;  // Z^T: 4 slices of 128 lanes (latent) x 64 columns (heads)
+enum { MB_Q = 0, MB_C, MB_S, MB_Z, MB_N };
+
+struct MlaMaps {
+  CUtensorMap q, c;
+};
+
+// offset of (position r, 16-byte chunk j) in an MN-major / TMA 128-byte-swizzled block
+__device__ __forceinline__ uint32_t sw128_row(int r, int j) {
+  return (uint32_t)r * 128u + ((uint32_t)(j ^ (r & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(MLA_NT, 1)
+    mla_latent_kernel(const MlaArgs a, const __grid_constant__ MlaMaps maps) {
+  extern __shared__ uint8_t mraw[];
+  const uint32_t raw = smem_u32(mraw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  uint8_t *sm = mraw + pad;
+  const uint32_t sb = raw + pad;
+  __shared__ __align__(8) uint64_t s_bar[MB_N];
+  __shared__ uint32_t s_tmem, s_abort, s_loads, s_mmas;
+  __shared__ float s_red[4][MH], s_m[MH], s_l[MH], s_mnew[MH], s_alpha[MH];
+  __shared__ int s_rescale;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x;
+  int len = a.lengths[b];
+  if (len < 0 || len > a.L_max) {  // a length outside the cache: flagged, nothing attended
+    if (tid == 0 && a.err) atomicOr(a.err, ERR_BAD_INDEX);
+    len = 0;
+  }
+  const int ntiles = (len + TP - 1) / TP;
+  auto bar = [&](int i) { return smem_u32(&s_bar[i]); };
+  if (tid == 0) {
+    for (int i = 0; i < MB_N; ++i) mbar_init(bar(i), 1);
+    mbar_fence_init();
+    s_abort = 0;
+    s_rescale = 0;
+    s_loads = 0;  // C tiles requested (the drain's parity)
+    s_mmas = 0;   // tiles whose products were issued
+  }
+  if (tid < MH) s_m[tid] = -INFINITY, s_l[tid] = 0.f;
+  if (warp == 0) tmem_alloc(smem_u32(&s_tmem), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = s_tmem;
+  const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+  auto load_tile = [&](int t) {  // the 9 key blocks of positions 128 t .. 128 t + 127
+    ++s_loads;
+    mbar_expect_tx(bar(MB_C), KB * TP * 128);
+    for (int kb = 0; kb < KB; ++kb)
+      tma_load_3d(sb + M_OFF_C + kb * TP * 128, &maps.c, 64 * kb, TP * t, b, bar(MB_C));
+  };
+  auto wait = [&](int i, uint32_t parity) {
+    if (!mbar_wait(bar(i), parity)) s_abort = 1;
+  };
+  if (tid == 0 && ntiles > 0) {
+    mbar_expect_tx(bar(MB_Q), KB * MH * 128);
+    for (int kb = 0; kb < KB; ++kb)
+      tma_load_3d(sb + M_OFF_Q + kb * MH * 128, &maps.q, 64 * kb, 0, b, bar(MB_Q));
+    load_tile(0);
+  }
+  // S: bf16 x bf16, M = 128 positions, N = 64 heads, both K-major
+  constexpr uint32_t ID_S = idesc(1, 128, 64, 0, 0);
+  // Z: M = 128 latent channels (A = C^T, MN-major), N = 64 heads (B = P^T, MN-major)
+  constexpr uint32_t ID_Z = idesc(1, 128, 64, 1, 1);
+
+  for (int t = 0; t < ntiles; ++t) {
+    const uint32_t par = (uint32_t)(t & 1);
+    if (tid == 0) {
+      if (t == 0) wait(MB_Q, 0);
+      wait(MB_C, par);
+      tc_fence_after();
+      for (int kb = 0; kb < KB; ++kb)
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t ad = sdesc_sw128(sb + M_OFF_C + kb * TP * 128 + ks * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sb + M_OFF_Q + kb * MH * 128 + ks * 32, 16, 1024);
+          mma_bf16_ss(tm + M_TM_S, ad, bd, ID_S, (kb | ks) != 0);
+        }
+      mma_commit(bar(MB_S));
+      ++s_mmas;
+    }
+    wait(MB_S, par);
+    tc_fence_after();
+
+    // ---- softmax over this tile's positions (thread = position 32 warp + lane) -----------
+    const int r = 32 * warp + lane;
+    const bool valid = TP * t + r < len;
+    float x[MH];
+    {
+      float v[32];
+      tmem_ld32(tm + lane_off + M_TM_S, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int h = 0; h < 32; ++h) x[h] = valid ? v[h] * a.scale_log2 : -INFINITY;
+      tmem_ld32(tm + lane_off + M_TM_S + 32, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int h = 0; h < 32; ++h) x[32 + h] = valid ? v[h] * a.scale_log2 : -INFINITY;
+    }
+    if (!valid) {  // a position past the sequence: its latent row must not reach Z (x 0)
+#pragma unroll 1
+      for (int kb = 0; kb < KB - 1; ++kb)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4 *>(sm + M_OFF_C + kb * TP * 128 + sw128_row(r, j)) =
+              make_uint4(0, 0, 0, 0);
+    }
+    // per-head maximum over the 128 positions: warp (transpose-reduce), then the four warps
+    {
+      float mx[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int h = 0; h < 32; ++h) mx[h] = x[32 * half + h];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+          const bool up = (lane & off) != 0;
+#pragma unroll
+          for (int h = 0; h < off; ++h) {
+            const float send = up ? mx[h] : mx[h + off];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+            mx[h] = fmaxf(up ? mx[h + off] : mx[h], recv);
+          }
+        }
+        s_red[warp][32 * half + lane] = mx[0];
+      }
+    }
+    __syncthreads();
+    if (tid < MH) {
+      const float mt = fmaxf(fmaxf(s_red[0][tid], s_red[1][tid]), fmaxf(s_red[2][tid], s_red[3][tid]));
+      const float mo = s_m[tid], mn = fmaxf(mo, mt);
+      const float al = mn == -INFINITY ? 1.f : exp2f(mo - mn);  // exp2(-inf) = 0 on a first max
+      s_mnew[tid] = mn;
+      s_alpha[tid] = al;
+      if (t > 0 && al != 1.f) s_rescale = 1;
+    }
+    __syncthreads();
+    // weights p = 2^(x - m), written as P^T (MN-major: row = position, 64 heads = 128 B)
+    float p[MH];
+#pragma unroll
+    for (int h = 0; h < MH; ++h) p[h] = x[h] == -INFINITY ? 0.f : exp2f(x[h] - s_mnew[h]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint4 w;
+      w.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 0])) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 1])) << 16);
+      w.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 2])) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 3])) << 16);
+      w.z = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 4])) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 5])) << 16);
+      w.w = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 6])) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 7])) << 16);
+      *reinterpret_cast<uint4 *>(sm + M_OFF_P + sw128_row(r, j)) = w;
+    }
+    // the row sums use the bf16 weights the product multiplies by
+    {
+      float sm32[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int h = 0; h < 32; ++h)
+          sm32[h] = __bfloat162float(__float2bfloat16_rn(p[32 * half + h]));
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+          const bool up = (lane & off) != 0;
+#pragma unroll
+          for (int h = 0; h < off; ++h) {
+            const float send = up ? sm32[h] : sm32[h + off];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+            sm32[h] = (up ? sm32[h + off] : sm32[h]) + recv;
+          }
+        }
+        s_red[warp][32 * half + lane] = sm32[0];
+      }
+    }
+    // Z^T columns (heads) whose maximum moved are rescaled before this tile is added
+    if (s_rescale) {
+#pragma unroll 1
+      for (int sl = 0; sl < 4; ++sl)
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[32];
+          const uint32_t col = M_TM_Z + 64 * sl + 32 * hh;
+          tmem_ld32(tm + lane_off + col, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 32; ++h) v[h] *= s_alpha[32 * hh + h];
+          tmem_st32(tm + lane_off + col, v);
+        }
+      tmem_wait_st();
+    }
+    fence_proxy_async();  // P and the zeroed rows, written by these threads, feed the product
+    tc_fence_before();
+    __syncthreads();
+    if (tid < MH) {
+      s_l[tid] = s_l[tid] * s_alpha[tid] + s_red[0][tid] + s_red[1][tid] + s_red[2][tid] +
+                 s_red[3][tid];
+      s_m[tid] = s_mnew[tid];
+    }
+    if (tid == 0) {
+      s_rescale = 0;
+      tc_fence_after();
+      for (int sl = 0; sl < 4; ++sl)
+        for (int ks = 0; ks < TP / 16; ++ks) {
+          // A = C^T: latent channels 128 sl .. 128 sl + 127 (key blocks 2 sl, 2 sl + 1, 16 KB
+          // apart), positions 16 ks .. 16 ks + 15 (two 8-row groups of 1 KB)
+          const uint64_t ad = sdesc_sw128(sb + M_OFF_C + 2 * sl * TP * 128 + ks * 2048,
+                                          TP * 128, 1024);
+          const uint64_t bd = sdesc_sw128(sb + M_OFF_P + ks * 2048, 1024, 1024);  // one atom
+          mma_bf16_ss(tm + M_TM_Z + 64 * sl, ad, bd, ID_Z, (t > 0 || ks > 0) ? 1u : 0u);
+        }
+      mma_commit(bar(MB_Z));
+      wait(MB_Z, par);  // the tile's C and P are read: the next tile may land on them
+      if (t + 1 < ntiles) load_tile(t + 1);
+    }
+    wait(MB_Z, par);
+    tc_fence_after();
+    __syncthreads();
+    if (s_abort) break;
+  }
+
+  // ---- z = Z / l per head (thread = latent channel of its lane quarter, per slice) ----------
+  float *z = a.z + (size_t)b * MH * ML;
+#pragma unroll 1
+  for (int sl = 0; sl < 4; ++sl)
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+      float v[32];
+      if (ntiles > 0 && !s_abort) {
+        tmem_ld32(tm + lane_off + M_TM_Z + 64 * sl + 32 * hh, v);
+        tmem_wait_ld();
+      }
+#pragma unroll
+      for (int h = 0; h < 32; ++h) {
+        const int head = 32 * hh + h;
+        const float l = s_l[head];
+        z[(size_t)head * ML + 128 * sl + 32 * warp + lane] =
+            (ntiles > 0 && !s_abort && l > 0.f) ? v[h] / l : 0.f;
+      }
+    }
+  if (tid == 0 && s_abort) {
+    // a bounded wait ran out: let the copies and products in flight land (bounded) before
+    // the CTA releases its memory, then report it
+    if (s_loads) mbar_wait(bar(MB_C), (s_loads - 1) & 1);
+    if (s_mmas) {
+      mbar_wait(bar(MB_S), (s_mmas - 1) & 1);
+      mbar_wait(bar(MB_Z), (s_mmas - 1) & 1);
+    }
+    if (a.err) atomicOr(a.err, ERR_MBAR_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tm, 512);
+}
+
+// q_cat[b][h] = [W_K,h^T q_nope[b][h] ; q_rope[b][h]] (bf16), 8 sequences per CTA
+constexpr int MQB = 8;
+__global__ void __launch_bounds__(128) mla_absorb_kernel(const MlaArgs a) {
+  const int h = blockIdx.x, b0 = blockIdx.y * MQB, tid = threadIdx.x;
+  __shared__ float s_q[MQB][MN];
+  for (int e = tid; e < MQB * MN; e += 128) {
+    const int bb = e / MN, n = e % MN;
+    s_q[bb][n] = b0 + bb < a.B ? __bfloat162float(
+                                     reinterpret_cast<const bf16 *>(a.q_nope)[((size_t)(b0 + bb) * MH + h) * MN + n])
+                               : 0.f;
+  }
+  __syncthreads();
+  float acc[MQB][4];
+#pragma unroll
+  for (int bb = 0; bb < MQB; ++bb) acc[bb][0] = acc[bb][1] = acc[bb][2] = acc[bb][3] = 0.f;
+  const bf16 *w = reinterpret_cast<const bf16 *>(a.w_uk) + (size_t)h * MN * ML + 4 * tid;
+#pragma unroll 4
+  for (int n = 0; n < MN; ++n) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(w + (size_t)n * ML);
+    const float w0 = __uint_as_float(u.x << 16), w1 = __uint_as_float(u.x & 0xffff0000u);
+    const float w2 = __uint_as_float(u.y << 16), w3 = __uint_as_float(u.y & 0xffff0000u);
+#pragma unroll
+    for (int bb = 0; bb < MQB; ++bb) {
+      const float q = s_q[bb][n];
+      acc[bb][0] = fmaf(w0, q, acc[bb][0]);
+      acc[bb][1] = fmaf(w1, q, acc[bb][1]);
+      acc[bb][2] = fmaf(w2, q, acc[bb][2]);
+      acc[bb][3] = fmaf(w3, q, acc[bb][3]);
+    }
+  }
+  bf16 *qc = reinterpret_cast<bf16 *>(a.q_cat);
+  for (int bb = 0; bb < MQB && b0 + bb < a.B; ++bb) {
+    bf16 *row = qc + ((size_t)(b0 + bb) * MH + h) * MK;
+#pragma unroll
+    for (int y = 0; y < 4; ++y) row[4 * tid + y] = __float2bfloat16_rn(acc[bb][y]);
+    if (tid < MR)
+      row[ML + tid] = reinterpret_cast<const bf16 *>(a.q_rope)[((size_t)(b0 + bb) * MH + h) * MR + tid];
+  }
+}
+
+// out[b][h] = W_V,h z[b][h] * sigmoid(gate[b][h]) (bf16), 8 sequences per CTA
+__global__ void __launch_bounds__(128) mla_up_gate_kernel(const MlaArgs a) {
+  const int h = blockIdx.x, b0 = blockIdx.y * MQB, v = threadIdx.x;
+  __shared__ float s_z[MQB][ML];
+  for (int e = v; e < MQB * ML; e += 128) {
+    const int bb = e / ML, l = e % ML;
+    s_z[bb][l] = b0 + bb < a.B ? a.z[((size_t)(b0 + bb) * MH + h) * ML + l] : 0.f;
+  }
+  __syncthreads();
+  float acc[MQB];
+#pragma unroll
+  for (int bb = 0; bb < MQB; ++bb) acc[bb] = 0.f;
+  const bf16 *w = reinterpret_cast<const bf16 *>(a.w_uv) + ((size_t)h * MV + v) * ML;
+#pragma unroll 2
+  for (int l = 0; l < ML; l += 8) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(w + l);
+    const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int y = 0; y < 4; ++y) {
+      const float wa = __uint_as_float(ws[y] << 16), wb = __uint_as_float(ws[y] & 0xffff0000u);
+#pragma unroll
+      for (int bb = 0; bb < MQB; ++bb)
+        acc[bb] = fmaf(wb, s_z[bb][l + 2 * y + 1], fmaf(wa, s_z[bb][l + 2 * y], acc[bb]));
+    }
+  }
+  for (int bb = 0; bb < MQB && b0 + bb < a.B; ++bb) {
+    const size_t hb = (size_t)(b0 + bb) * MH + h;
+    const float g = __bfloat162float(reinterpret_cast<const bf16 *>(a.gate)[hb]);
+    reinterpret_cast<bf16 *>(a.out)[hb * MV + v] = __float2bfloat16_rn(acc[bb] * sigmoidf_(g));
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 mla_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// [n3][rows][576] bf16, boxes of 64 elements x box_rows rows, 128-byte swizzle
+bool mla_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t n3, uint32_t box_rows) {
+  auto fn = mla_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)MK, (cuuint64_t)rows, (cuuint64_t)n3};
+  cuuint64_t strides[2] = {(cuuint64_t)MK * 2, (cuuint64_t)rows * MK * 2};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool mla_latent_supported() {
+  int dev = 0, major = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    return false;
+  return major == 10 && mla_encode_fn() != nullptr;
+}
+
+cudaError_t launch_mla_absorb(const MlaArgs &a, cudaStream_t s) {
+  if (a.B == 0) return cudaSuccess;
+  mla_absorb_kernel<<<dim3(MH, (a.B + MQB - 1) / MQB), 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mla_latent(const MlaArgs &a, cudaStream_t s) {
+  if (a.B == 0) return cudaSuccess;
+  MlaMaps maps;
+  memset(&maps, 0, sizeof maps);
+  if (!mla_map(&maps.q, a.q_cat, MH, a.B, MH) ||
+      !mla_map(&maps.c, a.cache, a.L_max > 0 ? a.L_max : 1, a.B, TP))
+    return cudaErrorInvalidValue;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(mla_latent_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, M_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  mla_latent_kernel<<<a.B, MLA_NT, M_SMEM, s>>>(a, maps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mla_up_gate(const MlaArgs &a, cudaStream_t s) {
+  if (a.B == 0) return cudaSuccess;
+  mla_up_gate_kernel<<<dim3(MH, (a.B + MQB - 1) / MQB), 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

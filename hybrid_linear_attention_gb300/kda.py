@@ -29,7 +29,7 @@ EXPORTS = (
     "kda_conv_tail_checkpoints",
     "kda_decode_step", "kda_conv_state_update",
     "kda_decode_step_fused", "kda_decode_step_fused_fp8", "kda_decode_multi", "kda_state_accept", "kda_check_device_error",
-    "kda_launch_count",
+    "kda_launch_count", "mla_decode_latent", "mla_decode",
 )
 
 
@@ -101,6 +101,9 @@ def load():
             "kda_state_accept": (_i32, [_P, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp]),
             "kda_check_device_error": (_i32, [_vp]),
             "kda_launch_count": (ctypes.c_uint64, []),
+            "mla_decode_latent": (_i32, [_vp, _vp, _i64, _vp, _i32, ctypes.c_float, _vp, _vp]),
+            "mla_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, ctypes.c_float,
+                                  _vp, _vp, _vp, _vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -318,3 +321,30 @@ def kda_conv_state_update(p, x_new, conv_w, conv_state, y, *, slot_idx=None, str
         _ptr(slot_idx, torch.int32, "slot_idx"), x_new.shape[0], x_new.shape[1],
         _ptr(y, io, "y"), _stream(stream))
     _check(st, "kda_conv_state_update")
+
+
+# ---- absorbed gated-MLA decode (mla.h) -----------------------------------------------------
+
+MLA_SCALE = 192 ** -0.5
+
+
+def mla_decode_latent(q_cat, cache, lengths, z, *, scale=MLA_SCALE, stream=None):
+    """q_cat [B,64,576] bf16, cache [B,L,576] bf16, lengths [B] int32, z [B,64,512] fp32."""
+    st = load().mla_decode_latent(
+        _ptr(q_cat, torch.bfloat16, "q_cat"), _ptr(cache, torch.bfloat16, "cache"),
+        cache.shape[1], _ptr(lengths, torch.int32, "lengths"), q_cat.shape[0], float(scale),
+        _ptr(z, torch.float32, "z"), _stream(stream))
+    _check(st, "mla_decode_latent")
+
+
+def mla_decode(q_nope, q_rope, w_uk, w_uv, cache, lengths, gate_logit, q_cat, z, out, *,
+               scale=MLA_SCALE, stream=None):
+    """One absorbed gated-MLA decode step; q_cat and z are caller-owned intermediates."""
+    bf = torch.bfloat16
+    st = load().mla_decode(
+        _ptr(q_nope, bf, "q_nope"), _ptr(q_rope, bf, "q_rope"), _ptr(w_uk, bf, "w_uk"),
+        _ptr(w_uv, bf, "w_uv"), _ptr(cache, bf, "cache"), cache.shape[1],
+        _ptr(lengths, torch.int32, "lengths"), q_nope.shape[0], _ptr(gate_logit, bf, "gate_logit"),
+        float(scale), _ptr(q_cat, bf, "q_cat"), _ptr(z, torch.float32, "z"), _ptr(out, bf, "out"),
+        _stream(stream))
+    _check(st, "mla_decode")

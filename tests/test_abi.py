@@ -1,4 +1,4 @@
-"""The C-ABI library loads, exports every entry point include/kda.h declares, and rejects
+"""The C-ABI library loads, exports every entry point include/*.h declares, and rejects
 bad arguments on the host before touching the GPU (no compute call is made here)."""
 import ctypes
 import os
@@ -10,7 +10,7 @@ import torch
 from hybrid_linear_attention_gb300 import build as kbuild
 from hybrid_linear_attention_gb300 import kda
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "kda.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
 
 
 @pytest.fixture(scope="module")
@@ -20,10 +20,12 @@ def lib():
 
 
 def _declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)
-    return sorted(set(names))
+    names = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, h)).read(), flags=re.S)
+            names |= set(re.findall(r"\b((?:kda|mla)_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_contract_calls():
@@ -185,3 +187,15 @@ def test_fp8_calls_reject_bad_arguments_on_host(lib):
     # decode: codes without scales
     assert lib.kda_decode_step_fused_fp8(P, buf, buf, buf, buf, buf, buf, 2, None, 2, None, None,
                                          buf, None, None) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_mla_calls_reject_bad_arguments_on_host(lib):
+    buf = ctypes.c_void_p(16)  # never dereferenced: every call fails validation first
+    assert lib.mla_decode_latent(buf, buf, 0, buf, 2, 0.07, buf, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.mla_decode_latent(buf, buf, 64, buf, 2, 0.0, buf, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.mla_decode_latent(buf, buf, 64, buf, -1, 0.07, buf, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.mla_decode_latent(buf, ctypes.c_void_p(24), 64, buf, 2, 0.07, buf,
+                                 None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.mla_decode_latent(None, None, 0, None, 0, 0.07, None, None) == kda.KDA_OK
+    assert lib.mla_decode(buf, buf, buf, buf, buf, 64, buf, 2, None, 0.07, buf, buf, buf,
+                          None) == kda.KDA_ERR_INVALID_ARG

@@ -1,0 +1,118 @@
+"""GPU parity: the absorbed gated-MLA decode against the fp64 oracle.
+
+Tolerance: bf16 operands with fp32 accumulation (the softmax weights are rounded to bf16 as
+tensor-core operands, the normaliser sums the same rounded weights), so the bound is the bf16
+one of the KDA path: max |err| <= 1e-2 of the output RMS, beyond one bf16 ulp for outputs
+stored in bf16.  Cache rows at or past a sequence's length hold NaN here: they must not
+reach the result.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hybrid_linear_attention_gb300 import kda
+from tests import _gpu
+from tests._parity import max_err_rel_rms, out_error, to64
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+def _case(lengths, L, seed, q_std=1.0):
+    g = torch.Generator().manual_seed(seed)
+    B = len(lengths)
+    bf = lambda *s, std=1.0: (torch.randn(*s, generator=g) * std).to(torch.bfloat16)
+    cache = bf(B, L, 576)
+    for b, n in enumerate(lengths):  # rows past the length: NaN, never to be read into z
+        if 0 <= n < L:
+            cache[b, n:] = float("nan")
+    return dict(q_cat=bf(B, 64, 576, std=q_std), cache=cache,
+                lengths=torch.tensor(lengths, dtype=torch.int32),
+                q_nope=bf(B, 64, 128), q_rope=bf(B, 64, 64),
+                w_uk=bf(64, 128, 512, std=0.05), w_uv=bf(64, 128, 512, std=0.05),
+                gate=bf(B, 64))
+
+
+def _latent(m):
+    _gpu.lib()
+    z = torch.full((m["q_cat"].shape[0], 64, 512), 7.0, device="cuda")
+    kda.mla_decode_latent(m["q_cat"].cuda(), m["cache"].cuda(), m["lengths"].cuda(), z)
+    torch.cuda.synchronize()
+    return z
+
+
+@pytest.mark.parametrize("q_std", [1.0, 4.0])
+def test_latent_attention_matches_the_oracle(q_std):
+    """Ragged lengths around the 128-position tile (1, 127, 128, 129, 300), peaked scores
+    (q_std 4: the running max moves and Z is rescaled), NaN past every length."""
+    lengths = [1, 127, 128, 129, 300, 256]
+    m = _case(lengths, 320, seed=800 + int(q_std), q_std=q_std)
+    z = _latent(m)
+    kda.kda_check_device_error()
+    clean = m["cache"].clone()
+    for b, n in enumerate(lengths):
+        clean[b, n:] = 0
+    ref, _ = oracle.mla_latent_attention(m["q_cat"], clean, np.array(lengths),
+                                         scale=kda.MLA_SCALE)
+    for b in range(len(lengths)):
+        e = max_err_rel_rms(z[b], ref[b])
+        assert e <= TOL, f"sequence {b} (length {lengths[b]}): {e:.3g}"
+    assert torch.isfinite(z).all()
+
+
+def test_latent_attention_long_cache_sampled():
+    """The bench's cache length (4096 positions, 32 tiles) on a few sequences."""
+    lengths = [4096, 4000, 2049]
+    m = _case(lengths, 4096, seed=810)
+    z = _latent(m)
+    kda.kda_check_device_error()
+    clean = m["cache"].clone()
+    for b, n in enumerate(lengths):
+        clean[b, n:] = 0
+    ref, _ = oracle.mla_latent_attention(m["q_cat"], clean, np.array(lengths),
+                                         scale=kda.MLA_SCALE)
+    assert max_err_rel_rms(z, ref) <= TOL
+
+
+def test_empty_and_out_of_range_lengths():
+    """Length 0 gives z = 0; a length outside 0..cache_len is treated as 0 and reported."""
+    m = _case([0, 5, -1, 1000], 64, seed=820)
+    z = _latent(m)
+    with pytest.raises(kda.KdaError) as ei:
+        kda.kda_check_device_error()
+    assert ei.value.status == kda.KDA_ERR_BAD_INDEX
+    assert not z[0].any() and not z[2].any() and not z[3].any()
+    clean = m["cache"][1:2].clone()
+    clean[0, 5:] = 0
+    ref, _ = oracle.mla_latent_attention(m["q_cat"][1:2], clean, np.array([5]),
+                                         scale=kda.MLA_SCALE)
+    assert max_err_rel_rms(z[1:2], ref) <= TOL
+
+
+def test_mla_decode_matches_the_expanded_oracle():
+    """The whole step (absorption, latent attention, value up-projection, gate) against the
+    pages' expanded reference path computed in fp64."""
+    lengths = [300, 1, 129, 64]
+    m = _case(lengths, 320, seed=830)
+    _gpu.lib()
+    B = len(lengths)
+    q_cat = torch.empty((B, 64, 576), dtype=torch.bfloat16, device="cuda")
+    z = torch.empty((B, 64, 512), device="cuda")
+    out = torch.empty((B, 64, 128), dtype=torch.bfloat16, device="cuda")
+    c = _gpu.cuda
+    kda.mla_decode(c(m["q_nope"]), c(m["q_rope"]), c(m["w_uk"]), c(m["w_uv"]), c(m["cache"]),
+                   c(m["lengths"]), c(m["gate"]), q_cat, z, out)
+    torch.cuda.synchronize()
+    kda.kda_check_device_error()
+    # the absorbed query: the oracle's fp64 value within the bf16 rounding of the operand
+    qa = oracle.mla_absorb(m["q_nope"], m["q_rope"], m["w_uk"])
+    assert out_error(q_cat.cpu(), qa, torch.bfloat16) <= TOL
+    clean = m["cache"].clone()
+    for b, n in enumerate(lengths):
+        clean[b, n:] = 0
+    ref = oracle.mla_decode_expanded(m["q_nope"], m["q_rope"], clean[..., :512],
+                                     clean[..., 512:], np.array(lengths), m["w_uk"], m["w_uv"],
+                                     m["gate"], scale=kda.MLA_SCALE)
+    assert out_error(out.cpu(), ref, torch.bfloat16) <= TOL
