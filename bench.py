@@ -373,10 +373,11 @@ def run_ours(args):
     e2e_line = _e2e(wl, flush, args, dist) if not args.no_e2e else None
 
     # ---- decode: 256 sequences x 100 fused steps --------------------------------------
-    dec = dmulti = None
+    dec = dmulti = mla = None
     if not args.no_decode:
         dec = _decode_bench(dev, kda, inputs, hbm, rank, args)
         dmulti = _decode_multi_bench(dev, kda, inputs, hbm, rank)
+        mla = _mla_bench(dev, kda, inputs, hbm, rank)
 
     if rank != 0:
         return
@@ -412,6 +413,7 @@ def run_ours(args):
         line["decode"] = dec
     if dmulti:
         line["decode_multi"] = dmulti
+        line["mla_decode"] = mla
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = _cpu_baseline()
     print(json.dumps(line), flush=True)
@@ -498,6 +500,53 @@ def _decode_bench(dev, kda, inputs, hbm, rank, args):
                          "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                          "traffic": _profiled_traffic("kda_decode_fused_N256_H64.md",
                                                       ["kda_recurrent.cu", "kda_common.cuh"]),
+                         "algorithmic_bytes_per_launch": b}}
+
+
+N_MLA, L_MLA = 256, 4096
+
+
+def _mla_bench(dev, kda, inputs, hbm, rank):
+    """Absorbed gated-MLA decode: 256 sequences x 4096 cached positions, 64 heads, 576-wide
+    bf16 latent cache (1.21 GB, > L2), one query token each; the latent attention streams the
+    cache once.  Also the whole step (absorption + attention + up-projection + gate)."""
+    B, L = N_MLA, L_MLA
+    cache = inputs.normal((B, L, 576), seed=600 + rank, device=dev)
+    q_nope = inputs.normal((B, 64, 128), seed=601 + rank, device=dev)
+    q_rope = inputs.normal((B, 64, 64), seed=602 + rank, device=dev)
+    w_uk = inputs.normal((64, 128, 512), seed=603 + rank, device=dev, std=0.05)
+    w_uv = inputs.normal((64, 128, 512), seed=604 + rank, device=dev, std=0.05)
+    gate = inputs.normal((B, 64), seed=605 + rank, device=dev)
+    lengths = torch.full((B,), L, dtype=torch.int32, device=dev)
+    q_cat = torch.empty((B, 64, 576), dtype=torch.bfloat16, device=dev)
+    z = torch.empty((B, 64, 512), dtype=torch.float32, device=dev)
+    out = torch.empty((B, 64, 128), dtype=torch.bfloat16, device=dev)
+    step = lambda: kda.mla_decode(q_nope, q_rope, w_uk, w_uv, cache, lengths, gate, q_cat, z, out)
+    lat = lambda: kda.mla_decode_latent(q_cat, cache, lengths, z)
+    reps = 20
+    res = {}
+    for name, fn in (("latent", lat), ("step", step)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        e1.synchronize()
+        res[name] = e0.elapsed_time(e1) / reps
+    kda.kda_check_device_error()
+    b = B * L * 576 * 2 + B * 64 * 576 * 2 + B * 64 * 512 * 4  # cache + query + z
+    gbs = b / (res["latent"] * 1e-3) / 1e9
+    return {"metric": "MLA decode latent-cache GB/s", "value": gbs, "unit": "GB/s",
+            "workload": "256 sequences x 4096 cached positions, 64 heads, 576-wide bf16 latent "
+                        "cache (512 latent + 64 positional key; 1.21 GB, > L2), one query token "
+                        "each, synthetic weights",
+            "ms_latent": res["latent"], "ms_step": res["step"],
+            "tokens_per_s": B / (res["step"] * 1e-3),
+            "roofline": {"kernel": "mla_decode_latent", "bound": "hbm", "achieved": gbs,
+                         "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                          "algorithmic_bytes_per_launch": b}}
 
 
