@@ -37,31 +37,36 @@ constexpr int MR = 64;        // positional-key width
 constexpr int MK = ML + MR;   // cached key width
 constexpr int MV = 128;       // per-head value width after the up-projection
 constexpr int MN = 128;       // per-head non-positional query width
-constexpr int TP = 128;       // cached positions per tile
+constexpr int TP = 64;        // cached positions per tile
 constexpr int KB = MK / 64;   // 64-element key blocks (128 bytes of bf16)
-constexpr int MLA_NT = 128;   // threads of the latent kernel (four warps = four TMEM lane quarters)
+constexpr int MLA_NT = 160;   // four softmax warps (the four TMEM lane quarters) + an issuer warp
 
-// shared memory of the latent kernel (1024-byte aligned base):
-//   Q: [KB][64 heads][128 B] K-major, 72 KB; C: [KB][128 positions][128 B], 144 KB, whose last
-//   (positional) block becomes P = softmax weights [128 positions][64 heads] bf16 once the
-//   score product has read it
+// shared memory of the latent kernel (1024-byte aligned base): Q [KB][64 heads][128 B]
+// (72 KB, K-major) and two cache tiles [KB][64 positions][128 B] (72 KB each, TMA, 128-byte
+// swizzle).  A tile's last (positional) block becomes P = its softmax weights, [64 heads]
+// [64 positions] bf16, once the score product has read it.
+constexpr uint32_t BLK = TP * 128;                 // one key block of a tile
+constexpr uint32_t TILE = KB * BLK;
 constexpr uint32_t M_OFF_Q = 0;
 constexpr uint32_t M_OFF_C = KB * MH * 128;
-constexpr uint32_t M_OFF_P = M_OFF_C + (KB - 1) * TP * 128;
-constexpr uint32_t M_SMEM = M_OFF_C + KB * TP * 128 + 1024;
-constexpr uint32_t M_TM_S = 0;    // S^T: 128 lanes (positions) x 64 columns (heads)
+constexpr uint32_t M_SMEM = M_OFF_C + 2 * TILE + 1024;
+constexpr uint32_t M_TM_S = 0;    // S: 2 buffers of 64 columns; M = 64 heads in lanes 32 w + 0..15
 constexpr uint32_t M_TM_Z = 256;  // Z^T: 4 slices of 128 lanes (latent) x 64 columns (heads)
-enum { MB_Q = 0, MB_C, MB_S, MB_Z, MB_N };
+enum { MB_Q = 0, MB_C0, MB_C1, MB_S0, MB_S1, MB_P, MB_Z, MB_N };
 
 struct MlaMaps {
   CUtensorMap q, c;
 };
 
-// offset of (position r, 16-byte chunk j) in an MN-major / TMA 128-byte-swizzled block
+// offset of (row r, 16-byte chunk j) in a 128-byte-swizzled block
 __device__ __forceinline__ uint32_t sw128_row(int r, int j) {
   return (uint32_t)r * 128u + ((uint32_t)(j ^ (r & 7)) << 4);
 }
 
+// Warps 0-3: softmax and rescale (warp w reads TMEM lanes 32 w .. 32 w + 31; in S, whose
+// M = 64 rows sit in lanes 32 w + 0..15, lane l < 16 of warp w owns head 16 w + l and its
+// running maximum m and normaliser l).  Warp 4: TMA loads and tensor-core issue.  The two
+// sides meet only on mbarriers: C tile landed, S ready, P ready, Z done.
 __global__ void __launch_bounds__(MLA_NT, 1)
     mla_latent_kernel(const MlaArgs a, const __grid_constant__ MlaMaps maps) {
   extern __shared__ uint8_t mraw[];
@@ -70,8 +75,10 @@ __global__ void __launch_bounds__(MLA_NT, 1)
   uint8_t *sm = mraw + pad;
   const uint32_t sb = raw + pad;
   __shared__ __align__(8) uint64_t s_bar[MB_N];
-  __shared__ uint32_t s_tmem, s_abort, s_loads, s_mmas;
-  __shared__ float s_red[4][MH], s_m[MH], s_l[MH], s_mnew[MH], s_alpha[MH];
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile uint32_t s_abort;
+  __shared__ uint32_t s_loads[2], s_mmas;
+  __shared__ float s_alpha[MH], s_l[MH];
   __shared__ int s_rescale;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -88,218 +95,196 @@ __global__ void __launch_bounds__(MLA_NT, 1)
     mbar_fence_init();
     s_abort = 0;
     s_rescale = 0;
-    s_loads = 0;  // C tiles requested (the drain's parity)
-    s_mmas = 0;   // tiles whose products were issued
+    s_loads[0] = s_loads[1] = 0;  // tiles requested into each buffer (the drain's parity)
+    s_mmas = 0;                   // value products issued
   }
-  if (tid < MH) s_m[tid] = -INFINITY, s_l[tid] = 0.f;
   if (warp == 0) tmem_alloc(smem_u32(&s_tmem), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = s_tmem;
-  const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-  auto load_tile = [&](int t) {  // the 9 key blocks of positions 128 t .. 128 t + 127
-    ++s_loads;
-    mbar_expect_tx(bar(MB_C), KB * TP * 128);
-    for (int kb = 0; kb < KB; ++kb)
-      tma_load_3d(sb + M_OFF_C + kb * TP * 128, &maps.c, 64 * kb, TP * t, b, bar(MB_C));
-  };
   auto wait = [&](int i, uint32_t parity) {
     if (!mbar_wait(bar(i), parity)) s_abort = 1;
+    return s_abort == 0;
   };
-  if (tid == 0 && ntiles > 0) {
-    mbar_expect_tx(bar(MB_Q), KB * MH * 128);
-    for (int kb = 0; kb < KB; ++kb)
-      tma_load_3d(sb + M_OFF_Q + kb * MH * 128, &maps.q, 64 * kb, 0, b, bar(MB_Q));
-    load_tile(0);
-  }
-  // S: bf16 x bf16, M = 128 positions, N = 64 heads, both K-major
-  constexpr uint32_t ID_S = idesc(1, 128, 64, 0, 0);
-  // Z: M = 128 latent channels (A = C^T, MN-major), N = 64 heads (B = P^T, MN-major)
-  constexpr uint32_t ID_Z = idesc(1, 128, 64, 1, 1);
 
-  for (int t = 0; t < ntiles; ++t) {
-    const uint32_t par = (uint32_t)(t & 1);
-    if (tid == 0) {
-      if (t == 0) wait(MB_Q, 0);
-      wait(MB_C, par);
-      tc_fence_after();
+  if (warp == 4) {
+    // ---- issuer: loads two tiles ahead, S of the next tile while this one is soft-maxed ----
+    if (lane == 0 && ntiles > 0) {
+      auto load_tile = [&](int t) {
+        const int j = t & 1;
+        ++s_loads[j];
+        mbar_expect_tx(bar(MB_C0 + j), TILE);
+        for (int kb = 0; kb < KB; ++kb)
+          tma_load_3d(sb + M_OFF_C + j * TILE + kb * BLK, &maps.c, 64 * kb, TP * t, b,
+                      bar(MB_C0 + j));
+      };
+      // S = Q C^T: M = 64 heads (A = Q), N = 64 positions (B = C), both K-major
+      constexpr uint32_t ID_S = idesc(1, 64, 64, 0, 0);
+      // Z^T = C^T P^T: M = 128 latent (A = C^T, MN-major), N = 64 heads (B = P, K-major)
+      constexpr uint32_t ID_Z = idesc(1, 128, 64, 1, 0);
+      auto issue_s = [&](int t) {
+        const int j = t & 1;
+        if (!wait(MB_C0 + j, (uint32_t)((t >> 1) & 1))) return false;
+        tc_fence_after();
+        for (int kb = 0; kb < KB; ++kb)
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t ad = sdesc_sw128(sb + M_OFF_Q + kb * MH * 128 + ks * 32, 16, 1024);
+            const uint64_t bd =
+                sdesc_sw128(sb + M_OFF_C + j * TILE + kb * BLK + ks * 32, 16, 1024);
+            mma_bf16_ss(tm + M_TM_S + 64 * j, ad, bd, ID_S, (kb | ks) != 0);
+          }
+        mma_commit(bar(MB_S0 + j));
+        return true;
+      };
+      mbar_expect_tx(bar(MB_Q), KB * MH * 128);
       for (int kb = 0; kb < KB; ++kb)
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t ad = sdesc_sw128(sb + M_OFF_C + kb * TP * 128 + ks * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sb + M_OFF_Q + kb * MH * 128 + ks * 32, 16, 1024);
-          mma_bf16_ss(tm + M_TM_S, ad, bd, ID_S, (kb | ks) != 0);
-        }
-      mma_commit(bar(MB_S));
-      ++s_mmas;
-    }
-    wait(MB_S, par);
-    tc_fence_after();
-
-    // ---- softmax over this tile's positions (thread = position 32 warp + lane) -----------
-    const int r = 32 * warp + lane;
-    const bool valid = TP * t + r < len;
-    float x[MH];
-    {
-      float v[32];
-      tmem_ld32(tm + lane_off + M_TM_S, v);
-      tmem_wait_ld();
-#pragma unroll
-      for (int h = 0; h < 32; ++h) x[h] = valid ? v[h] * a.scale_log2 : -INFINITY;
-      tmem_ld32(tm + lane_off + M_TM_S + 32, v);
-      tmem_wait_ld();
-#pragma unroll
-      for (int h = 0; h < 32; ++h) x[32 + h] = valid ? v[h] * a.scale_log2 : -INFINITY;
-    }
-    if (!valid) {  // a position past the sequence: its latent row must not reach Z (x 0)
-#pragma unroll 1
-      for (int kb = 0; kb < KB - 1; ++kb)
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint4 *>(sm + M_OFF_C + kb * TP * 128 + sw128_row(r, j)) =
-              make_uint4(0, 0, 0, 0);
-    }
-    // per-head maximum over the 128 positions: warp (transpose-reduce), then the four warps
-    {
-      float mx[32];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int h = 0; h < 32; ++h) mx[h] = x[32 * half + h];
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-          const bool up = (lane & off) != 0;
-#pragma unroll
-          for (int h = 0; h < off; ++h) {
-            const float send = up ? mx[h] : mx[h + off];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-            mx[h] = fmaxf(up ? mx[h + off] : mx[h], recv);
+        tma_load_3d(sb + M_OFF_Q + kb * MH * 128, &maps.q, 64 * kb, 0, b, bar(MB_Q));
+      load_tile(0);
+      if (ntiles > 1) load_tile(1);
+      bool go = wait(MB_Q, 0) && issue_s(0);
+      for (int t = 0; t < ntiles && go; ++t) {
+        const int j = t & 1;
+        if (t + 1 < ntiles && !issue_s(t + 1)) break;  // its S buffer was read by softmax(t - 1)
+        if (!wait(MB_P, (uint32_t)(t & 1))) break;      // P(t) written, Z rescaled
+        tc_fence_after();
+        const uint32_t tile = sb + M_OFF_C + j * TILE;
+        for (int sl = 0; sl < 4; ++sl)
+          for (int ks = 0; ks < TP / 16; ++ks) {
+            // A = C^T: latent 128 sl .. 128 sl + 127 = key blocks 2 sl, 2 sl + 1 (BLK apart),
+            // positions 16 ks .. 16 ks + 15 (two 8-row groups of 1 KB); B = P rows = heads
+            const uint64_t ad = sdesc_sw128(tile + 2 * sl * BLK + ks * 2048, BLK, 1024);
+            const uint64_t bd = sdesc_sw128(tile + (KB - 1) * BLK + ks * 32, 16, 1024);
+            mma_bf16_ss(tm + M_TM_Z + 64 * sl, ad, bd, ID_Z, (t > 0 || ks > 0) ? 1u : 0u);
           }
+        mma_commit(bar(MB_Z));
+        ++s_mmas;
+        if (t + 2 < ntiles) {  // buffer j is free once Z(t) has read it
+          if (!wait(MB_Z, (uint32_t)(t & 1))) break;
+          load_tile(t + 2);
         }
-        s_red[warp][32 * half + lane] = mx[0];
       }
     }
-    __syncthreads();
-    if (tid < MH) {
-      const float mt = fmaxf(fmaxf(s_red[0][tid], s_red[1][tid]), fmaxf(s_red[2][tid], s_red[3][tid]));
-      const float mo = s_m[tid], mn = fmaxf(mo, mt);
-      const float al = mn == -INFINITY ? 1.f : exp2f(mo - mn);  // exp2(-inf) = 0 on a first max
-      s_mnew[tid] = mn;
-      s_alpha[tid] = al;
-      if (t > 0 && al != 1.f) s_rescale = 1;
-    }
-    __syncthreads();
-    // weights p = 2^(x - m), written as P^T (MN-major: row = position, 64 heads = 128 B)
-    float p[MH];
-#pragma unroll
-    for (int h = 0; h < MH; ++h) p[h] = x[h] == -INFINITY ? 0.f : exp2f(x[h] - s_mnew[h]);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint4 w;
-      w.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 0])) |
-            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 1])) << 16);
-      w.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 2])) |
-            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 3])) << 16);
-      w.z = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 4])) |
-            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 5])) << 16);
-      w.w = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 6])) |
-            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p[8 * j + 7])) << 16);
-      *reinterpret_cast<uint4 *>(sm + M_OFF_P + sw128_row(r, j)) = w;
-    }
-    // the row sums use the bf16 weights the product multiplies by
-    {
-      float sm32[32];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int h = 0; h < 32; ++h)
-          sm32[h] = __bfloat162float(__float2bfloat16_rn(p[32 * half + h]));
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-          const bool up = (lane & off) != 0;
-#pragma unroll
-          for (int h = 0; h < off; ++h) {
-            const float send = up ? sm32[h] : sm32[h + off];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-            sm32[h] = (up ? sm32[h + off] : sm32[h]) + recv;
-          }
-        }
-        s_red[warp][32 * half + lane] = sm32[0];
-      }
-    }
-    // Z^T columns (heads) whose maximum moved are rescaled before this tile is added
-    if (s_rescale) {
-#pragma unroll 1
-      for (int sl = 0; sl < 4; ++sl)
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          float v[32];
-          const uint32_t col = M_TM_Z + 64 * sl + 32 * hh;
-          tmem_ld32(tm + lane_off + col, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int h = 0; h < 32; ++h) v[h] *= s_alpha[32 * hh + h];
-          tmem_st32(tm + lane_off + col, v);
-        }
-      tmem_wait_st();
-    }
-    fence_proxy_async();  // P and the zeroed rows, written by these threads, feed the product
-    tc_fence_before();
-    __syncthreads();
-    if (tid < MH) {
-      s_l[tid] = s_l[tid] * s_alpha[tid] + s_red[0][tid] + s_red[1][tid] + s_red[2][tid] +
-                 s_red[3][tid];
-      s_m[tid] = s_mnew[tid];
-    }
-    if (tid == 0) {
-      s_rescale = 0;
+  } else {
+    // ---- softmax warps -------------------------------------------------------------------
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const bool owner = lane < 16;          // lane l < 16 of warp w owns head 16 w + l
+    const int hd = 16 * warp + (lane & 15);
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int t = 0; t < ntiles; ++t) {
+      const int j = t & 1;
+      if (!wait(MB_S0 + j, (uint32_t)((t >> 1) & 1))) break;
+      if (t > 0 && !wait(MB_Z, (uint32_t)((t - 1) & 1))) break;  // Z(t-1) done: rescale, P
       tc_fence_after();
-      for (int sl = 0; sl < 4; ++sl)
-        for (int ks = 0; ks < TP / 16; ++ks) {
-          // A = C^T: latent channels 128 sl .. 128 sl + 127 (key blocks 2 sl, 2 sl + 1, 16 KB
-          // apart), positions 16 ks .. 16 ks + 15 (two 8-row groups of 1 KB)
-          const uint64_t ad = sdesc_sw128(sb + M_OFF_C + 2 * sl * TP * 128 + ks * 2048,
-                                          TP * 128, 1024);
-          const uint64_t bd = sdesc_sw128(sb + M_OFF_P + ks * 2048, 1024, 1024);  // one atom
-          mma_bf16_ss(tm + M_TM_Z + 64 * sl, ad, bd, ID_Z, (t > 0 || ks > 0) ? 1u : 0u);
-        }
-      mma_commit(bar(MB_Z));
-      wait(MB_Z, par);  // the tile's C and P are read: the next tile may land on them
-      if (t + 1 < ntiles) load_tile(t + 1);
-    }
-    wait(MB_Z, par);
-    tc_fence_after();
-    __syncthreads();
-    if (s_abort) break;
-  }
-
-  // ---- z = Z / l per head (thread = latent channel of its lane quarter, per slice) ----------
-  float *z = a.z + (size_t)b * MH * ML;
-#pragma unroll 1
-  for (int sl = 0; sl < 4; ++sl)
-#pragma unroll 1
-    for (int hh = 0; hh < 2; ++hh) {
-      float v[32];
-      if (ntiles > 0 && !s_abort) {
-        tmem_ld32(tm + lane_off + M_TM_Z + 64 * sl + 32 * hh, v);
+      uint8_t *tile = sm + M_OFF_C + j * TILE;
+      float x[64];
+      {
+        float v[32];
+        tmem_ld32(tm + lane_off + M_TM_S + 64 * j, v);
         tmem_wait_ld();
-      }
 #pragma unroll
-      for (int h = 0; h < 32; ++h) {
-        const int head = 32 * hh + h;
-        const float l = s_l[head];
-        z[(size_t)head * ML + 128 * sl + 32 * warp + lane] =
-            (ntiles > 0 && !s_abort && l > 0.f) ? v[h] / l : 0.f;
+        for (int c = 0; c < 32; ++c) x[c] = TP * t + c < len ? v[c] * a.scale_log2 : -INFINITY;
+        tmem_ld32(tm + lane_off + M_TM_S + 64 * j + 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          x[32 + c] = TP * t + 32 + c < len ? v[c] * a.scale_log2 : -INFINITY;
       }
+      if (owner) {
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) mt = fmaxf(mt, x[c]);
+        const float mn = fmaxf(m_run, mt);
+        const float al = mn == -INFINITY ? 1.f : exp2f(m_run - mn);  // 2^(-inf) = 0: first max
+        float ls = 0.f;
+        uint8_t *prow = tile + (KB - 1) * BLK;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {  // the head's 64 weights: one 128-byte row of P
+          uint32_t w[4];
+#pragma unroll
+          for (int y = 0; y < 4; ++y) {
+            const float p0 = x[8 * q + 2 * y] == -INFINITY ? 0.f : exp2f(x[8 * q + 2 * y] - mn);
+            const float p1 =
+                x[8 * q + 2 * y + 1] == -INFINITY ? 0.f : exp2f(x[8 * q + 2 * y + 1] - mn);
+            const __nv_bfloat16 b0 = __float2bfloat16_rn(p0), b1 = __float2bfloat16_rn(p1);
+            ls += __bfloat162float(b0) + __bfloat162float(b1);  // the weights the product uses
+            w[y] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
+          }
+          *reinterpret_cast<uint4 *>(prow + sw128_row(hd, q)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        l_run = l_run * al + ls;
+        m_run = mn;
+        s_alpha[hd] = al;
+        if (t > 0 && al != 1.f) s_rescale = 1;
+      }
+      // a position past the sequence: its latent row must not reach Z (its memory may hold
+      // anything, and 0 x NaN is NaN)
+      if (tid < TP && TP * t + tid >= len) {
+#pragma unroll 1
+        for (int kb = 0; kb < KB - 1; ++kb)
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4 *>(tile + kb * BLK + sw128_row(tid, q)) =
+                make_uint4(0, 0, 0, 0);
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (s_rescale) {  // Z^T columns of the heads whose maximum moved
+#pragma unroll 1
+        for (int sl = 0; sl < 4; ++sl)
+#pragma unroll 1
+          for (int hh = 0; hh < 2; ++hh) {
+            float v[32];
+            const uint32_t col = M_TM_Z + 64 * sl + 32 * hh;
+            tmem_ld32(tm + lane_off + col, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] *= s_alpha[32 * hh + c];
+            tmem_st32(tm + lane_off + col, v);
+          }
+        tmem_wait_st();
+      }
+      fence_proxy_async();  // P and the zeroed rows feed the tensor core
+      tc_fence_before();
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (tid == 0) {
+        s_rescale = 0;
+        mbar_arrive(bar(MB_P));
+      }
+      if (s_abort) break;
     }
-  if (tid == 0 && s_abort) {
+    if (owner) s_l[hd] = l_run;
+  }
+  __syncthreads();
+
+  // ---- z = Z / l per head (softmax warps: thread = latent channel of its lane quarter) -----
+  if (warp < 4) {
+    const bool done = ntiles > 0 && !s_abort && wait(MB_Z, (uint32_t)((ntiles - 1) & 1));
+    tc_fence_after();
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    float *z = a.z + (size_t)b * MH * ML;
+#pragma unroll 1
+    for (int sl = 0; sl < 4; ++sl)
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        float v[32];
+        if (done) {
+          tmem_ld32(tm + lane_off + M_TM_Z + 64 * sl + 32 * hh, v);
+          tmem_wait_ld();
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int head = 32 * hh + c;
+          const float l = s_l[head];
+          z[(size_t)head * ML + 128 * sl + 32 * warp + lane] = (done && l > 0.f) ? v[c] / l : 0.f;
+        }
+      }
+  }
+  if (tid == 128 && s_abort) {
     // a bounded wait ran out: let the copies and products in flight land (bounded) before
     // the CTA releases its memory, then report it
-    if (s_loads) mbar_wait(bar(MB_C), (s_loads - 1) & 1);
-    if (s_mmas) {
-      mbar_wait(bar(MB_S), (s_mmas - 1) & 1);
-      mbar_wait(bar(MB_Z), (s_mmas - 1) & 1);
-    }
+    for (int j = 0; j < 2; ++j)
+      if (s_loads[j]) mbar_wait(bar(MB_C0 + j), (s_loads[j] - 1) & 1);
+    if (s_mmas) mbar_wait(bar(MB_Z), (s_mmas - 1) & 1);
     if (a.err) atomicOr(a.err, ERR_MBAR_TIMEOUT);
   }
   tc_fence_before();
