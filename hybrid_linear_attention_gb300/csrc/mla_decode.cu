@@ -58,6 +58,12 @@ struct MlaMaps {
   CUtensorMap q, c;
 };
 
+// 2^x on the special-function unit (relative error ~2^-22; the weights are bf16 operands)
+__device__ __forceinline__ float ex2f_sfu(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 // offset of (row r, 16-byte chunk j) in a 128-byte-swizzled block
 __device__ __forceinline__ uint32_t sw128_row(int r, int j) {
   return (uint32_t)r * 128u + ((uint32_t)(j ^ (r & 7)) << 4);
@@ -194,8 +200,11 @@ __global__ void __launch_bounds__(MLA_NT, 1)
         float mt = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 64; ++c) mt = fmaxf(mt, x[c]);
+        // the running maximum: the largest weight is exactly 1 (no bf16 rounding on the
+        // dominant term; a reference allowed to lag by up to 2^8 measured 1.04e-2 of RMS on
+        // peaked rows, over the bound)
         const float mn = fmaxf(m_run, mt);
-        const float al = mn == -INFINITY ? 1.f : exp2f(m_run - mn);  // 2^(-inf) = 0: first max
+        const float al = mn == -INFINITY ? 1.f : ex2f_sfu(m_run - mn);  // 2^(-inf) = 0
         float ls = 0.f;
         uint8_t *prow = tile + (KB - 1) * BLK;
 #pragma unroll
@@ -203,9 +212,9 @@ __global__ void __launch_bounds__(MLA_NT, 1)
           uint32_t w[4];
 #pragma unroll
           for (int y = 0; y < 4; ++y) {
-            const float p0 = x[8 * q + 2 * y] == -INFINITY ? 0.f : exp2f(x[8 * q + 2 * y] - mn);
+            const float p0 = x[8 * q + 2 * y] == -INFINITY ? 0.f : ex2f_sfu(x[8 * q + 2 * y] - mn);
             const float p1 =
-                x[8 * q + 2 * y + 1] == -INFINITY ? 0.f : exp2f(x[8 * q + 2 * y + 1] - mn);
+                x[8 * q + 2 * y + 1] == -INFINITY ? 0.f : ex2f_sfu(x[8 * q + 2 * y + 1] - mn);
             const __nv_bfloat16 b0 = __float2bfloat16_rn(p0), b1 = __float2bfloat16_rn(p1);
             ls += __bfloat162float(b0) + __bfloat162float(b1);  // the weights the product uses
             w[y] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
