@@ -301,8 +301,8 @@ __global__ void __launch_bounds__(MLA_NT, 1)
   if (warp == 0) tmem_dealloc(tm, 512);
 }
 
-// q_cat[b][h] = [W_K,h^T q_nope[b][h] ; q_rope[b][h]] (bf16), 8 sequences per CTA
-constexpr int MQB = 8;
+// q_cat[b][h] = [W_K,h^T q_nope[b][h] ; q_rope[b][h]] (bf16), MQB sequences per CTA
+constexpr int MQB = 16;  // sequences per CTA: each head's weights are read once per 16
 __global__ void __launch_bounds__(128) mla_absorb_kernel(const MlaArgs a) {
   const int h = blockIdx.x, b0 = blockIdx.y * MQB, tid = threadIdx.x;
   __shared__ float s_q[MQB][MN];
@@ -332,7 +332,9 @@ __global__ void __launch_bounds__(128) mla_absorb_kernel(const MlaArgs a) {
     }
   }
   bf16 *qc = reinterpret_cast<bf16 *>(a.q_cat);
-  for (int bb = 0; bb < MQB && b0 + bb < a.B; ++bb) {
+#pragma unroll
+  for (int bb = 0; bb < MQB; ++bb) {  // unrolled: the accumulators stay in registers
+    if (b0 + bb >= a.B) break;
     bf16 *row = qc + ((size_t)(b0 + bb) * MH + h) * MK;
 #pragma unroll
     for (int y = 0; y < 4; ++y) row[4 * tid + y] = __float2bfloat16_rn(acc[bb][y]);
@@ -341,7 +343,7 @@ __global__ void __launch_bounds__(128) mla_absorb_kernel(const MlaArgs a) {
   }
 }
 
-// out[b][h] = W_V,h z[b][h] * sigmoid(gate[b][h]) (bf16), 8 sequences per CTA
+// out[b][h] = W_V,h z[b][h] * sigmoid(gate[b][h]) (bf16), MQB sequences per CTA
 __global__ void __launch_bounds__(128) mla_up_gate_kernel(const MlaArgs a) {
   const int h = blockIdx.x, b0 = blockIdx.y * MQB, v = threadIdx.x;
   __shared__ float s_z[MQB][ML];
@@ -366,7 +368,9 @@ __global__ void __launch_bounds__(128) mla_up_gate_kernel(const MlaArgs a) {
         acc[bb] = fmaf(wb, s_z[bb][l + 2 * y + 1], fmaf(wa, s_z[bb][l + 2 * y], acc[bb]));
     }
   }
-  for (int bb = 0; bb < MQB && b0 + bb < a.B; ++bb) {
+#pragma unroll
+  for (int bb = 0; bb < MQB; ++bb) {  // unrolled: the accumulators stay in registers
+    if (b0 + bb >= a.B) break;
     const size_t hb = (size_t)(b0 + bb) * MH + h;
     const float g = __bfloat162float(reinterpret_cast<const bf16 *>(a.gate)[hb]);
     reinterpret_cast<bf16 *>(a.out)[hb * MV + v] = __float2bfloat16_rn(acc[bb] * sigmoidf_(g));
