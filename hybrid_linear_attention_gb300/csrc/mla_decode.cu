@@ -84,8 +84,9 @@ __global__ void __launch_bounds__(MLA_NT, 1)
   __shared__ uint32_t s_tmem;
   __shared__ volatile uint32_t s_abort;
   __shared__ uint32_t s_loads[2], s_mmas;
+  __shared__ int s_stop;  // the softmax warps' exit decision, taken by one thread per tile
   __shared__ float s_alpha[MH], s_l[MH];
-  __shared__ int s_rescale;
+  __shared__ int s_rescale[2];  // by tile parity: set by the head owners, reset after use
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x;
@@ -100,7 +101,8 @@ __global__ void __launch_bounds__(MLA_NT, 1)
     for (int i = 0; i < MB_N; ++i) mbar_init(bar(i), 1);
     mbar_fence_init();
     s_abort = 0;
-    s_rescale = 0;
+    s_rescale[0] = s_rescale[1] = 0;
+    s_stop = 0;
     s_loads[0] = s_loads[1] = 0;  // tiles requested into each buffer (the drain's parity)
     s_mmas = 0;                   // value products issued
   }
@@ -179,8 +181,9 @@ __global__ void __launch_bounds__(MLA_NT, 1)
     float m_run = -INFINITY, l_run = 0.f;
     for (int t = 0; t < ntiles; ++t) {
       const int j = t & 1;
-      if (!wait(MB_S0 + j, (uint32_t)((t >> 1) & 1))) break;
-      if (t > 0 && !wait(MB_Z, (uint32_t)((t - 1) & 1))) break;  // Z(t-1) done: rescale, P
+      // a wait that runs out only raises s_abort: the four warps leave together, after a
+      // named barrier, on one thread's reading of it (never between named barriers)
+      wait(MB_S0 + j, (uint32_t)((t >> 1) & 1));
       tc_fence_after();
       uint8_t *tile = sm + M_OFF_C + j * TILE;
       float x[64];
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(MLA_NT, 1)
         l_run = l_run * al + ls;
         m_run = mn;
         s_alpha[hd] = al;
-        if (t > 0 && al != 1.f) s_rescale = 1;
+        if (t > 0 && al != 1.f) s_rescale[j] = 1;
       }
       // a position past the sequence: its latent row must not reach Z (its memory may hold
       // anything, and 0 x NaN is NaN)
@@ -236,8 +239,11 @@ __global__ void __launch_bounds__(MLA_NT, 1)
             *reinterpret_cast<uint4 *>(tile + kb * BLK + sw128_row(tid, q)) =
                 make_uint4(0, 0, 0, 0);
       }
+      // all of the above overlaps the previous tile's value product; the rescale needs it done
+      if (t > 0) wait(MB_Z, (uint32_t)((t - 1) & 1));
+      tc_fence_after();
       asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (s_rescale) {  // Z^T columns of the heads whose maximum moved
+      if (s_rescale[j]) {  // Z^T columns of the heads whose maximum moved
 #pragma unroll 1
         for (int sl = 0; sl < 4; ++sl)
 #pragma unroll 1
@@ -254,12 +260,13 @@ __global__ void __launch_bounds__(MLA_NT, 1)
       }
       fence_proxy_async();  // P and the zeroed rows feed the tensor core
       tc_fence_before();
+      if (tid == 0) s_stop = s_abort;
       asm volatile("bar.sync 1, 128;" ::: "memory");
       if (tid == 0) {
-        s_rescale = 0;
+        s_rescale[j] = 0;
         mbar_arrive(bar(MB_P));
       }
-      if (s_abort) break;
+      if (s_stop) break;
     }
     if (owner) s_l[hd] = l_run;
   }
