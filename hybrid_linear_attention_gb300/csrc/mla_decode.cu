@@ -131,9 +131,9 @@ __global__ void __launch_bounds__(MLA_NT, 1)
       constexpr uint32_t ID_S = idesc(1, 64, 64, 0, 0);
       // Z^T = C^T P^T: M = 128 latent (A = C^T, MN-major), N = 64 heads (B = P, K-major)
       constexpr uint32_t ID_Z = idesc(1, 128, 64, 1, 0);
-      auto issue_s = [&](int t) {
+      auto issue_s = [&](int t, bool landed) {
         const int j = t & 1;
-        if (!wait(MB_C0 + j, (uint32_t)((t >> 1) & 1))) return false;
+        if (!landed && !wait(MB_C0 + j, (uint32_t)((t >> 1) & 1))) return false;
         tc_fence_after();
         for (int kb = 0; kb < KB; ++kb)
           for (int ks = 0; ks < 4; ++ks) {
@@ -150,12 +150,19 @@ __global__ void __launch_bounds__(MLA_NT, 1)
         tma_load_3d(sb + M_OFF_Q + kb * MH * 128, &maps.q, 64 * kb, 0, b, bar(MB_Q));
       load_tile(0);
       if (ntiles > 1) load_tile(1);
-      bool go = wait(MB_Q, 0) && issue_s(0);
+      bool go = wait(MB_Q, 0) && issue_s(0, false);
       for (int t = 0; t < ntiles && go; ++t) {
         const int j = t & 1;
-        if (t + 1 < ntiles && !issue_s(t + 1)) break;  // its S buffer was read by softmax(t - 1)
-        if (!wait(MB_P, (uint32_t)(t & 1))) break;      // P(t) written, Z rescaled
+        if (!wait(MB_P, (uint32_t)(t & 1))) break;  // P(t) written, Z rescaled
         tc_fence_after();
+        // S(t+1) goes ahead of Z(t) when its tile has landed (one probe, no wait), so the
+        // softmax warps start the next tile while Z(t) runs; its S buffer was read by
+        // softmax(t - 1), which P(t - 1) closed
+        bool next_s = false;
+        if (t + 1 < ntiles && mbar_try_wait(bar(MB_C0 + (j ^ 1)), (uint32_t)(((t + 1) >> 1) & 1))) {
+          issue_s(t + 1, true);
+          next_s = true;
+        }
         const uint32_t tile = sb + M_OFF_C + j * TILE;
         for (int sl = 0; sl < 4; ++sl)
           for (int ks = 0; ks < TP / 16; ++ks) {
@@ -167,6 +174,7 @@ __global__ void __launch_bounds__(MLA_NT, 1)
           }
         mma_commit(bar(MB_Z));
         ++s_mmas;
+        if (t + 1 < ntiles && !next_s && !issue_s(t + 1, false)) break;
         if (t + 2 < ntiles) {  // buffer j is free once Z(t) has read it
           if (!wait(MB_Z, (uint32_t)(t & 1))) break;
           load_tile(t + 2);
