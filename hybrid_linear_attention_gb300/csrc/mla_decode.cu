@@ -253,17 +253,17 @@ __global__ void __launch_bounds__(MLA_NT, 1)
       asm volatile("bar.sync 1, 128;" ::: "memory");
       if (s_rescale[j]) {  // Z^T columns of the heads whose maximum moved
 #pragma unroll 1
-        for (int sl = 0; sl < 4; ++sl)
-#pragma unroll 1
-          for (int hh = 0; hh < 2; ++hh) {
-            float v[32];
-            const uint32_t col = M_TM_Z + 64 * sl + 32 * hh;
-            tmem_ld32(tm + lane_off + col, v);
-            tmem_wait_ld();
+        for (int sl = 0; sl < 4; ++sl) {  // a slice's 64 columns per round trip
+          float v[32], w2[32];
+          const uint32_t col = M_TM_Z + 64 * sl;
+          tmem_ld32(tm + lane_off + col, v);
+          tmem_ld32(tm + lane_off + col + 32, w2);
+          tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] *= s_alpha[32 * hh + c];
-            tmem_st32(tm + lane_off + col, v);
-          }
+          for (int c = 0; c < 32; ++c) v[c] *= s_alpha[c], w2[c] *= s_alpha[32 + c];
+          tmem_st32(tm + lane_off + col, v);
+          tmem_st32(tm + lane_off + col + 32, w2);
+        }
         tmem_wait_st();
       }
       fence_proxy_async();  // P and the zeroed rows feed the tensor core
