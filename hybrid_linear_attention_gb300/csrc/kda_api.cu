@@ -512,6 +512,11 @@ kda_status kda_check_device_error(cudaStream_t stream) {
   return KDA_OK;
 }
 
+kda_status kda_wait_probe(int64_t probes, cudaStream_t stream) {
+  if (probes < 1 || probes > ((int64_t)1 << 30)) return KDA_ERR_INVALID_ARG;
+  return finish(kda::launch_wait_probe((long)probes, device_error_ptr(), stream), 1);
+}
+
 uint64_t kda_launch_count(void) { return g_launches.load(); }
 
 }  // extern "C"

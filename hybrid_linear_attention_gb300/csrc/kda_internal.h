@@ -91,6 +91,7 @@ cudaError_t launch_state_accept(const void *step_states, void *pool, const int32
                                 int D, bool st_bf16, int *err, cudaStream_t s);
 cudaError_t launch_prologue(const ProArgs &a, int D, bool io_bf16, cudaStream_t s);
 // out[k] <- the three raw inputs before checkpoint k (conv tail at that position)
+cudaError_t launch_wait_probe(long limit, int *err, cudaStream_t s);
 bool mla_latent_supported();
 cudaError_t launch_mla_absorb(const MlaArgs &a, cudaStream_t s);
 cudaError_t launch_mla_latent(const MlaArgs &a, cudaStream_t s);

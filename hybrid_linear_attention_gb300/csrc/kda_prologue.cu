@@ -380,6 +380,34 @@ cudaError_t launch_conv_ckpt(const void *x, const void *conv_state, const int32_
   return cudaGetLastError();
 }
 
+// The bounded-wait path the tensor-core kernels take when an mbarrier phase never completes:
+// one thread waits on a barrier nothing arrives at, gives up after `limit` probes and raises
+// the library's sticky flag, as those kernels do (the failure is made on purpose, without a
+// GPU fault: the wait ends and the kernel returns).
+__global__ void wait_probe_kernel(long limit, int *err) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar);
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b));
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  bool done = false;
+  for (long it = 0; it < limit && !done; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(b)
+        : "memory");
+    done = ok != 0;
+  }
+  if (!done && err) atomicOr(err, ERR_MBAR_TIMEOUT);
+}
+
+cudaError_t launch_wait_probe(long limit, int *err, cudaStream_t s) {
+  wait_probe_kernel<<<1, 1, 0, s>>>(limit, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_conv_update(const ConvArgs &a, bool io_bf16, cudaStream_t s) {
   if (a.n_seqs == 0) return cudaSuccess;
   const dim3 grid((a.channels + 255) / 256, a.n_seqs);

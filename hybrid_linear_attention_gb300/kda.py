@@ -29,7 +29,7 @@ EXPORTS = (
     "kda_conv_tail_checkpoints",
     "kda_decode_step", "kda_conv_state_update",
     "kda_decode_step_fused", "kda_decode_step_fused_fp8", "kda_decode_multi", "kda_state_accept", "kda_check_device_error",
-    "kda_launch_count", "mla_decode_latent", "mla_decode",
+    "kda_launch_count", "kda_wait_probe", "mla_decode_latent", "mla_decode",
 )
 
 
@@ -101,6 +101,7 @@ def load():
             "kda_state_accept": (_i32, [_P, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp]),
             "kda_check_device_error": (_i32, [_vp]),
             "kda_launch_count": (ctypes.c_uint64, []),
+            "kda_wait_probe": (_i32, [_i64, _vp]),
             "mla_decode_latent": (_i32, [_vp, _vp, _i64, _vp, _i32, ctypes.c_float, _vp, _vp]),
             "mla_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, ctypes.c_float,
                                   _vp, _vp, _vp, _vp]),
@@ -169,6 +170,10 @@ def kda_prefill_workspace_size(p, n_seqs, total_tokens):
 
 def kda_launch_count():
     return int(load().kda_launch_count())
+
+
+def kda_wait_probe(probes, stream=None):
+    _check(load().kda_wait_probe(int(probes), _stream(stream)), "kda_wait_probe")
 
 
 def kda_check_device_error(stream=None):

@@ -328,6 +328,14 @@ kda_status kda_state_accept(const kda_params* p, const void* step_states, int n_
  * KDA_ERR_BAD_INDEX, KDA_ERR_BAD_SEQLENS (in that order of precedence) or KDA_ERR_CUDA. */
 kda_status kda_check_device_error(cudaStream_t stream);
 
+/* Failure detection without a GPU fault: launches a one-thread kernel that waits, with the
+ * same bounded mbarrier wait the tensor-core kernels use, on a barrier nothing ever arrives
+ * at; after `probes` (1 .. 2^30) unsuccessful probes it gives up and raises the sticky flag,
+ * exactly as a kernel whose copy or product never completed would, and returns.  A following
+ * kda_check_device_error then reports KDA_ERR_TIMEOUT and the context stays usable.  No
+ * counterpart interface is printed on the pages. */
+kda_status kda_wait_probe(int64_t probes, cudaStream_t stream);
+
 /* Number of kernels the library launched since load (host-side counter, for benchmarks). */
 uint64_t kda_launch_count(void);
 

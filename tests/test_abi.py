@@ -199,3 +199,8 @@ def test_mla_calls_reject_bad_arguments_on_host(lib):
     assert lib.mla_decode_latent(None, None, 0, None, 0, 0.07, None, None) == kda.KDA_OK
     assert lib.mla_decode(buf, buf, buf, buf, buf, 64, buf, 2, None, 0.07, buf, buf, buf,
                           None) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_wait_probe_rejects_bad_limits_on_host(lib):
+    assert lib.kda_wait_probe(0, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_wait_probe(1 << 31, None) == kda.KDA_ERR_INVALID_ARG

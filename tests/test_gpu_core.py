@@ -291,3 +291,20 @@ def test_decode_matches_prefill_over_same_tokens():
     assert out_error(torch.cat(outs), ref["out"], torch.bfloat16) <= TOL_BF16
     assert max_err_rel_rms(state, ref["final_state"]) <= TOL_STATE
     assert max_err_rel_rms(fin_pf, ref["final_state"]) <= TOL_STATE
+
+
+def test_bounded_wait_that_runs_out_is_reported_and_the_context_survives():
+    """Failure detection without a GPU fault: a bounded mbarrier wait on a barrier nothing
+    arrives at gives up, raises the sticky flag (KDA_ERR_TIMEOUT) and returns; the flag is
+    cleared by the read and the next launches run normally."""
+    _gpu.lib()
+    kda.kda_wait_probe(20000)
+    torch.cuda.synchronize()
+    with pytest.raises(kda.KdaError) as ei:
+        kda.kda_check_device_error()
+    assert ei.value.status == kda.KDA_ERR_TIMEOUT
+    kda.kda_check_device_error()  # cleared
+    inp = inputs.kda_inputs([70], 2, 128, seed=90)
+    p = kda.params(H=2, d=128)
+    _check_prefill(inp, p)
+    kda.kda_check_device_error()
