@@ -81,6 +81,15 @@ def _prefill_bytes(T, H, d, with_state_out=True):
     return T * per_tok + (H * d * d * 4 if with_state_out else 0)
 
 
+def _prefill_flops(T, H, d, C=64):
+    """Algorithmic tensor FLOPs of the chunked form, each dense contraction counted once per
+    64-token chunk and head: A and P (two C x C x d_k), T = (I + A)^-1 (C^3 / 3), X = [K Gamma;
+    Q Gamma] S (2C x d_k x d_v), u = T Y (C x C x d_v), O += P' u (C x C x d_v), S += Kbar^T u
+    (d_k x C x d_v); 2 flops per multiply-add."""
+    per = 2 * (2 * C * C * d + C ** 3 / 3 + 2 * C * d * d + 2 * C * C * d + d * C * d)
+    return T / C * H * per
+
+
 def _prologue_bytes(T, H, d):
     """kda_prologue as the step runs it: read raw x (3Hd bf16) + beta logits; write q, k, v
     (bf16) and beta (fp32)."""
@@ -382,6 +391,7 @@ def run_ours(args):
     if rank != 0:
         return
     pf_bytes = _prefill_bytes(T_PREFILL, H, D)
+    pf_flops = _prefill_flops(T_PREFILL, H, D)
     achieved = pf_bytes / (pf * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
@@ -401,7 +411,15 @@ def run_ours(args):
                      "traffic": _profiled_traffic(
                          "kda_prefill_tc_T4096_H64.md",
                          ["kda_prefill_tc.cu", "kda_tc_ptx.cuh", "kda_common.cuh"]),
-                     "algorithmic_bytes_per_launch": pf_bytes},
+                     "algorithmic_bytes_per_launch": pf_bytes,
+                     # the same launch against the tensor-core peak (the chunked form's dense
+                     # contractions, counted once; intensity ~107 flop/B is under the ridge,
+                     # so HBM is the binding roofline)
+                     "tensor": {"achieved_tflops": pf_flops / (pf * 1e-3) / 1e12,
+                                "peak_tflops": tflops,
+                                "frac": pf_flops / (pf * 1e-3) / 1e12 / tflops,
+                                "peak_kind": f"{peak_kind} bf16_tflops (burst)",
+                                "algorithmic_flops_per_launch": pf_flops}},
         "gpu_launches": int(launches),
         "gpu_launches_per_step": launches / args.steps,
         "wall_s_timed_region": wall,
