@@ -557,6 +557,8 @@ def _mla_bench(dev, kda, inputs, hbm, rank):
     kda.kda_check_device_error()
     b = B * L * 576 * 2 + B * 64 * 576 * 2 + B * 64 * 512 * 4  # cache + query + z
     gbs = b / (res["latent"] * 1e-3) / 1e9
+    del cache
+    small = _mla_small_batch(dev, kda, inputs, hbm, rank)
     return {"metric": "MLA decode latent-cache GB/s", "value": gbs, "unit": "GB/s",
             "workload": "256 sequences x 4096 cached positions, 64 heads, 576-wide bf16 latent "
                         "cache (512 latent + 64 positional key; 1.21 GB, > L2), one query token "
@@ -565,7 +567,40 @@ def _mla_bench(dev, kda, inputs, hbm, rank):
             "tokens_per_s": B / (res["step"] * 1e-3),
             "roofline": {"kernel": "mla_decode_latent", "bound": "hbm", "achieved": gbs,
                          "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                         "algorithmic_bytes_per_launch": b}}
+                         "algorithmic_bytes_per_launch": b},
+            "small_batch": small}
+
+
+def _mla_small_batch(dev, kda, inputs, hbm, rank):
+    """4 sequences x 65536 cached positions (302 MB, > L2): one CTA per sequence leaves most
+    SMs idle; with the workspace each sequence's positions are split across CTAs and merged."""
+    B, L, reps = 4, 65536, 20
+    cache = inputs.normal((B, L, 576), seed=610 + rank, device=dev)
+    q_cat = inputs.normal((B, 64, 576), seed=611 + rank, device=dev)
+    lengths = torch.full((B,), L, dtype=torch.int32, device=dev)
+    z = torch.empty((B, 64, 512), dtype=torch.float32, device=dev)
+    ws_bytes = kda.mla_decode_workspace_size(B, L)
+    ws = torch.empty((ws_bytes + 3) // 4, dtype=torch.float32, device=dev)
+    res = {}
+    for name, w in (("split", ws), ("one_cta_per_sequence", None)):
+        fn = lambda: kda.mla_decode_latent(q_cat, cache, lengths, z, workspace=w)
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        e1.synchronize()
+        res[name] = e0.elapsed_time(e1) / reps
+    kda.kda_check_device_error()
+    b = B * L * 576 * 2 + B * 64 * 576 * 2 + B * 64 * 512 * 4
+    gbs = b / (res["split"] * 1e-3) / 1e9
+    return {"workload": "4 sequences x 65536 cached positions (302 MB latent cache)",
+            "workspace_bytes": ws_bytes, "ms_latent_split": res["split"],
+            "ms_latent_one_cta_per_sequence": res["one_cta_per_sequence"],
+            "gbs": gbs, "frac": gbs / hbm}
 
 
 def _decode_multi_bench(dev, kda, inputs, hbm, rank):

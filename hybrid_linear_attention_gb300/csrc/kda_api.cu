@@ -456,43 +456,63 @@ static kda_status mla_common(const void *cache, int64_t cache_len, const int32_t
   return KDA_OK;
 }
 
+size_t mla_decode_workspace_size(int n_seqs, int64_t cache_len) {
+  if (n_seqs < 1 || n_seqs > 65535 || cache_len < 1) return 0;
+  return kda::mla_split_bytes(kda::mla_preferred_split(n_seqs, cache_len), n_seqs);
+}
+
+// the preferred split of each sequence's positions, lowered to what the workspace holds
+static int mla_split_for(int n_seqs, int64_t cache_len, size_t ws_bytes) {
+  int ns = kda::mla_preferred_split(n_seqs, cache_len);
+  while (ns > 1 && kda::mla_split_bytes(ns, n_seqs) > ws_bytes) --ns;
+  return ns;
+}
+
 kda_status mla_decode_latent(const void *q_cat, const void *cache, int64_t cache_len,
                              const int32_t *lengths, int n_seqs, float scale, float *z,
-                             cudaStream_t stream) {
+                             void *workspace, size_t ws_bytes, cudaStream_t stream) {
   kda_status st = mla_common(cache, cache_len, lengths, n_seqs, scale, z);
   if (st != KDA_OK || n_seqs == 0) return st;
-  if (!q_cat || !aligned16(q_cat)) return KDA_ERR_INVALID_ARG;
+  if (!q_cat || !aligned16(q_cat) || !opt_aligned16(workspace)) return KDA_ERR_INVALID_ARG;
+  if (!workspace) ws_bytes = 0;
   if (!kda::mla_latent_supported()) return KDA_ERR_UNSUPPORTED;
   kda::MlaArgs a;
   std::memset(&a, 0, sizeof a);
   a.B = n_seqs, a.L_max = cache_len, a.scale_log2 = scale * 1.4426950408889634f;
   a.q_cat = const_cast<void *>(q_cat), a.cache = cache, a.lengths = lengths, a.z = z;
+  a.n_split = mla_split_for(n_seqs, cache_len, ws_bytes);
+  a.part = static_cast<float *>(workspace);
   a.err = device_error_ptr();
-  return finish(kda::launch_mla_latent(a, stream), 1);
+  return finish(kda::launch_mla_latent(a, stream), a.n_split > 1 ? 2 : 1);
 }
 
 kda_status mla_decode(const void *q_nope, const void *q_rope, const void *w_uk,
                       const void *w_uv, const void *cache, int64_t cache_len,
                       const int32_t *lengths, int n_seqs, const void *gate_logit, float scale,
-                      void *q_cat, float *z, void *out, cudaStream_t stream) {
+                      void *q_cat, float *z, void *out, void *workspace, size_t ws_bytes,
+                      cudaStream_t stream) {
   kda_status st = mla_common(cache, cache_len, lengths, n_seqs, scale, z);
   if (st != KDA_OK || n_seqs == 0) return st;
   if (!q_nope || !q_rope || !w_uk || !w_uv || !gate_logit || !q_cat || !out)
     return KDA_ERR_INVALID_ARG;
   if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(w_uv) ||
-      !aligned16(gate_logit) || !aligned16(q_cat) || !aligned16(out))
+      !aligned16(gate_logit) || !aligned16(q_cat) || !aligned16(out) ||
+      !opt_aligned16(workspace))
     return KDA_ERR_INVALID_ARG;
+  if (!workspace) ws_bytes = 0;
   if (!kda::mla_latent_supported()) return KDA_ERR_UNSUPPORTED;
   kda::MlaArgs a;
   std::memset(&a, 0, sizeof a);
   a.B = n_seqs, a.L_max = cache_len, a.scale_log2 = scale * 1.4426950408889634f;
   a.q_nope = q_nope, a.q_rope = q_rope, a.w_uk = w_uk, a.w_uv = w_uv, a.gate = gate_logit;
   a.q_cat = q_cat, a.cache = cache, a.lengths = lengths, a.z = z, a.out = out;
+  a.n_split = mla_split_for(n_seqs, cache_len, ws_bytes);
+  a.part = static_cast<float *>(workspace);
   a.err = device_error_ptr();
   cudaError_t e = kda::launch_mla_absorb(a, stream);
   if (e == cudaSuccess) e = kda::launch_mla_latent(a, stream);
   if (e == cudaSuccess) e = kda::launch_mla_up_gate(a, stream);
-  return finish(e, 3);
+  return finish(e, a.n_split > 1 ? 4 : 3);
 }
 
 kda_status kda_check_device_error(cudaStream_t stream) {

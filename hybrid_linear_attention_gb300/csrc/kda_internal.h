@@ -53,6 +53,8 @@ struct MlaArgs {
   const void *cache;           // [B, L_max, 576] bf16: latent | positional key per row
   const int32_t *lengths;      // [B] cached positions of each sequence
   float *z;                    // [B, 64, 512] fp32 attention output (latent)
+  int n_split;                 // splits of each sequence's positions (1: none)
+  float *part;                 // split partials: [n_split, B, 64, 512] Z, then [.., 64, 2] (m, l)
   void *out;                   // [B, 64, 128] bf16 gated head outputs
   int *err;
 };
@@ -93,6 +95,8 @@ cudaError_t launch_prologue(const ProArgs &a, int D, bool io_bf16, cudaStream_t 
 // out[k] <- the three raw inputs before checkpoint k (conv tail at that position)
 cudaError_t launch_wait_probe(long limit, int *err, cudaStream_t s);
 bool mla_latent_supported();
+int mla_preferred_split(int n_seqs, int64_t cache_len);
+size_t mla_split_bytes(int n_split, int n_seqs);
 cudaError_t launch_mla_absorb(const MlaArgs &a, cudaStream_t s);
 cudaError_t launch_mla_latent(const MlaArgs &a, cudaStream_t s);
 cudaError_t launch_mla_up_gate(const MlaArgs &a, cudaStream_t s);

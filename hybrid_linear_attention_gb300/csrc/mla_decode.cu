@@ -23,6 +23,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cstdlib>
 
 #include <cstring>
 
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(MLA_NT, 1)
   __shared__ volatile uint32_t s_abort;
   __shared__ uint32_t s_loads[2], s_mmas;
   __shared__ int s_stop;  // the softmax warps' exit decision, taken by one thread per tile
-  __shared__ float s_alpha[MH], s_l[MH];
+  __shared__ float s_alpha[MH], s_l[MH], s_mfin[MH];
   __shared__ int s_rescale[2];  // by tile parity: set by the head owners, reset after use
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -95,7 +96,12 @@ __global__ void __launch_bounds__(MLA_NT, 1)
     if (tid == 0 && a.err) atomicOr(a.err, ERR_BAD_INDEX);
     len = 0;
   }
-  const int ntiles = (len + TP - 1) / TP;
+  // split-KV: CTA (b, split) walks tiles [tbase, tbase + ntiles) of its sequence
+  const int all_tiles = (len + TP - 1) / TP;
+  const int per_split = (all_tiles + (int)gridDim.y - 1) / (int)gridDim.y;
+  const int tbase = (int)blockIdx.y * per_split;
+  const int ntiles = all_tiles - tbase < per_split ? (all_tiles - tbase > 0 ? all_tiles - tbase : 0)
+                                                   : per_split;
   auto bar = [&](int i) { return smem_u32(&s_bar[i]); };
   if (tid == 0) {
     for (int i = 0; i < MB_N; ++i) mbar_init(bar(i), 1);
@@ -124,7 +130,7 @@ __global__ void __launch_bounds__(MLA_NT, 1)
         ++s_loads[j];
         mbar_expect_tx(bar(MB_C0 + j), TILE);
         for (int kb = 0; kb < KB; ++kb)
-          tma_load_3d(sb + M_OFF_C + j * TILE + kb * BLK, &maps.c, 64 * kb, TP * t, b,
+          tma_load_3d(sb + M_OFF_C + j * TILE + kb * BLK, &maps.c, 64 * kb, TP * (tbase + t), b,
                       bar(MB_C0 + j));
       };
       // S = Q C^T: M = 64 heads (A = Q), N = 64 positions (B = C), both K-major
@@ -200,12 +206,13 @@ __global__ void __launch_bounds__(MLA_NT, 1)
         tmem_ld32(tm + lane_off + M_TM_S + 64 * j, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) x[c] = TP * t + c < len ? v[c] * a.scale_log2 : -INFINITY;
+        for (int c = 0; c < 32; ++c)
+          x[c] = TP * (tbase + t) + c < len ? v[c] * a.scale_log2 : -INFINITY;
         tmem_ld32(tm + lane_off + M_TM_S + 64 * j + 32, v);
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-          x[32 + c] = TP * t + 32 + c < len ? v[c] * a.scale_log2 : -INFINITY;
+          x[32 + c] = TP * (tbase + t) + 32 + c < len ? v[c] * a.scale_log2 : -INFINITY;
       }
       if (owner) {
         float mt = -INFINITY;
@@ -239,7 +246,7 @@ __global__ void __launch_bounds__(MLA_NT, 1)
       }
       // a position past the sequence: its latent row must not reach Z (its memory may hold
       // anything, and 0 x NaN is NaN)
-      if (tid < TP && TP * t + tid >= len) {
+      if (tid < TP && TP * (tbase + t) + tid >= len) {
 #pragma unroll 1
         for (int kb = 0; kb < KB - 1; ++kb)
 #pragma unroll
@@ -276,7 +283,7 @@ __global__ void __launch_bounds__(MLA_NT, 1)
       }
       if (s_stop) break;
     }
-    if (owner) s_l[hd] = l_run;
+    if (owner) s_l[hd] = l_run, s_mfin[hd] = m_run;
   }
   __syncthreads();
 
@@ -285,7 +292,10 @@ __global__ void __launch_bounds__(MLA_NT, 1)
     const bool done = ntiles > 0 && !s_abort && wait(MB_Z, (uint32_t)((ntiles - 1) & 1));
     tc_fence_after();
     const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-    float *z = a.z + (size_t)b * MH * ML;
+    // one split: z = Z / l; several: this split's unnormalised Z with its (m, l) per head
+    const bool split = gridDim.y > 1;
+    const size_t row = (size_t)blockIdx.y * a.B + b;
+    float *z = split ? a.part + row * MH * ML : a.z + (size_t)b * MH * ML;
 #pragma unroll 1
     for (int sl = 0; sl < 4; ++sl)
 #pragma unroll 1
@@ -299,9 +309,15 @@ __global__ void __launch_bounds__(MLA_NT, 1)
         for (int c = 0; c < 32; ++c) {
           const int head = 32 * hh + c;
           const float l = s_l[head];
-          z[(size_t)head * ML + 128 * sl + 32 * warp + lane] = (done && l > 0.f) ? v[c] / l : 0.f;
+          z[(size_t)head * ML + 128 * sl + 32 * warp + lane] =
+              split ? (done ? v[c] : 0.f) : ((done && l > 0.f) ? v[c] / l : 0.f);
         }
       }
+    if (split && tid < MH) {  // (m in log2 units, l) of each head; an empty range: (-inf, 0)
+      float *ml = a.part + (size_t)gridDim.y * a.B * MH * ML + (row * MH + tid) * 2;
+      ml[0] = done ? s_mfin[tid] : -INFINITY;
+      ml[1] = done ? s_l[tid] : 0.f;
+    }
   }
   if (tid == 128 && s_abort) {
     // a bounded wait ran out: let the copies and products in flight land (bounded) before
@@ -392,6 +408,28 @@ __global__ void __launch_bounds__(128) mla_up_gate_kernel(const MlaArgs a) {
   }
 }
 
+// z[b][h] = sum_s 2^(m_s - M) Z_s / sum_s 2^(m_s - M) l_s over the splits (M = max_s m_s)
+__global__ void __launch_bounds__(128) mla_combine_kernel(const MlaArgs a, int n_split) {
+  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const float *ml = a.part + (size_t)n_split * a.B * MH * ML;
+  float M = -INFINITY;
+  for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, ml[(((size_t)sp * a.B + b) * MH + h) * 2]);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, L = 0.f;
+  for (int sp = 0; sp < n_split; ++sp) {
+    const size_t row = (size_t)sp * a.B + b;
+    const float m = ml[(row * MH + h) * 2];
+    if (m == -INFINITY) continue;
+    const float w = exp2f(m - M);
+    L = fmaf(w, ml[(row * MH + h) * 2 + 1], L);
+    const float4 zz = *reinterpret_cast<const float4 *>(a.part + (row * MH + h) * ML + 4 * tid);
+    acc[0] = fmaf(w, zz.x, acc[0]), acc[1] = fmaf(w, zz.y, acc[1]);
+    acc[2] = fmaf(w, zz.z, acc[2]), acc[3] = fmaf(w, zz.w, acc[3]);
+  }
+  const float r = L > 0.f ? 1.f / L : 0.f;
+  *reinterpret_cast<float4 *>(a.z + ((size_t)b * MH + h) * ML + 4 * tid) =
+      make_float4(acc[0] * r, acc[1] * r, acc[2] * r, acc[3] * r);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 mla_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static bool tried = false;
@@ -421,6 +459,31 @@ bool mla_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t n3, uint32_t
 }
 
 }  // namespace
+
+// splits per sequence: as many CTAs as fill the SMs in one wave (one CTA per SM fits; a
+// second, partial wave costs more than the split saves), each split at least 8 tiles (512
+// positions); KDA_MLA_SPLIT=n forces n (1..64, tuning)
+int mla_preferred_split(int n_seqs, int64_t cache_len) {
+  if (const char *env = getenv("KDA_MLA_SPLIT")) {
+    const int n = atoi(env);
+    if (n >= 1 && n <= 64) return n;
+  }
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm < 1)
+    nsm = 1;
+  if (n_seqs < 1) return 1;
+  const int64_t tiles = (cache_len + TP - 1) / TP;
+  int64_t want = nsm / n_seqs;
+  const int64_t most = tiles / 8 > 1 ? tiles / 8 : 1;
+  if (want > most) want = most;
+  if (want > 64) want = 64;
+  return want > 1 ? (int)want : 1;
+}
+
+size_t mla_split_bytes(int n_split, int n_seqs) {
+  return n_split > 1 ? (size_t)n_split * n_seqs * MH * (ML + 2) * sizeof(float) : 0;
+}
 
 bool mla_latent_supported() {
   int dev = 0, major = 0;
@@ -452,7 +515,11 @@ cudaError_t launch_mla_latent(const MlaArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  mla_latent_kernel<<<a.B, MLA_NT, M_SMEM, s>>>(a, maps);
+  const int ns = a.n_split > 1 ? a.n_split : 1;
+  mla_latent_kernel<<<dim3(a.B, ns), MLA_NT, M_SMEM, s>>>(a, maps);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || ns == 1) return e;
+  mla_combine_kernel<<<dim3(a.B, MH), 128, 0, s>>>(a, ns);
   return cudaGetLastError();
 }
 

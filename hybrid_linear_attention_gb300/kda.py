@@ -29,7 +29,8 @@ EXPORTS = (
     "kda_conv_tail_checkpoints",
     "kda_decode_step", "kda_conv_state_update",
     "kda_decode_step_fused", "kda_decode_step_fused_fp8", "kda_decode_multi", "kda_state_accept", "kda_check_device_error",
-    "kda_launch_count", "kda_wait_probe", "mla_decode_latent", "mla_decode",
+    "kda_launch_count", "kda_wait_probe", "mla_decode_workspace_size", "mla_decode_latent",
+    "mla_decode",
 )
 
 
@@ -102,9 +103,11 @@ def load():
             "kda_check_device_error": (_i32, [_vp]),
             "kda_launch_count": (ctypes.c_uint64, []),
             "kda_wait_probe": (_i32, [_i64, _vp]),
-            "mla_decode_latent": (_i32, [_vp, _vp, _i64, _vp, _i32, ctypes.c_float, _vp, _vp]),
+            "mla_decode_workspace_size": (_sz, [_i32, _i64]),
+            "mla_decode_latent": (_i32, [_vp, _vp, _i64, _vp, _i32, ctypes.c_float, _vp, _vp,
+                                         _sz, _vp]),
             "mla_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, ctypes.c_float,
-                                  _vp, _vp, _vp, _vp]),
+                                  _vp, _vp, _vp, _vp, _sz, _vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -333,17 +336,26 @@ def kda_conv_state_update(p, x_new, conv_w, conv_state, y, *, slot_idx=None, str
 MLA_SCALE = 192 ** -0.5
 
 
-def mla_decode_latent(q_cat, cache, lengths, z, *, scale=MLA_SCALE, stream=None):
+def mla_decode_workspace_size(n_seqs, cache_len):
+    return int(load().mla_decode_workspace_size(int(n_seqs), int(cache_len)))
+
+
+def _ws(workspace):
+    return (_ptr(workspace, None, "workspace"),
+            workspace.numel() * workspace.element_size() if workspace is not None else 0)
+
+
+def mla_decode_latent(q_cat, cache, lengths, z, *, scale=MLA_SCALE, workspace=None, stream=None):
     """q_cat [B,64,576] bf16, cache [B,L,576] bf16, lengths [B] int32, z [B,64,512] fp32."""
     st = load().mla_decode_latent(
         _ptr(q_cat, torch.bfloat16, "q_cat"), _ptr(cache, torch.bfloat16, "cache"),
         cache.shape[1], _ptr(lengths, torch.int32, "lengths"), q_cat.shape[0], float(scale),
-        _ptr(z, torch.float32, "z"), _stream(stream))
+        _ptr(z, torch.float32, "z"), *_ws(workspace), _stream(stream))
     _check(st, "mla_decode_latent")
 
 
 def mla_decode(q_nope, q_rope, w_uk, w_uv, cache, lengths, gate_logit, q_cat, z, out, *,
-               scale=MLA_SCALE, stream=None):
+               scale=MLA_SCALE, workspace=None, stream=None):
     """One absorbed gated-MLA decode step; q_cat and z are caller-owned intermediates."""
     bf = torch.bfloat16
     st = load().mla_decode(
@@ -351,5 +363,5 @@ def mla_decode(q_nope, q_rope, w_uk, w_uv, cache, lengths, gate_logit, q_cat, z,
         _ptr(w_uv, bf, "w_uv"), _ptr(cache, bf, "cache"), cache.shape[1],
         _ptr(lengths, torch.int32, "lengths"), q_nope.shape[0], _ptr(gate_logit, bf, "gate_logit"),
         float(scale), _ptr(q_cat, bf, "q_cat"), _ptr(z, torch.float32, "z"), _ptr(out, bf, "out"),
-        _stream(stream))
+        *_ws(workspace), _stream(stream))
     _check(st, "mla_decode")

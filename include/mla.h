@@ -32,6 +32,12 @@
 extern "C" {
 #endif
 
+/* Device workspace that lets mla_decode_latent / mla_decode split each sequence's cached
+ * positions across several CTAs (so a small batch still fills the GPU): partial sums of each
+ * split, merged by a second launch.  0 when no split pays (then no workspace is needed).
+ * With less than this, the calls use as many splits as fit (down to none). */
+size_t mla_decode_workspace_size(int n_seqs, int64_t cache_len);
+
 /*
  * mla_decode_latent -- the attention over the latent cache (the part that streams it).
  *
@@ -42,13 +48,16 @@ extern "C" {
  *              treated as 0 and reported (KDA_ERR_BAD_INDEX).  Length 0 gives z = 0.
  *   scale      score scale (> 0).
  *   z          [n_seqs, 64, 512] fp32 output.
+ *   workspace / ws_bytes: caller-owned, up to mla_decode_workspace_size() bytes, or NULL / 0
+ *              (one CTA per sequence).  Splits write each head's unnormalised sum with its
+ *              running maximum and normaliser; the merge rescales them to a common maximum.
  * Scores and the weighted sum run on the tensor cores with bf16 operands and fp32
  * accumulation (the weights are rounded to bf16 as operands; the normaliser sums the same
  * rounded weights).
  */
 kda_status mla_decode_latent(const void* q_cat, const void* cache, int64_t cache_len,
                              const int32_t* lengths, int n_seqs, float scale, float* z,
-                             cudaStream_t stream);
+                             void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * mla_decode -- one absorbed gated-MLA decode step: absorption, mla_decode_latent, value
@@ -60,12 +69,13 @@ kda_status mla_decode_latent(const void* q_cat, const void* cache, int64_t cache
  *   q_cat      [n_seqs, 64, 576] bf16 and z [n_seqs, 64, 512] fp32: caller-owned
  *              intermediates (the absorbed query, the latent attention output).
  *   out        [n_seqs, 64, 128] bf16: o_i of every head.
- *   cache, cache_len, lengths, scale as mla_decode_latent.
+ *   cache, cache_len, lengths, scale, workspace, ws_bytes as mla_decode_latent.
  */
 kda_status mla_decode(const void* q_nope, const void* q_rope, const void* w_uk,
                       const void* w_uv, const void* cache, int64_t cache_len,
                       const int32_t* lengths, int n_seqs, const void* gate_logit, float scale,
-                      void* q_cat, float* z, void* out, cudaStream_t stream);
+                      void* q_cat, float* z, void* out, void* workspace, size_t ws_bytes,
+                      cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -191,14 +191,17 @@ def test_fp8_calls_reject_bad_arguments_on_host(lib):
 
 def test_mla_calls_reject_bad_arguments_on_host(lib):
     buf = ctypes.c_void_p(16)  # never dereferenced: every call fails validation first
-    assert lib.mla_decode_latent(buf, buf, 0, buf, 2, 0.07, buf, None) == kda.KDA_ERR_INVALID_ARG
-    assert lib.mla_decode_latent(buf, buf, 64, buf, 2, 0.0, buf, None) == kda.KDA_ERR_INVALID_ARG
-    assert lib.mla_decode_latent(buf, buf, 64, buf, -1, 0.07, buf, None) == kda.KDA_ERR_INVALID_ARG
-    assert lib.mla_decode_latent(buf, ctypes.c_void_p(24), 64, buf, 2, 0.07, buf,
+    assert lib.mla_decode_latent(buf, buf, 0, buf, 2, 0.07, buf, None, 0, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.mla_decode_latent(buf, buf, 64, buf, 2, 0.0, buf, None, 0, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.mla_decode_latent(buf, buf, 64, buf, -1, 0.07, buf, None, 0, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.mla_decode_latent(buf, ctypes.c_void_p(24), 64, buf, 2, 0.07, buf, None, 0,
                                  None) == kda.KDA_ERR_INVALID_ARG
-    assert lib.mla_decode_latent(None, None, 0, None, 0, 0.07, None, None) == kda.KDA_OK
-    assert lib.mla_decode(buf, buf, buf, buf, buf, 64, buf, 2, None, 0.07, buf, buf, buf,
+    assert lib.mla_decode_latent(buf, buf, 64, buf, 2, 0.07, buf, ctypes.c_void_p(40), 1 << 20,
+                                 None) == kda.KDA_ERR_INVALID_ARG          # misaligned workspace
+    assert lib.mla_decode_latent(None, None, 0, None, 0, 0.07, None, None, 0, None) == kda.KDA_OK
+    assert lib.mla_decode(buf, buf, buf, buf, buf, 64, buf, 2, None, 0.07, buf, buf, buf, None, 0,
                           None) == kda.KDA_ERR_INVALID_ARG
+    assert kda.mla_decode_workspace_size(0, 64) == 0 and kda.mla_decode_workspace_size(4, 0) == 0
 
 
 def test_wait_probe_rejects_bad_limits_on_host(lib):

@@ -116,3 +116,82 @@ def test_mla_decode_matches_the_expanded_oracle():
                                      clean[..., 512:], np.array(lengths), m["w_uk"], m["w_uv"],
                                      m["gate"], scale=kda.MLA_SCALE)
     assert out_error(out.cpu(), ref, torch.bfloat16) <= TOL
+
+
+def _latent_ws(m, ws_bytes=None):
+    """The latent attention with a split workspace (the size the library asks for, or less)."""
+    _gpu.lib()
+    B, L = m["cache"].shape[:2]
+    need = kda.mla_decode_workspace_size(B, L)
+    assert need > 0, "a small batch over a long cache is split"
+    n = need if ws_bytes is None else ws_bytes
+    ws = torch.empty((n + 3) // 4, dtype=torch.float32, device="cuda")
+    z = torch.full((B, 64, 512), 7.0, device="cuda")
+    kda.mla_decode_latent(m["q_cat"].cuda(), m["cache"].cuda(), m["lengths"].cuda(), z,
+                          workspace=ws)
+    torch.cuda.synchronize()
+    return z
+
+
+@pytest.mark.parametrize("q_std", [1.0, 4.0])
+def test_split_latent_attention_matches_the_oracle(q_std):
+    """A small batch over a long cache: each sequence's positions are split across CTAs whose
+    partial sums are merged.  Lengths that leave some splits empty (1, 513) or ragged
+    (2049, 4000), and peaked scores (q_std 4) so each split's maximum differs."""
+    lengths = [4096, 1, 513, 2049, 4000]
+    m = _case(lengths, 4096, seed=840 + int(q_std), q_std=q_std)
+    z = _latent_ws(m)
+    kda.kda_check_device_error()
+    clean = m["cache"].clone()
+    for b, n in enumerate(lengths):
+        clean[b, n:] = 0
+    ref, _ = oracle.mla_latent_attention(m["q_cat"], clean, np.array(lengths),
+                                         scale=kda.MLA_SCALE)
+    for b in range(len(lengths)):
+        e = max_err_rel_rms(z[b], ref[b])
+        assert e <= TOL, f"sequence {b} (length {lengths[b]}): {e:.3g}"
+    # without a workspace the same call runs one CTA per sequence: same values within rounding
+    z1 = _latent(m)
+    assert max_err_rel_rms(z1, z.double().cpu()) <= TOL
+
+
+def test_split_with_a_short_workspace_and_empty_sequences():
+    """A workspace for two splits only (the call uses what fits); a sequence of length 0 and
+    one with an out-of-range length still give z = 0 through the merge."""
+    lengths = [2048, 0, 1500, -3]
+    m = _case(lengths, 2048, seed=850)
+    two = 2 * 4 * 64 * 514 * 4
+    z = _latent_ws(m, ws_bytes=two)
+    with pytest.raises(kda.KdaError) as ei:
+        kda.kda_check_device_error()
+    assert ei.value.status == kda.KDA_ERR_BAD_INDEX
+    assert not z[1].any() and not z[3].any()
+    clean = m["cache"].clone()
+    clean[2, 1500:] = 0
+    ref, _ = oracle.mla_latent_attention(m["q_cat"][[0, 2]], clean[[0, 2]],
+                                         np.array([2048, 1500]), scale=kda.MLA_SCALE)
+    assert max_err_rel_rms(z[[0, 2]], ref) <= TOL
+
+
+def test_split_mla_decode_matches_the_expanded_oracle():
+    """The whole step with a split workspace on two long sequences."""
+    lengths = [3000, 4096]
+    m = _case(lengths, 4096, seed=860)
+    _gpu.lib()
+    B = len(lengths)
+    ws = torch.empty(kda.mla_decode_workspace_size(B, 4096) // 4, dtype=torch.float32,
+                     device="cuda")
+    q_cat = torch.empty((B, 64, 576), dtype=torch.bfloat16, device="cuda")
+    z = torch.empty((B, 64, 512), device="cuda")
+    out = torch.empty((B, 64, 128), dtype=torch.bfloat16, device="cuda")
+    c = _gpu.cuda
+    kda.mla_decode(c(m["q_nope"]), c(m["q_rope"]), c(m["w_uk"]), c(m["w_uv"]), c(m["cache"]),
+                   c(m["lengths"]), c(m["gate"]), q_cat, z, out, workspace=ws)
+    torch.cuda.synchronize()
+    kda.kda_check_device_error()
+    clean = m["cache"].clone()
+    clean[0, 3000:] = 0
+    ref = oracle.mla_decode_expanded(m["q_nope"], m["q_rope"], clean[..., :512],
+                                     clean[..., 512:], np.array(lengths), m["w_uk"], m["w_uv"],
+                                     m["gate"], scale=kda.MLA_SCALE)
+    assert out_error(out.cpu(), ref, torch.bfloat16) <= TOL
