@@ -486,6 +486,27 @@ kda_status mla_decode_latent(const void *q_cat, const void *cache, int64_t cache
   return finish(kda::launch_mla_latent(a, stream), a.n_split > 1 ? 2 : 1);
 }
 
+kda_status mla_decode_latent_noalloc(const void *q_cat, const void *cache, int64_t cache_len,
+                                     const int32_t *lengths, int n_seqs, float scale, float *z,
+                                     cudaStream_t stream) {
+  kda_status st = mla_common(cache, cache_len, lengths, n_seqs, scale, z);
+  if (st != KDA_OK || n_seqs == 0) return st;
+  if (!q_cat || !aligned16(q_cat)) return KDA_ERR_INVALID_ARG;
+  const size_t need = mla_decode_workspace_size(n_seqs, cache_len);
+  if (need > kda::mla_static_scratch_bytes()) return KDA_ERR_WORKSPACE;
+  if (!kda::mla_latent_supported()) return KDA_ERR_UNSUPPORTED;
+  void *scratch = need ? kda::mla_static_scratch() : nullptr;
+  if (need && !scratch) return KDA_ERR_CUDA;
+  kda::MlaArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.B = n_seqs, a.L_max = cache_len, a.scale_log2 = scale * 1.4426950408889634f;
+  a.q_cat = const_cast<void *>(q_cat), a.cache = cache, a.lengths = lengths, a.z = z;
+  a.n_split = mla_split_for(n_seqs, cache_len, need);
+  a.part = static_cast<float *>(scratch);
+  a.err = device_error_ptr();
+  return finish(kda::launch_mla_latent(a, stream), a.n_split > 1 ? 2 : 1);
+}
+
 kda_status mla_decode(const void *q_nope, const void *q_rope, const void *w_uk,
                       const void *w_uv, const void *cache, int64_t cache_len,
                       const int32_t *lengths, int n_seqs, const void *gate_logit, float scale,

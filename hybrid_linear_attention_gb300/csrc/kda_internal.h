@@ -97,6 +97,8 @@ cudaError_t launch_wait_probe(long limit, int *err, cudaStream_t s);
 bool mla_latent_supported();
 int mla_preferred_split(int n_seqs, int64_t cache_len);
 size_t mla_split_bytes(int n_split, int n_seqs);
+size_t mla_static_scratch_bytes();
+void *mla_static_scratch();  // this device's copy, or nullptr
 cudaError_t launch_mla_absorb(const MlaArgs &a, cudaStream_t s);
 cudaError_t launch_mla_latent(const MlaArgs &a, cudaStream_t s);
 cudaError_t launch_mla_up_gate(const MlaArgs &a, cudaStream_t s);

@@ -458,7 +458,26 @@ bool mla_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t n3, uint32_t
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// the split partial sums of one mla_decode_latent_noalloc call (one wave of CTAs on up to
+// 191 SMs fits); cudaGetSymbolAddress gives each device's copy
+constexpr size_t MLA_STATIC_SCRATCH = (size_t)24 << 20;
+__device__ __align__(256) unsigned char g_mla_scratch[MLA_STATIC_SCRATCH];
+
 }  // namespace
+
+size_t mla_static_scratch_bytes() { return MLA_STATIC_SCRATCH; }
+
+void *mla_static_scratch() {
+  static void *addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_mla_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
 
 // splits per sequence: as many CTAs as fill the SMs in one wave (one CTA per SM fits; a
 // second, partial wave costs more than the split saves), each split at least 8 tiles (512

@@ -30,6 +30,7 @@ EXPORTS = (
     "kda_decode_step", "kda_conv_state_update",
     "kda_decode_step_fused", "kda_decode_step_fused_fp8", "kda_decode_multi", "kda_state_accept", "kda_check_device_error",
     "kda_launch_count", "kda_wait_probe", "mla_decode_workspace_size", "mla_decode_latent",
+    "mla_decode_latent_noalloc",
     "mla_decode",
 )
 
@@ -106,6 +107,8 @@ def load():
             "mla_decode_workspace_size": (_sz, [_i32, _i64]),
             "mla_decode_latent": (_i32, [_vp, _vp, _i64, _vp, _i32, ctypes.c_float, _vp, _vp,
                                          _sz, _vp]),
+            "mla_decode_latent_noalloc": (_i32, [_vp, _vp, _i64, _vp, _i32, ctypes.c_float, _vp,
+                                                 _vp]),
             "mla_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, ctypes.c_float,
                                   _vp, _vp, _vp, _vp, _sz, _vp]),
         }
@@ -352,6 +355,15 @@ def mla_decode_latent(q_cat, cache, lengths, z, *, scale=MLA_SCALE, workspace=No
         cache.shape[1], _ptr(lengths, torch.int32, "lengths"), q_cat.shape[0], float(scale),
         _ptr(z, torch.float32, "z"), *_ws(workspace), _stream(stream))
     _check(st, "mla_decode_latent")
+
+
+def mla_decode_latent_noalloc(q_cat, cache, lengths, z, *, scale=MLA_SCALE, stream=None):
+    """mla_decode_latent with its split scratch in the library's fixed device buffer."""
+    st = load().mla_decode_latent_noalloc(
+        _ptr(q_cat, torch.bfloat16, "q_cat"), _ptr(cache, torch.bfloat16, "cache"),
+        cache.shape[1], _ptr(lengths, torch.int32, "lengths"), q_cat.shape[0], float(scale),
+        _ptr(z, torch.float32, "z"), _stream(stream))
+    _check(st, "mla_decode_latent_noalloc")
 
 
 def mla_decode(q_nope, q_rope, w_uk, w_uv, cache, lengths, gate_logit, q_cat, z, out, *,

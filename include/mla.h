@@ -60,6 +60,20 @@ kda_status mla_decode_latent(const void* q_cat, const void* cache, int64_t cache
                              void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * mla_decode_latent_noalloc -- mla_decode_latent with no caller workspace and no allocation.
+ * No counterpart on the pages (they describe the attention, not how its scratch memory is
+ * provided): the split partial sums go to a fixed 24 MiB device buffer inside the library
+ * (each device its own copy), so the call needs no memory from the caller.  The split count
+ * is the one mla_decode_workspace_size() sizes; if that needs more than the fixed buffer, the
+ * call returns KDA_ERR_WORKSPACE and launches nothing.  Calls on one device share the buffer:
+ * issue them in one stream (or otherwise ordered), never concurrently.  Arguments, layouts
+ * and results as mla_decode_latent; bit-identical to it with a workspace of that size.
+ */
+kda_status mla_decode_latent_noalloc(const void* q_cat, const void* cache, int64_t cache_len,
+                                     const int32_t* lengths, int n_seqs, float scale, float* z,
+                                     cudaStream_t stream);
+
+/*
  * mla_decode -- one absorbed gated-MLA decode step: absorption, mla_decode_latent, value
  * up-projection and gate.
  *
