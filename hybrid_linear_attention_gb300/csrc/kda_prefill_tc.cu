@@ -1140,9 +1140,15 @@ __global__ void __launch_bounds__(NT, 1)
         s_abort = 1;
       if (!(ok = sync())) break;
       extract(nv, peer + off_lp(b), pA);
+      fence_cluster();
+      fence_proxy_async();
       if (!(ok = sync())) break;
-      if (grp == 2) {
+      if (grp == 2) {  // FULL as soon as T has landed: the consumer does not wait for P1 below
         inverse(peer + off_lt(b), pA, pT, pS);
+        fence_cluster();
+        fence_proxy_async();
+        asm volatile("bar.sync 3, 128;" ::: "memory");
+        if (tid == 256) mbar_arrive_remote(bar(BAR_F0 + b), 0);  // T and P' of chunk c landed
       } else if (more) {  // P1 and the operands of chunk c + 1 on groups 0 and 1
         const int64_t t1 = t0 + C;
         const int nv1 = (int)((eos - t1) < C ? (eos - t1) : C);
@@ -1150,10 +1156,8 @@ __global__ void __launch_bounds__(NT, 1)
         asm volatile("bar.sync 1, 256;" ::: "memory");
         ap_operands(nv1, 256);
       }
-      fence_cluster();
       fence_proxy_async();
       if (!(ok = sync())) break;
-      if (tid == 0) mbar_arrive_remote(bar(BAR_F0 + b), 0);  // T and P' of chunk c landed
     }
   }
 

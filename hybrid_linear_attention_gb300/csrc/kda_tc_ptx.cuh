@@ -271,10 +271,12 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 }
 
 // fp32 -> tf32, round to nearest (ties away), low 13 bits cleared.
+// fp32 -> tf32 (10 stored mantissa bits), round to nearest with ties away from zero, on the
+// bit pattern: half a tf32 unit (bit 12) is added to the magnitude and the 13 low bits cleared
+// (a carry into the exponent is the rounding up to the next binade).  Exact for finite x;
+// integer ALU work instead of a conversion instruction (measured faster in the chunk loop)
 __device__ __forceinline__ float to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
 
 }  // namespace tc
