@@ -339,16 +339,19 @@ __global__ void __launch_bounds__(NT, 1)
   //      at the chunk end and Gamma_C; and per channel the decay between block starts
   //      2^(gam_R0 - gam_R'0) for the pairs (1,0) (2,1) (3,2) (2,0) (3,1) (3,0).
   //      It runs before the walk for chunk 0 and during the output phase of chunk cc - 1
-  //      (t: the thread's index in the 128 running it).
-  auto p1 = [&](int cc, int t) {
+  //      (t: the thread's index in the 128 running it).  part 1: beta and the row norms;
+  //      part 2: the prefix sums; part 3: both (two groups of 128 may split it).  beta is
+  //      stored last, so the global load's latency stalls nothing.
+  auto p1 = [&](int cc, int t, int part) {
     const int64_t tc = bos + (int64_t)cc * C;
     const int nvc = (int)((eos - tc) < C ? (eos - tc) : C);
     const uint32_t pc = (uint32_t)(cc & 1);
-    if (t < C) s_beta[t] = t < nvc ? a.beta[(size_t)(tc + t) * H + h] : 0.f;
+    float bv = 0.f;
+    if ((part & 1) && t < nvc) bv = a.beta[(size_t)(tc + t) * H + h];
     wait(BAR_Q, pc);
     wait(BAR_K, pc);
     wait(BAR_G, pc);
-    {
+    if (part & 1) {
       const int r = t >> 1, hf = t & 1;
       float sq = 0.f, sk = 0.f, sqk = 0.f;
       if (r < nvc) {
@@ -370,8 +373,9 @@ __global__ void __launch_bounds__(NT, 1)
         const float rk = r < nvc ? (a.qk_l2norm ? rsqrtf(sk + a.l2_eps) : 1.f) : 0.f;
         s_rq[r] = rq, s_rk[r] = rk, s_pd[pc][r] = sqk * rq * rk;
       }
+      if (t < C) s_beta[t] = bv;
     }
-    {
+    if (part & 2) {
       const int i = t;
       float run = 0.f;
 #pragma unroll 1
@@ -413,7 +417,7 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t ID_AP160 = idesc(1, 128, 160, 0, 0);
   const uint32_t ID_AP112 = idesc(1, 128, 112, 0, 0);
   uint32_t mma_par = 0;
-  if (ok && nchunks > 0 && grp == 2) p1(0, tid - 256);
+  if (ok && nchunks > 0 && grp == 2) p1(0, tid - 256, 3);
   ok = sync();
 
   // ---- prefix-state checkpoints: after chunk c (cnt tokens of the sequence done), warp group
@@ -698,7 +702,23 @@ __global__ void __launch_bounds__(NT, 1)
   };
   // ---- groups 0 and 1: wait for MMA1, Y^T = beta (V - K Gamma S)^T (tf32 hi + lo in TA),
   //      decay S^T by Gamma_C
-  auto y_decay = [&](int nv, uint32_t par) {
+  // (decay_g0 / decay_n: the first group-relative 32-column block and how many this group
+  //  decays; the cluster-pair consumer hands the whole decay to warp group 2, which is free
+  //  while groups 0 and 1 form Y)
+  auto decay = [&](int first, int nblk) {
+#pragma unroll 1
+      for (int g32 = first; g32 < first + nblk; ++g32) {
+        float v[32];
+        const int i0 = 32 * g32;
+        tmem_ld32(tm + lane_off + TM_S + i0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) v[x] *= s_GC[i0 + x];
+        tmem_st32(tm + lane_off + TM_S + i0, v);
+      }
+      tmem_wait_st();
+  };
+  auto y_decay = [&](int nv, uint32_t par, bool with_decay) {
       wait(BAR_MMA, mma_par);  // MMA1 done
       tc_fence_after();
       wait(BAR_V, par);
@@ -716,17 +736,8 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_st32(tm + lane_off + TM_A + 32 * grp, hi);
         tmem_st32(tm + lane_off + TM_A + 64 + 32 * grp, xk);
       }
-#pragma unroll 1
-      for (int g32 = 0; g32 < 2; ++g32) {  // decay: this group's 64 key channels
-        float v[32];
-        const int i0 = 64 * grp + 32 * g32;
-        tmem_ld32(tm + lane_off + TM_S + i0, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int x = 0; x < 32; ++x) v[x] *= s_GC[i0 + x];
-        tmem_st32(tm + lane_off + TM_S + i0, v);
-      }
-      tmem_wait_st();
+      if (with_decay) decay(2 * grp, 2);  // this group's 64 key channels
+      else tmem_wait_st();
   };
   // thread 0: u^T = Y^T T^T, hi then lo (T at shared offset t_off)
   auto mmau_issue = [&](uint32_t t_off) {
@@ -1028,7 +1039,7 @@ __global__ void __launch_bounds__(NT, 1)
       if (grp == 2)  // in flight with MMA1 and the Y / decay work
         inverse(sm + OFF_T, reinterpret_cast<const float *>(sm + OFF_A),
                 reinterpret_cast<float *>(sm + OFF_T), s_M);
-      else y_decay(nv, par);
+      else y_decay(nv, par, true);
       mma_par ^= 1;  // MMA1's phase (waited by groups 0 and 1)
       fence_proxy_async();
       if (!(ok = sync())) break;
@@ -1047,7 +1058,7 @@ __global__ void __launch_bounds__(NT, 1)
       fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0) p7_issue(OFF_P);
-      if (grp == 2 && more) p1(c + 1, tid - 256);  // overlapped with the update and the output phase
+      if (grp == 2 && more) p1(c + 1, tid - 256, 3);  // overlapped with the update and the output phase
       wait(BAR_MMA, mma_par);
       mma_par ^= 1;
       tc_fence_after();
@@ -1076,7 +1087,13 @@ __global__ void __launch_bounds__(NT, 1)
         if (more) issue(1u << BAR_Q, c + 1);  // q is consumed
         mma1_issue();
       }
-      if (grp < 2) y_decay(nv, par);
+      if (grp < 2) {
+        y_decay(nv, par, false);
+      } else {  // S^T *= Gamma_C once MMA1, which reads S, is done
+        wait(BAR_MMA, mma_par);
+        tc_fence_after();
+        decay(0, 4);
+      }
       mma_par ^= 1;
       fence_proxy_async();
       if (!(ok = sync())) break;
@@ -1100,7 +1117,7 @@ __global__ void __launch_bounds__(NT, 1)
       fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0) p7_issue(off_lp(b));
-      if (grp == 2 && more) p1(c + 1, tid - 256);
+      if (grp == 2 && more) p1(c + 1, tid - 256, 3);
       wait(BAR_MMA, mma_par);
       mma_par ^= 1;
       tc_fence_after();
@@ -1149,12 +1166,15 @@ __global__ void __launch_bounds__(NT, 1)
         fence_proxy_async();
         asm volatile("bar.sync 3, 128;" ::: "memory");
         if (tid == 256) mbar_arrive_remote(bar(BAR_F0 + b), 0);  // T and P' of chunk c landed
-      } else if (more) {  // P1 and the operands of chunk c + 1 on groups 0 and 1
-        const int64_t t1 = t0 + C;
-        const int nv1 = (int)((eos - t1) < C ? (eos - t1) : C);
-        if (grp == 0) p1(c + 1, tid);
+      } else if (more) {  // P1 of chunk c + 1 on groups 0 and 1
+        p1(c + 1, tid & 127, grp == 0 ? 2 : 1);  // prefix sums | beta and norms
         asm volatile("bar.sync 1, 256;" ::: "memory");
-        ap_operands(nv1, 256);
+        asm volatile("bar.arrive 5, 384;" ::: "memory");  // P1 done: group 2 may join
+      }
+      if (more) {  // the operands of chunk c + 1 on all three groups (group 2 after the inverse)
+        if (grp == 2) asm volatile("bar.sync 5, 384;" ::: "memory");
+        const int64_t t1 = t0 + C;
+        ap_operands((int)((eos - t1) < C ? (eos - t1) : C), NT);
       }
       fence_proxy_async();
       if (!(ok = sync())) break;
