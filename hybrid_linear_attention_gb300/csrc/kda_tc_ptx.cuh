@@ -55,6 +55,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 }
 constexpr long kWaitLimit = 1L << 24;
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+#pragma unroll 1  // inlined at every phase boundary: kept short (code size costs time)
   for (long it = 0; it < kWaitLimit; ++it)
     if (mbar_try_wait_cluster(bar, parity)) return true;
   return false;
@@ -86,6 +87,7 @@ __device__ __forceinline__ void cluster_sync() {
                    "memory");
 }
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+#pragma unroll 1  // inlined at every phase boundary: kept short (code size costs time)
   for (long it = 0; it < kWaitLimit; ++it)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
