@@ -41,6 +41,8 @@
 #include "kda_prefill_tc.h"
 #include "kda_tc_ptx.cuh"
 
+extern __shared__ uint8_t prefill_dyn_smem[];  // the dynamic shared memory base
+
 namespace kda {
 namespace {
 
@@ -212,23 +214,113 @@ struct Maps {
   CUtensorMap q, k, v, g, out, gate;
 };
 
+// Per-CTA shared state that P1 (out of line, below) shares with the kernel
+__shared__ float s_beta[C], s_rq[C], s_rk[C], s_pd[2][C];  // s_pd by chunk parity
+__shared__ __align__(16) float s_g0[4][D];  // log2-retention just before each 16-block
+__shared__ __align__(16) float s_gC[D];     // log2-retention at the chunk's last token
+__shared__ float s_GC[D];                   // Gamma_C
+__shared__ __align__(16) float s_M[3 * 256];  // inverse scratch; block decays P1 -> P2
+__shared__ __align__(8) uint64_t s_bar[NBAR];
+__shared__ uint32_t s_abort;
+
+// ---- P1 of chunk cc, by a warp group (128 threads): beta; row norms and q.k (two threads
+//      per row); per channel (one thread each) the prefix sums of the clamped
+//      log2-retention, written back over g, with its value before each 16-token block,
+//      at the chunk end and Gamma_C; and per channel the decay between block starts
+//      2^(gam_R0 - gam_R'0) for the pairs (1,0) (2,1) (3,2) (2,0) (3,1) (3,0).
+//      It runs before the walk for chunk 0 and during the output phase of chunk cc - 1
+//      (t: the thread's index in the 128 running it).  part 1: beta and the row norms;
+//      part 2: the prefix sums; part 3: both (two groups of 128 may split it).  beta is
+//      stored last, so the global load's latency stalls nothing.  One out-of-line copy
+//      serves every call site: the kernel is larger than the instruction cache, and code
+//      size costs time.
+__device__ __noinline__ void p1_run(const float *beta, int64_t bos, int64_t eos, int h, int H,
+                                    bool l2norm, float l2_eps, float g_min, uint32_t pad,
+                                    int cc, int t, int part) {
+  uint8_t *sm = prefill_dyn_smem + pad;
+  auto wait = [&](int b, uint32_t parity) {
+    if (!mbar_wait(smem_u32(&s_bar[b]), parity)) s_abort = 1;
+  };
+  const int64_t tc = bos + (int64_t)cc * C;
+  const int nvc = (int)((eos - tc) < C ? (eos - tc) : C);
+  const uint32_t pc = (uint32_t)(cc & 1);
+  float bv = 0.f;
+  if ((part & 1) && t < nvc) bv = beta[(size_t)(tc + t) * H + h];
+  wait(BAR_Q, pc);
+  wait(BAR_K, pc);
+  wait(BAR_G, pc);
+  if (part & 1) {
+    const int r = t >> 1, hf = t & 1;
+    float sq = 0.f, sk = 0.f, sqk = 0.f;
+    if (r < nvc) {
+#pragma unroll 2
+      for (int c8 = 0; c8 < 8; ++c8) {  // two at a time: p1 is inlined at three places
+        float qv[8], kv[8];
+        bf_row8(sm + OFF_Q, r, 8 * hf + c8, qv);
+        bf_row8(sm + OFF_K, r, 8 * hf + c8, kv);
+#pragma unroll
+        for (int y = 0; y < 8; ++y)
+          sq = fmaf(qv[y], qv[y], sq), sk = fmaf(kv[y], kv[y], sk), sqk = fmaf(qv[y], kv[y], sqk);
+      }
+    }
+    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+    sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+    sqk += __shfl_xor_sync(0xffffffffu, sqk, 1);
+    if (hf == 0) {
+      const float rq = r < nvc ? (l2norm ? rsqrtf(sq + l2_eps) : 1.f) : 0.f;
+      const float rk = r < nvc ? (l2norm ? rsqrtf(sk + l2_eps) : 1.f) : 0.f;
+      s_rq[r] = rq, s_rk[r] = rk, s_pd[pc][r] = sqk * rq * rk;
+    }
+    if (t < C) s_beta[t] = bv;
+  }
+  if (part & 2) {
+    const int i = t;
+    float run = 0.f;
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {  // 16 rows at a time, running sum carried over
+      s_g0[blk][i] = run;
+#pragma unroll 1
+      for (int x0 = 0; x0 < 16; x0 += 8) {  // 8 loads in flight, then the 8 sums
+        float v[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          const int r = 16 * blk + x0 + x;
+          const float gv = *reinterpret_cast<const float *>(sm + OFF_G + swz<4>(r, i));
+          v[x] = r < nvc ? fmaxf(gv, g_min) * LOG2E : 0.f;
+        }
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          run += v[x];
+          *reinterpret_cast<float *>(sm + OFF_G + swz<4>(16 * blk + x0 + x, i)) = run;
+        }
+      }
+    }
+    float g0[4];
+#pragma unroll
+    for (int R = 0; R < 4; ++R) g0[R] = s_g0[R][i];
+    s_gC[i] = run;
+    s_GC[i] = ex2(run);
+    s_M[0 * D + i] = ex2(g0[1] - g0[0]);
+    s_M[1 * D + i] = ex2(g0[2] - g0[1]);
+    s_M[2 * D + i] = ex2(g0[3] - g0[2]);
+    s_M[3 * D + i] = ex2(g0[2] - g0[0]);
+    s_M[4 * D + i] = ex2(g0[3] - g0[1]);
+    s_M[5 * D + i] = ex2(g0[3] - g0[0]);
+  }
+}
+
+
 // PAIR: a cluster of two CTAs per (head, sequence), rank 0 the consumer (state walk), rank 1
 // the producer (A, P', T); otherwise one CTA does both.
 template <typename ST, bool GATE, bool PAIR, bool QUANT>
 __global__ void __launch_bounds__(NT, 1)
     prefill_tc_kernel(const TcArgs a, const __grid_constant__ Maps maps) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ float s_beta[C], s_rq[C], s_rk[C], s_pd[2][C];  // s_pd by chunk parity
-  __shared__ __align__(16) float s_g0[4][D];  // log2-retention just before each 16-block
-  __shared__ __align__(16) float s_gC[D];     // log2-retention at the chunk's last token
-  __shared__ float s_GC[D];                   // Gamma_C
   __shared__ float s_red[4][C];
   __shared__ float s_amx[4][C];  // FP8 output: each row's amax by TMEM lane quarter
   __shared__ float s_inv[C];     // FP8 output: each row's 448 / amax
   __shared__ float s_nrm[C];     // gated output: each row's 1 / RMS
-  __shared__ __align__(16) float s_M[3 * 256];  // inverse scratch; block decays P1 -> P2
-  __shared__ __align__(8) uint64_t s_bar[NBAR];
-  __shared__ uint32_t s_tmem, s_abort, s_pend, s_ppar[NBAR];
+  __shared__ uint32_t s_tmem, s_pend, s_ppar[NBAR];
 
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_u32 & 1023u)) & 1023u;
@@ -333,82 +425,8 @@ __global__ void __launch_bounds__(NT, 1)
     issue((1u << BAR_Q) | (1u << BAR_K) | (producer ? 0u : (1u << BAR_V)) | (1u << BAR_G), 0);
   bool ok = sync();
 
-  // ---- P1 of chunk cc, by warp group 2 (128 threads): beta; row norms and q.k (two threads
-  //      per row); per channel (one thread each) the prefix sums of the clamped
-  //      log2-retention, written back over g, with its value before each 16-token block,
-  //      at the chunk end and Gamma_C; and per channel the decay between block starts
-  //      2^(gam_R0 - gam_R'0) for the pairs (1,0) (2,1) (3,2) (2,0) (3,1) (3,0).
-  //      It runs before the walk for chunk 0 and during the output phase of chunk cc - 1
-  //      (t: the thread's index in the 128 running it).  part 1: beta and the row norms;
-  //      part 2: the prefix sums; part 3: both (two groups of 128 may split it).  beta is
-  //      stored last, so the global load's latency stalls nothing.
   auto p1 = [&](int cc, int t, int part) {
-    const int64_t tc = bos + (int64_t)cc * C;
-    const int nvc = (int)((eos - tc) < C ? (eos - tc) : C);
-    const uint32_t pc = (uint32_t)(cc & 1);
-    float bv = 0.f;
-    if ((part & 1) && t < nvc) bv = a.beta[(size_t)(tc + t) * H + h];
-    wait(BAR_Q, pc);
-    wait(BAR_K, pc);
-    wait(BAR_G, pc);
-    if (part & 1) {
-      const int r = t >> 1, hf = t & 1;
-      float sq = 0.f, sk = 0.f, sqk = 0.f;
-      if (r < nvc) {
-#pragma unroll 2
-        for (int c8 = 0; c8 < 8; ++c8) {  // two at a time: p1 is inlined at three places
-          float qv[8], kv[8];
-          bf_row8(sm + OFF_Q, r, 8 * hf + c8, qv);
-          bf_row8(sm + OFF_K, r, 8 * hf + c8, kv);
-#pragma unroll
-          for (int y = 0; y < 8; ++y)
-            sq = fmaf(qv[y], qv[y], sq), sk = fmaf(kv[y], kv[y], sk), sqk = fmaf(qv[y], kv[y], sqk);
-        }
-      }
-      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-      sqk += __shfl_xor_sync(0xffffffffu, sqk, 1);
-      if (hf == 0) {
-        const float rq = r < nvc ? (a.qk_l2norm ? rsqrtf(sq + a.l2_eps) : 1.f) : 0.f;
-        const float rk = r < nvc ? (a.qk_l2norm ? rsqrtf(sk + a.l2_eps) : 1.f) : 0.f;
-        s_rq[r] = rq, s_rk[r] = rk, s_pd[pc][r] = sqk * rq * rk;
-      }
-      if (t < C) s_beta[t] = bv;
-    }
-    if (part & 2) {
-      const int i = t;
-      float run = 0.f;
-#pragma unroll 1
-      for (int blk = 0; blk < 4; ++blk) {  // 16 rows at a time, running sum carried over
-        s_g0[blk][i] = run;
-#pragma unroll 1
-        for (int x0 = 0; x0 < 16; x0 += 8) {  // 8 loads in flight, then the 8 sums
-          float v[8];
-#pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            const int r = 16 * blk + x0 + x;
-            const float gv = *reinterpret_cast<const float *>(sm + OFF_G + swz<4>(r, i));
-            v[x] = r < nvc ? fmaxf(gv, a.g_min) * LOG2E : 0.f;
-          }
-#pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            run += v[x];
-            *reinterpret_cast<float *>(sm + OFF_G + swz<4>(16 * blk + x0 + x, i)) = run;
-          }
-        }
-      }
-      float g0[4];
-#pragma unroll
-      for (int R = 0; R < 4; ++R) g0[R] = s_g0[R][i];
-      s_gC[i] = run;
-      s_GC[i] = ex2(run);
-      s_M[0 * D + i] = ex2(g0[1] - g0[0]);
-      s_M[1 * D + i] = ex2(g0[2] - g0[1]);
-      s_M[2 * D + i] = ex2(g0[3] - g0[2]);
-      s_M[3 * D + i] = ex2(g0[2] - g0[0]);
-      s_M[4 * D + i] = ex2(g0[3] - g0[1]);
-      s_M[5 * D + i] = ex2(g0[3] - g0[0]);
-    }
+    p1_run(a.beta, bos, eos, h, H, a.qk_l2norm, a.l2_eps, a.g_min, pad, cc, t, part);
   };
 
   const uint32_t ID_64 = idesc(2, 128, 64, 0, 0);
