@@ -743,11 +743,19 @@ __global__ void __launch_bounds__(NT, 1)
       {
         float xk[32], hi[32];
         tmem_ld32(tm + lane_off + TM_C + 32 * grp, xk);
+        // v[s][j] of rows s = 32 grp + x: the tile's 128-byte swizzle depends on x mod 8 only,
+        // so eight base addresses serve all 32 rows (row x at + 128 x)
+        const uint8_t *vb = sm + OFF_V + (j >> 6) * 8192 + ((2 * j) & 15) + 32 * grp * 128;
+        const int jc = (j & 63) >> 3;
+        const uint8_t *vp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) vp[k] = vb + ((jc ^ k) << 4);
         tmem_wait_ld();
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
           const int s = 32 * grp + x;
-          const float y = s < nv ? s_beta[s] * (bf_at(sm + OFF_V, s, j) - xk[x]) : 0.f;
+          const float vv = __bfloat162float(*reinterpret_cast<const bf16 *>(vp[x & 7] + 128 * x));
+          const float y = s < nv ? s_beta[s] * (vv - xk[x]) : 0.f;
           hi[x] = to_tf32(y);
           xk[x] = to_tf32(y - hi[x]);
         }
