@@ -567,6 +567,9 @@ def _mla_bench(dev, kda, inputs, hbm, rank):
             "tokens_per_s": B / (res["step"] * 1e-3),
             "roofline": {"kernel": "mla_decode_latent", "bound": "hbm", "achieved": gbs,
                          "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                         "traffic": _profiled_traffic(
+                             "mla_latent_B256_L4096.md",
+                             ["mla_decode.cu", "kda_tc_ptx.cuh", "kda_common.cuh"]),
                          "algorithmic_bytes_per_launch": b},
             "small_batch": small}
 
