@@ -143,9 +143,6 @@ __device__ __forceinline__ void f_row8(const uint8_t *tile, int row, int c8, flo
       ((uint32_t)(((2 * c8 + 1) & 7) ^ (row & 7)) << 4));
   o[0] = a.x, o[1] = a.y, o[2] = a.z, o[3] = a.w, o[4] = b.x, o[5] = b.y, o[6] = b.z, o[7] = b.w;
 }
-__device__ __forceinline__ float bf_at(const uint8_t *tile, int row, int ch) {
-  return __bfloat162float(*reinterpret_cast<const bf16 *>(tile + swz<2>(row, ch)));
-}
 // two fp32 -> packed bf16 pair (round to nearest even), low half = first
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
   uint32_t d;  // one conversion for the pair: the first source lands in the upper half
@@ -435,6 +432,7 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t ID_AP160 = idesc(1, 128, 160, 0, 0);
   const uint32_t ID_AP112 = idesc(1, 128, 112, 0, 0);
   uint32_t mma_par = 0;
+  int full_seen = 0;  // consumer thread 0: chunks whose T and P' it has waited for
   if (ok && nchunks > 0 && grp == 2) p1(0, tid - 256, 3);
   ok = sync();
 
@@ -1126,6 +1124,7 @@ __global__ void __launch_bounds__(NT, 1)
       if (tid == 0) {
         if (GATE) issue(1u << BAR_GT, c);  // V is consumed: the gate tile takes its place
         if (mbar_wait_cluster(bar(BAR_F0 + b), (uint32_t)((c >> 1) & 1))) {
+          full_seen = c + 1;
           fence_proxy_async();
           mmau_issue(off_lt(b));
         } else {
@@ -1162,6 +1161,11 @@ __global__ void __launch_bounds__(NT, 1)
     float *pA = reinterpret_cast<float *>(sm + OFF_X);
     float *pS = reinterpret_cast<float *>(sm + OFF_X + 20480);
     float *pT = reinterpret_cast<float *>(sm + OFF_V);
+    // the tf32 T of chunk c is staged here (by chunk parity: buffer b is rewritten only after
+    // the consumer has handed landing buffer b back, so its copy has been read) and sent by one
+    // bulk copy that completes on the consumer's FULL barrier: no cluster fence on the remote
+    // stores of 16 KB
+    auto off_st = [](int b) { return OFF_X + 32768u + 16384u * (uint32_t)b; };
     if (ok && nchunks > 0) {
       ap_operands((int)((eos - bos) < C ? (eos - bos) : C), NT);
       fence_proxy_async();
@@ -1186,12 +1190,13 @@ __global__ void __launch_bounds__(NT, 1)
       fence_cluster();
       fence_proxy_async();
       if (!(ok = sync())) break;
-      if (grp == 2) {  // FULL as soon as T has landed: the consumer does not wait for P1 below
-        inverse(peer + off_lt(b), pA, pT, pS);
-        fence_cluster();
+      if (grp == 2) {  // FULL once T has landed: the consumer does not wait for P1 below
+        // P' is visible in the consumer (cluster fence + barrier above): arrive, and expect T
+        if (tid == 256) mbar_arrive_expect_tx_remote(bar(BAR_F0 + b), 0, 16384);
+        inverse(sm + off_st(b), pA, pT, pS);
         fence_proxy_async();
         asm volatile("bar.sync 3, 128;" ::: "memory");
-        if (tid == 256) mbar_arrive_remote(bar(BAR_F0 + b), 0);  // T and P' of chunk c landed
+        if (tid == 256) bulk_copy_to_peer(sb + off_lt(b), sb + off_st(b), 16384, bar(BAR_F0 + b), 0);
       } else if (more) {  // P1 of chunk c + 1 on groups 0 and 1
         p1(c + 1, tid & 127, grp == 0 ? 2 : 1);  // prefix sums | beta and norms
         asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -1230,6 +1235,11 @@ __global__ void __launch_bounds__(NT, 1)
     // wait returns at once when that phase has completed
     for (int b = 0; b < NBAR; ++b)
       if (s_pend & (1u << b)) mbar_wait(bar(b), s_ppar[b]);
+    // a consumer that stops early: the producer's bulk copies of T for the next two chunks
+    // may be in flight into this CTA's shared memory; let them land (bounded) before it goes
+    if (PAIR && !producer)
+      for (int k = full_seen; k < full_seen + 2 && k < nchunks; ++k)
+        mbar_wait_cluster(bar(BAR_F0 + (k & 1)), (uint32_t)((k >> 1) & 1));
   }
   tc_fence_before();
   __syncthreads();

@@ -79,6 +79,29 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank) 
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rb)
                : "memory");
 }
+// arrive on CTA `rank`'s mbarrier (this CTA's offset `bar`) and raise its expected
+// transaction bytes by tx: its phase completes once tx more bytes have landed
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t bar, uint32_t rank,
+                                                             uint32_t tx) {
+  uint32_t rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(bar), "r"(rank));
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(rb),
+               "r"(tx)
+               : "memory");
+}
+// bulk copy of `bytes` (multiple of 16) from this CTA's shared memory at `src` to CTA
+// `rank`'s shared memory at this CTA's offset `dst`, completing on that CTA's mbarrier at
+// this CTA's offset `bar` (complete_tx); addresses 16-byte aligned
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar, uint32_t rank) {
+  uint32_t rd, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rd) : "r"(dst), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(bar), "r"(rank));
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(rd),
+      "r"(src), "r"(bytes), "r"(rb)
+      : "memory");
+}
 __device__ __forceinline__ void fence_cluster() {
   asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }
