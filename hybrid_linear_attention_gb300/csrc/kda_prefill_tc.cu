@@ -212,7 +212,7 @@ struct Maps {
 };
 
 // Per-CTA shared state that P1 (out of line, below) shares with the kernel
-__shared__ float s_beta[C], s_rq[C], s_rk[C], s_pd[2][C];  // s_pd by chunk parity
+__shared__ float s_beta[2][C], s_rq[C], s_rk[C], s_pd[2][C];  // beta, s_pd by chunk parity
 __shared__ __align__(16) float s_g0[4][D];  // log2-retention just before each 16-block
 __shared__ __align__(16) float s_gC[D];     // log2-retention at the chunk's last token
 __shared__ float s_GC[D];                   // Gamma_C
@@ -268,7 +268,7 @@ __device__ __noinline__ void p1_run(const float *beta, int64_t bos, int64_t eos,
       const float rk = r < nvc ? (l2norm ? rsqrtf(sk + l2_eps) : 1.f) : 0.f;
       s_rq[r] = rq, s_rk[r] = rk, s_pd[pc][r] = sqk * rq * rk;
     }
-    if (t < C) s_beta[t] = bv;
+    if (t < C) s_beta[pc][t] = bv;
   }
   if (part & 2) {
     const int i = t;
@@ -609,7 +609,7 @@ __global__ void __launch_bounds__(NT, 1)
                sm + OFF_X + kmaj_f32<128>(64 + r, 8 * c8 + 4), oq8);
     }
   };
-  auto extract = [&](int nv, uint8_t *pbase, float *Am) {
+  auto extract = [&](int nv, uint8_t *pbase, float *Am, uint32_t par) {
     // ---- P3: A (beta-scaled, strict lower, fp32 rows of LDA) and P' (strict lower, tf32,
     //      K-major) from the product, one tensor-memory lane per row (lanes 0-63: A, 64-127:
     //      P), in 16-column pieces that each hold one block R and 16 consecutive s; zeros in
@@ -618,11 +618,12 @@ __global__ void __launch_bounds__(NT, 1)
       const int L = j, r = L & 63, R = r >> 4;
       const bool isp = L >= 64;
       // pieces of this warp: rows 0-31 (R = 0, 1): piece 3 + grp; rows 32-63 (R = 2, 3):
-      // group 0 pieces 0-2, group 1 pieces 6-7, group 2 pieces 8-9
+      // group 2 pieces 0-2 (it inverts next, after every piece is in), group 0 pieces 6-7,
+      // group 1 pieces 8-9
       const bool lo_rows = (quarter & 1) == 0;
-      const int p0 = lo_rows ? 3 + grp : (grp == 0 ? 0 : 4 + 2 * grp);
-      const int np = lo_rows ? 1 : (grp == 0 ? 3 : 2);
-      const float br = s_beta[r];
+      const int p0 = lo_rows ? 3 + grp : (grp == 2 ? 0 : 6 + 2 * grp);
+      const int np = lo_rows ? 1 : (grp == 2 ? 3 : 2);
+      const float br = s_beta[par][r];
       for (int pc = p0; pc < p0 + np; ++pc) {
         float v[16];
         tmem_ld16(tm + lane_off + TM_D + 16 * pc, v);
@@ -753,7 +754,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int x = 0; x < 32; ++x) {
           const int s = 32 * grp + x;
           const float vv = __bfloat162float(*reinterpret_cast<const bf16 *>(vp[x & 7] + 128 * x));
-          const float y = s < nv ? s_beta[s] * (vv - xk[x]) : 0.f;
+          const float y = s < nv ? s_beta[par][s] * (vv - xk[x]) : 0.f;
           hi[x] = to_tf32(y);
           xk[x] = to_tf32(y - hi[x]);
         }
@@ -1053,7 +1054,7 @@ __global__ void __launch_bounds__(NT, 1)
       wait(BAR_MMA, mma_par);
       mma_par ^= 1;
       tc_fence_after();
-      extract(nv, sm + OFF_P, reinterpret_cast<float *>(sm + OFF_A));
+      extract(nv, sm + OFF_P, reinterpret_cast<float *>(sm + OFF_A), par);
       fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0) {
@@ -1186,21 +1187,25 @@ __global__ void __launch_bounds__(NT, 1)
       if (c >= 2 && !mbar_wait_cluster(bar(BAR_E0 + b), (uint32_t)(((c - 2) >> 1) & 1)))
         s_abort = 1;
       if (!(ok = sync())) break;
-      extract(nv, peer + off_lp(b), pA);
+      extract(nv, peer + off_lp(b), pA, (uint32_t)(c & 1));
       fence_cluster();
       fence_proxy_async();
-      if (!(ok = sync())) break;
+      // only the inverting group waits for every warp's rows; groups 0 and 1 go on to P1
       if (grp == 2) {  // FULL once T has landed: the consumer does not wait for P1 below
+        asm volatile("bar.sync 6, 384;" ::: "memory");
         // P' is visible in the consumer (cluster fence + barrier above): arrive, and expect T
         if (tid == 256) mbar_arrive_expect_tx_remote(bar(BAR_F0 + b), 0, 16384);
         inverse(sm + off_st(b), pA, pT, pS);
         fence_proxy_async();
         asm volatile("bar.sync 3, 128;" ::: "memory");
         if (tid == 256) bulk_copy_to_peer(sb + off_lt(b), sb + off_st(b), 16384, bar(BAR_F0 + b), 0);
-      } else if (more) {  // P1 of chunk c + 1 on groups 0 and 1
-        p1(c + 1, tid & 127, grp == 0 ? 2 : 1);  // prefix sums | beta and norms
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        asm volatile("bar.arrive 5, 384;" ::: "memory");  // P1 done: group 2 may join
+      } else {
+        asm volatile("bar.arrive 6, 384;" ::: "memory");
+        if (more) {  // P1 of chunk c + 1 on groups 0 and 1
+          p1(c + 1, tid & 127, grp == 0 ? 2 : 1);  // prefix sums | beta and norms
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+          asm volatile("bar.arrive 5, 384;" ::: "memory");  // P1 done: group 2 may join
+        }
       }
       if (more) {  // the operands of chunk c + 1 on all three groups (group 2 after the inverse)
         if (grp == 2) asm volatile("bar.sync 5, 384;" ::: "memory");
