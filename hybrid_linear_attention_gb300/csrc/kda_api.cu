@@ -69,6 +69,12 @@ kda::RecArgs base_args(const kda_params *p) {
 
 }  // namespace
 
+namespace kda {
+// for the other host-side entry points of the library (kda_host_stream.cu)
+kda_status validate_params(const kda_params *p) { return check_params(p); }
+void note_launches(int n) { g_launches += (uint64_t)n; }
+}  // namespace kda
+
 extern "C" {
 
 void kda_params_default(kda_params *p) {

@@ -26,7 +26,7 @@ _TORCH_OF = {KDA_F32: torch.float32, KDA_BF16: torch.bfloat16}
 EXPORTS = (
     "kda_params_default", "kda_status_string", "kda_state_bytes", "kda_prefill_workspace_size",
     "kda_prologue", "kda_prefill", "kda_prefill_fp8", "kda_prefill_checkpointed",
-    "kda_conv_tail_checkpoints",
+    "kda_conv_tail_checkpoints", "kda_prefill_host_workspace_size", "kda_prefill_host",
     "kda_decode_step", "kda_conv_state_update",
     "kda_decode_step_fused", "kda_decode_step_fused_fp8", "kda_decode_multi", "kda_state_accept", "kda_check_device_error",
     "kda_launch_count", "kda_wait_probe", "mla_decode_workspace_size", "mla_decode_latent",
@@ -90,6 +90,9 @@ def load():
                                                 _vp, _sz, _vp]),
             "kda_conv_tail_checkpoints": (_i32, [_P, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _i32,
                                                  _vp, _vp]),
+            "kda_prefill_host_workspace_size": (_sz, [_P, _i32, _i64, _i32]),
+            "kda_prefill_host": (_i32, [_P, _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp,
+                                        _vp, _vp, _vp, _vp, _sz, _i64, _vp]),
             "kda_decode_step": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _vp,
                                        _vp, _vp, _vp]),
             "kda_conv_state_update": (_i32, [_P, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _vp,
@@ -161,6 +164,21 @@ def _ptr(t, dtype=None, name="tensor"):
     return t.data_ptr()
 
 
+def _hptr(t, dtype=None, name="tensor"):
+    """Host pointer of a CPU tensor (page-locked memory lets the library overlap its copies)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch tensor or None")
+    if t.is_cuda:
+        raise ValueError(f"{name}: must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
 def _stream(stream):
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
@@ -212,6 +230,31 @@ def kda_prefill(p, q, k, v, g, beta, cu_seqlens, out, *, init_state=None, final_
         _ptr(final_state, sd, "final_state"), _ptr(workspace, None, "workspace"), ws_bytes,
         _stream(stream))
     _check(st, "kda_prefill")
+
+
+def kda_prefill_host_workspace_size(p, n_seqs, segment_tokens, with_gate=False):
+    return int(load().kda_prefill_host_workspace_size(ctypes.byref(p), int(n_seqs),
+                                                       int(segment_tokens), 1 if with_gate else 0))
+
+
+def kda_prefill_host(p, x_raw, conv_w, conv_state, cu_seqlens, beta_logit, g_raw, out, *,
+                     workspace, segment_tokens=512, init_state=None, final_state=None,
+                     gate_logit=None, norm_w=None, stream=None):
+    """Prologue + prefill of a packed batch in host memory, streamed through the GPU in
+    segments: x_raw, conv_state (in/out or None), cu_seqlens (int32), beta_logit, g_raw,
+    init_state, gate_logit, out and final_state are CPU tensors (pinned for overlap); conv_w,
+    norm_w and the uint8 workspace are CUDA tensors.  The outputs are in host memory once
+    `stream` (default: the current stream) has been synchronised."""
+    io = p.io_torch
+    st = load().kda_prefill_host(
+        ctypes.byref(p), _hptr(x_raw, io, "x_raw"), _ptr(conv_w, io, "conv_w"),
+        _hptr(conv_state, io, "conv_state"), _hptr(cu_seqlens, torch.int32, "cu_seqlens"),
+        cu_seqlens.numel() - 1, x_raw.shape[0], _hptr(beta_logit, torch.float32, "beta_logit"),
+        _hptr(g_raw, torch.float32, "g_raw"), _hptr(init_state, torch.float32, "init_state"),
+        _hptr(gate_logit, io, "gate_logit"), _ptr(norm_w, torch.float32, "norm_w"),
+        _hptr(out, io, "out"), _hptr(final_state, torch.float32, "final_state"),
+        *_ws(workspace), int(segment_tokens), _stream(stream))
+    _check(st, "kda_prefill_host")
 
 
 def kda_prefill_fp8(p, q, k, v, g, beta, cu_seqlens, out_q, out_scale, *, init_state=None,

@@ -322,6 +322,67 @@ kda_status kda_state_accept(const kda_params* p, const void* step_states, int n_
                             const int32_t* accept_len, void* state, int n_slots,
                             const int32_t* slot_idx, cudaStream_t stream);
 
+/*
+ * kda_prefill_host_workspace_size -- device bytes kda_prefill_host needs for n_seqs sequences
+ * cut into segments of at most segment_tokens rows (a positive multiple of 64, at most 2^24),
+ * with gate logits when with_gate is nonzero: two sets of segment buffers (raw projections,
+ * log-retention, write-strength logits, gate logits, output), one set of convolved q, k, v
+ * and beta, and every sequence's carried fp32 state and conv tail: at H = 64, d = 128 with
+ * bf16 I/O about 241 KB per segment row (273 KB with gate logits) plus 4.3 MB per sequence.
+ * Returns 0 for invalid arguments.
+ */
+size_t kda_prefill_host_workspace_size(const kda_params* p, int n_seqs, int64_t segment_tokens,
+                                       int with_gate);
+
+/*
+ * kda_prefill_host -- the prefill hot path (kda_prologue: short convolution, SiLU and
+ * beta = sigmoid(logit); then kda_prefill: q/k L2 norm, the clamp of g at p->g_min, the
+ * chunked recurrence and the optional output norm and gate) for a packed batch whose inputs
+ * and outputs are in HOST memory.  The batch is streamed through the GPU in segments of at
+ * most segment_tokens rows: while the kernels run on one segment, the next segment's inputs
+ * are copied in and the previous segment's output is copied out.  Every inner segment
+ * boundary falls on a chunk edge (a multiple of 64 tokens from the start of the sequence it
+ * cuts), and the state and conv tail of a cut sequence are carried on the device to the next
+ * segment -- the way a serving engine runs a long prompt's prefill in pieces ("Ling-3.1-flash:
+ * What 63 Linear-Attention Layers Do to the KV Budget", section "Where the hybrid makes
+ * serving harder": a recurrent state summarises everything before it).  The results are the
+ * same bits as kda_prologue (conv_state in place, l2norm_qk = 0, no g output) followed by one
+ * kda_prefill over the whole batch on device copies of these buffers, when both runs choose
+ * the same kernel form (as they do for batches of up to SM count / (2 H) sequences).
+ *
+ * HOST pointers (page-locked memory lets the copies overlap the kernels; pageable memory
+ * works but serialises them):
+ *   x_raw       [T_tot, 3*H*d] io_dtype raw q|k|v projections, as in kda_prologue.
+ *   conv_state  [n_seqs, 3, 3*H*d] io_dtype, in/out (the conv tails, updated as kda_prologue
+ *               updates them), or NULL: zeros in, nothing written back.
+ *   cu_seqlens  [n_seqs + 1] int32: 0, non-decreasing, ending at total_tokens (checked here,
+ *               KDA_ERR_INVALID_ARG otherwise).
+ *   beta_logit  [T_tot, H] fp32 write-strength logits; g_raw [T_tot, H, d] fp32 raw
+ *               log-retention (clamped inside).
+ *   init_state  [n_seqs, H, d, d] fp32 or NULL (zeros).
+ *   gate_logit  [T_tot, H, d] io_dtype or NULL (no output norm/gate).
+ *   out         [T_tot, H, d] io_dtype.
+ *   final_state [n_seqs, H, d, d] fp32 or NULL; may alias init_state.
+ * DEVICE pointers: conv_w [3*H*d, 4] io_dtype and norm_w [d] fp32 or NULL (layer weights,
+ * resident on the GPU); workspace: kda_prefill_host_workspace_size() bytes, 256-byte aligned,
+ * owned by the caller and not to be touched until the call's work has finished.
+ *
+ * Only fp32 state storage (p->state_dtype == KDA_F32; KDA_ERR_UNSUPPORTED otherwise): a bf16
+ * state would be rounded at every segment boundary.  The call enqueues its work and returns;
+ * the kernels run on `stream`, the copies on three copy streams of the library (created on the
+ * first call on each device and kept until the process exits) that start after the work
+ * already on `stream`, and `stream` is made to wait for all of it: synchronising `stream`
+ * (or kda_check_device_error(stream)) means the outputs are in host memory.  Calls are
+ * serialised per device while they enqueue.  Not meant for CUDA-graph capture.  Arguments are
+ * checked on the host before any CUDA call.
+ */
+kda_status kda_prefill_host(const kda_params* p, const void* x_raw, const void* conv_w,
+                            void* conv_state, const int32_t* cu_seqlens, int n_seqs,
+                            int64_t total_tokens, const float* beta_logit, const float* g_raw,
+                            const void* init_state, const void* gate_logit,
+                            const float* norm_w, void* out, void* final_state, void* workspace,
+                            size_t ws_bytes, int64_t segment_tokens, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the library's sticky device error flag
  * (set when a bounded device wait ran out, a device-side index was out of range, or a
  * sequence's offsets fell outside the token rows).  Returns KDA_OK, KDA_ERR_TIMEOUT,

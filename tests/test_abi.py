@@ -207,3 +207,43 @@ def test_mla_calls_reject_bad_arguments_on_host(lib):
 def test_wait_probe_rejects_bad_limits_on_host(lib):
     assert lib.kda_wait_probe(0, None) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_wait_probe(1 << 31, None) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_host_prefill_workspace_size(lib):
+    p = kda.params()
+    H, d = 64, 128
+    per_row = 2 * (3 * H * d * 2 + H * d * 4 + H * 4 + H * d * 2) + 3 * H * d * 2 + H * 4
+    per_seq = H * d * d * 4 + 3 * 3 * H * d * 2
+    ws = kda.kda_prefill_host_workspace_size(p, 1, 512)
+    assert 512 * per_row + per_seq <= ws <= 512 * per_row + per_seq + 16 * 256
+    gated = kda.kda_prefill_host_workspace_size(p, 1, 512, with_gate=True)
+    assert gated - ws == 2 * 512 * H * d * 2
+    assert kda.kda_prefill_host_workspace_size(p, 1, 100) == 0       # not a chunk multiple
+    assert kda.kda_prefill_host_workspace_size(p, 0, 512) == 0
+    assert kda.kda_prefill_host_workspace_size(kda.params(d=64), 1, 512) == 0
+
+
+def test_host_prefill_rejects_bad_arguments_before_any_cuda_call(lib):
+    p = kda.params(H=2)
+    P = ctypes.byref(p)
+    ws_need = kda.kda_prefill_host_workspace_size(p, 2, 64)
+
+    def call(pp=P, cu=(0, 64, 100), T=100, seg=64, ws=4096, wsb=None, x=16, out=16, w=16):
+        arr = (ctypes.c_int32 * len(cu))(*cu)
+        return lib.kda_prefill_host(pp, x, w, None, arr, len(cu) - 1, T, 16, 16, None, None,
+                                    None, out, None, ws, ws_need if wsb is None else wsb,
+                                    seg, None)
+
+    assert call(cu=(1, 64, 100)) == kda.KDA_ERR_INVALID_ARG          # does not start at 0
+    assert call(cu=(0, 80, 64)) == kda.KDA_ERR_INVALID_ARG           # runs backwards
+    assert call(cu=(0, 64, 99)) == kda.KDA_ERR_INVALID_ARG           # does not end at T
+    assert call(seg=96) == kda.KDA_ERR_INVALID_ARG                   # not a chunk multiple
+    assert call(seg=0) == kda.KDA_ERR_INVALID_ARG
+    assert call(x=None) == kda.KDA_ERR_INVALID_ARG
+    assert call(out=None) == kda.KDA_ERR_INVALID_ARG
+    assert call(w=24) == kda.KDA_ERR_INVALID_ARG                     # misaligned weights
+    assert call(wsb=ws_need - 1) == kda.KDA_ERR_WORKSPACE
+    assert call(ws=4096 + 16) == kda.KDA_ERR_INVALID_ARG             # workspace not 256-aligned
+    assert call(pp=None) == kda.KDA_ERR_INVALID_ARG
+    pb = kda.params(H=2, state_dtype=torch.bfloat16)
+    assert call(pp=ctypes.byref(pb)) == kda.KDA_ERR_UNSUPPORTED      # fp32 state only
