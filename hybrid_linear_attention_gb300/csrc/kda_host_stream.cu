@@ -130,19 +130,26 @@ int seq_containing(const int32_t *cu, int n_seqs, int64_t r) {
 }
 
 // Cuts [0, T) into segments of at most S rows whose inner boundaries lie on the chunk grid of
-// the sequence they fall in; each segment but the last holds more than S - 64 rows.
+// the sequence they fall in.  The last 2S rows are cut in halves (S, S/2, ..., 64 rows), so
+// that little of the work is left once the last inputs have arrived: the kernels and the
+// copy-out of the last segment are all that does not overlap the copies in.
 std::vector<Seg> plan(const int32_t *cu, int n_seqs, int64_t T, int64_t S) {
   std::vector<Seg> segs;
   int64_t r0 = 0;
   while (r0 < T) {
-    int64_t r1 = r0 + S;
+    int64_t want = S;  // a multiple of the chunk, at least one chunk
+    if (T - r0 <= 2 * S) {
+      want = (T - r0) / 2 / kChunk * kChunk;
+      if (want < kChunk) want = kChunk;
+    }
+    int64_t r1 = r0 + want;
     if (r1 >= T) {
       r1 = T;
     } else {
       const int n = seq_containing(cu, n_seqs, r1);
       // down to the chunk grid of sequence n.  Still > r0: if n also holds r0, r0 is on its
-      // grid (a sequence start or an earlier boundary) and S is a multiple of the chunk, so
-      // nothing is cut; otherwise r1 >= cu[n] > r0.
+      // grid (a sequence start or an earlier boundary) and `want` is a multiple of the chunk,
+      // so nothing is cut; otherwise r1 >= cu[n] > r0.
       r1 = cu[n] + (r1 - cu[n]) / kChunk * kChunk;
     }
     const int a = seq_containing(cu, n_seqs, r0), b = seq_containing(cu, n_seqs, r1 - 1);

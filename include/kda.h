@@ -339,7 +339,8 @@ size_t kda_prefill_host_workspace_size(const kda_params* p, int n_seqs, int64_t 
  * beta = sigmoid(logit); then kda_prefill: q/k L2 norm, the clamp of g at p->g_min, the
  * chunked recurrence and the optional output norm and gate) for a packed batch whose inputs
  * and outputs are in HOST memory.  The batch is streamed through the GPU in segments of at
- * most segment_tokens rows: while the kernels run on one segment, the next segment's inputs
+ * most segment_tokens rows (the last ones halving down to 64 rows, so that little work is left
+ * once the last inputs are in): while the kernels run on one segment, the next segment's inputs
  * are copied in and the previous segment's output is copied out.  Every inner segment
  * boundary falls on a chunk edge (a multiple of 64 tokens from the start of the sequence it
  * cuts), and the state and conv tail of a cut sequence are carried on the device to the next
