@@ -21,7 +21,6 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
-#include <vector>
 
 namespace kda {
 kda_status validate_params(const kda_params *p);
@@ -130,13 +129,18 @@ int seq_containing(const int32_t *cu, int n_seqs, int64_t r) {
 }
 
 // Cuts [0, T) into segments of at most S rows whose inner boundaries lie on the chunk grid of
-// the sequence they fall in.  The last 2S rows are cut in halves (S, S/2, ..., 64 rows), so
-// that little of the work is left once the last inputs have arrived: the kernels and the
-// copy-out of the last segment are all that does not overlap the copies in.
-std::vector<Seg> plan(const int32_t *cu, int n_seqs, int64_t T, int64_t S) {
-  std::vector<Seg> segs;
-  int64_t r0 = 0;
-  while (r0 < T) {
+// the sequence they fall in, one segment per call of next() (nothing is stored: a long batch
+// cut into short segments costs no host memory).  The last 2S rows are cut in halves (S,
+// S/2, ..., 64 rows), so that little of the work is left once the last inputs have arrived:
+// the kernels and the copy-out of the last segment are all that does not overlap the copies
+// in.
+struct Planner {
+  const int32_t *cu;
+  int n_seqs;
+  int64_t T, S, r0 = 0;
+
+  bool next(Seg *sg) {
+    if (r0 >= T) return false;
     int64_t want = S;  // a multiple of the chunk, at least one chunk
     if (T - r0 <= 2 * S) {
       want = (T - r0) / 2 / kChunk * kChunk;
@@ -153,11 +157,11 @@ std::vector<Seg> plan(const int32_t *cu, int n_seqs, int64_t T, int64_t S) {
       r1 = cu[n] + (r1 - cu[n]) / kChunk * kChunk;
     }
     const int a = seq_containing(cu, n_seqs, r0), b = seq_containing(cu, n_seqs, r1 - 1);
-    segs.push_back(Seg{r0, r1, a, b - a + 1});
+    *sg = Seg{r0, r1, a, b - a + 1};
     r0 = r1;
+    return true;
   }
-  return segs;
-}
+};
 
 bool aligned(const void *ptr, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0;
@@ -203,7 +207,7 @@ kda_status kda_prefill_host(const kda_params *p, const void *x_raw, const void *
   const size_t e = p->io_dtype == KDA_BF16 ? 2 : 4, H = (size_t)p->H, d = (size_t)p->d_k;
   const size_t x_row = 3 * H * d * e, g_row = H * d * 4, bl_row = H * 4, o_row = H * d * e;
   const size_t st_seq = H * d * d * 4, conv_seq = 3 * 3 * H * d * e;
-  const std::vector<Seg> segs = plan(cu_seqlens, n_seqs, total_tokens, segment_tokens);
+  Planner planner{cu_seqlens, n_seqs, total_tokens, segment_tokens};
 
   // ---- enqueue
   int dev = 0;
@@ -237,8 +241,9 @@ kda_status kda_prefill_host(const kda_params *p, const void *x_raw, const void *
   chk(cudaEventRecord(pp->carry_in, pp->in_g));
 
   int fills = 0;
-  for (size_t i = 0; i < segs.size() && ok; ++i) {
-    const Seg &sg = segs[i];
+  kda_status fail = KDA_OK;  // a launch that failed part-way
+  Seg sg;
+  for (int64_t i = 0; ok && fail == KDA_OK && planner.next(&sg); ++i) {
     const int s = (int)(i & 1);
     const size_t rows = (size_t)(sg.r1 - sg.r0), r0 = (size_t)sg.r0;
     // inputs of segment i into slot s, once segment i - 2 has used that slot
@@ -276,14 +281,20 @@ kda_status kda_prefill_host(const kda_params *p, const void *x_raw, const void *
                       reinterpret_cast<const float *>(ws + L.bl[s]), nullptr, ws + L.q,
                       ws + L.k, ws + L.v, reinterpret_cast<float *>(ws + L.beta), nullptr,
                       stream);
-    if (st != KDA_OK) return st;
+    if (st != KDA_OK) {
+      fail = st;
+      break;
+    }
     if (i >= 2) chk(cudaStreamWaitEvent(stream, pp->out_free[s], 0));  // output slot copied out
     st = kda_prefill(p, ws + L.q, ws + L.k, ws + L.v,
                      reinterpret_cast<const float *>(ws + L.g[s]),
                      reinterpret_cast<const float *>(ws + L.beta), state_c, cu_dev, sg.count,
                      (int64_t)rows, with_gate ? ws + L.gate[s] : nullptr, norm_w, ws + L.out[s],
                      state_c, nullptr, 0, stream);
-    if (st != KDA_OK) return st;
+    if (st != KDA_OK) {
+      fail = st;
+      break;
+    }
     chk(cudaEventRecord(pp->used[s], stream));
 
     // outputs of segment i back to the host
@@ -293,6 +304,17 @@ kda_status kda_prefill_host(const kda_params *p, const void *x_raw, const void *
     chk(cudaEventRecord(pp->out_free[s], pp->out));
   }
   kda::note_launches(fills);
+  if (!ok || fail != KDA_OK) {
+    // nothing more is enqueued, but `stream` still waits for the copies already on their way,
+    // so that none of them runs on once the caller has synchronised it
+    cudaEventRecord(pp->in_x_done[0], pp->in_x);
+    cudaEventRecord(pp->in_g_done[0], pp->in_g);
+    cudaEventRecord(pp->end, pp->out);
+    cudaStreamWaitEvent(stream, pp->in_x_done[0], 0);
+    cudaStreamWaitEvent(stream, pp->in_g_done[0], 0);
+    cudaStreamWaitEvent(stream, pp->end, 0);
+    return fail != KDA_OK ? fail : KDA_ERR_CUDA;
+  }
   // final states and conv tails (after the last segment's kernels, which the output stream
   // has waited for; with no tokens, after the carries came in)
   chk(cudaStreamWaitEvent(pp->out, pp->carry_in, 0));

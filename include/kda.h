@@ -375,7 +375,9 @@ size_t kda_prefill_host_workspace_size(const kda_params* p, int n_seqs, int64_t 
  * already on `stream`, and `stream` is made to wait for all of it: synchronising `stream`
  * (or kda_check_device_error(stream)) means the outputs are in host memory.  Calls are
  * serialised per device while they enqueue.  Not meant for CUDA-graph capture.  Arguments are
- * checked on the host before any CUDA call.
+ * checked on the host before any CUDA call.  A launch or copy that fails part-way returns its
+ * error (KDA_ERR_CUDA) after making `stream` wait for the copies already issued; the outputs
+ * are then undefined.
  */
 kda_status kda_prefill_host(const kda_params* p, const void* x_raw, const void* conv_w,
                             void* conv_state, const int32_t* cu_seqlens, int n_seqs,
