@@ -10,7 +10,8 @@ neither a clamped copy of g nor normalised q, k.
 Also reported: the prefill kernel alone, the decode workload (256 sequences x 1 token,
 H=64, d=128, fp32 state pool ~N(0,0.02), fused conv + decode, 100 consecutive steps) as
 state GB/s, the roofline of the dominant kernel against MEASURED_PEAKS.json, an end-to-end
-number through the same API with host buffers, and the oracle timed on the host cores.
+number through the host-buffer call kda_prefill_host (copies in and out inside the timed
+region), and the oracle timed on the host cores.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -378,7 +379,7 @@ def run_ours(args):
     kda.kda_check_device_error()
     pf8 = _max_over_ranks(dist, sum(pf8_ms) / len(pf8_ms))
 
-    # ---- end to end through the same API with host buffers ---------------------------
+    # ---- end to end through the host-buffer call (kda_prefill_host) -----------------
     e2e_line = _e2e(wl, flush, args, dist) if not args.no_e2e else None
 
     # ---- decode: 256 sequences x 100 fused steps --------------------------------------
