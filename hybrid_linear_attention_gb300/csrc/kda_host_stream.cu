@@ -179,6 +179,26 @@ size_t kda_prefill_host_workspace_size(const kda_params *p, int n_seqs, int64_t 
   return layout(p, n_seqs, segment_tokens, with_gate != 0).total;
 }
 
+int64_t kda_prefill_host_plan(const int32_t *cu_seqlens, int n_seqs, int64_t total_tokens,
+                              int64_t segment_tokens, int64_t *bounds, int64_t max_segments) {
+  if (!cu_seqlens || n_seqs < 1 || n_seqs > 65535 || total_tokens < 0 ||
+      total_tokens > INT32_MAX || segment_tokens < kChunk || segment_tokens % kChunk != 0 ||
+      segment_tokens > kMaxSegment || max_segments < 0 || (max_segments > 0 && !bounds))
+    return -1;
+  if (cu_seqlens[0] != 0 || (int64_t)cu_seqlens[n_seqs] != total_tokens) return -1;
+  for (int n = 0; n < n_seqs; ++n)
+    if (cu_seqlens[n + 1] < cu_seqlens[n]) return -1;
+  Planner planner{cu_seqlens, n_seqs, total_tokens, segment_tokens};
+  Seg sg;
+  int64_t k = 0;
+  if (max_segments > 0) bounds[0] = 0;
+  while (planner.next(&sg)) {
+    ++k;
+    if (k <= max_segments) bounds[k] = sg.r1;
+  }
+  return k;
+}
+
 kda_status kda_prefill_host(const kda_params *p, const void *x_raw, const void *conv_w,
                             void *conv_state, const int32_t *cu_seqlens, int n_seqs,
                             int64_t total_tokens, const float *beta_logit, const float *g_raw,

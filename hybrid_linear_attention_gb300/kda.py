@@ -27,6 +27,7 @@ EXPORTS = (
     "kda_params_default", "kda_status_string", "kda_state_bytes", "kda_prefill_workspace_size",
     "kda_prologue", "kda_prefill", "kda_prefill_fp8", "kda_prefill_checkpointed",
     "kda_conv_tail_checkpoints", "kda_prefill_host_workspace_size", "kda_prefill_host",
+    "kda_prefill_host_plan",
     "kda_decode_step", "kda_conv_state_update",
     "kda_decode_step_fused", "kda_decode_step_fused_fp8", "kda_decode_multi", "kda_state_accept", "kda_check_device_error",
     "kda_launch_count", "kda_wait_probe", "mla_decode_workspace_size", "mla_decode_latent",
@@ -93,6 +94,7 @@ def load():
             "kda_prefill_host_workspace_size": (_sz, [_P, _i32, _i64, _i32]),
             "kda_prefill_host": (_i32, [_P, _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp,
                                         _vp, _vp, _vp, _vp, _sz, _i64, _vp]),
+            "kda_prefill_host_plan": (_i64, [_vp, _i32, _i64, _i64, _vp, _i64]),
             "kda_decode_step": (_i32, [_P, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _vp,
                                        _vp, _vp, _vp]),
             "kda_conv_state_update": (_i32, [_P, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _vp,
@@ -235,6 +237,21 @@ def kda_prefill(p, q, k, v, g, beta, cu_seqlens, out, *, init_state=None, final_
 def kda_prefill_host_workspace_size(p, n_seqs, segment_tokens, with_gate=False):
     return int(load().kda_prefill_host_workspace_size(ctypes.byref(p), int(n_seqs),
                                                        int(segment_tokens), 1 if with_gate else 0))
+
+
+def kda_prefill_host_plan(cu_seqlens, segment_tokens):
+    """Row boundaries of the segments kda_prefill_host cuts a batch into (cu_seqlens: a CPU
+    int32 tensor); a list [0, b_1, ..., total_tokens]."""
+    cu = cu_seqlens.to(torch.int32).contiguous()
+    n, T = cu.numel() - 1, int(cu[-1])
+    k = load().kda_prefill_host_plan(_hptr(cu, torch.int32, "cu_seqlens"), n, T,
+                                     int(segment_tokens), None, 0)
+    if k < 0:
+        raise KdaError(KDA_ERR_INVALID_ARG, "kda_prefill_host_plan")
+    bounds = (ctypes.c_int64 * (k + 1))()
+    load().kda_prefill_host_plan(_hptr(cu, torch.int32, "cu_seqlens"), n, T,
+                                 int(segment_tokens), bounds, k)
+    return [int(b) for b in bounds] if k > 0 else [0]
 
 
 def kda_prefill_host(p, x_raw, conv_w, conv_state, cu_seqlens, beta_logit, g_raw, out, *,

@@ -386,6 +386,18 @@ kda_status kda_prefill_host(const kda_params* p, const void* x_raw, const void* 
                             const float* norm_w, void* out, void* final_state, void* workspace,
                             size_t ws_bytes, int64_t segment_tokens, cudaStream_t stream);
 
+/*
+ * kda_prefill_host_plan -- the segments kda_prefill_host cuts a batch into (host only, no CUDA
+ * call): with cu_seqlens a HOST array as in kda_prefill_host, writes the row boundaries
+ * 0 = b_0 < b_1 < ... < b_k = total_tokens to bounds[0 .. min(k, max_segments)] and returns
+ * k, the number of segments (0 for an empty batch); -1 for invalid arguments (the checks of
+ * kda_prefill_host).  Every segment holds at most segment_tokens rows; every inner boundary
+ * lies a multiple of 64 tokens after the start of the sequence it falls in; the last
+ * 2 * segment_tokens rows are cut in halves down to 64 rows.
+ */
+int64_t kda_prefill_host_plan(const int32_t* cu_seqlens, int n_seqs, int64_t total_tokens,
+                              int64_t segment_tokens, int64_t* bounds, int64_t max_segments);
+
 /* Synchronises `stream`, then reads and clears the library's sticky device error flag
  * (set when a bounded device wait ran out, a device-side index was out of range, or a
  * sequence's offsets fell outside the token rows).  Returns KDA_OK, KDA_ERR_TIMEOUT,
