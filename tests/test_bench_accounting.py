@@ -1,0 +1,48 @@
+"""The roofline accounting of bench.py (no GPU): the algorithmic bytes and FLOPs per launch
+that every reported fraction divides by, against sums written out tensor by tensor from the
+workloads' definitions (one layer: H = 64 heads, d = 128, 64-token chunks).
+"""
+import bench
+
+T, H, D, C = 4096, 64, 128, 64
+BF16, F32 = 2, 4
+
+
+def test_prefill_bytes_are_the_tensors_it_must_move():
+    q_k_v = 3 * T * H * D * BF16
+    g = T * H * D * F32
+    beta = T * H * F32
+    out = T * H * D * BF16
+    final_state = H * D * D * F32
+    assert bench._prefill_bytes(T, H, D) == q_k_v + g + beta + out + final_state == 407_896_064
+    # 98,560 bytes per token at 64 heads, plus one layer's 4 MiB state
+    assert bench._prefill_bytes(T, H, D, with_state_out=False) == T * 98_560
+
+
+def test_prefill_flops_count_each_contraction_once_per_chunk_and_head():
+    mac = (2 * C * C * D        # A = K~ K^T and P = Q~ K^T
+           + C ** 3 / 3         # T = (I + A)^-1, unit lower triangular
+           + 2 * C * D * D      # X = [K Gamma; Q Gamma] S
+           + C * C * D          # u = T Y
+           + C * C * D          # O += P' u
+           + D * C * D)         # S += Kbar^T u
+    per_launch = 2 * mac * (T // C) * H
+    assert abs(bench._prefill_flops(T, H, D) - per_launch) < 1.0
+    assert round(per_launch / 1e9, 1) == 43.7
+
+
+def test_prologue_bytes():
+    raw_x, qkv = T * 3 * H * D * BF16, T * 3 * H * D * BF16
+    beta_logit, beta = T * H * F32, T * H * F32
+    assert bench._prologue_bytes(T, H, D) == raw_x + qkv + beta_logit + beta == 404_750_336
+
+
+def test_decode_bytes_stream_the_state_once_each_way():
+    n, ch = 256, 3 * H * D
+    state = 2 * n * H * D * D * F32                  # read + write, in place
+    conv_tail = 2 * n * 3 * ch * BF16                # read + write
+    inputs_ = n * ch * BF16 + n * H * D * F32 + n * H * F32
+    weights = ch * 4 * BF16
+    out = n * H * D * BF16
+    assert bench._decode_bytes(n, H, D) == state + conv_tail + inputs_ + weights + out
+    assert state == 2 * 2**30                         # 1 GiB pool, read and written
