@@ -46,3 +46,29 @@ def test_decode_bytes_stream_the_state_once_each_way():
     out = n * H * D * BF16
     assert bench._decode_bytes(n, H, D) == state + conv_tail + inputs_ + weights + out
     assert state == 2 * 2**30                         # 1 GiB pool, read and written
+
+
+def test_clock_summary_keeps_the_timed_window_and_its_throttle_reasons(tmp_path):
+    import datetime
+    t = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    rows = [  # before, inside (3), after the window
+        (0.0, 1500, "Not Active", "Not Active"),
+        (1.0, 2070, "Not Active", "Not Active"),
+        (1.1, 2000, "Active", "Not Active"),
+        (1.2, 1900, "Not Active", "Active"),
+        (3.0, 900, "Active", "Active"),
+    ]
+    path = tmp_path / "clocks.csv"
+    with open(path, "w") as f:
+        for dt, mhz, hw, cap in rows:
+            ts = (t + datetime.timedelta(seconds=dt)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+            f.write(f"{ts}, 0, {mhz}, 2070, 900.0, 0x0, {hw}, Not Active, Not Active, {cap}\n")
+    cs = bench.ClockSampler(0)
+    cs.path = str(path)
+    cs.t0 = t + datetime.timedelta(seconds=0.5)
+    cs.t1 = t + datetime.timedelta(seconds=2.0)
+    s = cs.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 2000 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    cs.path = str(tmp_path / "missing.csv")
+    assert cs.summary()["reasons"] == ["unsampled"]
