@@ -72,3 +72,19 @@ def test_clock_summary_keeps_the_timed_window_and_its_throttle_reasons(tmp_path)
     assert s["reasons"] == ["hw_slowdown", "sw_power_cap"]
     cs.path = str(tmp_path / "missing.csv")
     assert cs.summary()["reasons"] == ["unsampled"]
+
+
+def test_reference_arm_prints_one_contract_line(capsys):
+    """bench.py --impl reference: the oracle timed on the host cores, one JSON line with the
+    keys the driver reads (rank 0 only; no GPU involved)."""
+    import json
+    import types
+    bench.run_reference(types.SimpleNamespace(gpus=1, steps=1, warmup=0))
+    lines = [x for x in capsys.readouterr().out.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["value"] > 0 and line["unit"] == "tokens/s" and line["higher_is_better"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s",
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
