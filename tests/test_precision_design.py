@@ -1,0 +1,59 @@
+"""The tensor-core prefill's precision design, checked on the CPU with a numerical model of
+its operand roundings (tests/_kernel_numerics.py) against the fp64 oracle.
+
+Bounds (the workload definition's, in the forms the GPU tests use): bf16-stored output within
+1e-2 of RMS beyond one bf16 ulp, final fp32 state within 1e-3 of RMS.  The model without
+rounding is the recurrence itself; with the kernel's roundings (bf16 hi + lo A/P operands on
+the band, tf32 elsewhere, hi + lo Y, three-term bf16 state update, the state operand truncated
+to tf32) it meets the bounds; with every operand in a single bf16 it does not, which is why
+the kernel splits operands at all.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from hybrid_linear_attention_gb300 import inputs
+from tests._kernel_numerics import prefill_head
+from tests._parity import excess_over_ulp, max_err_rel_rms
+
+D = 128
+
+
+def _run(T, H, seed, scheme, *, gate, init=None):
+    inp = inputs.kda_inputs([T], H, D, seed=seed, gate=gate, init_state=init)
+    s0 = inp.get("init_state")
+    ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                             inp["cu_seqlens"], init_state=s0,
+                             gate=inp.get("gate") if gate else None,
+                             norm_w=inp.get("norm_w") if gate else None)
+    eo = es = 0.0
+    for h in range(H):
+        def f(x):
+            return x[:, h].float().numpy()
+        out, S = prefill_head(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(inp["g"]),
+                              inp["beta"][:, h].numpy(),
+                              s0[0, h].numpy() if s0 is not None else np.zeros((D, D)),
+                              scheme, gate=f(inp["gate"]) if gate else None)
+        ro, rs = ref["out"][:, h], ref["final_state"][0, h]
+        eo = max(eo, max_err_rel_rms(out, ro) if scheme == "exact" else excess_over_ulp(out, ro))
+        es = max(es, max_err_rel_rms(S, rs))
+    return eo, es
+
+
+@pytest.mark.parametrize("gate", [False, True])
+def test_model_without_rounding_is_the_recurrence(gate):
+    eo, es = _run(192, 1, 5, "exact", gate=gate, init="all")
+    assert eo < 1e-10 and es < 1e-10
+
+
+@pytest.mark.parametrize("seed", [300, 301, 302])
+def test_kernel_roundings_meet_the_bounds(seed):
+    eo, es = _run(512, 2, seed, "kernel", gate=False, init="all")
+    assert eo <= 1e-2 and es <= 1e-3, (eo, es)
+    eo_g, _ = _run(512, 2, seed, "kernel", gate=True)
+    assert eo_g <= 1e-2, eo_g
+
+
+def test_single_bf16_operands_miss_the_state_bound():
+    _, es = _run(512, 2, 300, "all_bf16", gate=False)
+    assert es > 1e-3, es
