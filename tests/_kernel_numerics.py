@@ -48,7 +48,8 @@ def _ident(x):
 
 
 SCHEMES = {
-    # band: True = hi*lo + lo*hi on the row's own block and the one before; "all" = every block
+    # band: True = hi*lo + lo*hi on the row's own block and the one before; "own" = its own
+    # block only; "all" = every block.  split_q False: the query rows (P) take hi*hi only
     "kernel": dict(dt=np.float32, split_ap=True, band=True, p=tf32, inv=tf32, t=tf32,
                    x=tf32, s=tf32_trunc, y_split=True, y=tf32, u=tf32, upd="bf16x3"),
     "all_bf16": dict(dt=np.float32, split_ap=False, band=False, p=bf16, inv=bf16, t=bf16,
@@ -125,9 +126,10 @@ def prefill_head(q, k, v, g, beta, S0, scheme, *, gate=None, norm_w=None, g_min=
             for Rs in range(R + 1):
                 cb = slice(16 * Rs, 16 * Rs + 16)
                 Kh = Kh_own[cb] if Rs == R else Kh_own[cb] * np.exp2(g0[R] - g0[Rs])
-                band = sc["band"] == "all" or (sc["band"] and R - Rs <= 1)
+                band = sc["band"] == "all" or (sc["band"] == "own" and R == Rs) or (
+                    sc["band"] is True and R - Rs <= 1)
                 Dk[rb, cb] = _prod(Kt[rb], Kh, sc, band)
-                Dq[rb, cb] = _prod(Qt[rb], Kh, sc, band)
+                Dq[rb, cb] = _prod(Qt[rb], Kh, sc, band and sc.get("split_q", True))
         low = np.tril(np.ones((C, C), dtype=bool), -1)
         A = np.where(low, bc[:, None] * Dk, 0).astype(dt)
         P = np.where(low, sc["p"](Dq), 0).astype(dt)
@@ -148,6 +150,12 @@ def prefill_head(q, k, v, g, beta, S0, scheme, *, gate=None, norm_w=None, g_min=
         if sc["upd"] == "bf16x3":
             Kbh, uh = bf16(Kb), bf16(u)
             upd = Kbh.T @ uh + bf16(Kb - Kbh).T @ uh + Kbh.T @ bf16(u - uh)
+        elif sc["upd"] == "bf16x2k":  # hi*hi + lo*hi (the key's residual only)
+            Kbh = bf16(Kb)
+            upd = Kbh.T @ bf16(u) + bf16(Kb - Kbh).T @ bf16(u)
+        elif sc["upd"] == "bf16x2u":  # hi*hi + hi*lo (the write's residual only)
+            Kbh, uh = bf16(Kb), bf16(u)
+            upd = Kbh.T @ uh + Kbh.T @ bf16(u - uh)
         elif sc["upd"] == "bf16":
             upd = bf16(Kb).T @ bf16(u)
         else:

@@ -57,3 +57,32 @@ def test_kernel_roundings_meet_the_bounds(seed):
 def test_single_bf16_operands_miss_the_state_bound():
     _, es = _run(512, 2, 300, "all_bf16", gate=False)
     assert es > 1e-3, es
+
+
+# Each split the kernel pays for is needed: dropping any one of them misses a bound (the
+# model's values at these sizes are in the comments; the bounds are 1e-2 and 1e-3).
+CHEAPER = [
+    # name, change to the kernel's scheme, tokens, metric that fails
+    ("lo terms on the own block only", dict(band="own"), 1024, "gated"),      # 1.8e-2
+    ("query rows (P) without lo terms", dict(split_q=False), 512, "gated"),   # 4.1e-2
+    ("A and P from bf16 hi alone", dict(band=False), 512, "gated"),            # 4.1e-2
+    ("Y as one tf32 operand", dict(y_split=False), 512, "state"),              # 2.0e-3
+    ("update without u's lo term", dict(upd="bf16x2k"), 512, "state"),         # 2.3e-2
+    ("update without Kbar's lo term", dict(upd="bf16x2u"), 512, "state"),      # 1.5e-2
+]
+
+
+@pytest.mark.parametrize("name,change,T,metric", CHEAPER, ids=[c[0] for c in CHEAPER])
+def test_every_split_of_the_kernel_is_needed(name, change, T, metric):
+    from tests import _kernel_numerics as kn
+    key = "cheaper: " + name
+    kn.SCHEMES[key] = dict(kn.SCHEMES["kernel"], **change)
+    try:
+        if metric == "gated":
+            err, _ = _run(T, 2, 300, key, gate=True, init="all")
+            assert err > 1e-2, err
+        else:
+            _, err = _run(T, 2, 300, key, gate=False, init="all")
+            assert err > 1e-3, err
+    finally:
+        del kn.SCHEMES[key]
