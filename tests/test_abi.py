@@ -247,3 +247,12 @@ def test_host_prefill_rejects_bad_arguments_before_any_cuda_call(lib):
     assert call(pp=None) == kda.KDA_ERR_INVALID_ARG
     pb = kda.params(H=2, state_dtype=torch.bfloat16)
     assert call(pp=ctypes.byref(pb)) == kda.KDA_ERR_UNSUPPORTED      # fp32 state only
+
+
+def test_mla_split_workspace_holds_the_partial_sums(lib, monkeypatch):
+    """A forced split (the tuning override) needs, per split and sequence, the 64 x 512 fp32
+    partial latent sums plus each head's running maximum and normaliser."""
+    monkeypatch.setenv("KDA_MLA_SPLIT", "4")
+    assert kda.mla_decode_workspace_size(3, 65536) == 4 * 3 * 64 * (512 + 2) * 4
+    monkeypatch.setenv("KDA_MLA_SPLIT", "1")
+    assert kda.mla_decode_workspace_size(3, 65536) == 0                   # no split, no scratch
