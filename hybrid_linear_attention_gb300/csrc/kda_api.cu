@@ -9,6 +9,16 @@
 
 #include "kda_internal.h"
 #include "kda_prefill_tc.h"
+#include "kda_trace.h"
+
+namespace kda {
+const char *const kTraceNames[TR_COUNT] = {
+    "kda_prologue", "kda_prefill", "kda_prefill_fp8", "kda_prefill_checkpointed",
+    "kda_conv_tail_checkpoints", "kda_decode_step", "kda_decode_step_fused",
+    "kda_decode_step_fused_fp8", "kda_conv_state_update", "kda_decode_multi", "kda_state_accept",
+    "kda_prefill_host", "mla_decode_latent", "mla_decode_latent_noalloc", "mla_decode",
+    "kda_check_device_error", "kda_wait_probe"};
+}  // namespace kda
 
 namespace {
 
@@ -42,6 +52,8 @@ kda_status check_params(const kda_params *p) {
   if (p->scale != p->scale) return KDA_ERR_INVALID_ARG;
   if ((p->io_dtype != KDA_F32 && p->io_dtype != KDA_BF16) ||
       (p->state_dtype != KDA_F32 && p->state_dtype != KDA_BF16))
+    return KDA_ERR_INVALID_ARG;
+  if (p->prefill_form < KDA_PREFILL_AUTO || p->prefill_form > KDA_PREFILL_PAIR)
     return KDA_ERR_INVALID_ARG;
   if (p->d_k != p->d_v) return KDA_ERR_UNSUPPORTED;
   if (p->d_k != 16 && p->d_k != 128) return KDA_ERR_UNSUPPORTED;
@@ -88,6 +100,7 @@ void kda_params_default(kda_params *p) {
   p->qk_l2norm = 1;
   p->io_dtype = KDA_BF16;
   p->state_dtype = KDA_F32;
+  p->prefill_form = KDA_PREFILL_AUTO;
 }
 
 const char *kda_status_string(kda_status s) {
@@ -122,6 +135,7 @@ kda_status kda_prologue(const kda_params *p, const void *x_raw, const void *conv
                         int64_t total_tokens, int l2norm_qk, const float *beta_logit,
                         const float *g_raw, void *q, void *k, void *v, float *beta, float *g,
                         cudaStream_t stream) {
+  KDA_TRACE(TR_PROLOGUE);
   kda_status st = check_params(p);
   if (st != KDA_OK) return st;
   if (n_seqs < 0 || total_tokens < 0 || n_seqs > 65535) return KDA_ERR_INVALID_ARG;
@@ -210,6 +224,7 @@ static kda_status prefill_impl(const kda_params *p, const void *q, const void *k
     t.out_q = out_q, t.out_scale = out_scale;
     t.total = total_tokens, t.n_ckpt = n_ckpt;
     t.err = device_error_ptr();
+    t.form = p->prefill_form;
     return finish(kda::launch_prefill_tc(t, total_tokens, st_bf16, stream), 1);
   }
   kda::RecArgs a = base_args(p);
@@ -234,6 +249,7 @@ kda_status kda_prefill(const kda_params *p, const void *q, const void *k, const 
                        const void *gate_logit, const float *norm_w, void *out,
                        void *final_state, void *workspace, size_t ws_bytes,
                        cudaStream_t stream) {
+  KDA_TRACE(TR_PREFILL);
   return prefill_impl(p, q, k, v, g, beta, init_state, cu_seqlens, n_seqs, total_tokens,
                       gate_logit, norm_w, out, nullptr, nullptr, final_state, nullptr, nullptr, 0,
                       nullptr, workspace, ws_bytes, stream);
@@ -245,6 +261,7 @@ kda_status kda_prefill_fp8(const kda_params *p, const void *q, const void *k, co
                            const void *gate_logit, const float *norm_w, uint8_t *out_q,
                            float *out_scale, void *final_state, void *workspace,
                            size_t ws_bytes, cudaStream_t stream) {
+  KDA_TRACE(TR_PREFILL_FP8);
   if (total_tokens > 0 && !out_q) return KDA_ERR_INVALID_ARG;
   return prefill_impl(p, q, k, v, g, beta, init_state, cu_seqlens, n_seqs, total_tokens,
                       gate_logit, norm_w, nullptr, out_q, out_scale, final_state, nullptr,
@@ -259,6 +276,7 @@ kda_status kda_prefill_checkpointed(const kda_params *p, const void *q, const vo
                                     const int32_t *ckpt_cu, const int32_t *ckpt_pos,
                                     int n_ckpt, void *ckpt_states, void *workspace,
                                     size_t ws_bytes, cudaStream_t stream) {
+  KDA_TRACE(TR_PREFILL_CKPT);
   if (n_ckpt < 1) return KDA_ERR_INVALID_ARG;
   return prefill_impl(p, q, k, v, g, beta, init_state, cu_seqlens, n_seqs, total_tokens,
                       gate_logit, norm_w, out, nullptr, nullptr, final_state, ckpt_cu, ckpt_pos,
@@ -270,6 +288,7 @@ kda_status kda_conv_tail_checkpoints(const kda_params *p, const void *x_raw,
                                      int n_seqs, int64_t total_tokens, const int32_t *ckpt_cu,
                                      const int32_t *ckpt_pos, int n_ckpt, void *conv_ckpt,
                                      cudaStream_t stream) {
+  KDA_TRACE(TR_CONV_TAIL_CKPT);
   kda_status st = check_params(p);
   if (st != KDA_OK) return st;
   if (n_seqs < 1 || n_seqs > 65535 || n_ckpt < 0 || n_ckpt > 65535) return KDA_ERR_INVALID_ARG;
@@ -305,6 +324,7 @@ kda_status kda_decode_step(const kda_params *p, const void *q, const void *k, co
                            const float *g, const float *beta, void *state, int n_slots,
                            const int32_t *slot_idx, int n_seqs, const void *gate_logit,
                            const float *norm_w, void *out, cudaStream_t stream) {
+  KDA_TRACE(TR_DECODE);
   kda_status st = decode_common(p, g, beta, state, n_slots, slot_idx, n_seqs, gate_logit,
                                 norm_w, out);
   if (st != KDA_OK || n_seqs == 0) return st;
@@ -362,6 +382,7 @@ kda_status kda_decode_step_fused(const kda_params *p, const void *x_raw, const v
                                  void *state, int n_slots, const int32_t *slot_idx, int n_seqs,
                                  const void *gate_logit, const float *norm_w, void *out,
                                  cudaStream_t stream) {
+  KDA_TRACE(TR_DECODE_FUSED);
   return decode_fused_impl(p, x_raw, conv_w, conv_state, g, beta, state, n_slots, slot_idx,
                            n_seqs, gate_logit, norm_w, out, nullptr, nullptr, stream);
 }
@@ -372,6 +393,7 @@ kda_status kda_decode_step_fused_fp8(const kda_params *p, const void *x_raw,
                                      const int32_t *slot_idx, int n_seqs,
                                      const void *gate_logit, const float *norm_w,
                                      uint8_t *out_q, float *out_scale, cudaStream_t stream) {
+  KDA_TRACE(TR_DECODE_FUSED_FP8);
   return decode_fused_impl(p, x_raw, conv_w, conv_state, g, beta, state, n_slots, slot_idx,
                            n_seqs, gate_logit, norm_w, nullptr, out_q, out_scale, stream);
 }
@@ -379,6 +401,7 @@ kda_status kda_decode_step_fused_fp8(const kda_params *p, const void *x_raw,
 kda_status kda_conv_state_update(const kda_params *p, const void *x_new, const void *conv_w,
                                  void *conv_state, int n_slots, const int32_t *slot_idx,
                                  int n_seqs, int channels, void *y, cudaStream_t stream) {
+  KDA_TRACE(TR_CONV_UPDATE);
   if (!p) return KDA_ERR_INVALID_ARG;
   if (p->io_dtype != KDA_F32 && p->io_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
   if (n_seqs < 0 || n_seqs > 65535 || channels < 1 || n_slots < 0) return KDA_ERR_INVALID_ARG;
@@ -405,6 +428,7 @@ kda_status kda_decode_multi(const kda_params *p, const void *q, const void *k, c
                             const int32_t *slot_idx, int n_seqs, int K, const void *gate_logit,
                             const float *norm_w, void *out, void *step_states, int commit_final,
                             cudaStream_t stream) {
+  KDA_TRACE(TR_DECODE_MULTI);
   if (K < 1 || K > 64) return KDA_ERR_INVALID_ARG;
   if ((int64_t)n_seqs * K > 65535 * 64) return KDA_ERR_UNSUPPORTED;
   kda_status st = decode_common(p, g, beta, state, n_slots, slot_idx, n_seqs, gate_logit,
@@ -435,6 +459,7 @@ kda_status kda_decode_multi(const kda_params *p, const void *q, const void *k, c
 kda_status kda_state_accept(const kda_params *p, const void *step_states, int n_seqs, int K,
                             const int32_t *accept_len, void *state, int n_slots,
                             const int32_t *slot_idx, cudaStream_t stream) {
+  KDA_TRACE(TR_STATE_ACCEPT);
   kda_status st = check_params(p);
   if (st != KDA_OK) return st;
   if (n_seqs < 0 || n_seqs > 65535 || K < 1 || K > 64 || n_slots < 0) return KDA_ERR_INVALID_ARG;
@@ -462,6 +487,10 @@ static kda_status mla_common(const void *cache, int64_t cache_len, const int32_t
   return KDA_OK;
 }
 
+kda_status mla_set_split_override(int n_split) {
+  return kda::mla_set_split(n_split) ? KDA_OK : KDA_ERR_INVALID_ARG;
+}
+
 size_t mla_decode_workspace_size(int n_seqs, int64_t cache_len) {
   if (n_seqs < 1 || n_seqs > 65535 || cache_len < 1) return 0;
   return kda::mla_split_bytes(kda::mla_preferred_split(n_seqs, cache_len), n_seqs);
@@ -477,6 +506,7 @@ static int mla_split_for(int n_seqs, int64_t cache_len, size_t ws_bytes) {
 kda_status mla_decode_latent(const void *q_cat, const void *cache, int64_t cache_len,
                              const int32_t *lengths, int n_seqs, float scale, float *z,
                              void *workspace, size_t ws_bytes, cudaStream_t stream) {
+  KDA_TRACE(TR_MLA_LATENT);
   kda_status st = mla_common(cache, cache_len, lengths, n_seqs, scale, z);
   if (st != KDA_OK || n_seqs == 0) return st;
   if (!q_cat || !aligned16(q_cat) || !opt_aligned16(workspace)) return KDA_ERR_INVALID_ARG;
@@ -495,6 +525,7 @@ kda_status mla_decode_latent(const void *q_cat, const void *cache, int64_t cache
 kda_status mla_decode_latent_noalloc(const void *q_cat, const void *cache, int64_t cache_len,
                                      const int32_t *lengths, int n_seqs, float scale, float *z,
                                      cudaStream_t stream) {
+  KDA_TRACE(TR_MLA_LATENT_NOALLOC);
   kda_status st = mla_common(cache, cache_len, lengths, n_seqs, scale, z);
   if (st != KDA_OK || n_seqs == 0) return st;
   if (!q_cat || !aligned16(q_cat)) return KDA_ERR_INVALID_ARG;
@@ -518,6 +549,7 @@ kda_status mla_decode(const void *q_nope, const void *q_rope, const void *w_uk,
                       const int32_t *lengths, int n_seqs, const void *gate_logit, float scale,
                       void *q_cat, float *z, void *out, void *workspace, size_t ws_bytes,
                       cudaStream_t stream) {
+  KDA_TRACE(TR_MLA_DECODE);
   kda_status st = mla_common(cache, cache_len, lengths, n_seqs, scale, z);
   if (st != KDA_OK || n_seqs == 0) return st;
   if (!q_nope || !q_rope || !w_uk || !w_uv || !gate_logit || !q_cat || !out)
@@ -543,6 +575,7 @@ kda_status mla_decode(const void *q_nope, const void *q_rope, const void *w_uk,
 }
 
 kda_status kda_check_device_error(cudaStream_t stream) {
+  KDA_TRACE(TR_CHECK_ERROR);
   if (cudaStreamSynchronize(stream) != cudaSuccess) return KDA_ERR_CUDA;
   int *ptr = device_error_ptr();
   if (!ptr) return KDA_ERR_CUDA;
@@ -560,10 +593,16 @@ kda_status kda_check_device_error(cudaStream_t stream) {
 }
 
 kda_status kda_wait_probe(int64_t probes, cudaStream_t stream) {
+  KDA_TRACE(TR_WAIT_PROBE);
   if (probes < 1 || probes > ((int64_t)1 << 30)) return KDA_ERR_INVALID_ARG;
   return finish(kda::launch_wait_probe((long)probes, device_error_ptr(), stream), 1);
 }
 
 uint64_t kda_launch_count(void) { return g_launches.load(); }
+
+int kda_trace_ranges(const char **names, int max_names) {
+  for (int i = 0; names && i < max_names && i < kda::TR_COUNT; ++i) names[i] = kda::kTraceNames[i];
+  return kda::TR_COUNT;
+}
 
 }  // extern "C"

@@ -22,6 +22,8 @@
 #include <cstring>
 #include <mutex>
 
+#include "kda_trace.h"
+
 namespace kda {
 kda_status validate_params(const kda_params *p);
 void note_launches(int n);
@@ -205,6 +207,7 @@ kda_status kda_prefill_host(const kda_params *p, const void *x_raw, const void *
                             const void *init_state, const void *gate_logit,
                             const float *norm_w, void *out, void *final_state, void *workspace,
                             size_t ws_bytes, int64_t segment_tokens, cudaStream_t stream) {
+  KDA_TRACE(TR_PREFILL_HOST);
   // ---- host-side checks, before any CUDA call
   kda_status st = kda::validate_params(p);
   if (st != KDA_OK) return st;

@@ -96,6 +96,7 @@ cudaError_t launch_prologue(const ProArgs &a, int D, bool io_bf16, cudaStream_t 
 cudaError_t launch_wait_probe(long limit, int *err, cudaStream_t s);
 bool mla_latent_supported();
 int mla_preferred_split(int n_seqs, int64_t cache_len);
+bool mla_set_split(int n);  // 0: the automatic rule; 1..64: that split count
 size_t mla_split_bytes(int n_split, int n_seqs);
 size_t mla_static_scratch_bytes();
 void *mla_static_scratch();  // this device's copy, or nullptr

@@ -24,6 +24,12 @@
 // order.  The fp32 state lives in tensor memory, transposed (lane = value channel j,
 // column = key channel i), and is fed to the tensor core directly as the A operand.
 //   TMEM columns   [0,128) S^T   [128,256) TA   [256,384) TB   [384,512) TC
+// The read of the state by the query rows, O = (Q Gamma) S + P u, can nearly cancel, so a
+// tf32 rounding of either factor (the tensor core also truncates a tf32 operand it reads from
+// tensor memory) would show in the output after its norm: the query rows' read is three bf16
+// products (hi*hi + hi*lo + lo*hi) of Q Gamma and of the state split into bf16 hi + lo (the
+// split state kept in TA while TA is otherwise idle), good to ~2^-16.  The key rows, whose
+// products feed the writes, read the truncated tf32 state against tf32 K Gamma.
 // A and P (64 x 64 each, K = 128) come from one product on the tensor core:
 // [Ktil; Qtil] (128 rows, bf16 hi + lo in tensor memory) times the stacked Khat^(R) rows
 // (160, bf16 in shared memory), hi*hi everywhere and hi*lo + lo*hi on the band (a 16-token
@@ -56,7 +62,7 @@ constexpr uint32_t OFF_Q = 0;        // q bf16 [64][128], two 128B-swizzled boxe
 constexpr uint32_t OFF_K = 16384;    // k
 constexpr uint32_t OFF_V = 32768;    // v
 constexpr uint32_t OFF_G = 49152;    // g -> cumulative log2-retention, fp32, 4 boxes of 32
-constexpr uint32_t OFF_X = 81920;    // 64 KB: [K Gamma; Q Gamma] tf32 -> Kbar hi | Kbar lo |
+constexpr uint32_t OFF_X = 81920;    // 64 KB: K Gamma tf32 | Q Gamma bf16 hi | lo -> Kbar hi | Kbar lo |
                                      //        u hi | u lo
 constexpr uint32_t OFF_T = 147456;   // 16 KB: T fp32 (plain) -> T tf32 (K-major)
 constexpr uint32_t OFF_P = 163840;   // 16 KB: P' tf32 (K-major)
@@ -210,6 +216,21 @@ __device__ __forceinline__ void warp_store16(float *D, int ld, const float (&d)[
 struct Maps {
   CUtensorMap q, k, v, g, out, gate;
 };
+
+// 32 fp32 state values of one lane (key channels 32 g32 .. 32 g32 + 31) split into bf16 hi +
+// lo, stored as packed pairs (low half = the even channel) in TA: hi at columns 16 g32 ..,
+// lo 64 columns further (the A operand of the query rows' read)
+__device__ __forceinline__ void split_state_block(uint32_t t_lane, int g32, const float (&v)[32]) {
+  float hw[16], lw[16];
+#pragma unroll
+  for (int y = 0; y < 16; ++y) {
+    const uint32_t h = pack_bf2(v[2 * y], v[2 * y + 1]);
+    hw[y] = __uint_as_float(h);
+    lw[y] = __uint_as_float(pack_bf2(v[2 * y] - bf_lo(h), v[2 * y + 1] - bf_hi(h)));
+  }
+  tmem_st16(t_lane + TM_A + 16u * (uint32_t)g32, hw);
+  tmem_st16(t_lane + TM_A + 64u + 16u * (uint32_t)g32, lw);
+}
 
 // Per-CTA shared state that P1 (out of line, below) shares with the kernel
 __shared__ float s_beta[2][C], s_rq[C], s_rk[C], s_pd[2][C];  // beta, s_pd by chunk parity
@@ -415,6 +436,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
       for (int x = 0; x < 32; ++x) v[x] = s0 ? to_f(s0[(size_t)(i0 + x) * D + j]) : 0.f;
       tmem_st32(tm + lane_off + TM_S + i0, v);
+      split_state_block(tm + lane_off, i0 >> 5, v);
     }
     tmem_wait_st();
   }
@@ -427,7 +449,7 @@ __global__ void __launch_bounds__(NT, 1)
   };
 
   const uint32_t ID_64 = idesc(2, 128, 64, 0, 0);
-  const uint32_t ID_128 = idesc(2, 128, 128, 0, 0);
+  const uint32_t ID_XQ = idesc(1, 128, 64, 0, 0);
   const uint32_t ID_UPD = idesc(1, 128, 128, 0, 1);
   const uint32_t ID_AP160 = idesc(1, 128, 160, 0, 0);
   const uint32_t ID_AP112 = idesc(1, 128, 112, 0, 0);
@@ -583,11 +605,13 @@ __global__ void __launch_bounds__(NT, 1)
       }
       commit(mma_par);
   };
-  // X = [K Gamma; Q Gamma] (tf32, K-major, 128 rows)
+  // K Gamma (tf32, K-major, 64 rows) at X[0, 32K); Q Gamma as bf16 hi | lo (K-major, 64
+  // rows) at X[32K, 48K) | X[48K, 64K)
   auto x_rows = [&](int nv) {
-    for (int it = tid; it < C * 16; it += NT) {  // (token, 8-channel group): rows r, 64 + r
+    for (int it = tid; it < C * 16; it += NT) {  // (token, 8-channel group)
       const int r = it >> 4, c8 = it & 15;
-      float ok8[8], oq8[8];
+      float ok8[8];
+      uint32_t qh[4], ql[4];
       if (r < nv) {
         float kv[8], qv[8], gg[8];
         bf_row8(sm + OFF_K, r, c8, kv);
@@ -598,15 +622,23 @@ __global__ void __launch_bounds__(NT, 1)
         for (int y = 0; y < 8; ++y) {
           const float G = ex2(gg[y]);
           ok8[y] = to_tf32(kv[y] * rk * G);
-          oq8[y] = to_tf32(qv[y] * rq * G);
+          qv[y] = qv[y] * rq * G;
+        }
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          qh[y] = pack_bf2(qv[2 * y], qv[2 * y + 1]);
+          ql[y] = pack_bf2(qv[2 * y] - bf_lo(qh[y]), qv[2 * y + 1] - bf_hi(qh[y]));
         }
       } else {
 #pragma unroll
-        for (int y = 0; y < 8; ++y) ok8[y] = oq8[y] = 0.f;
+        for (int y = 0; y < 8; ++y) ok8[y] = 0.f;
+#pragma unroll
+        for (int y = 0; y < 4; ++y) qh[y] = ql[y] = 0u;
       }
-      st_f32x8(sm + OFF_X + kmaj_f32<128>(r, 8 * c8), sm + OFF_X + kmaj_f32<128>(r, 8 * c8 + 4), ok8);
-      st_f32x8(sm + OFF_X + kmaj_f32<128>(64 + r, 8 * c8),
-               sm + OFF_X + kmaj_f32<128>(64 + r, 8 * c8 + 4), oq8);
+      st_f32x8(sm + OFF_X + kmaj_f32<64>(r, 8 * c8), sm + OFF_X + kmaj_f32<64>(r, 8 * c8 + 4), ok8);
+      const uint32_t qo = kmaj_bf16<64>(r, 8 * c8);
+      *reinterpret_cast<uint4 *>(sm + OFF_X + 32768 + qo) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
+      *reinterpret_cast<uint4 *>(sm + OFF_X + 49152 + qo) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
     }
   };
   auto extract = [&](int nv, uint8_t *pbase, float *Am, uint32_t par) {
@@ -659,13 +691,36 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
   };
-  // ---- MMA1: X^T = S^T [K Gamma; Q Gamma]^T (A = S^T from TMEM) -> TC (thread 0)
+  // ---- MMA1 (thread 0): X_k^T = S^T (K Gamma)^T (tf32, A = S^T from TMEM) -> TC[0, 64),
+  //      committed on its own (the state chain waits only for it); then the query rows
+  //      X_q^T = S^T (Q Gamma)^T -> TC[64, 128) as bf16 hi*hi + hi*lo + lo*hi with the split
+  //      state from TA, completed under the next commit (u = T Y, issued after it)
   auto mma1_issue = [&]() {
       for (int ks = 0; ks < 16; ++ks) {
-        const uint64_t bd = sdesc_sw128(sb + OFF_X + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-        mma_tf32_ts(tm + TM_C, tm + TM_S + 8 * ks, bd, ID_128, ks > 0);
+        const uint64_t bd = sdesc_sw128(sb + OFF_X + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+        mma_tf32_ts(tm + TM_C, tm + TM_S + 8 * ks, bd, ID_64, ks > 0);
       }
       commit(mma_par);
+      for (int term = 0; term < 3; ++term) {
+        const uint32_t a_col = TM_A + (term == 2 ? 64 : 0);              // S hi | S lo
+        const uint32_t b_off = OFF_X + (term == 1 ? 49152 : 32768);      // Q hi | Q lo
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t bd = sdesc_sw128(sb + b_off + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+          mma_bf16_ts(tm + TM_C + 64, tm + a_col + 8 * ks, bd, ID_XQ, term > 0 || ks > 0);
+        }
+      }
+  };
+  // the state split into bf16 hi | lo (packed pairs) in TA, 32-column blocks first ..
+  // first+n-1 of this thread's lane quarter (the state's final value for the next MMA1)
+  auto s_split = [&](int first, int nblk) {
+#pragma unroll 1
+      for (int g32 = first; g32 < first + nblk; ++g32) {
+        float v[32];
+        tmem_ld32(tm + lane_off + TM_S + 32 * g32, v);
+        tmem_wait_ld();
+        split_state_block(tm + lane_off, g32, v);
+      }
+      tmem_wait_st();
   };
   // ---- T = (I + A)^-1 by 16x16 blocks on warp group 2, fp32, then tf32 K-major [r][s]
   //      at tbase
@@ -717,7 +772,7 @@ __global__ void __launch_bounds__(NT, 1)
         *reinterpret_cast<float *>(tbase + kmaj_f32<64>(e >> 6, e & 63)) = tv[q];
       }
   };
-  // ---- groups 0 and 1: wait for MMA1, Y^T = beta (V - K Gamma S)^T (tf32 hi + lo in TA),
+  // ---- groups 0 and 1: wait for MMA1, Y^T = beta (V - K Gamma S)^T (tf32 hi + lo in TB),
   //      decay S^T by Gamma_C
   // (decay_g0 / decay_n: the first group-relative 32-column block and how many this group
   //  decays; the cluster-pair consumer hands the whole decay to warp group 2, which is free
@@ -758,18 +813,19 @@ __global__ void __launch_bounds__(NT, 1)
           hi[x] = to_tf32(y);
           xk[x] = to_tf32(y - hi[x]);
         }
-        tmem_st32(tm + lane_off + TM_A + 32 * grp, hi);
-        tmem_st32(tm + lane_off + TM_A + 64 + 32 * grp, xk);
+        tmem_st32(tm + lane_off + TM_B + 32 * grp, hi);
+        tmem_st32(tm + lane_off + TM_B + 64 + 32 * grp, xk);
       }
       if (with_decay) decay(2 * grp, 2);  // this group's 64 key channels
       else tmem_wait_st();
   };
-  // thread 0: u^T = Y^T T^T, hi then lo (T at shared offset t_off)
+  // thread 0: u^T = Y^T T^T, hi then lo (T at shared offset t_off), into TC[0, 64) (X_k has
+  // been read by the Y pass)
   auto mmau_issue = [&](uint32_t t_off) {
       for (int ks = 0; ks < 16; ++ks) {
         const int k8 = ks & 7;
         const uint64_t bd = sdesc_sw128(sb + t_off + (k8 >> 2) * 8192 + (k8 & 3) * 32, 16, 1024);
-        mma_tf32_ts(tm + TM_B, tm + TM_A + 64 * (ks >> 3) + 8 * k8, bd, ID_64, ks > 0);
+        mma_tf32_ts(tm + TM_C, tm + TM_B + 64 * (ks >> 3) + 8 * k8, bd, ID_64, ks > 0);
       }
       commit(mma_par);
   };
@@ -805,16 +861,16 @@ __global__ void __launch_bounds__(NT, 1)
     }
   };
   auto p6 = [&]() {
-    // ---- P6: u (fp32 -> TA[0,64), tf32 -> TA[64,128)) and u hi | lo (bf16, K-major
-    //      [j][s]) into X[32K, 64K) ---------------------------------------------------------
+    // ---- P6: u from TC[0, 64) (fp32 -> TB[0,64) for the output, tf32 -> TB[64,128) for
+    //      P'u) and u hi | lo (bf16, K-major [j][s]) into X[32K, 64K) -----------------------
     if (grp < 2) {
       float u[32], t[32];
-      tmem_ld32(tm + lane_off + TM_B + 32 * grp, u);
+      tmem_ld32(tm + lane_off + TM_C + 32 * grp, u);
       tmem_wait_ld();
-      tmem_st32(tm + lane_off + TM_A + 32 * grp, u);
+      tmem_st32(tm + lane_off + TM_B + 32 * grp, u);
 #pragma unroll
       for (int x = 0; x < 32; ++x) t[x] = to_tf32(u[x]);
-      tmem_st32(tm + lane_off + TM_A + 64 + 32 * grp, t);
+      tmem_st32(tm + lane_off + TM_B + 64 + 32 * grp, t);
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
         uint32_t hw[4], lw[4];
@@ -836,7 +892,7 @@ __global__ void __launch_bounds__(NT, 1)
   auto p7_issue = [&](uint32_t p_off) {
       for (int ks = 0; ks < 8; ++ks) {
         const uint64_t bd = sdesc_sw128(sb + p_off + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-        mma_tf32_ts(tm + TM_C + 64, tm + TM_A + 64 + 8 * ks, bd, ID_64, 1);
+        mma_tf32_ts(tm + TM_C + 64, tm + TM_B + 64 + 8 * ks, bd, ID_64, 1);
       }
       for (int term = 0; term < 3; ++term) {
         const uint32_t a_off = OFF_X + (term == 2 ? 49152 : 32768);
@@ -882,7 +938,7 @@ __global__ void __launch_bounds__(NT, 1)
       auto load_o = [&](float (&o)[32]) {  // o of rows 32 grp + x, this thread's channel
         float u[32];
         tmem_ld32(tm + lane_off + TM_C + 64 + 32 * grp, o);
-        tmem_ld32(tm + lane_off + TM_A + 32 * grp, u);
+        tmem_ld32(tm + lane_off + TM_B + 32 * grp, u);
         tmem_wait_ld();
 #pragma unroll
         for (int x = 0; x < 32; ++x) o[x] = a.scale * fmaf(s_pd[par][32 * grp + x], u[x], o[x]);
@@ -890,7 +946,7 @@ __global__ void __launch_bounds__(NT, 1)
       auto o_slice = [&](int sl, float (&v)[8]) {  // o of rows 32 grp + 8 sl + y, this channel
         float u8[8];
         tmem_ld8(tm + lane_off + TM_C + 64 + 32 * grp + 8 * sl, v);
-        tmem_ld8(tm + lane_off + TM_A + 32 * grp + 8 * sl, u8);
+        tmem_ld8(tm + lane_off + TM_B + 32 * grp + 8 * sl, u8);
         tmem_wait_ld();
 #pragma unroll
         for (int y = 0; y < 8; ++y) v[y] = a.scale * fmaf(s_pd[par][32 * grp + 8 * sl + y], u8[y], v[y]);
@@ -986,7 +1042,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int sl = 0; sl < 4; ++sl) {  // 8 rows at a time, o re-read: a short loop body
           float o8[8], u8[8];
           tmem_ld8(tm + lane_off + TM_C + 64 + 32 * grp + 8 * sl, o8);
-          tmem_ld8(tm + lane_off + TM_A + 32 * grp + 8 * sl, u8);
+          tmem_ld8(tm + lane_off + TM_B + 32 * grp + 8 * sl, u8);
           tmem_wait_ld();
 #pragma unroll
           for (int y = 0; y < 8; ++y) {
@@ -1004,7 +1060,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int sl = 0; sl < 4; ++sl) {  // 8 rows at a time: a short loop body
           float o8[8], u8[8];
           tmem_ld8(tm + lane_off + TM_C + 64 + 32 * grp + 8 * sl, o8);
-          tmem_ld8(tm + lane_off + TM_A + 32 * grp + 8 * sl, u8);
+          tmem_ld8(tm + lane_off + TM_B + 32 * grp + 8 * sl, u8);
           tmem_wait_ld();
 #pragma unroll
           for (int y = 0; y < 8; y += 2) {  // two rows per packed conversion
@@ -1055,6 +1111,7 @@ __global__ void __launch_bounds__(NT, 1)
       mma_par ^= 1;
       tc_fence_after();
       extract(nv, sm + OFF_P, reinterpret_cast<float *>(sm + OFF_A), par);
+      if (grp < 2) s_split(2 * grp, 2);  // TA is free once the A/P product is done
       fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0) {
@@ -1148,6 +1205,7 @@ __global__ void __launch_bounds__(NT, 1)
       mma_par ^= 1;
       tc_fence_after();
       if (tid == 0) mbar_arrive_remote(bar(BAR_E0 + b), 1);  // landing buffer b is free
+      if (grp == 2 && more) s_split(0, 4);  // TA is free once the query rows' read is done
       p8(nv, t0, par);
       ckpt_write((int64_t)c * C + nv);
       if (!(ok = sync())) break;
@@ -1331,12 +1389,10 @@ cudaError_t launch_typed(const TcArgs &a, const Maps &maps, cudaStream_t s) {
 }
 
 // A cluster pair per (head, sequence) when the pairs fit on the device at once (small
-// batches: otherwise the SMs are better spent on more units); KDA_PREFILL_PAIR=0 / 1
-// forces one form (tests run both).
+// batches: otherwise the SMs are better spent on more units), unless the caller chose a form.
 bool use_pair(const TcArgs &a) {
-  const char *env = getenv("KDA_PREFILL_PAIR");
-  if (env && env[0] == '0') return false;
-  if (env && env[0] == '1') return true;
+  if (a.form == 1) return false;
+  if (a.form == 2) return true;
   int dev = 0, nsm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)

@@ -27,6 +27,7 @@ struct TcArgs {
   const int32_t *ckpt_pos;     // tokens of the sequence before each checkpoint
   void *ckpt_states;           // [n_ckpt, H, 128, 128] state dtype
   int *err;
+  int form;                    // kda_prefill_form: 0 automatic, 1 one CTA, 2 cluster pair
 };
 
 // True when the tensor-core path serves this shape (d = 128, bf16 I/O).

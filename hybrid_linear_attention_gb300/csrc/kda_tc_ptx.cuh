@@ -295,7 +295,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
-// fp32 -> tf32, round to nearest (ties away), low 13 bits cleared.
 // fp32 -> tf32 (10 stored mantissa bits), round to nearest with ties away from zero, on the
 // bit pattern: half a tf32 unit (bit 12) is added to the magnitude and the 13 low bits cleared
 // (a carry into the exponent is the rounding up to the next binade).  Exact for finite x;

@@ -23,7 +23,9 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <atomic>
 #include <cstdlib>
+#include <mutex>
 
 #include <cstring>
 
@@ -467,26 +469,26 @@ __device__ __align__(256) unsigned char g_mla_scratch[MLA_STATIC_SCRATCH];
 
 size_t mla_static_scratch_bytes() { return MLA_STATIC_SCRATCH; }
 
+// The device address of this device's copy of the buffer, looked up with that device current
+// (a host-side name of a __device__ array is not a device address).  Looked up on every call,
+// under a lock: the lookup is cheap next to the launches, and a cached address would outlive
+// a device reset that reloads the module.
 void *mla_static_scratch() {
-  static void *addr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!addr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_mla_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
-  }
-  return addr[dev];
+  static std::mutex lock;
+  std::lock_guard<std::mutex> guard(lock);
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_mla_scratch) != cudaSuccess) return nullptr;
+  return p;
 }
+
+// a split count set by mla_set_split_override (0: none)
+std::atomic<int> g_split_override{0};
 
 // splits per sequence: as many CTAs as fill the SMs in one wave (one CTA per SM fits; a
 // second, partial wave costs more than the split saves), each split at least 8 tiles (512
-// positions); KDA_MLA_SPLIT=n forces n (1..64, tuning)
+// positions); mla_set_split_override(n) forces n (1..64, tuning and tests)
 int mla_preferred_split(int n_seqs, int64_t cache_len) {
-  if (const char *env = getenv("KDA_MLA_SPLIT")) {
-    const int n = atoi(env);
-    if (n >= 1 && n <= 64) return n;
-  }
+  if (const int n = g_split_override.load()) return n;
   int dev = 0, nsm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm < 1)
@@ -498,6 +500,12 @@ int mla_preferred_split(int n_seqs, int64_t cache_len) {
   if (want > most) want = most;
   if (want > 64) want = 64;
   return want > 1 ? (int)want : 1;
+}
+
+bool mla_set_split(int n) {
+  if (n < 0 || n > 64) return false;
+  g_split_override.store(n);
+  return true;
 }
 
 size_t mla_split_bytes(int n_split, int n_seqs) {

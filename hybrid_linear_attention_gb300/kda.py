@@ -28,11 +28,11 @@ EXPORTS = (
     "kda_prologue", "kda_prefill", "kda_prefill_fp8", "kda_prefill_checkpointed",
     "kda_conv_tail_checkpoints", "kda_prefill_host_workspace_size", "kda_prefill_host",
     "kda_prefill_host_plan",
-    "kda_decode_step", "kda_conv_state_update",
-    "kda_decode_step_fused", "kda_decode_step_fused_fp8", "kda_decode_multi", "kda_state_accept", "kda_check_device_error",
-    "kda_launch_count", "kda_wait_probe", "mla_decode_workspace_size", "mla_decode_latent",
-    "mla_decode_latent_noalloc",
-    "mla_decode",
+    "kda_decode_step", "kda_conv_state_update", "kda_decode_step_fused",
+    "kda_decode_step_fused_fp8", "kda_decode_multi", "kda_state_accept",
+    "kda_check_device_error", "kda_launch_count", "kda_trace_ranges", "kda_wait_probe",
+    "mla_decode_workspace_size", "mla_set_split_override", "mla_decode_latent",
+    "mla_decode_latent_noalloc", "mla_decode",
 )
 
 
@@ -42,12 +42,16 @@ class KdaError(RuntimeError):
         super().__init__(f"{where}: {status_string(status)} ({status})")
 
 
+PREFILL_FORMS = {"auto": 0, "fused": 1, "pair": 2}
+
+
 class KdaParams(ctypes.Structure):
     _fields_ = [
         ("H", ctypes.c_int), ("d_k", ctypes.c_int), ("d_v", ctypes.c_int),
         ("scale", ctypes.c_float), ("l2_eps", ctypes.c_float), ("norm_eps", ctypes.c_float),
         ("g_min", ctypes.c_float), ("qk_l2norm", ctypes.c_int),
         ("io_dtype", ctypes.c_int), ("state_dtype", ctypes.c_int),
+        ("prefill_form", ctypes.c_int),
     ]
 
     @property
@@ -108,8 +112,10 @@ def load():
             "kda_state_accept": (_i32, [_P, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp]),
             "kda_check_device_error": (_i32, [_vp]),
             "kda_launch_count": (ctypes.c_uint64, []),
+            "kda_trace_ranges": (_i32, [ctypes.POINTER(ctypes.c_char_p), _i32]),
             "kda_wait_probe": (_i32, [_i64, _vp]),
             "mla_decode_workspace_size": (_sz, [_i32, _i64]),
+            "mla_set_split_override": (_i32, [_i32]),
             "mla_decode_latent": (_i32, [_vp, _vp, _i64, _vp, _i32, ctypes.c_float, _vp, _vp,
                                          _sz, _vp]),
             "mla_decode_latent_noalloc": (_i32, [_vp, _vp, _i64, _vp, _i32, ctypes.c_float, _vp,
@@ -138,12 +144,14 @@ def _check(status, where):
 
 
 def params(H=64, d=128, *, scale=1.0, l2_eps=1e-6, norm_eps=1e-6, g_min=-5.0, qk_l2norm=True,
-           io_dtype=torch.bfloat16, state_dtype=torch.float32):
-    """Builds a kda_params struct (defaults: the pages' configuration)."""
+           io_dtype=torch.bfloat16, state_dtype=torch.float32, prefill_form="auto"):
+    """Builds a kda_params struct (defaults: the pages' configuration).  prefill_form:
+    "auto", "fused" or "pair" (the tensor-core prefill's kernel form)."""
     code = {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16}
     return KdaParams(H=H, d_k=d, d_v=d, scale=scale, l2_eps=l2_eps, norm_eps=norm_eps,
                      g_min=g_min, qk_l2norm=1 if qk_l2norm else 0,
-                     io_dtype=code[io_dtype], state_dtype=code[state_dtype])
+                     io_dtype=code[io_dtype], state_dtype=code[state_dtype],
+                     prefill_form=PREFILL_FORMS[prefill_form])
 
 
 def kda_params_default():
@@ -399,8 +407,35 @@ def kda_conv_state_update(p, x_new, conv_w, conv_state, y, *, slot_idx=None, str
 MLA_SCALE = 192 ** -0.5
 
 
+def kda_trace_ranges():
+    """Names of the NVTX ranges the library opens around its calls."""
+    lib = load()
+    n = lib.kda_trace_ranges(None, 0)
+    arr = (ctypes.c_char_p * n)()
+    lib.kda_trace_ranges(arr, n)
+    return [x.decode() for x in arr]
+
+
 def mla_decode_workspace_size(n_seqs, cache_len):
     return int(load().mla_decode_workspace_size(int(n_seqs), int(cache_len)))
+
+
+def mla_set_split_override(n_split):
+    """Tuning and testing only: force the MLA split count (0 = the automatic rule)."""
+    _check(load().mla_set_split_override(int(n_split)), "mla_set_split_override")
+
+
+class mla_split:
+    """Context manager: the MLA split count forced to n inside the block."""
+
+    def __init__(self, n):
+        self.n = n
+
+    def __enter__(self):
+        mla_set_split_override(self.n)
+
+    def __exit__(self, *exc):
+        mla_set_split_override(0)
 
 
 def _ws(workspace):

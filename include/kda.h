@@ -67,6 +67,15 @@ typedef enum {
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 
+/* Kernel form of the tensor-core prefill (d = 128, bf16 I/O); other shapes ignore it.  Every
+ * form computes the same function; they differ in how the SMs are spent. */
+typedef enum {
+  KDA_PREFILL_AUTO = 0,  /* the library chooses by the batch's shape and the device's SMs */
+  KDA_PREFILL_FUSED = 1, /* one CTA per (head, sequence) walks its chunks                 */
+  KDA_PREFILL_PAIR = 2   /* a cluster of two CTAs per (head, sequence): one builds each
+                            chunk's intra-chunk products, the other walks the state       */
+} kda_prefill_form;
+
 /* Layer configuration.  Defaults in brackets are the pages' configuration. */
 typedef struct {
   int H;                 /* heads [64]                                                  */
@@ -78,10 +87,11 @@ typedef struct {
   int qk_l2norm;         /* 1: L2-normalise q and k inside the call [1]                 */
   kda_dtype io_dtype;    /* q, k, v, raw x, conv weights/state, gate logits, out [BF16] */
   kda_dtype state_dtype; /* recurrent state storage [F32]; BF16 = bf16 storage variant   */
+  int prefill_form;      /* kda_prefill_form [KDA_PREFILL_AUTO]                          */
 } kda_params;
 
 /* Fills *p with the pages' configuration (H 64, d 128, scale 1, eps 1e-6, g_min -5,
- * qk_l2norm 1, bf16 I/O, fp32 state). */
+ * qk_l2norm 1, bf16 I/O, fp32 state) and the automatic prefill form. */
 void kda_params_default(kda_params* p);
 
 /* Human-readable name of a status code (static storage). */
@@ -414,6 +424,12 @@ kda_status kda_wait_probe(int64_t probes, cudaStream_t stream);
 
 /* Number of kernels the library launched since load (host-side counter, for benchmarks). */
 uint64_t kda_launch_count(void);
+
+/* Names of the NVTX ranges the library opens around its calls (one per traced entry point:
+ * the compute calls, kda_prefill_host, kda_check_device_error and kda_wait_probe; each range
+ * spans the call's host-side work and names the kernels it enqueues on a timeline).  Writes up
+ * to max_names pointers to static strings into names (may be NULL) and returns the count. */
+int kda_trace_ranges(const char** names, int max_names);
 
 #ifdef __cplusplus
 }

@@ -38,6 +38,13 @@ extern "C" {
  * With less than this, the calls use as many splits as fit (down to none). */
 size_t mla_decode_workspace_size(int n_seqs, int64_t cache_len);
 
+/* Tuning and testing only: forces the split count of every later mla_decode_latent /
+ * mla_decode_latent_noalloc / mla_decode call and of mla_decode_workspace_size in this
+ * process (1..64; 0 restores the automatic rule: as many splits as fill the SMs in one wave,
+ * each at least 512 positions).  Process-wide, not per device or stream; set it only while
+ * no MLA call is being issued.  KDA_ERR_INVALID_ARG outside 0..64. */
+kda_status mla_set_split_override(int n_split);
+
 /*
  * mla_decode_latent -- the attention over the latent cache (the part that streams it).
  *

@@ -261,12 +261,12 @@ def conv_tail_bytes(H, d, width, elem_bytes):
 # activations dynamically ("Ling-3.1-flash: Grouped Routing and Two Different MLA Caches",
 # section "Production boundaries"); the serving setup fuses the quantisation of the KDA output
 # feeding o_proj into the KDA kernel ("Ling-3.1-flash: What 63 Linear-Attention Layers Do to
-# the KV Budget", section "Fitting it on a node").  Reading: one group per (token, head), the
-# 128 value channels that meet one 128-row block of o_proj's weight; with a = max(amax, 1e-10),
-# fp32 scale = a / 448 (what o_proj multiplies back) and code = E4M3 (1 sign, 4 exponent bits
-# with bias 7, 3 mantissa bits, no infinities, largest finite 448) of x * (448 / a), rounded to
-# nearest even and saturated: the multiply-by-reciprocal form of block quantisation, so a
-# group costs one division and each value one product.
+# the KV Budget", section "Fitting it on a node").  Reading: the activation-side counterpart
+# of the weights' block scaling -- one group per (token, head), the 128 value channels that
+# meet one 128-row block of o_proj's weight -- with the dynamic scale s = a / 448,
+# a = max(amax, 1e-10), so that the group's largest magnitude lands on E4M3's largest finite
+# value; code = E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no infinities,
+# largest finite 448) of x / s, rounded to nearest even and saturated.  Everything in fp64.
 
 FP8_MAX = 448.0
 FP8_EPS = 1e-10
@@ -311,18 +311,15 @@ def fp8_e4m3_decode(codes):
     return s * val
 
 
-def fp8_quantize_groups(x, group=128, dtype=np.float64):
-    """Dynamic FP8 quantisation of the last axis of x in groups of `group` channels:
-    returns (codes uint8 with x's shape, scales with x.shape[:-1] + (n_groups,)).  `dtype`
-    is the precision the scale, the reciprocal and the product are taken in (float32
-    reproduces a device that rounds each of them in IEEE fp32)."""
-    x = np.asarray(x).astype(dtype)
+def fp8_quantize_groups(x, group=128):
+    """Dynamic FP8 quantisation of the last axis of x in groups of `group` channels, in
+    fp64: returns (codes uint8 with x's shape, fp64 scales with x.shape[:-1] + (n_groups,)),
+    scale = max(amax, 1e-10) / 448 and code = E4M3(x / scale)."""
+    x = np.asarray(x, dtype=np.float64)
     shp = x.shape
     xg = x.reshape(shp[:-1] + (shp[-1] // group, group))
-    a = np.maximum(np.abs(xg).max(axis=-1), dtype(FP8_EPS)).astype(dtype)
-    scale = (a / dtype(FP8_MAX)).astype(dtype)
-    inv = (dtype(FP8_MAX) / a).astype(dtype)
-    codes = fp8_e4m3_encode((xg * inv[..., None]).astype(dtype))
+    scale = np.maximum(np.abs(xg).max(axis=-1), FP8_EPS) / FP8_MAX
+    codes = fp8_e4m3_encode(xg / scale[..., None])
     return codes.reshape(shp), scale
 
 

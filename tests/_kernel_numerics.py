@@ -10,8 +10,11 @@ type, so the model rounds each operand exactly there and accumulates in fp32:
     every column and hi*lo + lo*hi over the band (the row's own block and the one before);
   * T = (I + A)^-1: diagonal 16 x 16 blocks in fp32, off-diagonal blocks from tf32 products;
     T and P' stored as tf32 (round half away, as the kernel rounds on the bit pattern);
-  * X = [K Gamma; Q Gamma] S (tf32 product): K Gamma, Q Gamma rounded to tf32, the fp32 state
-    truncated to tf32 by the hardware;
+  * X_k = (K Gamma) S (tf32 product): K Gamma rounded to tf32, the fp32 state truncated to
+    tf32 by the hardware;
+  * X_q = (Q Gamma) S as three bf16 products (hi*hi + hi*lo + lo*hi) of Q Gamma and of the
+    state, both split into bf16 hi + lo: the read can nearly cancel against P u, so it is
+    kept at ~2^-16;
   * u = T Y with Y = beta (V - K Gamma S) split into tf32 hi + lo; O = X_q + P' tf32(u);
   * S <- Gamma_C S + Kbar^T u as three bf16 products (hi*hi + hi*lo + lo*hi).
 
@@ -51,7 +54,8 @@ SCHEMES = {
     # band: True = hi*lo + lo*hi on the row's own block and the one before; "own" = its own
     # block only; "all" = every block.  split_q False: the query rows (P) take hi*hi only
     "kernel": dict(dt=np.float32, split_ap=True, band=True, p=tf32, inv=tf32, t=tf32,
-                   x=tf32, s=tf32_trunc, y_split=True, y=tf32, u=tf32, upd="bf16x3"),
+                   x=tf32, s=tf32_trunc, xq="bf16x3", y_split=True, y=tf32, u=tf32,
+                   upd="bf16x3"),
     "all_bf16": dict(dt=np.float32, split_ap=False, band=False, p=bf16, inv=bf16, t=bf16,
                      x=bf16, s=bf16, y_split=False, y=bf16, u=bf16, upd="bf16"),
     "exact": dict(dt=np.float64, split_ap=False, band=False, p=_ident, inv=_ident, t=_ident,
@@ -138,6 +142,10 @@ def prefill_head(q, k, v, g, beta, S0, scheme, *, gate=None, norm_w=None, g_min=
         KG, QG = sc["x"](kc * rkc * G), sc["x"](qc * rqc * G)
         St = sc["s"](S)
         Xk, Xq = KG @ St, QG @ St
+        if sc.get("xq") == "bf16x3":  # the query rows: three bf16 products of split operands
+            QGe = (qc * rqc * G).astype(dt)
+            Qh, Sh = bf16(QGe), bf16(S)
+            Xq = Qh @ Sh + bf16(QGe - Qh) @ Sh + Qh @ bf16(S - Sh)
         Y = bc[:, None] * (vc - Xk)
         if sc["y_split"]:
             Yh = sc["y"](Y)
@@ -169,3 +177,25 @@ def prefill_head(q, k, v, g, beta, S0, scheme, *, gate=None, norm_w=None, g_min=
         out[sl] = o
     stored = out if dt == np.float64 else bf16(out.astype(np.float32)).astype(np.float64)
     return stored, S.astype(np.float64)
+
+
+# ---------------------------------------------------------------------------------------
+# The FP8 output quantiser as the kernels round it (a model of the device, not the oracle):
+# the group's amax clamped at 1e-10, the scale amax / 448 and the factor 448 / amax each
+# divided once in IEEE fp32 (round to nearest), every value multiplied by that factor in
+# fp32, then converted to E4M3 (nearest even, saturated).  The oracle's quantiser is the
+# fp64 definition code = E4M3(x / scale); the two differ only where the fp32 product lands
+# on the other side of an E4M3 rounding boundary than the exact quotient.
+# ---------------------------------------------------------------------------------------
+
+def fp8_quantize_groups_device(x, group=128):
+    from oracle import FP8_EPS, FP8_MAX, fp8_e4m3_encode
+
+    x = np.asarray(x, dtype=np.float32)
+    shp = x.shape
+    xg = x.reshape(shp[:-1] + (shp[-1] // group, group))
+    a = np.maximum(np.abs(xg).max(axis=-1), np.float32(FP8_EPS)).astype(np.float32)
+    scale = (a / np.float32(FP8_MAX)).astype(np.float32)
+    inv = (np.float32(FP8_MAX) / a).astype(np.float32)
+    codes = fp8_e4m3_encode((xg * inv[..., None]).astype(np.float32))
+    return codes.reshape(shp), scale

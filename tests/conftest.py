@@ -25,3 +25,20 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _device_guard_bands(request, monkeypatch):
+    """Every test marked gpu allocates its CUDA buffers inside guard bands, checked after the
+    test (tests/_canary.py)."""
+    if "gpu" not in request.keywords:
+        yield
+        return
+    import torch
+    if not torch.cuda.is_available():
+        yield
+        return
+    from tests import _canary
+    with _canary.guarded(monkeypatch) as reg:
+        yield
+    reg.check()

@@ -249,10 +249,39 @@ def test_host_prefill_rejects_bad_arguments_before_any_cuda_call(lib):
     assert call(pp=ctypes.byref(pb)) == kda.KDA_ERR_UNSUPPORTED      # fp32 state only
 
 
-def test_mla_split_workspace_holds_the_partial_sums(lib, monkeypatch):
+def test_mla_split_workspace_holds_the_partial_sums(lib):
     """A forced split (the tuning override) needs, per split and sequence, the 64 x 512 fp32
     partial latent sums plus each head's running maximum and normaliser."""
-    monkeypatch.setenv("KDA_MLA_SPLIT", "4")
-    assert kda.mla_decode_workspace_size(3, 65536) == 4 * 3 * 64 * (512 + 2) * 4
-    monkeypatch.setenv("KDA_MLA_SPLIT", "1")
-    assert kda.mla_decode_workspace_size(3, 65536) == 0                   # no split, no scratch
+    with kda.mla_split(4):
+        assert kda.mla_decode_workspace_size(3, 65536) == 4 * 3 * 64 * (512 + 2) * 4
+    with kda.mla_split(1):
+        assert kda.mla_decode_workspace_size(3, 65536) == 0               # no split, no scratch
+    assert lib.mla_set_split_override(65) == kda.KDA_ERR_INVALID_ARG
+    assert lib.mla_set_split_override(-1) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_prefill_form_is_validated(lib):
+    """kda_params.prefill_form selects the tensor-core prefill's kernel form explicitly (no
+    environment variable is read); values outside the enum are rejected before any launch."""
+    for form in (3, -1):
+        p = kda.params(H=2)
+        p.prefill_form = form
+        assert lib.kda_prefill(ctypes.byref(p), *([None] * 6), None, 0, 0, None, None, None,
+                               None, None, 0, None) == kda.KDA_ERR_INVALID_ARG
+    assert kda.params(H=2, prefill_form="pair").prefill_form == 2
+
+
+def test_every_call_opens_an_nvtx_range(lib):
+    """Each entry point that enqueues GPU work (every kda_status call of the headers but the
+    host-side tuning switch) is traced by an NVTX range of its own name."""
+    text = ""
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            text += re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, h)).read(), flags=re.S)
+    calls = set(re.findall(r"kda_status\s+((?:kda|mla)_[a-z0-9_]+)\s*\(", text))
+    calls -= {"mla_set_split_override"}
+    ranges = kda.kda_trace_ranges()
+    assert len(ranges) == len(set(ranges))
+    assert calls <= set(ranges), sorted(calls - set(ranges))
+    src = open(os.path.join(os.path.dirname(kbuild.__file__), "csrc", "kda_trace.h")).read()
+    assert "nvtxRangePushA" in src and "nvtxRangePop" in src

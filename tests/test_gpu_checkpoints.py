@@ -64,7 +64,7 @@ def _run(inp, p, ck_cu, ck_pos, gate):
 
 
 @pytest.mark.parametrize("path", ["fused", "pair", "token_serial"])
-def test_prefill_checkpoints_equal_prefix_final_states(path, monkeypatch):
+def test_prefill_checkpoints_equal_prefix_final_states(path):
     """Chunk-edge and sequence-end checkpoints over ragged sequences (an empty one, a
     one-token one, exact chunk multiples, ragged tails), some with a nonzero initial state,
     through the chunked kernel in both of its forms and through the token-serial kernel."""
@@ -72,12 +72,12 @@ def test_prefill_checkpoints_equal_prefix_final_states(path, monkeypatch):
         d, io = 16, torch.float32
     else:
         d, io = 128, torch.bfloat16
-        monkeypatch.setenv("KDA_PREFILL_PAIR", "1" if path == "pair" else "0")
     lens = [200, 0, 64, 130, 1, 256]
     cps = [[64, 128, 192, 200], [], [64], [64, 130], [1], [128, 256]]
     inp = inputs.kda_inputs(lens, 2, d, seed=40, io_dtype=io, init_state="even", gate=True)
     inp["norm_w"] = inputs.normal((d,), seed=41, dtype=torch.float32)
-    p = kda.params(H=2, d=d, io_dtype=io)
+    p = kda.params(H=2, d=d, io_dtype=io,
+                   prefill_form="auto" if path == "token_serial" else path)
     ck_cu, ck_pos, flat = _ckpt_tables(cps)
 
     out, fin, ck = _run(inp, p, ck_cu, ck_pos, gate=True)
@@ -112,15 +112,14 @@ def test_token_serial_checkpoints_at_any_position():
         assert e <= TOL_F32, f"checkpoint {j} (sequence {n}, {pos} tokens): {e:.3g}"
 
 
-@pytest.mark.parametrize("pair", ["0", "1"])
-def test_checkpoint_rule_breaks_are_flagged_not_followed(pair, monkeypatch):
+@pytest.mark.parametrize("form", ["fused", "pair"])
+def test_checkpoint_rule_breaks_are_flagged_not_followed(form):
     """Positions off a chunk edge (chunked kernel), 0, past the sequence end, out of order,
     and a checkpoint range past n_ckpt: skipped, reported as KDA_ERR_BAD_INDEX, and the
     outputs, final states and the valid checkpoints are unaffected."""
-    monkeypatch.setenv("KDA_PREFILL_PAIR", pair)
     lens = [130, 64, 100]
     inp = inputs.kda_inputs(lens, 2, 128, seed=43, init_state="all")
-    p = kda.params(H=2, d=128)
+    p = kda.params(H=2, d=128, prefill_form=form)
     out0, fin0 = _gpu.prefill(inp, p)
     torch.cuda.synchronize()
     ref64 = _prefix_state(inp, 0, 64, gate=False)

@@ -30,16 +30,16 @@ def _tol(io):
 
 
 @pytest.mark.parametrize("path", ["pair", "fused", "token-serial"])
-def test_log_retention_below_the_bound_gives_the_bits_of_the_bound(path, monkeypatch):
+def test_log_retention_below_the_bound_gives_the_bits_of_the_bound(path):
     if path == "token-serial":
         d, io = 16, torch.float32
     else:
         d, io = 128, torch.bfloat16
-        monkeypatch.setenv("KDA_PREFILL_PAIR", "1" if path == "pair" else "0")
     inp = inputs.kda_inputs([70, 130], 2, d, seed=61, io_dtype=io, init_state="all", gate=True)
     inp["g"] = inputs.uniform(tuple(inp["g"].shape), -50.0, 0.0, seed=62)
     assert float((inp["g"] < -5).float().mean()) > 0.8
-    p = kda.params(H=2, d=d, io_dtype=io)
+    p = kda.params(H=2, d=d, io_dtype=io,
+                   prefill_form="auto" if path == "token-serial" else path)
     out_raw, fin_raw = _gpu.prefill(inp, p, gate=True)
     clamped = dict(inp, g=inp["g"].clamp(min=-5.0))
     out_c, fin_c = _gpu.prefill(clamped, p, gate=True)

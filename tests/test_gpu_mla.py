@@ -2,7 +2,7 @@
 
 Tolerance: bf16 operands with fp32 accumulation (the softmax weights are rounded to bf16 as
 tensor-core operands, the normaliser sums the same rounded weights), so the bound is the bf16
-one of the KDA path: max |err| <= 1e-2 of the output RMS, beyond one bf16 ulp for outputs
+one of the KDA path: max |err| <= 1e-2 of the output RMS, beyond half a bf16 ulp for outputs
 stored in bf16.  Cache rows at or past a sequence's length hold NaN here: they must not
 reach the result.
 """

@@ -2,7 +2,7 @@
 its operand roundings (tests/_kernel_numerics.py) against the fp64 oracle.
 
 Bounds (the workload definition's, in the forms the GPU tests use): bf16-stored output within
-1e-2 of RMS beyond one bf16 ulp, final fp32 state within 1e-3 of RMS.  The model without
+1e-2 of RMS beyond half a bf16 ulp, final fp32 state within 1e-3 of RMS.  The model without
 rounding is the recurrence itself; with the kernel's roundings (bf16 hi + lo A/P operands on
 the band, tf32 elsewhere, hi + lo Y, three-term bf16 state update, the state operand truncated
 to tf32) it meets the bounds; with every operand in a single bf16 it does not, which is why
@@ -14,7 +14,7 @@ import pytest
 import oracle
 from hybrid_linear_attention_gb300 import inputs
 from tests._kernel_numerics import prefill_head
-from tests._parity import excess_over_ulp, max_err_rel_rms
+from tests._parity import excess_over_half_ulp, max_err_rel_rms
 
 D = 128
 
@@ -35,7 +35,7 @@ def _run(T, H, seed, scheme, *, gate, init=None):
                               s0[0, h].numpy() if s0 is not None else np.zeros((D, D)),
                               scheme, gate=f(inp["gate"]) if gate else None)
         ro, rs = ref["out"][:, h], ref["final_state"][0, h]
-        eo = max(eo, max_err_rel_rms(out, ro) if scheme == "exact" else excess_over_ulp(out, ro))
+        eo = max(eo, max_err_rel_rms(out, ro) if scheme == "exact" else excess_over_half_ulp(out, ro))
         es = max(es, max_err_rel_rms(S, rs))
     return eo, es
 
@@ -86,3 +86,41 @@ def test_every_split_of_the_kernel_is_needed(name, change, T, metric):
             assert err > 1e-3, err
     finally:
         del kn.SCHEMES[key]
+
+
+def test_device_fp8_model_differs_from_the_definition_only_at_rounding_boundaries():
+    """The tests-side model of the kernels' fp32 quantiser against the oracle's fp64
+    definition: the same scales up to fp32 rounding, and codes that differ, if at all, by
+    one E4M3 step and only where x / scale lies within fp32 rounding of a code boundary."""
+    from tests._kernel_numerics import fp8_quantize_groups_device
+
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((400, 256)) * np.exp2(rng.uniform(-8, 8, (400, 1)))).astype(np.float32)
+    c_ref, s_ref = oracle.fp8_quantize_groups(x, 128)
+    c_dev, s_dev = fp8_quantize_groups_device(x, 128)
+    np.testing.assert_allclose(s_dev, s_ref, rtol=2 ** -23)
+    v_ref = oracle.fp8_e4m3_decode(c_ref)
+    v_dev = oracle.fp8_e4m3_decode(c_dev)
+    diff = c_ref != c_dev
+    assert diff.mean() < 1e-3
+    y = np.abs(x.astype(np.float64).reshape(400, 2, 128) / s_ref[..., None]).reshape(400, 256)
+    # where they differ, both codes are neighbours of y (one step apart)
+    lo, hi = np.minimum(np.abs(v_ref), np.abs(v_dev)), np.maximum(np.abs(v_ref), np.abs(v_dev))
+    assert ((lo[diff] <= y[diff] * (1 + 2 ** -20)) & (y[diff] <= hi[diff] * (1 + 2 ** -20))).all()
+
+
+def test_query_rows_need_the_split_read_of_the_state():
+    """The query rows' read of the state: as one tf32 product (the state truncated, Q Gamma
+    rounded) one draw of the gated workload misses the bound (model: 1.96e-2, seed 8, four
+    heads, T = 1024); as the kernel takes it, three bf16 products of the split state and the
+    split Q Gamma, the same draw stays at ~1.3e-3."""
+    from tests import _kernel_numerics as kn
+    key = "cheaper: one tf32 read"
+    kn.SCHEMES[key] = dict(kn.SCHEMES["kernel"], xq=None)
+    try:
+        err_one, _ = _run(1024, 4, 8, key, gate=True)
+    finally:
+        del kn.SCHEMES[key]
+    err_kernel, _ = _run(1024, 4, 8, "kernel", gate=True)
+    assert err_one > 1e-2, err_one
+    assert err_kernel < 3e-3, err_kernel

@@ -24,7 +24,7 @@ def lib():
     return kda.load()
 
 
-def test_exported_and_host_checks(lib, monkeypatch):
+def test_exported_and_host_checks(lib):
     """Exported; bad arguments rejected; an oversize split refused on the host."""
     assert hasattr(lib, "mla_decode_latent_noalloc")
     buf = ctypes.c_void_p(256)  # aligned, never dereferenced: every case returns before a launch
@@ -33,11 +33,11 @@ def test_exported_and_host_checks(lib, monkeypatch):
     assert f(None, buf, 64, buf, 2, 0.07, buf, None) == kda.KDA_ERR_INVALID_ARG
     assert f(buf, buf, 64, buf, 2, 0.0, buf, None) == kda.KDA_ERR_INVALID_ARG
     assert f(ctypes.c_void_p(24), buf, 64, buf, 2, 0.07, buf, None) == kda.KDA_ERR_INVALID_ARG
-    monkeypatch.setenv("KDA_MLA_SPLIT", "64")  # 64 splits x 16 sequences: 135 MB of partials
-    assert kda.mla_decode_workspace_size(16, 65536) > STATIC_BYTES
-    assert f(buf, buf, 65536, buf, 16, 0.07, buf, None) == kda.KDA_ERR_WORKSPACE
-    monkeypatch.setenv("KDA_MLA_SPLIT", "2")  # 2 x 16 sequences fit
-    assert 0 < kda.mla_decode_workspace_size(16, 65536) <= STATIC_BYTES
+    with kda.mla_split(64):  # 64 splits x 16 sequences: 135 MB of partials
+        assert kda.mla_decode_workspace_size(16, 65536) > STATIC_BYTES
+        assert f(buf, buf, 65536, buf, 16, 0.07, buf, None) == kda.KDA_ERR_WORKSPACE
+    with kda.mla_split(2):  # 2 x 16 sequences fit
+        assert 0 < kda.mla_decode_workspace_size(16, 65536) <= STATIC_BYTES
 
 
 def _case(lengths, L, seed):
@@ -80,13 +80,12 @@ def test_noalloc_equals_the_workspace_call(lengths, L):
 
 
 @pytest.mark.gpu
-def test_noalloc_refuses_oversize_without_launching(monkeypatch):
+def test_noalloc_refuses_oversize_without_launching():
     from tests import _gpu
     _gpu.lib()
-    monkeypatch.setenv("KDA_MLA_SPLIT", "64")  # 64 x 8 sequences: 67 MB of partials
     q, cache, lens = _case([64] * 8, 64, seed=950)
     z = torch.full((8, 64, 512), 3.0, device="cuda")
-    with pytest.raises(kda.KdaError) as ei:
+    with kda.mla_split(64), pytest.raises(kda.KdaError) as ei:  # 64 x 8: 67 MB of partials
         kda.mla_decode_latent_noalloc(q.cuda(), cache.cuda(), lens.cuda(), z)
     assert ei.value.status == kda.KDA_ERR_WORKSPACE
     torch.cuda.synchronize()
