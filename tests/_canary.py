@@ -11,6 +11,8 @@ import torch
 
 GUARD = 256
 PATTERN = 0xA5
+# the allocators as torch defines them (the guarded versions below must not call themselves)
+_EMPTY, _EMPTY_LIKE, _ZEROS, _FULL = torch.empty, torch.empty_like, torch.zeros, torch.full
 
 
 class Registry:
@@ -44,8 +46,8 @@ def _guarded_alloc(reg, shape, dtype, device):
     n = 1
     for s in shape:
         n *= s
-    nbytes = n * torch.empty((), dtype=dtype).element_size()
-    buf = torch.full((nbytes + 2 * GUARD,), PATTERN, dtype=torch.uint8, device=device)
+    nbytes = n * _EMPTY((), dtype=dtype).element_size()
+    buf = _FULL((nbytes + 2 * GUARD,), PATTERN, dtype=torch.uint8, device=device)
     t = buf[GUARD:GUARD + nbytes].view(dtype).view(shape)
     reg.bufs.append((buf, f"{dtype} {list(shape)}"))
     return t
@@ -63,8 +65,7 @@ def _shape(args, kw):
 @contextlib.contextmanager
 def guarded(monkeypatch):
     reg = Registry()
-    orig_empty, orig_empty_like = torch.empty, torch.empty_like
-    orig_zeros, orig_full = torch.zeros, torch.full
+    orig_empty, orig_empty_like, orig_zeros, orig_full = _EMPTY, _EMPTY_LIKE, _ZEROS, _FULL
     plain = {"dtype", "device"}
 
     def empty(*args, **kw):
