@@ -80,7 +80,11 @@ constexpr uint32_t TM_AH = 128, TM_AL = 192, TM_D = 256;
 
 // TMA loads and tensor-core completion; in a cluster pair, the consumer's FULL (landing
 // buffer 0 / 1 holds T and P') and the producer's EMPTY (buffer 0 / 1 may be rewritten)
-enum { BAR_Q = 0, BAR_K, BAR_V, BAR_G, BAR_MMA, BAR_F0, BAR_F1, BAR_E0, BAR_E1, BAR_GT, NBAR };
+// (a cluster-pair consumer commits its state read on BAR_X, key rows, and BAR_XQ, query rows:
+// it issues that product from another thread than the rest, and a commit tracks only the
+// products of the thread that issues it)
+enum { BAR_Q = 0, BAR_K, BAR_V, BAR_G, BAR_MMA, BAR_F0, BAR_F1, BAR_E0, BAR_E1, BAR_GT, BAR_X,
+       BAR_XQ, NBAR };
 // consumer landing buffers b = 0, 1: T then P' (16 KB each, tf32 K-major); buffer 0 is the
 // fused kernel's own T and P' region
 __host__ __device__ constexpr uint32_t off_lt(int b) { return 147456u + 32768u * (uint32_t)b; }
@@ -293,23 +297,34 @@ __device__ __noinline__ void p1_run(const float *beta, int64_t bos, int64_t eos,
   }
   if (part & 2) {
     const int i = t;
+    // the swizzle repeats every 8 rows: row 8m + x of channel i sits at 1024 m + off[x]
+    uint32_t off[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) off[x] = OFF_G + swz<4>(x, i);
     float run = 0.f;
 #pragma unroll 1
     for (int blk = 0; blk < 4; ++blk) {  // 16 rows at a time, running sum carried over
       s_g0[blk][i] = run;
 #pragma unroll 1
       for (int x0 = 0; x0 < 16; x0 += 8) {  // 8 loads in flight, then the 8 sums
+        const int r0 = 16 * blk + x0;
+        uint8_t *rows = sm + (uint32_t)r0 * 128u;
         float v[8];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          const int r = 16 * blk + x0 + x;
-          const float gv = *reinterpret_cast<const float *>(sm + OFF_G + swz<4>(r, i));
-          v[x] = r < nvc ? fmaxf(gv, g_min) * LOG2E : 0.f;
-        }
+        for (int x = 0; x < 8; ++x)
+          v[x] = fmaxf(*reinterpret_cast<const float *>(rows + off[x]), g_min);
+        if (nvc == C) {  // a full chunk: every row counts
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          run += v[x];
-          *reinterpret_cast<float *>(sm + OFF_G + swz<4>(16 * blk + x0 + x, i)) = run;
+          for (int x = 0; x < 8; ++x) {
+            run = fmaf(v[x], LOG2E, run);
+            *reinterpret_cast<float *>(rows + off[x]) = run;
+          }
+        } else {
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            if (r0 + x < nvc) run = fmaf(v[x], LOG2E, run);
+            *reinterpret_cast<float *>(rows + off[x]) = run;
+          }
         }
       }
     }
@@ -407,11 +422,12 @@ __global__ void __launch_bounds__(NT, 1)
       if (mask & (1u << b)) s_ppar[b] = (uint32_t)(c & 1);
     atomicOr(&s_pend, mask);
   };
-  auto commit = [&](uint32_t parity) {
-    mma_commit(bar(BAR_MMA));
-    s_ppar[BAR_MMA] = parity;
-    atomicOr(&s_pend, 1u << BAR_MMA);
+  auto commit_on = [&](int b, uint32_t parity) {
+    mma_commit(bar(b));
+    s_ppar[b] = parity;
+    atomicOr(&s_pend, 1u << b);
   };
+  auto commit = [&](uint32_t parity) { commit_on(BAR_MMA, parity); };
   // a bounded wait; one that runs out only raises the CTA's abort flag (reported once, at
   // exit): waits are inlined at every phase boundary, and the chunk loop's code size costs time
   auto wait = [&](int b, uint32_t parity) {
@@ -641,7 +657,15 @@ __global__ void __launch_bounds__(NT, 1)
       *reinterpret_cast<uint4 *>(sm + OFF_X + 49152 + qo) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
     }
   };
-  auto extract = [&](int nv, uint8_t *pbase, float *Am, uint32_t par) {
+  // P' rows go to pbase (this CTA's shared memory) or, with rbase != 0, into the consumer's
+  // shared memory at shared::cluster address rbase by asynchronous stores completing on the
+  // consumer's barrier rbar
+  auto extract = [&](int nv, uint8_t *pbase, uint32_t rbase, uint32_t rbar, float *Am,
+                     uint32_t par) {
+    auto put_p = [&](uint32_t off, float4 val) {
+      if (rbase) st_async_v4(rbase + off, val, rbar);
+      else *reinterpret_cast<float4 *>(pbase + off) = val;
+    };
     // ---- P3: A (beta-scaled, strict lower, fp32 rows of LDA) and P' (strict lower, tf32,
     //      K-major) from the product, one tensor-memory lane per row (lanes 0-63: A, 64-127:
     //      P), in 16-column pieces that each hold one block R and 16 consecutive s; zeros in
@@ -674,11 +698,11 @@ __global__ void __launch_bounds__(NT, 1)
                             s + 2 < r ? br * v[4 * q4 + 2] : 0.f,
                             s + 3 < r ? br * v[4 * q4 + 3] : 0.f);
           } else {
-            *reinterpret_cast<float4 *>(pbase + kmaj_f32<64>(r, s)) =
-                make_float4(s < r ? to_tf32(v[4 * q4]) : 0.f,
-                            s + 1 < r ? to_tf32(v[4 * q4 + 1]) : 0.f,
-                            s + 2 < r ? to_tf32(v[4 * q4 + 2]) : 0.f,
-                            s + 3 < r ? to_tf32(v[4 * q4 + 3]) : 0.f);
+            put_p(kmaj_f32<64>(r, s),
+                  make_float4(s < r ? to_tf32(v[4 * q4]) : 0.f,
+                              s + 1 < r ? to_tf32(v[4 * q4 + 1]) : 0.f,
+                              s + 2 < r ? to_tf32(v[4 * q4 + 2]) : 0.f,
+                              s + 3 < r ? to_tf32(v[4 * q4 + 3]) : 0.f));
           }
         }
       }
@@ -686,21 +710,23 @@ __global__ void __launch_bounds__(NT, 1)
         const int pr = tid >> 6, rr16 = (tid >> 2) & 15, c4 = tid & 3;
         const int Rz = pr < 3 ? 0 : pr < 5 ? 1 : 2;
         const int Rpz = pr < 3 ? pr + 1 : pr < 5 ? pr - 1 : 3;
-        *reinterpret_cast<float4 *>(pbase + kmaj_f32<64>(16 * Rz + rr16, 16 * Rpz + 4 * c4)) =
-            make_float4(0.f, 0.f, 0.f, 0.f);
+        put_p(kmaj_f32<64>(16 * Rz + rr16, 16 * Rpz + 4 * c4), make_float4(0.f, 0.f, 0.f, 0.f));
       }
     }
   };
   // ---- MMA1 (thread 0): X_k^T = S^T (K Gamma)^T (tf32, A = S^T from TMEM) -> TC[0, 64),
   //      committed on its own (the state chain waits only for it); then the query rows
   //      X_q^T = S^T (Q Gamma)^T -> TC[64, 128) as bf16 hi*hi + hi*lo + lo*hi with the split
-  //      state from TA, completed under the next commit (u = T Y, issued after it)
-  auto mma1_issue = [&]() {
+  //      state from TA.  One CTA: both on BAR_MMA, the query rows completing under the next
+  //      commit (u = T Y, issued after them by the same thread); cluster-pair consumer
+  //      (issued by thread 256): key rows on BAR_X, query rows on BAR_XQ, phase = chunk parity
+  auto mma1_issue = [&](bool own_bars, uint32_t par) {
       for (int ks = 0; ks < 16; ++ks) {
         const uint64_t bd = sdesc_sw128(sb + OFF_X + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
         mma_tf32_ts(tm + TM_C, tm + TM_S + 8 * ks, bd, ID_64, ks > 0);
       }
-      commit(mma_par);
+      if (own_bars) commit_on(BAR_X, par);
+      else commit(mma_par);
       for (int term = 0; term < 3; ++term) {
         const uint32_t a_col = TM_A + (term == 2 ? 64 : 0);              // S hi | S lo
         const uint32_t b_off = OFF_X + (term == 1 ? 49152 : 32768);      // Q hi | Q lo
@@ -709,6 +735,7 @@ __global__ void __launch_bounds__(NT, 1)
           mma_bf16_ts(tm + TM_C + 64, tm + a_col + 8 * ks, bd, ID_XQ, term > 0 || ks > 0);
         }
       }
+      if (own_bars) commit_on(BAR_XQ, par);
   };
   // the state split into bf16 hi | lo (packed pairs) in TA, 32-column blocks first ..
   // first+n-1 of this thread's lane quarter (the state's final value for the next MMA1)
@@ -790,8 +817,9 @@ __global__ void __launch_bounds__(NT, 1)
       }
       tmem_wait_st();
   };
-  auto y_decay = [&](int nv, uint32_t par, bool with_decay) {
-      wait(BAR_MMA, mma_par);  // MMA1 done
+  auto y_decay = [&](int nv, uint32_t par, bool with_decay, bool own_bars) {
+      if (own_bars) wait(BAR_X, par);  // the key rows of MMA1 done
+      else wait(BAR_MMA, mma_par);
       tc_fence_after();
       wait(BAR_V, par);
       {
@@ -1110,18 +1138,18 @@ __global__ void __launch_bounds__(NT, 1)
       wait(BAR_MMA, mma_par);
       mma_par ^= 1;
       tc_fence_after();
-      extract(nv, sm + OFF_P, reinterpret_cast<float *>(sm + OFF_A), par);
+      extract(nv, sm + OFF_P, 0u, 0u, reinterpret_cast<float *>(sm + OFF_A), par);
       if (grp < 2) s_split(2 * grp, 2);  // TA is free once the A/P product is done
       fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0) {
         if (more) issue(1u << BAR_Q, c + 1);  // q is consumed
-        mma1_issue();
+        mma1_issue(false, 0);
       }
       if (grp == 2)  // in flight with MMA1 and the Y / decay work
         inverse(sm + OFF_T, reinterpret_cast<const float *>(sm + OFF_A),
                 reinterpret_cast<float *>(sm + OFF_T), s_M);
-      else y_decay(nv, par, true);
+      else y_decay(nv, par, true, false);
       mma_par ^= 1;  // MMA1's phase (waited by groups 0 and 1)
       fence_proxy_async();
       if (!(ok = sync())) break;
@@ -1165,18 +1193,15 @@ __global__ void __launch_bounds__(NT, 1)
       x_rows(nv);
       fence_proxy_async();
       if (!(ok = sync())) break;
-      if (tid == 0) {
-        if (more) issue(1u << BAR_Q, c + 1);  // q is consumed
-        mma1_issue();
-      }
+      if (tid == 0 && more) issue(1u << BAR_Q, c + 1);  // q is consumed
+      if (tid == 256) mma1_issue(true, par);  // group 2 only decays in this phase
       if (grp < 2) {
-        y_decay(nv, par, false);
-      } else {  // S^T *= Gamma_C once MMA1, which reads S, is done
-        wait(BAR_MMA, mma_par);
+        y_decay(nv, par, false, true);
+      } else {  // S^T *= Gamma_C once the key rows of MMA1, which read S, are done
+        wait(BAR_X, par);
         tc_fence_after();
         decay(0, 4);
       }
-      mma_par ^= 1;
       fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0) {
@@ -1195,6 +1220,7 @@ __global__ void __launch_bounds__(NT, 1)
       if (tid == 0 && more) issue((1u << BAR_K) | (1u << BAR_G), c + 1);
       wait(BAR_MMA, mma_par);  // u ready
       mma_par ^= 1;
+      if (grp < 2) wait(BAR_XQ, par);  // p6 rewrites the query rows' operands
       tc_fence_after();
       p6();
       fence_proxy_async();
@@ -1205,7 +1231,9 @@ __global__ void __launch_bounds__(NT, 1)
       mma_par ^= 1;
       tc_fence_after();
       if (tid == 0) mbar_arrive_remote(bar(BAR_E0 + b), 1);  // landing buffer b is free
-      if (grp == 2 && more) s_split(0, 4);  // TA is free once the query rows' read is done
+      // TA is free once the query rows' read is done; groups 0 and 1 split the state while
+      // group 2 is still in P1
+      if (grp < 2 && more) s_split(2 * grp, 2);
       p8(nv, t0, par);
       ckpt_write((int64_t)c * C + nv);
       if (!(ok = sync())) break;
@@ -1213,7 +1241,6 @@ __global__ void __launch_bounds__(NT, 1)
   } else {
     // ---- producer of a cluster pair: A and P' of each chunk, the inverse T, written into the
     //      consumer's landing buffer c & 1 -------------------------------------------------
-    uint8_t *peer = reinterpret_cast<uint8_t *>(map_rank(sm, 0));
     // the producer loads no v and builds no X: A, the fp32 T and the inverse's block scratch
     // live there, clear of the operand regions, so the next chunk's operands can be built
     // while the inverse runs
@@ -1245,14 +1272,15 @@ __global__ void __launch_bounds__(NT, 1)
       if (c >= 2 && !mbar_wait_cluster(bar(BAR_E0 + b), (uint32_t)(((c - 2) >> 1) & 1)))
         s_abort = 1;
       if (!(ok = sync())) break;
-      extract(nv, peer + off_lp(b), pA, (uint32_t)(c & 1));
-      fence_cluster();
+      // FULL of landing buffer b completes once P' (16 KB of asynchronous stores from every
+      // warp) and T (one 16 KB bulk copy after the inverse) have landed
+      if (tid == 256) mbar_arrive_expect_tx_remote(bar(BAR_F0 + b), 0, 32768);
+      extract(nv, nullptr, map_shared_rank(sb + off_lp(b), 0), map_shared_rank(bar(BAR_F0 + b), 0),
+              pA, (uint32_t)(c & 1));
       fence_proxy_async();
-      // only the inverting group waits for every warp's rows; groups 0 and 1 go on to P1
+      // only the inverting group waits for every warp's rows of A; groups 0 and 1 go on to P1
       if (grp == 2) {  // FULL once T has landed: the consumer does not wait for P1 below
         asm volatile("bar.sync 6, 384;" ::: "memory");
-        // P' is visible in the consumer (cluster fence + barrier above): arrive, and expect T
-        if (tid == 256) mbar_arrive_expect_tx_remote(bar(BAR_F0 + b), 0, 16384);
         inverse(sm + off_st(b), pA, pT, pS);
         fence_proxy_async();
         asm volatile("bar.sync 3, 128;" ::: "memory");

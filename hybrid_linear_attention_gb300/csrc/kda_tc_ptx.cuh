@@ -102,6 +102,23 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, ui
       "r"(src), "r"(bytes), "r"(rb)
       : "memory");
 }
+// the shared::cluster address of this CTA's shared-memory location `addr` in CTA `rank`
+__device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// asynchronous 16-byte store into another CTA's shared memory (shared::cluster address
+// `raddr`), completing on that CTA's mbarrier `rbar` (complete_tx of 16 bytes): the receiver
+// sees the data once it observes the barrier's phase, with no cluster fence by the sender
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float4 v, uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          raddr),
+      "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+      "r"(__float_as_uint(v.w)), "r"(rbar)
+      : "memory");
+}
 __device__ __forceinline__ void fence_cluster() {
   asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }
