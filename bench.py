@@ -91,6 +91,22 @@ def _prefill_flops(T, H, d, C=64):
     return T / C * H * per
 
 
+# the survey's triangle-aware count of the prefill's dense work per head and token at d = 128,
+# C = 64: 2 (3 d^2 + 2.5 C d)
+SURVEY_FLOPS_PER_HEAD_TOKEN = 2 * (3 * 128 * 128 + 2.5 * 64 * 128)
+
+
+def _prefill_bytes_batch(lengths, H, d, *, gate, state_in, state_bytes=4):
+    """Algorithmic HBM bytes of one kda_prefill launch over a packed batch: per token q, k, v,
+    out (bf16), g (fp32), beta (fp32) and, with the output norm and gate, the gate logits
+    (bf16); per sequence the final state and, when given, the initial state."""
+    T = int(sum(lengths))
+    per_tok = H * d * (2 * 3 + 4 + 2) + H * 4 + (H * d * 2 if gate else 0)
+    n = len(lengths)
+    st = H * d * d * state_bytes
+    return T * per_tok + n * st * (2 if state_in else 1)
+
+
 def _prologue_bytes(T, H, d):
     """kda_prologue as the step runs it: read raw x (3Hd bf16) + beta logits; write q, k, v
     (bf16) and beta (fp32)."""
@@ -232,13 +248,35 @@ def _oracle_prefill_sample(heads, seed=0):
 CPU_SAMPLE_HEADS = 32
 
 
+CPU_SINGLE_HEADS = 4
+
+
+def _oracle_single_thread(heads=CPU_SINGLE_HEADS, seed=5):
+    """The oracle's fp64 recurrence on one host thread over `heads` heads of the prefill
+    workload (T = 4096, post-conv inputs drawn directly); returns seconds."""
+    import oracle
+    from hybrid_linear_attention_gb300 import inputs
+
+    inp = inputs.kda_inputs([T_PREFILL], heads, D, seed=seed)
+    t0 = time.perf_counter()
+    oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["cu_seqlens"],
+                       n_threads=1)
+    return time.perf_counter() - t0
+
+
 def _cpu_baseline():
     secs, threads = _oracle_prefill_sample(CPU_SAMPLE_HEADS)
     # tokens/s/layer: the sample covers CPU_SAMPLE_HEADS of the layer's H heads
     value = T_PREFILL * CPU_SAMPLE_HEADS / H / secs
+    s1 = _oracle_single_thread()
+    v1 = T_PREFILL * CPU_SINGLE_HEADS / H / s1
     return {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"T=4096 tokens x {CPU_SAMPLE_HEADS} of 64 heads (prologue + fp64 "
-                      f"recurrence), scaled to one full layer; {secs:.2f} s wall"}
+                      f"recurrence), scaled to one full layer; {secs:.2f} s wall",
+            "single_thread": {"value": v1, "unit": "tokens/s", "cores": 1,
+                              "sample": f"T=4096 tokens x {CPU_SINGLE_HEADS} of 64 heads (fp64 "
+                                        f"recurrence, one host thread), scaled to one full "
+                                        f"layer; {s1:.2f} s wall"}}
 
 
 def run_reference(args):
@@ -382,6 +420,13 @@ def run_ours(args):
     # ---- end to end through the host-buffer call (kda_prefill_host) -----------------
     e2e_line = _e2e(wl, flush, args, dist) if not args.no_e2e else None
 
+    # ---- the other prefill workloads: long-context gated (4 x 32768) and the packed
+    #      variable-length batch (~500K tokens; fp32 and bf16 state storage) ----------------
+    long_ctx = varlen = None
+    if not args.no_configs:
+        long_ctx = _long_context_bench(dev, kda, inputs, hbm, tflops, args)
+        varlen = _varlen_bench(dev, kda, inputs, hbm, args)
+
     # ---- decode: 256 sequences x 100 fused steps --------------------------------------
     dec = dmulti = mla = None
     if not args.no_decode:
@@ -420,7 +465,11 @@ def run_ours(args):
                                 "peak_tflops": tflops,
                                 "frac": pf_flops / (pf * 1e-3) / 1e12 / tflops,
                                 "peak_kind": f"{peak_kind} bf16_tflops (burst)",
-                                "algorithmic_flops_per_launch": pf_flops}},
+                                "algorithmic_flops_per_launch": pf_flops,
+                                # the survey's triangle-aware count, 139,264 flop per head-token
+                                "survey_flops_per_head_token": SURVEY_FLOPS_PER_HEAD_TOKEN,
+                                "survey_frac": SURVEY_FLOPS_PER_HEAD_TOKEN * T_PREFILL * H
+                                               / (pf * 1e-3) / 1e12 / tflops}},
         "gpu_launches": int(launches),
         "gpu_launches_per_step": launches / args.steps,
         "wall_s_timed_region": wall,
@@ -428,6 +477,10 @@ def run_ours(args):
     }
     if e2e_line:
         line["e2e"] = e2e_line
+    if long_ctx:
+        line["long_context_gated"] = long_ctx
+    if varlen:
+        line["varlen_500k"] = varlen
     if dec:
         line["decode"] = dec
     if dmulti:
@@ -474,6 +527,83 @@ def _e2e(wl, flush, args, dist):
     return {"value": ws_ * T_PREFILL / (e2e * 1e-3), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e,
             "api": "kda_prefill_host", "segment_tokens": E2E_SEGMENT}
+
+
+def _time_prefill(kda, p, inp, out, fin, *, gate, reps, flush):
+    """CUDA-event milliseconds of kda_prefill over a resident batch (L2 flushed between
+    launches; 3 untimed launches first)."""
+    ts = []
+    for i in range(3 + reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        kda.kda_prefill(p, inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                        inp["cu_seqlens"], out, init_state=inp.get("init_state"),
+                        final_state=fin, gate_logit=inp["gate"] if gate else None,
+                        norm_w=inp["norm_w"] if gate else None)
+        e1.record()
+        e1.synchronize()
+        if i >= 3:
+            ts.append(e0.elapsed_time(e1))
+    kda.kda_check_device_error()
+    return sum(ts) / len(ts)
+
+
+def _long_context_bench(dev, kda, inputs, hbm, tflops, args):
+    """Long-context prefill: 4 sequences x 32768 tokens, H = 64, d = 128, bf16 q, k, v drawn
+    N(0,1) as the post-conv streams, fp32 log-retention U(-5,0) and beta, nonzero initial
+    state ~N(0,0.02), the output RMSNorm x sigmoid(gate) with gate logits ~N(0,1)."""
+    lens = [32768] * 4
+    inp = inputs.kda_inputs(lens, H, D, seed=700, device=dev, init_state="all", gate=True)
+    p = kda.params(H=H, d=D)
+    T = sum(lens)
+    out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((len(lens), H, D, D), dtype=torch.float32, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    ms = _time_prefill(kda, p, inp, out, fin, gate=True, reps=min(args.steps, 5), flush=flush)
+    b = _prefill_bytes_batch(lens, H, D, gate=True, state_in=True)
+    gbs = b / (ms * 1e-3) / 1e9
+    tf = SURVEY_FLOPS_PER_HEAD_TOKEN * T * H / (ms * 1e-3) / 1e12
+    del inp, out, fin
+    torch.cuda.empty_cache()
+    return {"workload": "4 x 32768 tokens, H=64, d=128, bf16 q/k/v, fp32 g/beta/state, initial "
+                        "state ~N(0,0.02), output RMSNorm(128) x sigmoid(gate), gate logits "
+                        "~N(0,1) bf16",
+            "ms": ms, "tokens_per_s": T / (ms * 1e-3),
+            "roofline": {"kernel": "kda_prefill (gated)", "bound": "hbm", "achieved": gbs,
+                         "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                         "algorithmic_bytes_per_launch": b,
+                         "bytes_per_token": 114944,
+                         "tensor_frac": tf / tflops}}
+
+
+def _varlen_bench(dev, kda, inputs, hbm, args):
+    """The packed variable-length batch: 32 sequences, lengths log-uniform in [512, 65536]
+    (total ~500K tokens), even-indexed sequences from a nonzero initial state; once with fp32
+    and once with bf16 state storage."""
+    lens, _ = inputs.varlen_lengths(n_seqs=32, seed=0)
+    T = sum(lens)
+    res = {"workload": f"32 sequences, log-uniform lengths in [512, 65536], {T} tokens packed "
+                       f"by cu_seqlens, H=64, d=128, bf16 I/O, even sequences from ~N(0,0.02)",
+           "tokens": T}
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    for name, sd in (("fp32_state", torch.float32), ("bf16_state", torch.bfloat16)):
+        inp = inputs.kda_inputs(lens, H, D, seed=710, device=dev, init_state="even",
+                                state_dtype=sd)
+        p = kda.params(H=H, d=D, state_dtype=sd)
+        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+        fin = torch.empty((len(lens), H, D, D), dtype=sd, device=dev)
+        ms = _time_prefill(kda, p, inp, out, fin, gate=False, reps=min(args.steps, 3),
+                           flush=flush)
+        b = _prefill_bytes_batch(lens, H, D, gate=False, state_in=True,
+                                 state_bytes=2 if sd == torch.bfloat16 else 4)
+        gbs = b / (ms * 1e-3) / 1e9
+        res[name] = {"ms": ms, "tokens_per_s": T / (ms * 1e-3),
+                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                  "frac": gbs / hbm, "algorithmic_bytes_per_launch": b}}
+        del inp, out, fin
+        torch.cuda.empty_cache()
+    return res
 
 
 def _decode_bench(dev, kda, inputs, hbm, rank, args):
@@ -668,6 +798,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

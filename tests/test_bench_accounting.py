@@ -88,3 +88,23 @@ def test_reference_arm_prints_one_contract_line(capsys):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"] == {"value": line["value"], "unit": "tokens/s",
                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_batch_prefill_bytes_for_the_gated_and_varlen_workloads():
+    """Per token q, k, v, out (bf16), g, beta (fp32) and the gate logits (bf16) when the output
+    norm and gate run: the survey's 114,944 bytes per token at 64 heads; per sequence the
+    initial and final state."""
+    lens = [32768] * 4
+    per_tok = 3 * H * D * BF16 + H * D * F32 + H * F32 + H * D * BF16 + H * D * BF16
+    assert per_tok == 114_944
+    states = 4 * 2 * H * D * D * F32
+    assert bench._prefill_bytes_batch(lens, H, D, gate=True, state_in=True) == \
+        sum(lens) * per_tok + states
+    # bf16 state storage halves the state bytes; without an initial state only the final
+    assert bench._prefill_bytes_batch([100, 28], H, D, gate=False, state_in=False,
+                                      state_bytes=2) == 128 * 98_560 + 2 * H * D * D * 2
+
+
+def test_survey_flop_count_per_head_token():
+    # 2 (3 d^2 + 2.5 C d) at d = 128, C = 64
+    assert bench.SURVEY_FLOPS_PER_HEAD_TOKEN == 139_264
