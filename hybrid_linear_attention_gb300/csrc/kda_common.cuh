@@ -3,6 +3,8 @@
 
 #include "kda_internal.h"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -12,6 +14,21 @@
 namespace kda {
 
 typedef __nv_bfloat16 bf16;
+
+// The driver's tensor-map encoder (cuTensorMapEncodeTiled), looked up once through the
+// runtime; nullptr when the driver does not provide it.
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
+  return fn;
+}
 
 // Sticky device error bits (written by kernels whose bounded waits ran out).
 // device error flag bits (ERR_*): kda_internal.h

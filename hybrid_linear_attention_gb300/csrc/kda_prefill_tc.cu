@@ -1340,20 +1340,6 @@ __global__ void __launch_bounds__(NT, 1)
 
 // ---- host side --------------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    cudaDriverEntryPointQueryResult q;
-    void *p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
 
 bool make_map(CUtensorMap *m, const void *ptr, bool f32, int64_t T, int H) {
   const int esz = f32 ? 4 : 2;
@@ -1361,7 +1347,7 @@ bool make_map(CUtensorMap *m, const void *ptr, bool f32, int64_t T, int H) {
   cuuint64_t strides[2] = {(cuuint64_t)D * esz, (cuuint64_t)H * D * esz};
   cuuint32_t box[3] = {(cuuint32_t)(128 / esz), 1, (cuuint32_t)C};
   cuuint32_t es[3] = {1, 1, 1};
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
             const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1377,7 +1363,7 @@ bool make_out_map(CUtensorMap *m, void *ptr, int64_t T, int H, bool fp8) {
   cuuint64_t strides[2] = {(cuuint64_t)D * esz, (cuuint64_t)H * D * esz};
   cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)C};
   cuuint32_t es[3] = {1, 1, 1};
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   return fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr,
             dims, strides, box, es,
@@ -1453,7 +1439,7 @@ bool prefill_tc_supported(int d, bool io_bf16) {
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
     return false;
-  return major == 10 && encode_fn() != nullptr;
+  return major == 10 && tensor_map_encoder() != nullptr;
 }
 
 cudaError_t launch_prefill_tc(const TcArgs &a, int64_t total_tokens, bool st_bf16,

@@ -9,14 +9,13 @@
 // up-projection W_V,i comes after the weighted sum; a per-head sigmoid gate scales the head's
 // 128-wide output.
 //
-// Kernels:
-//   mla_absorb_kernel   q_cat = [W_K,i^T q_i^N ; q_i^R] (bf16), a CTA per (head, 8 sequences).
+// Kernels (the two projections around the attention are in mla_proj.cu):
 //   mla_latent_kernel   per sequence, all 64 heads: S^T = C Q^T over 128-position tiles of the
 //                       cache (tcgen05, C K-major, Q K-major, fp32 in TMEM), online softmax on
 //                       the CUDA cores, Z^T += C^T P^T with the same C tile read MN-major and P
 //                       written MN-major over the tile's positional block (tcgen05, 4 M-slices
 //                       of 128 latent channels); Z rescaled in TMEM when a head's max moves.
-//   mla_up_gate_kernel  o_i = W_V,i z_i * sigmoid(gate_i), a CTA per (head, 8 sequences).
+//   mla_combine_kernel  the split partial sums merged to a common maximum.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_tc_ptx.cuh"
@@ -38,8 +37,6 @@ constexpr int MH = 64;        // heads
 constexpr int ML = 512;       // latent width
 constexpr int MR = 64;        // positional-key width
 constexpr int MK = ML + MR;   // cached key width
-constexpr int MV = 128;       // per-head value width after the up-projection
-constexpr int MN = 128;       // per-head non-positional query width
 constexpr int TP = 64;        // cached positions per tile
 constexpr int KB = MK / 64;   // 64-element key blocks (128 bytes of bf16)
 constexpr int MLA_NT = 160;   // four softmax warps (the four TMEM lane quarters) + an issuer warp
@@ -334,82 +331,6 @@ __global__ void __launch_bounds__(MLA_NT, 1)
   if (warp == 0) tmem_dealloc(tm, 512);
 }
 
-// q_cat[b][h] = [W_K,h^T q_nope[b][h] ; q_rope[b][h]] (bf16), MQB sequences per CTA
-constexpr int MQB = 16;  // sequences per CTA: each head's weights are read once per 16
-__global__ void __launch_bounds__(128) mla_absorb_kernel(const MlaArgs a) {
-  const int h = blockIdx.x, b0 = blockIdx.y * MQB, tid = threadIdx.x;
-  __shared__ float s_q[MQB][MN];
-  for (int e = tid; e < MQB * MN; e += 128) {
-    const int bb = e / MN, n = e % MN;
-    s_q[bb][n] = b0 + bb < a.B ? __bfloat162float(
-                                     reinterpret_cast<const bf16 *>(a.q_nope)[((size_t)(b0 + bb) * MH + h) * MN + n])
-                               : 0.f;
-  }
-  __syncthreads();
-  float acc[MQB][4];
-#pragma unroll
-  for (int bb = 0; bb < MQB; ++bb) acc[bb][0] = acc[bb][1] = acc[bb][2] = acc[bb][3] = 0.f;
-  const bf16 *w = reinterpret_cast<const bf16 *>(a.w_uk) + (size_t)h * MN * ML + 4 * tid;
-#pragma unroll 4
-  for (int n = 0; n < MN; ++n) {
-    const uint2 u = *reinterpret_cast<const uint2 *>(w + (size_t)n * ML);
-    const float w0 = __uint_as_float(u.x << 16), w1 = __uint_as_float(u.x & 0xffff0000u);
-    const float w2 = __uint_as_float(u.y << 16), w3 = __uint_as_float(u.y & 0xffff0000u);
-#pragma unroll
-    for (int bb = 0; bb < MQB; ++bb) {
-      const float q = s_q[bb][n];
-      acc[bb][0] = fmaf(w0, q, acc[bb][0]);
-      acc[bb][1] = fmaf(w1, q, acc[bb][1]);
-      acc[bb][2] = fmaf(w2, q, acc[bb][2]);
-      acc[bb][3] = fmaf(w3, q, acc[bb][3]);
-    }
-  }
-  bf16 *qc = reinterpret_cast<bf16 *>(a.q_cat);
-#pragma unroll
-  for (int bb = 0; bb < MQB; ++bb) {  // unrolled: the accumulators stay in registers
-    if (b0 + bb >= a.B) break;
-    bf16 *row = qc + ((size_t)(b0 + bb) * MH + h) * MK;
-#pragma unroll
-    for (int y = 0; y < 4; ++y) row[4 * tid + y] = __float2bfloat16_rn(acc[bb][y]);
-    if (tid < MR)
-      row[ML + tid] = reinterpret_cast<const bf16 *>(a.q_rope)[((size_t)(b0 + bb) * MH + h) * MR + tid];
-  }
-}
-
-// out[b][h] = W_V,h z[b][h] * sigmoid(gate[b][h]) (bf16), MQB sequences per CTA
-__global__ void __launch_bounds__(128) mla_up_gate_kernel(const MlaArgs a) {
-  const int h = blockIdx.x, b0 = blockIdx.y * MQB, v = threadIdx.x;
-  __shared__ float s_z[MQB][ML];
-  for (int e = v; e < MQB * ML; e += 128) {
-    const int bb = e / ML, l = e % ML;
-    s_z[bb][l] = b0 + bb < a.B ? a.z[((size_t)(b0 + bb) * MH + h) * ML + l] : 0.f;
-  }
-  __syncthreads();
-  float acc[MQB];
-#pragma unroll
-  for (int bb = 0; bb < MQB; ++bb) acc[bb] = 0.f;
-  const bf16 *w = reinterpret_cast<const bf16 *>(a.w_uv) + ((size_t)h * MV + v) * ML;
-#pragma unroll 2
-  for (int l = 0; l < ML; l += 8) {
-    const uint4 u = *reinterpret_cast<const uint4 *>(w + l);
-    const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int y = 0; y < 4; ++y) {
-      const float wa = __uint_as_float(ws[y] << 16), wb = __uint_as_float(ws[y] & 0xffff0000u);
-#pragma unroll
-      for (int bb = 0; bb < MQB; ++bb)
-        acc[bb] = fmaf(wb, s_z[bb][l + 2 * y + 1], fmaf(wa, s_z[bb][l + 2 * y], acc[bb]));
-    }
-  }
-#pragma unroll
-  for (int bb = 0; bb < MQB; ++bb) {  // unrolled: the accumulators stay in registers
-    if (b0 + bb >= a.B) break;
-    const size_t hb = (size_t)(b0 + bb) * MH + h;
-    const float g = __bfloat162float(reinterpret_cast<const bf16 *>(a.gate)[hb]);
-    reinterpret_cast<bf16 *>(a.out)[hb * MV + v] = __float2bfloat16_rn(acc[bb] * sigmoidf_(g));
-  }
-}
-
 // z[b][h] = sum_s 2^(m_s - M) Z_s / sum_s 2^(m_s - M) l_s over the splits (M = max_s m_s)
 __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaArgs a, int n_split) {
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
@@ -432,24 +353,10 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaArgs a, int n
       make_float4(acc[0] * r, acc[1] * r, acc[2] * r, acc[3] * r);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 mla_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    cudaDriverEntryPointQueryResult q;
-    void *p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
 
 // [n3][rows][576] bf16, boxes of 64 elements x box_rows rows, 128-byte swizzle
 bool mla_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t n3, uint32_t box_rows) {
-  auto fn = mla_encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)MK, (cuuint64_t)rows, (cuuint64_t)n3};
   cuuint64_t strides[2] = {(cuuint64_t)MK * 2, (cuuint64_t)rows * MK * 2};
@@ -517,13 +424,7 @@ bool mla_latent_supported() {
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
     return false;
-  return major == 10 && mla_encode_fn() != nullptr;
-}
-
-cudaError_t launch_mla_absorb(const MlaArgs &a, cudaStream_t s) {
-  if (a.B == 0) return cudaSuccess;
-  mla_absorb_kernel<<<dim3(MH, (a.B + MQB - 1) / MQB), 128, 0, s>>>(a);
-  return cudaGetLastError();
+  return major == 10 && tensor_map_encoder() != nullptr;
 }
 
 cudaError_t launch_mla_latent(const MlaArgs &a, cudaStream_t s) {
@@ -547,12 +448,6 @@ cudaError_t launch_mla_latent(const MlaArgs &a, cudaStream_t s) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || ns == 1) return e;
   mla_combine_kernel<<<dim3(a.B, MH), 128, 0, s>>>(a, ns);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_mla_up_gate(const MlaArgs &a, cudaStream_t s) {
-  if (a.B == 0) return cudaSuccess;
-  mla_up_gate_kernel<<<dim3(MH, (a.B + MQB - 1) / MQB), 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 
