@@ -92,6 +92,10 @@ cudaError_t launch_state_accept(const void *step_states, void *pool, const int32
                                 const int32_t *slot_idx, int n_slots, int n_seqs, int K, int H,
                                 int D, bool st_bf16, int *err, cudaStream_t s);
 cudaError_t launch_prologue(const ProArgs &a, int D, bool io_bf16, cudaStream_t s);
+// the one-token decode step at d = 128 (kda_decode.cu): serves decode calls without step
+// states or checkpoints
+bool decode_one_serves(const RecArgs &a, int D);
+cudaError_t launch_decode_one(const RecArgs &a, bool io_bf16, bool st_bf16, cudaStream_t s);
 // out[k] <- the three raw inputs before checkpoint k (conv tail at that position)
 cudaError_t launch_wait_probe(long limit, int *err, cudaStream_t s);
 bool mla_latent_supported();

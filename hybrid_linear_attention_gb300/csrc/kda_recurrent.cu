@@ -360,6 +360,7 @@ cudaError_t launch_state_accept(const void *step_states, void *pool, const int32
 
 cudaError_t launch_recurrent(const RecArgs &a, int D, bool io_bf16, bool st_bf16,
                              cudaStream_t s) {
+  if (decode_one_serves(a, D)) return launch_decode_one(a, io_bf16, st_bf16, s);
   if (D == 128) return launch_d<128, 256>(a, io_bf16, st_bf16, s);
   if (D == 16) return launch_d<16, 64>(a, io_bf16, st_bf16, s);
   return cudaErrorInvalidValue;
