@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
       const ST *src = reinterpret_cast<const ST *>(a.state_in) + sbase;
 #pragma unroll
       for (int r = 0; r < RPT; ++r) {
-        const float4 x = load4(src + (size_t)(rg * RPT + r) * D + 4 * cg);
+        const float4 x = load4_stream(src + (size_t)(rg * RPT + r) * D + 4 * cg);
         S[r][0] = x.x, S[r][1] = x.y, S[r][2] = x.z, S[r][3] = x.w;
       }
     } else {
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
           ST *dst = reinterpret_cast<ST *>(a.step_states) + ((size_t)(t0 + tt) * H + h) * D * D;
 #pragma unroll
           for (int r = 0; r < RPT; ++r)
-            store4(dst + (size_t)(rg * RPT + r) * D + 4 * cg,
+            store4_stream(dst + (size_t)(rg * RPT + r) * D + 4 * cg,
                    make_float4(S[r][0], S[r][1], S[r][2], S[r][3]));
         }
         const size_t row = ((size_t)(t0 + tt) * H + h) * D + tid;
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const RecArgs a) {
       ST *dst = reinterpret_cast<ST *>(a.state_out) + sbase;
 #pragma unroll
       for (int r = 0; r < RPT; ++r)
-        store4(dst + (size_t)(rg * RPT + r) * D + 4 * cg,
+        store4_stream(dst + (size_t)(rg * RPT + r) * D + 4 * cg,
                make_float4(S[r][0], S[r][1], S[r][2], S[r][3]));
     }
   }  // units
