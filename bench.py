@@ -677,8 +677,12 @@ def _mla_bench(dev, kda, inputs, hbm, rank):
     q_cat = torch.empty((B, 64, 576), dtype=torch.bfloat16, device=dev)
     z = torch.empty((B, 64, 512), dtype=torch.float32, device=dev)
     out = torch.empty((B, 64, 128), dtype=torch.bfloat16, device=dev)
-    step = lambda: kda.mla_decode(q_nope, q_rope, w_uk, w_uv, cache, lengths, gate, q_cat, z, out)
-    lat = lambda: kda.mla_decode_latent(q_cat, cache, lengths, z)
+    # the workspace the library asks for (none at 256 sequences: no split pays)
+    ws_n = kda.mla_decode_workspace_size(B, L)
+    ws = torch.empty(max(ws_n // 4, 1), dtype=torch.float32, device=dev) if ws_n else None
+    step = lambda: kda.mla_decode(q_nope, q_rope, w_uk, w_uv, cache, lengths, gate, q_cat, z, out,
+                                  workspace=ws)
+    lat = lambda: kda.mla_decode_latent(q_cat, cache, lengths, z, workspace=ws)
     reps = 20
     res = {}
     for name, fn in (("latent", lat), ("step", step)):
@@ -701,7 +705,7 @@ def _mla_bench(dev, kda, inputs, hbm, rank):
             "workload": "256 sequences x 4096 cached positions, 64 heads, 576-wide bf16 latent "
                         "cache (512 latent + 64 positional key; 1.21 GB, > L2), one query token "
                         "each, synthetic weights",
-            "ms_latent": res["latent"], "ms_step": res["step"],
+            "ms_latent": res["latent"], "ms_step": res["step"], "workspace_bytes": ws_n,
             "tokens_per_s": B / (res["step"] * 1e-3),
             "roofline": {"kernel": "mla_decode_latent", "bound": "hbm", "achieved": gbs,
                          "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
