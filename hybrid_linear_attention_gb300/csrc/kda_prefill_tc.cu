@@ -26,10 +26,10 @@
 //   TMEM columns   [0,128) S^T   [128,256) TA   [256,384) TB   [384,512) TC
 // The read of the state by the query rows, O = (Q Gamma) S + P u, can nearly cancel, so a
 // tf32 rounding of either factor (the tensor core also truncates a tf32 operand it reads from
-// tensor memory) would show in the output after its norm: the query rows' read is three bf16
-// products (hi*hi + hi*lo + lo*hi) of Q Gamma and of the state split into bf16 hi + lo (the
-// split state kept in TA while TA is otherwise idle), good to ~2^-16.  The key rows, whose
-// products feed the writes, read the truncated tf32 state against tf32 K Gamma.
+// tensor memory) would show in the output after its norm: the state read X = [K Gamma;
+// Q Gamma] S is three bf16 products (hi*hi + hi*lo + lo*hi) of [K Gamma; Q Gamma] and of the
+// state split into bf16 hi + lo (the split state kept in TA while TA is otherwise idle), good
+// to ~2^-16, one product of N = 128 for the key and the query rows together.
 // A and P (64 x 64 each, K = 128) come from one product on the tensor core:
 // [Ktil; Qtil] (128 rows, bf16 hi + lo in tensor memory) times the stacked Khat^(R) rows
 // (160, bf16 in shared memory), hi*hi everywhere and hi*lo + lo*hi on the band (a 16-token
@@ -62,7 +62,7 @@ constexpr uint32_t OFF_Q = 0;        // q bf16 [64][128], two 128B-swizzled boxe
 constexpr uint32_t OFF_K = 16384;    // k
 constexpr uint32_t OFF_V = 32768;    // v
 constexpr uint32_t OFF_G = 49152;    // g -> cumulative log2-retention, fp32, 4 boxes of 32
-constexpr uint32_t OFF_X = 81920;    // 64 KB: K Gamma tf32 | Q Gamma bf16 hi | lo -> Kbar hi | Kbar lo |
+constexpr uint32_t OFF_X = 81920;    // 64 KB: [K Gamma; Q Gamma] bf16 hi | lo -> Kbar hi | Kbar lo |
                                      //        u hi | u lo
 constexpr uint32_t OFF_T = 147456;   // 16 KB: T fp32 (plain) -> T tf32 (K-major)
 constexpr uint32_t OFF_P = 163840;   // 16 KB: P' tf32 (K-major)
@@ -80,11 +80,10 @@ constexpr uint32_t TM_AH = 128, TM_AL = 192, TM_D = 256;
 
 // TMA loads and tensor-core completion; in a cluster pair, the consumer's FULL (landing
 // buffer 0 / 1 holds T and P') and the producer's EMPTY (buffer 0 / 1 may be rewritten)
-// (a cluster-pair consumer commits its state read on BAR_X, key rows, and BAR_XQ, query rows:
-// it issues that product from another thread than the rest, and a commit tracks only the
-// products of the thread that issues it)
+// (a cluster-pair consumer commits its state read on BAR_X: it issues that product from another
+// thread than the rest, and a commit tracks only the products of the thread that issues it)
 enum { BAR_Q = 0, BAR_K, BAR_V, BAR_G, BAR_MMA, BAR_F0, BAR_F1, BAR_E0, BAR_E1, BAR_GT, BAR_X,
-       BAR_XQ, NBAR };
+       NBAR };
 // consumer landing buffers b = 0, 1: T then P' (16 KB each, tf32 K-major); buffer 0 is the
 // fused kernel's own T and P' region
 __host__ __device__ constexpr uint32_t off_lt(int b) { return 147456u + 32768u * (uint32_t)b; }
@@ -223,7 +222,7 @@ struct Maps {
 
 // 32 fp32 state values of one lane (key channels 32 g32 .. 32 g32 + 31) split into bf16 hi +
 // lo, stored as packed pairs (low half = the even channel) in TA: hi at columns 16 g32 ..,
-// lo 64 columns further (the A operand of the query rows' read)
+// lo 64 columns further (the A operand of the state read)
 __device__ __forceinline__ void split_state_block(uint32_t t_lane, int g32, const float (&v)[32]) {
   float hw[16], lw[16];
 #pragma unroll
@@ -465,7 +464,7 @@ __global__ void __launch_bounds__(NT, 1)
   };
 
   const uint32_t ID_64 = idesc(2, 128, 64, 0, 0);
-  const uint32_t ID_XQ = idesc(1, 128, 64, 0, 0);
+  const uint32_t ID_X = idesc(1, 128, 128, 0, 0);
   const uint32_t ID_UPD = idesc(1, 128, 128, 0, 1);
   const uint32_t ID_AP160 = idesc(1, 128, 160, 0, 0);
   const uint32_t ID_AP112 = idesc(1, 128, 112, 0, 0);
@@ -621,13 +620,12 @@ __global__ void __launch_bounds__(NT, 1)
       }
       commit(mma_par);
   };
-  // K Gamma (tf32, K-major, 64 rows) at X[0, 32K); Q Gamma as bf16 hi | lo (K-major, 64
-  // rows) at X[32K, 48K) | X[48K, 64K)
+  // [K Gamma; Q Gamma] as bf16 hi | lo, K-major 128 rows (K rows 0-63, Q rows 64-127), at
+  // X[0, 32K) | X[32K, 64K)
   auto x_rows = [&](int nv) {
-    for (int it = tid; it < C * 16; it += NT) {  // (token, 8-channel group)
+    for (int it = tid; it < C * 16; it += NT) {  // (token, 8-channel group): rows r, 64 + r
       const int r = it >> 4, c8 = it & 15;
-      float ok8[8];
-      uint32_t qh[4], ql[4];
+      uint32_t kh[4], kl[4], qh[4], ql[4];
       if (r < nv) {
         float kv[8], qv[8], gg[8];
         bf_row8(sm + OFF_K, r, c8, kv);
@@ -637,24 +635,25 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int y = 0; y < 8; ++y) {
           const float G = ex2(gg[y]);
-          ok8[y] = to_tf32(kv[y] * rk * G);
+          kv[y] = kv[y] * rk * G;
           qv[y] = qv[y] * rq * G;
         }
 #pragma unroll
         for (int y = 0; y < 4; ++y) {
+          kh[y] = pack_bf2(kv[2 * y], kv[2 * y + 1]);
+          kl[y] = pack_bf2(kv[2 * y] - bf_lo(kh[y]), kv[2 * y + 1] - bf_hi(kh[y]));
           qh[y] = pack_bf2(qv[2 * y], qv[2 * y + 1]);
           ql[y] = pack_bf2(qv[2 * y] - bf_lo(qh[y]), qv[2 * y + 1] - bf_hi(qh[y]));
         }
       } else {
 #pragma unroll
-        for (int y = 0; y < 8; ++y) ok8[y] = 0.f;
-#pragma unroll
-        for (int y = 0; y < 4; ++y) qh[y] = ql[y] = 0u;
+        for (int y = 0; y < 4; ++y) kh[y] = kl[y] = qh[y] = ql[y] = 0u;
       }
-      st_f32x8(sm + OFF_X + kmaj_f32<64>(r, 8 * c8), sm + OFF_X + kmaj_f32<64>(r, 8 * c8 + 4), ok8);
-      const uint32_t qo = kmaj_bf16<64>(r, 8 * c8);
-      *reinterpret_cast<uint4 *>(sm + OFF_X + 32768 + qo) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
-      *reinterpret_cast<uint4 *>(sm + OFF_X + 49152 + qo) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
+      const uint32_t ko = kmaj_bf16<128>(r, 8 * c8), qo = kmaj_bf16<128>(64 + r, 8 * c8);
+      *reinterpret_cast<uint4 *>(sm + OFF_X + ko) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+      *reinterpret_cast<uint4 *>(sm + OFF_X + 32768 + ko) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
+      *reinterpret_cast<uint4 *>(sm + OFF_X + qo) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
+      *reinterpret_cast<uint4 *>(sm + OFF_X + 32768 + qo) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
     }
   };
   // P' rows go to pbase (this CTA's shared memory) or, with rbase != 0, into the consumer's
@@ -714,28 +713,22 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
   };
-  // ---- MMA1 (thread 0): X_k^T = S^T (K Gamma)^T (tf32, A = S^T from TMEM) -> TC[0, 64),
-  //      committed on its own (the state chain waits only for it); then the query rows
-  //      X_q^T = S^T (Q Gamma)^T -> TC[64, 128) as bf16 hi*hi + hi*lo + lo*hi with the split
-  //      state from TA.  One CTA: both on BAR_MMA, the query rows completing under the next
-  //      commit (u = T Y, issued after them by the same thread); cluster-pair consumer
-  //      (issued by thread 256): key rows on BAR_X, query rows on BAR_XQ, phase = chunk parity
-  auto mma1_issue = [&](bool own_bars, uint32_t par) {
-      for (int ks = 0; ks < 16; ++ks) {
-        const uint64_t bd = sdesc_sw128(sb + OFF_X + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-        mma_tf32_ts(tm + TM_C, tm + TM_S + 8 * ks, bd, ID_64, ks > 0);
-      }
-      if (own_bars) commit_on(BAR_X, par);
-      else commit(mma_par);
+  // ---- MMA1: X^T = S^T [K Gamma; Q Gamma]^T -> TC (N = 128: key rows in TC[0, 64), query
+  //      rows in TC[64, 128)) as bf16 hi*hi + hi*lo + lo*hi with the split state from TA.
+  //      One CTA: issued by thread 0, committed on BAR_MMA; cluster-pair consumer: issued by
+  //      thread 256 and committed on BAR_X (phase = chunk parity), since a commit tracks only
+  //      the products of the thread that issues it
+  auto mma1_issue = [&](bool own_bar, uint32_t par) {
       for (int term = 0; term < 3; ++term) {
         const uint32_t a_col = TM_A + (term == 2 ? 64 : 0);              // S hi | S lo
-        const uint32_t b_off = OFF_X + (term == 1 ? 49152 : 32768);      // Q hi | Q lo
+        const uint32_t b_off = OFF_X + (term == 1 ? 32768 : 0);          // hi | lo rows
         for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t bd = sdesc_sw128(sb + b_off + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-          mma_bf16_ts(tm + TM_C + 64, tm + a_col + 8 * ks, bd, ID_XQ, term > 0 || ks > 0);
+          const uint64_t bd = sdesc_sw128(sb + b_off + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+          mma_bf16_ts(tm + TM_C, tm + a_col + 8 * ks, bd, ID_X, term > 0 || ks > 0);
         }
       }
-      if (own_bars) commit_on(BAR_XQ, par);
+      if (own_bar) commit_on(BAR_X, par);
+      else commit(mma_par);
   };
   // the state split into bf16 hi | lo (packed pairs) in TA, 32-column blocks first ..
   // first+n-1 of this thread's lane quarter (the state's final value for the next MMA1)
@@ -799,11 +792,9 @@ __global__ void __launch_bounds__(NT, 1)
         *reinterpret_cast<float *>(tbase + kmaj_f32<64>(e >> 6, e & 63)) = tv[q];
       }
   };
-  // ---- groups 0 and 1: wait for MMA1, Y^T = beta (V - K Gamma S)^T (tf32 hi + lo in TB),
-  //      decay S^T by Gamma_C
-  // (decay_g0 / decay_n: the first group-relative 32-column block and how many this group
-  //  decays; the cluster-pair consumer hands the whole decay to warp group 2, which is free
-  //  while groups 0 and 1 form Y)
+  // ---- S^T *= Gamma_C on 32-column blocks first .. first + nblk - 1 of this warp's lane
+  //      quarter (the cluster-pair consumer hands the whole decay to warp group 2, which is
+  //      free while groups 0 and 1 form Y)
   auto decay = [&](int first, int nblk) {
 #pragma unroll 1
       for (int g32 = first; g32 < first + nblk; ++g32) {
@@ -817,8 +808,12 @@ __global__ void __launch_bounds__(NT, 1)
       }
       tmem_wait_st();
   };
+  // ---- groups 0 and 1: (one CTA) decay this group's 64 key channels of S^T while MMA1
+  //      runs, since MMA1 reads the split state in TA, not S; then wait for MMA1 and form
+  //      Y^T = beta (V - K Gamma S)^T (tf32 hi + lo in TB)
   auto y_decay = [&](int nv, uint32_t par, bool with_decay, bool own_bars) {
-      if (own_bars) wait(BAR_X, par);  // the key rows of MMA1 done
+      if (with_decay) decay(2 * grp, 2);
+      if (own_bars) wait(BAR_X, par);  // MMA1 done
       else wait(BAR_MMA, mma_par);
       tc_fence_after();
       wait(BAR_V, par);
@@ -844,8 +839,7 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_st32(tm + lane_off + TM_B + 32 * grp, hi);
         tmem_st32(tm + lane_off + TM_B + 64 + 32 * grp, xk);
       }
-      if (with_decay) decay(2 * grp, 2);  // this group's 64 key channels
-      else tmem_wait_st();
+      tmem_wait_st();
   };
   // thread 0: u^T = Y^T T^T, hi then lo (T at shared offset t_off), into TC[0, 64) (X_k has
   // been read by the Y pass)
@@ -1197,9 +1191,7 @@ __global__ void __launch_bounds__(NT, 1)
       if (tid == 256) mma1_issue(true, par);  // group 2 only decays in this phase
       if (grp < 2) {
         y_decay(nv, par, false, true);
-      } else {  // S^T *= Gamma_C once the key rows of MMA1, which read S, are done
-        wait(BAR_X, par);
-        tc_fence_after();
+      } else {  // S^T *= Gamma_C: MMA1 reads the split state in TA, not S
         decay(0, 4);
       }
       fence_proxy_async();
@@ -1220,7 +1212,6 @@ __global__ void __launch_bounds__(NT, 1)
       if (tid == 0 && more) issue((1u << BAR_K) | (1u << BAR_G), c + 1);
       wait(BAR_MMA, mma_par);  // u ready
       mma_par ^= 1;
-      if (grp < 2) wait(BAR_XQ, par);  // p6 rewrites the query rows' operands
       tc_fence_after();
       p6();
       fence_proxy_async();
@@ -1231,7 +1222,7 @@ __global__ void __launch_bounds__(NT, 1)
       mma_par ^= 1;
       tc_fence_after();
       if (tid == 0) mbar_arrive_remote(bar(BAR_E0 + b), 1);  // landing buffer b is free
-      // TA is free once the query rows' read is done; groups 0 and 1 split the state while
+      // TA is free once the state read is done; groups 0 and 1 split the state while
       // group 2 is still in P1
       if (grp < 2 && more) s_split(2 * grp, 2);
       p8(nv, t0, par);

@@ -10,11 +10,9 @@ type, so the model rounds each operand exactly there and accumulates in fp32:
     every column and hi*lo + lo*hi over the band (the row's own block and the one before);
   * T = (I + A)^-1: diagonal 16 x 16 blocks in fp32, off-diagonal blocks from tf32 products;
     T and P' stored as tf32 (round half away, as the kernel rounds on the bit pattern);
-  * X_k = (K Gamma) S (tf32 product): K Gamma rounded to tf32, the fp32 state truncated to
-    tf32 by the hardware;
-  * X_q = (Q Gamma) S as three bf16 products (hi*hi + hi*lo + lo*hi) of Q Gamma and of the
-    state, both split into bf16 hi + lo: the read can nearly cancel against P u, so it is
-    kept at ~2^-16;
+  * X = [K Gamma; Q Gamma] S as three bf16 products (hi*hi + hi*lo + lo*hi) of [K Gamma;
+    Q Gamma] and of the state, both split into bf16 hi + lo (~2^-16): the query rows' read
+    can nearly cancel against P u, and one product serves both row sets;
   * u = T Y with Y = beta (V - K Gamma S) split into tf32 hi + lo; O = X_q + P' tf32(u);
   * S <- Gamma_C S + Kbar^T u as three bf16 products (hi*hi + hi*lo + lo*hi).
 
@@ -54,8 +52,8 @@ SCHEMES = {
     # band: True = hi*lo + lo*hi on the row's own block and the one before; "own" = its own
     # block only; "all" = every block.  split_q False: the query rows (P) take hi*hi only
     "kernel": dict(dt=np.float32, split_ap=True, band=True, p=tf32, inv=tf32, t=tf32,
-                   x=tf32, s=tf32_trunc, xq="bf16x3", y_split=True, y=tf32, u=tf32,
-                   upd="bf16x3"),
+                   x=tf32, s=tf32_trunc, xq="bf16x3", xk="bf16x3", y_split=True, y=tf32,
+                   u=tf32, upd="bf16x3"),
     "all_bf16": dict(dt=np.float32, split_ap=False, band=False, p=bf16, inv=bf16, t=bf16,
                      x=bf16, s=bf16, y_split=False, y=bf16, u=bf16, upd="bf16"),
     "exact": dict(dt=np.float64, split_ap=False, band=False, p=_ident, inv=_ident, t=_ident,
@@ -146,6 +144,10 @@ def prefill_head(q, k, v, g, beta, S0, scheme, *, gate=None, norm_w=None, g_min=
             QGe = (qc * rqc * G).astype(dt)
             Qh, Sh = bf16(QGe), bf16(S)
             Xq = Qh @ Sh + bf16(QGe - Qh) @ Sh + Qh @ bf16(S - Sh)
+        if sc.get("xk") == "bf16x3":  # the key rows likewise
+            KGe = (kc * rkc * G).astype(dt)
+            Kh, Sh = bf16(KGe), bf16(S)
+            Xk = Kh @ Sh + bf16(KGe - Kh) @ Sh + Kh @ bf16(S - Sh)
         Y = bc[:, None] * (vc - Xk)
         if sc["y_split"]:
             Yh = sc["y"](Y)
