@@ -10,11 +10,12 @@
 // 128-wide output.
 //
 // Kernels (the two projections around the attention are in mla_proj.cu):
-//   mla_latent_kernel   per sequence, all 64 heads: S^T = C Q^T over 128-position tiles of the
-//                       cache (tcgen05, C K-major, Q K-major, fp32 in TMEM), online softmax on
-//                       the CUDA cores, Z^T += C^T P^T with the same C tile read MN-major and P
-//                       written MN-major over the tile's positional block (tcgen05, 4 M-slices
-//                       of 128 latent channels); Z rescaled in TMEM when a head's max moves.
+//   mla_latent_kernel   per sequence, all 64 heads: S = Q C^T over 64-position tiles of the
+//                       cache (tcgen05, M = 64 heads, Q and C K-major, fp32 in TMEM), online
+//                       softmax on the CUDA cores, Z^T += C^T P^T with the same C tile read
+//                       MN-major and P written K-major over the tile's positional block
+//                       (tcgen05, 4 M-slices of 128 latent channels); Z rescaled in TMEM when
+//                       a head's max moves.
 //   mla_combine_kernel  the split partial sums merged to a common maximum.
 #include "kda_common.cuh"
 #include "kda_internal.h"
@@ -39,7 +40,7 @@ constexpr int MR = 64;        // positional-key width
 constexpr int MK = ML + MR;   // cached key width
 constexpr int TP = 64;        // cached positions per tile
 constexpr int KB = MK / 64;   // 64-element key blocks (128 bytes of bf16)
-constexpr int MLA_NT = 160;   // four softmax warps (the four TMEM lane quarters) + an issuer warp
+constexpr int MLA_NT = 288;   // eight softmax warps (two per TMEM lane quarter) + an issuer warp
 
 // shared memory of the latent kernel (1024-byte aligned base): Q [KB][64 heads][128 B]
 // (72 KB, K-major) and two cache tiles [KB][64 positions][128 B] (72 KB each, TMA, 128-byte
@@ -69,10 +70,11 @@ __device__ __forceinline__ uint32_t sw128_row(int r, int j) {
   return (uint32_t)r * 128u + ((uint32_t)(j ^ (r & 7)) << 4);
 }
 
-// Warps 0-3: softmax and rescale (warp w reads TMEM lanes 32 w .. 32 w + 31; in S, whose
-// M = 64 rows sit in lanes 32 w + 0..15, lane l < 16 of warp w owns head 16 w + l and its
-// running maximum m and normaliser l).  Warp 4: TMA loads and tensor-core issue.  The two
-// sides meet only on mbarriers: C tile landed, S ready, P ready, Z done.
+// Warps 0-7: softmax and rescale (warp w reads TMEM lanes 32 (w & 3) .. + 31; in S, whose
+// M = 64 rows sit in lanes 32 (w & 3) + 0..15, lane l < 16 of warps w and w + 4 owns head
+// 16 (w & 3) + l, the first warp for a tile's positions 0-31 and the second for 32-63).
+// Warp 8: TMA loads and tensor-core issue.  The two sides meet only on mbarriers: C tile
+// landed, S ready, P ready, Z done.
 __global__ void __launch_bounds__(MLA_NT, 1)
     mla_latent_kernel(const MlaArgs a, const __grid_constant__ MlaMaps maps) {
   extern __shared__ uint8_t mraw[];
@@ -86,6 +88,7 @@ __global__ void __launch_bounds__(MLA_NT, 1)
   __shared__ uint32_t s_loads[2], s_mmas;
   __shared__ int s_stop;  // the softmax warps' exit decision, taken by one thread per tile
   __shared__ float s_alpha[MH], s_l[MH], s_mfin[MH];
+  __shared__ float s_pmax[2][MH], s_lpart[MH];  // a tile's half maxima; the second half's l
   __shared__ int s_rescale[2];  // by tile parity: set by the head owners, reset after use
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(MLA_NT, 1)
     return s_abort == 0;
   };
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---- issuer: loads two tiles ahead, S of the next tile while this one is soft-maxed ----
     if (lane == 0 && ntiles > 0) {
       auto load_tile = [&](int t) {
@@ -187,61 +190,67 @@ __global__ void __launch_bounds__(MLA_NT, 1)
       }
     }
   } else {
-    // ---- softmax warps -------------------------------------------------------------------
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-    const bool owner = lane < 16;          // lane l < 16 of warp w owns head 16 w + l
-    const int hd = 16 * warp + (lane & 15);
+    // ---- softmax warps: warps w and w + 4 share TMEM lane quarter w & 3, the first taking
+    //      positions 0-31 of a tile and the second 32-63; the tile's maximum is exchanged
+    //      through shared memory, and each half keeps its own running sum l (both halves
+    //      scale by the same factor, so l is their sum at the end) -------------------------
+    const int qw = warp & 3, hf = warp >> 2;
+    const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
+    const bool owner = lane < 16;          // lane l < 16 owns head 16 (w & 3) + l
+    const int hd = 16 * qw + (lane & 15);
     float m_run = -INFINITY, l_run = 0.f;
     for (int t = 0; t < ntiles; ++t) {
       const int j = t & 1;
-      // a wait that runs out only raises s_abort: the four warps leave together, after a
+      // a wait that runs out only raises s_abort: the eight warps leave together, after a
       // named barrier, on one thread's reading of it (never between named barriers)
       wait(MB_S0 + j, (uint32_t)((t >> 1) & 1));
       tc_fence_after();
       uint8_t *tile = sm + M_OFF_C + j * TILE;
-      float x[64];
+      const int p0 = TP * (tbase + t) + 32 * hf;  // this half's first position
+      float x[32];
       {
         float v[32];
-        tmem_ld32(tm + lane_off + M_TM_S + 64 * j, v);
+        tmem_ld32(tm + lane_off + M_TM_S + 64 * j + 32 * hf, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          x[c] = TP * (tbase + t) + c < len ? v[c] * a.scale_log2 : -INFINITY;
-        tmem_ld32(tm + lane_off + M_TM_S + 64 * j + 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          x[32 + c] = TP * (tbase + t) + 32 + c < len ? v[c] * a.scale_log2 : -INFINITY;
+        for (int c = 0; c < 32; ++c) x[c] = p0 + c < len ? v[c] * a.scale_log2 : -INFINITY;
       }
+      float mt = -INFINITY;
       if (owner) {
-        float mt = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) mt = fmaxf(mt, x[c]);
+        for (int c = 0; c < 32; ++c) mt = fmaxf(mt, x[c]);
+        s_pmax[hf][hd] = mt;
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (owner) {
         // the running maximum: the largest weight is exactly 1 (no bf16 rounding on the
         // dominant term; a reference allowed to lag by up to 2^8 measured 1.04e-2 of RMS on
         // peaked rows, over the bound)
-        const float mn = fmaxf(m_run, mt);
+        const float mn = fmaxf(m_run, fmaxf(mt, s_pmax[hf ^ 1][hd]));
         const float al = mn == -INFINITY ? 1.f : ex2f_sfu(m_run - mn);  // 2^(-inf) = 0
         float ls = 0.f;
         uint8_t *prow = tile + (KB - 1) * BLK;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {  // the head's 64 weights: one 128-byte row of P
+        for (int q = 0; q < 4; ++q) {  // this half's 32 weights: four 16-byte chunks of P's row
           uint32_t w[4];
 #pragma unroll
           for (int y = 0; y < 4; ++y) {
-            const float p0 = x[8 * q + 2 * y] == -INFINITY ? 0.f : ex2f_sfu(x[8 * q + 2 * y] - mn);
-            const float p1 =
+            const float e0 = x[8 * q + 2 * y] == -INFINITY ? 0.f : ex2f_sfu(x[8 * q + 2 * y] - mn);
+            const float e1 =
                 x[8 * q + 2 * y + 1] == -INFINITY ? 0.f : ex2f_sfu(x[8 * q + 2 * y + 1] - mn);
-            const __nv_bfloat16 b0 = __float2bfloat16_rn(p0), b1 = __float2bfloat16_rn(p1);
+            const __nv_bfloat16 b0 = __float2bfloat16_rn(e0), b1 = __float2bfloat16_rn(e1);
             ls += __bfloat162float(b0) + __bfloat162float(b1);  // the weights the product uses
             w[y] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
           }
-          *reinterpret_cast<uint4 *>(prow + sw128_row(hd, q)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4 *>(prow + sw128_row(hd, 4 * hf + q)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
         }
         l_run = l_run * al + ls;
         m_run = mn;
-        s_alpha[hd] = al;
-        if (t > 0 && al != 1.f) s_rescale[j] = 1;
+        if (hf == 0) {
+          s_alpha[hd] = al;
+          if (t > 0 && al != 1.f) s_rescale[j] = 1;
+        }
       }
       // a position past the sequence: its latent row must not reach Z (its memory may hold
       // anything, and 0 x NaN is NaN)
@@ -256,10 +265,10 @@ __global__ void __launch_bounds__(MLA_NT, 1)
       // all of the above overlaps the previous tile's value product; the rescale needs it done
       if (t > 0) wait(MB_Z, (uint32_t)((t - 1) & 1));
       tc_fence_after();
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (s_rescale[j]) {  // Z^T columns of the heads whose maximum moved
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (s_rescale[j]) {  // Z^T columns of the heads whose maximum moved: slices 2 hf, 2 hf + 1
 #pragma unroll 1
-        for (int sl = 0; sl < 4; ++sl) {  // a slice's 64 columns per round trip
+        for (int sl = 2 * hf; sl < 2 * hf + 2; ++sl) {  // a slice's 64 columns per round trip
           float v[32], w2[32];
           const uint32_t col = M_TM_Z + 64 * sl;
           tmem_ld32(tm + lane_off + col, v);
@@ -275,28 +284,35 @@ __global__ void __launch_bounds__(MLA_NT, 1)
       fence_proxy_async();  // P and the zeroed rows feed the tensor core
       tc_fence_before();
       if (tid == 0) s_stop = s_abort;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
       if (tid == 0) {
         s_rescale[j] = 0;
         mbar_arrive(bar(MB_P));
       }
       if (s_stop) break;
     }
-    if (owner) s_l[hd] = l_run, s_mfin[hd] = m_run;
+    if (owner) {
+      if (hf == 0) s_l[hd] = l_run, s_mfin[hd] = m_run;
+      else s_lpart[hd] = l_run;
+    }
   }
   __syncthreads();
+  if (tid < MH) s_l[tid] += s_lpart[tid];
+  __syncthreads();
 
-  // ---- z = Z / l per head (softmax warps: thread = latent channel of its lane quarter) -----
-  if (warp < 4) {
+  // ---- z = Z / l per head (softmax warps: thread = latent channel of its lane quarter;
+  //      warps w and w + 4 take slices 0-1 and 2-3) ------------------------------------------
+  if (warp < 8) {
     const bool done = ntiles > 0 && !s_abort && wait(MB_Z, (uint32_t)((ntiles - 1) & 1));
     tc_fence_after();
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const int qw = warp & 3, hf = warp >> 2;
+    const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
     // one split: z = Z / l; several: this split's unnormalised Z with its (m, l) per head
     const bool split = gridDim.y > 1;
     const size_t row = (size_t)blockIdx.y * a.B + b;
     float *z = split ? a.part + row * MH * ML : a.z + (size_t)b * MH * ML;
 #pragma unroll 1
-    for (int sl = 0; sl < 4; ++sl)
+    for (int sl = 2 * hf; sl < 2 * hf + 2; ++sl)
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         float v[32];
@@ -308,7 +324,7 @@ __global__ void __launch_bounds__(MLA_NT, 1)
         for (int c = 0; c < 32; ++c) {
           const int head = 32 * hh + c;
           const float l = s_l[head];
-          z[(size_t)head * ML + 128 * sl + 32 * warp + lane] =
+          z[(size_t)head * ML + 128 * sl + 32 * qw + lane] =
               split ? (done ? v[c] : 0.f) : ((done && l > 0.f) ? v[c] / l : 0.f);
         }
       }
