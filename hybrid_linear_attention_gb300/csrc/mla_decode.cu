@@ -40,7 +40,7 @@ constexpr int MR = 64;        // positional-key width
 constexpr int MK = ML + MR;   // cached key width
 constexpr int TP = 64;        // cached positions per tile
 constexpr int KB = MK / 64;   // 64-element key blocks (128 bytes of bf16)
-constexpr int MLA_NT = 288;   // eight softmax warps (two per TMEM lane quarter) + an issuer warp
+constexpr int MLA_NT = 320;   // eight softmax warps (two per TMEM lane quarter) + two issuer warps
 
 // shared memory of the latent kernel (1024-byte aligned base): Q [KB][64 heads][128 B]
 // (72 KB, K-major) and two cache tiles [KB][64 positions][128 B] (72 KB each, TMA, 128-byte
@@ -53,7 +53,8 @@ constexpr uint32_t M_OFF_C = KB * MH * 128;
 constexpr uint32_t M_SMEM = M_OFF_C + 2 * TILE + 1024;
 constexpr uint32_t M_TM_S = 0;    // S: 2 buffers of 64 columns; M = 64 heads in lanes 32 w + 0..15
 constexpr uint32_t M_TM_Z = 256;  // Z^T: 4 slices of 128 lanes (latent) x 64 columns (heads)
-enum { MB_Q = 0, MB_C0, MB_C1, MB_S0, MB_S1, MB_P, MB_Z, MB_N };
+// MB_SF0/1: the softmax warps have read S buffer 0 / 1 (it may be overwritten)
+enum { MB_Q = 0, MB_C0, MB_C1, MB_S0, MB_S1, MB_SF0, MB_SF1, MB_P, MB_Z, MB_N };
 
 struct MlaMaps {
   CUtensorMap q, c;
@@ -73,8 +74,8 @@ __device__ __forceinline__ uint32_t sw128_row(int r, int j) {
 // Warps 0-7: softmax and rescale (warp w reads TMEM lanes 32 (w & 3) .. + 31; in S, whose
 // M = 64 rows sit in lanes 32 (w & 3) + 0..15, lane l < 16 of warps w and w + 4 owns head
 // 16 (w & 3) + l, the first warp for a tile's positions 0-31 and the second for 32-63).
-// Warp 8: TMA loads and tensor-core issue.  The two sides meet only on mbarriers: C tile
-// landed, S ready, P ready, Z done.
+// Warps 8 and 9: TMA loads and tensor-core issue (S products | Z products).  The sides meet
+// only on mbarriers: C tile landed, S ready, S read, P ready, Z done.
 __global__ void __launch_bounds__(MLA_NT, 1)
     mla_latent_kernel(const MlaArgs a, const __grid_constant__ MlaMaps maps) {
   extern __shared__ uint8_t mraw[];
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(MLA_NT, 1)
   __shared__ __align__(8) uint64_t s_bar[MB_N];
   __shared__ uint32_t s_tmem;
   __shared__ volatile uint32_t s_abort;
-  __shared__ uint32_t s_loads[2], s_mmas;
+  __shared__ uint32_t s_loads[2], s_smmas[2], s_mmas;
   __shared__ int s_stop;  // the softmax warps' exit decision, taken by one thread per tile
   __shared__ float s_alpha[MH], s_l[MH], s_mfin[MH];
   __shared__ float s_pmax[2][MH], s_lpart[MH];  // a tile's half maxima; the second half's l
@@ -113,6 +114,7 @@ __global__ void __launch_bounds__(MLA_NT, 1)
     s_stop = 0;
     s_loads[0] = s_loads[1] = 0;  // tiles requested into each buffer (the drain's parity)
     s_mmas = 0;                   // value products issued
+    s_smmas[0] = s_smmas[1] = 0;  // score products issued into each S buffer
   }
   if (warp == 0) tmem_alloc(smem_u32(&s_tmem), 512);
   tc_fence_before();
@@ -124,8 +126,14 @@ __global__ void __launch_bounds__(MLA_NT, 1)
     return s_abort == 0;
   };
 
-  if (warp == 8) {
-    // ---- issuer: loads two tiles ahead, S of the next tile while this one is soft-maxed ----
+  if (warp >= 8) {
+    // ---- issuers (lane 0 of warps 8 and 9).  One thread issues a tcgen05 product every ~90
+    //      cycles here (measured; two issuing warps reach ~50 between them), so the two
+    //      chains run on two warps: warp 8 loads the queries and the first two tiles and
+    //      issues S of each tile once it has landed and the softmax has read that S buffer's
+    //      previous tile, so S(t+1) runs while tile t is soft-maxed; warp 9 issues Z of each
+    //      tile once its P is written, then loads the tile two ahead into the buffer Z has
+    //      finished reading.
     if (lane == 0 && ntiles > 0) {
       auto load_tile = [&](int t) {
         const int j = t & 1;
@@ -135,57 +143,53 @@ __global__ void __launch_bounds__(MLA_NT, 1)
           tma_load_3d(sb + M_OFF_C + j * TILE + kb * BLK, &maps.c, 64 * kb, TP * (tbase + t), b,
                       bar(MB_C0 + j));
       };
-      // S = Q C^T: M = 64 heads (A = Q), N = 64 positions (B = C), both K-major
-      constexpr uint32_t ID_S = idesc(1, 64, 64, 0, 0);
-      // Z^T = C^T P^T: M = 128 latent (A = C^T, MN-major), N = 64 heads (B = P, K-major)
-      constexpr uint32_t ID_Z = idesc(1, 128, 64, 1, 0);
-      auto issue_s = [&](int t, bool landed) {
-        const int j = t & 1;
-        if (!landed && !wait(MB_C0 + j, (uint32_t)((t >> 1) & 1))) return false;
-        tc_fence_after();
+      if (warp == 8) {
+        // S = Q C^T: M = 64 heads (A = Q), N = 64 positions (B = C), both K-major
+        constexpr uint32_t ID_S = idesc(1, 64, 64, 0, 0);
+        mbar_expect_tx(bar(MB_Q), KB * MH * 128);
         for (int kb = 0; kb < KB; ++kb)
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ad = sdesc_sw128(sb + M_OFF_Q + kb * MH * 128 + ks * 32, 16, 1024);
-            const uint64_t bd =
-                sdesc_sw128(sb + M_OFF_C + j * TILE + kb * BLK + ks * 32, 16, 1024);
-            mma_bf16_ss(tm + M_TM_S + 64 * j, ad, bd, ID_S, (kb | ks) != 0);
-          }
-        mma_commit(bar(MB_S0 + j));
-        return true;
-      };
-      mbar_expect_tx(bar(MB_Q), KB * MH * 128);
-      for (int kb = 0; kb < KB; ++kb)
-        tma_load_3d(sb + M_OFF_Q + kb * MH * 128, &maps.q, 64 * kb, 0, b, bar(MB_Q));
-      load_tile(0);
-      if (ntiles > 1) load_tile(1);
-      bool go = wait(MB_Q, 0) && issue_s(0, false);
-      for (int t = 0; t < ntiles && go; ++t) {
-        const int j = t & 1;
-        if (!wait(MB_P, (uint32_t)(t & 1))) break;  // P(t) written, Z rescaled
-        tc_fence_after();
-        // S(t+1) goes ahead of Z(t) when its tile has landed (one probe, no wait), so the
-        // softmax warps start the next tile while Z(t) runs; its S buffer was read by
-        // softmax(t - 1), which P(t - 1) closed
-        bool next_s = false;
-        if (t + 1 < ntiles && mbar_try_wait(bar(MB_C0 + (j ^ 1)), (uint32_t)(((t + 1) >> 1) & 1))) {
-          issue_s(t + 1, true);
-          next_s = true;
+          tma_load_3d(sb + M_OFF_Q + kb * MH * 128, &maps.q, 64 * kb, 0, b, bar(MB_Q));
+        load_tile(0);
+        if (ntiles > 1) load_tile(1);
+        const bool go = wait(MB_Q, 0);
+        for (int t = 0; t < ntiles && go; ++t) {
+          const int j = t & 1;
+          if (!wait(MB_C0 + j, (uint32_t)((t >> 1) & 1))) break;  // tile t landed
+          // S buffer j was last read by the softmax of tile t - 2
+          if (t >= 2 && !wait(MB_SF0 + j, (uint32_t)(((t >> 1) - 1) & 1))) break;
+          tc_fence_after();
+          for (int kb = 0; kb < KB; ++kb)
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t ad = sdesc_sw128(sb + M_OFF_Q + kb * MH * 128 + ks * 32, 16, 1024);
+              const uint64_t bd =
+                  sdesc_sw128(sb + M_OFF_C + j * TILE + kb * BLK + ks * 32, 16, 1024);
+              mma_bf16_ss(tm + M_TM_S + 64 * j, ad, bd, ID_S, (kb | ks) != 0);
+            }
+          mma_commit(bar(MB_S0 + j));
+          ++s_smmas[j];
         }
-        const uint32_t tile = sb + M_OFF_C + j * TILE;
-        for (int sl = 0; sl < 4; ++sl)
-          for (int ks = 0; ks < TP / 16; ++ks) {
-            // A = C^T: latent 128 sl .. 128 sl + 127 = key blocks 2 sl, 2 sl + 1 (BLK apart),
-            // positions 16 ks .. 16 ks + 15 (two 8-row groups of 1 KB); B = P rows = heads
-            const uint64_t ad = sdesc_sw128(tile + 2 * sl * BLK + ks * 2048, BLK, 1024);
-            const uint64_t bd = sdesc_sw128(tile + (KB - 1) * BLK + ks * 32, 16, 1024);
-            mma_bf16_ss(tm + M_TM_Z + 64 * sl, ad, bd, ID_Z, (t > 0 || ks > 0) ? 1u : 0u);
+      } else {
+        // Z^T = C^T P^T: M = 128 latent (A = C^T, MN-major), N = 64 heads (B = P, K-major)
+        constexpr uint32_t ID_Z = idesc(1, 128, 64, 1, 0);
+        for (int t = 0; t < ntiles; ++t) {
+          const int j = t & 1;
+          if (!wait(MB_P, (uint32_t)(t & 1))) break;  // P(t) written, Z rescaled
+          tc_fence_after();
+          const uint32_t tile = sb + M_OFF_C + j * TILE;
+          for (int sl = 0; sl < 4; ++sl)
+            for (int ks = 0; ks < TP / 16; ++ks) {
+              // A = C^T: latent 128 sl .. 128 sl + 127 = key blocks 2 sl, 2 sl + 1 (BLK
+              // apart), positions 16 ks .. 16 ks + 15 (two 8-row groups of 1 KB); B = P rows
+              const uint64_t ad = sdesc_sw128(tile + 2 * sl * BLK + ks * 2048, BLK, 1024);
+              const uint64_t bd = sdesc_sw128(tile + (KB - 1) * BLK + ks * 32, 16, 1024);
+              mma_bf16_ss(tm + M_TM_Z + 64 * sl, ad, bd, ID_Z, (t > 0 || ks > 0) ? 1u : 0u);
+            }
+          mma_commit(bar(MB_Z));
+          ++s_mmas;
+          if (t + 2 < ntiles) {  // buffer j is free once Z(t) has read it
+            if (!wait(MB_Z, (uint32_t)(t & 1))) break;
+            load_tile(t + 2);
           }
-        mma_commit(bar(MB_Z));
-        ++s_mmas;
-        if (t + 1 < ntiles && !next_s && !issue_s(t + 1, false)) break;
-        if (t + 2 < ntiles) {  // buffer j is free once Z(t) has read it
-          if (!wait(MB_Z, (uint32_t)(t & 1))) break;
-          load_tile(t + 2);
         }
       }
     }
@@ -221,7 +225,9 @@ __global__ void __launch_bounds__(MLA_NT, 1)
         for (int c = 0; c < 32; ++c) mt = fmaxf(mt, x[c]);
         s_pmax[hf][hd] = mt;
       }
+      tc_fence_before();
       asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (tid == 0) mbar_arrive(bar(MB_SF0 + j));  // S buffer j has been read
       if (owner) {
         // the running maximum: the largest weight is exactly 1 (no bf16 rounding on the
         // dominant term; a reference allowed to lag by up to 2^8 measured 1.04e-2 of RMS on
@@ -339,6 +345,8 @@ __global__ void __launch_bounds__(MLA_NT, 1)
     // the CTA releases its memory, then report it
     for (int j = 0; j < 2; ++j)
       if (s_loads[j]) mbar_wait(bar(MB_C0 + j), (s_loads[j] - 1) & 1);
+    for (int j = 0; j < 2; ++j)
+      if (s_smmas[j]) mbar_wait(bar(MB_S0 + j), (s_smmas[j] - 1) & 1);
     if (s_mmas) mbar_wait(bar(MB_Z), (s_mmas - 1) & 1);
     if (a.err) atomicOr(a.err, ERR_MBAR_TIMEOUT);
   }
