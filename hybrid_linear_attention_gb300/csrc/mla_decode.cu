@@ -40,7 +40,7 @@ constexpr int MR = 64;        // positional-key width
 constexpr int MK = ML + MR;   // cached key width
 constexpr int TP = 64;        // cached positions per tile
 constexpr int KB = MK / 64;   // 64-element key blocks (128 bytes of bf16)
-constexpr int MLA_NT = 320;   // eight softmax warps (two per TMEM lane quarter) + two issuer warps
+constexpr int MLA_NT = 384;   // eight softmax warps (two per TMEM lane quarter) + four issuer warps
 
 // shared memory of the latent kernel (1024-byte aligned base): Q [KB][64 heads][128 B]
 // (72 KB, K-major) and two cache tiles [KB][64 positions][128 B] (72 KB each, TMA, 128-byte
@@ -52,6 +52,7 @@ constexpr uint32_t M_OFF_Q = 0;
 constexpr uint32_t M_OFF_C = KB * MH * 128;
 constexpr uint32_t M_SMEM = M_OFF_C + 2 * TILE + 1024;
 constexpr uint32_t M_TM_S = 0;    // S: 2 buffers of 64 columns; M = 64 heads in lanes 32 w + 0..15
+constexpr uint32_t M_TM_S2 = 128;  // the second partial sum of S (key blocks 5-8), 2 buffers
 constexpr uint32_t M_TM_Z = 256;  // Z^T: 4 slices of 128 lanes (latent) x 64 columns (heads)
 // MB_SF0/1: the softmax warps have read S buffer 0 / 1 (it may be overwritten)
 enum { MB_Q = 0, MB_C0, MB_C1, MB_S0, MB_S1, MB_SF0, MB_SF1, MB_P, MB_Z, MB_N };
@@ -74,8 +75,8 @@ __device__ __forceinline__ uint32_t sw128_row(int r, int j) {
 // Warps 0-7: softmax and rescale (warp w reads TMEM lanes 32 (w & 3) .. + 31; in S, whose
 // M = 64 rows sit in lanes 32 (w & 3) + 0..15, lane l < 16 of warps w and w + 4 owns head
 // 16 (w & 3) + l, the first warp for a tile's positions 0-31 and the second for 32-63).
-// Warps 8 and 9: TMA loads and tensor-core issue (S products | Z products).  The sides meet
-// only on mbarriers: C tile landed, S ready, S read, P ready, Z done.
+// Warps 8-11: TMA loads and tensor-core issue (S products on 8 and 9, Z products on 10 and
+// 11).  The sides meet only on mbarriers: C tile landed, S ready, S read, P ready, Z done.
 __global__ void __launch_bounds__(MLA_NT, 1)
     mla_latent_kernel(const MlaArgs a, const __grid_constant__ MlaMaps maps) {
   extern __shared__ uint8_t mraw[];
@@ -107,7 +108,9 @@ __global__ void __launch_bounds__(MLA_NT, 1)
                                                    : per_split;
   auto bar = [&](int i) { return smem_u32(&s_bar[i]); };
   if (tid == 0) {
-    for (int i = 0; i < MB_N; ++i) mbar_init(bar(i), 1);
+    // S and Z each complete on the commits of two issuing threads
+    for (int i = 0; i < MB_N; ++i)
+      mbar_init(bar(i), i == MB_S0 || i == MB_S1 || i == MB_Z ? 2 : 1);
     mbar_fence_init();
     s_abort = 0;
     s_rescale[0] = s_rescale[1] = 0;
@@ -127,13 +130,14 @@ __global__ void __launch_bounds__(MLA_NT, 1)
   };
 
   if (warp >= 8) {
-    // ---- issuers (lane 0 of warps 8 and 9).  One thread issues a tcgen05 product every ~90
-    //      cycles here (measured; two issuing warps reach ~50 between them), so the two
-    //      chains run on two warps: warp 8 loads the queries and the first two tiles and
-    //      issues S of each tile once it has landed and the softmax has read that S buffer's
-    //      previous tile, so S(t+1) runs while tile t is soft-maxed; warp 9 issues Z of each
-    //      tile once its P is written, then loads the tile two ahead into the buffer Z has
-    //      finished reading.
+    // ---- issuers (lane 0 of warps 8-11).  One thread issues a tcgen05 product every ~90
+    //      cycles here (measured; two issuing warps reach ~50 between them), so the products
+    //      are spread over four warps: warps 8 and 9 issue S of each tile, as two partial sums
+    //      over key blocks 0-4 and 5-8, once the tile has landed and the softmax has read that
+    //      S buffer's previous tile, so S(t+1) runs while tile t is soft-maxed; warps 10 and
+    //      11 issue Z of each tile (latent slices 0-1 | 2-3) once its P is written, and warp
+    //      10 then loads the tile two ahead into the buffer Z has finished reading.  Warp 8
+    //      loads the queries and the first two tiles.
     if (lane == 0 && ntiles > 0) {
       auto load_tile = [&](int t) {
         const int j = t & 1;
@@ -143,14 +147,18 @@ __global__ void __launch_bounds__(MLA_NT, 1)
           tma_load_3d(sb + M_OFF_C + j * TILE + kb * BLK, &maps.c, 64 * kb, TP * (tbase + t), b,
                       bar(MB_C0 + j));
       };
-      if (warp == 8) {
+      if (warp < 10) {
         // S = Q C^T: M = 64 heads (A = Q), N = 64 positions (B = C), both K-major
         constexpr uint32_t ID_S = idesc(1, 64, 64, 0, 0);
-        mbar_expect_tx(bar(MB_Q), KB * MH * 128);
-        for (int kb = 0; kb < KB; ++kb)
-          tma_load_3d(sb + M_OFF_Q + kb * MH * 128, &maps.q, 64 * kb, 0, b, bar(MB_Q));
-        load_tile(0);
-        if (ntiles > 1) load_tile(1);
+        const int kb0 = warp == 8 ? 0 : 5, kb1 = warp == 8 ? 5 : KB;
+        const uint32_t d0 = warp == 8 ? M_TM_S : M_TM_S2;
+        if (warp == 8) {
+          mbar_expect_tx(bar(MB_Q), KB * MH * 128);
+          for (int kb = 0; kb < KB; ++kb)
+            tma_load_3d(sb + M_OFF_Q + kb * MH * 128, &maps.q, 64 * kb, 0, b, bar(MB_Q));
+          load_tile(0);
+          if (ntiles > 1) load_tile(1);
+        }
         const bool go = wait(MB_Q, 0);
         for (int t = 0; t < ntiles && go; ++t) {
           const int j = t & 1;
@@ -158,25 +166,26 @@ __global__ void __launch_bounds__(MLA_NT, 1)
           // S buffer j was last read by the softmax of tile t - 2
           if (t >= 2 && !wait(MB_SF0 + j, (uint32_t)(((t >> 1) - 1) & 1))) break;
           tc_fence_after();
-          for (int kb = 0; kb < KB; ++kb)
+          for (int kb = kb0; kb < kb1; ++kb)
             for (int ks = 0; ks < 4; ++ks) {
               const uint64_t ad = sdesc_sw128(sb + M_OFF_Q + kb * MH * 128 + ks * 32, 16, 1024);
               const uint64_t bd =
                   sdesc_sw128(sb + M_OFF_C + j * TILE + kb * BLK + ks * 32, 16, 1024);
-              mma_bf16_ss(tm + M_TM_S + 64 * j, ad, bd, ID_S, (kb | ks) != 0);
+              mma_bf16_ss(tm + d0 + 64 * j, ad, bd, ID_S, (kb != kb0 || ks) ? 1u : 0u);
             }
           mma_commit(bar(MB_S0 + j));
-          ++s_smmas[j];
+          if (warp == 8) ++s_smmas[j];
         }
       } else {
         // Z^T = C^T P^T: M = 128 latent (A = C^T, MN-major), N = 64 heads (B = P, K-major)
         constexpr uint32_t ID_Z = idesc(1, 128, 64, 1, 0);
+        const int sl0 = warp == 10 ? 0 : 2;
         for (int t = 0; t < ntiles; ++t) {
           const int j = t & 1;
           if (!wait(MB_P, (uint32_t)(t & 1))) break;  // P(t) written, Z rescaled
           tc_fence_after();
           const uint32_t tile = sb + M_OFF_C + j * TILE;
-          for (int sl = 0; sl < 4; ++sl)
+          for (int sl = sl0; sl < sl0 + 2; ++sl)
             for (int ks = 0; ks < TP / 16; ++ks) {
               // A = C^T: latent 128 sl .. 128 sl + 127 = key blocks 2 sl, 2 sl + 1 (BLK
               // apart), positions 16 ks .. 16 ks + 15 (two 8-row groups of 1 KB); B = P rows
@@ -185,10 +194,12 @@ __global__ void __launch_bounds__(MLA_NT, 1)
               mma_bf16_ss(tm + M_TM_Z + 64 * sl, ad, bd, ID_Z, (t > 0 || ks > 0) ? 1u : 0u);
             }
           mma_commit(bar(MB_Z));
-          ++s_mmas;
-          if (t + 2 < ntiles) {  // buffer j is free once Z(t) has read it
-            if (!wait(MB_Z, (uint32_t)(t & 1))) break;
-            load_tile(t + 2);
+          if (warp == 10) {
+            ++s_mmas;
+            if (t + 2 < ntiles) {  // buffer j is free once both halves of Z(t) have read it
+              if (!wait(MB_Z, (uint32_t)(t & 1))) break;
+              load_tile(t + 2);
+            }
           }
         }
       }
@@ -214,10 +225,12 @@ __global__ void __launch_bounds__(MLA_NT, 1)
       float x[32];
       {
         float v[32];
-        tmem_ld32(tm + lane_off + M_TM_S + 64 * j + 32 * hf, v);
+        tmem_ld32(tm + lane_off + M_TM_S + 64 * j + 32 * hf, x);
+        tmem_ld32(tm + lane_off + M_TM_S2 + 64 * j + 32 * hf, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) x[c] = p0 + c < len ? v[c] * a.scale_log2 : -INFINITY;
+        for (int c = 0; c < 32; ++c)
+          x[c] = p0 + c < len ? (x[c] + v[c]) * a.scale_log2 : -INFINITY;
       }
       float mt = -INFINITY;
       if (owner) {
