@@ -39,6 +39,7 @@
 // (hi*hi + hi*lo + lo*hi), which keeps the state at fp32-level accuracy.  Inputs arrive by
 // TMA in 128-byte-swizzled tiles; every operand is built with 16-byte vector accesses.
 #include <cuda.h>
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <cudaTypedefs.h>
@@ -1364,14 +1365,14 @@ bool make_out_map(CUtensorMap *m, void *ptr, int64_t T, int H, bool fp8) {
 
 template <typename ST, bool GATE, bool PAIR, bool QUANT>
 cudaError_t launch_typed(const TcArgs &a, const Maps &maps, cudaStream_t s) {
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // the opt-in done, per device (idempotent if raced)
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<ST, GATE, PAIR, QUANT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true);
   }
   if (!PAIR) {
     prefill_tc_kernel<ST, GATE, PAIR, QUANT><<<dim3(a.H, a.n_seqs), NT, SMEM_BYTES, s>>>(a, maps);

@@ -471,14 +471,14 @@ cudaError_t launch_mla_latent(const MlaArgs &a, cudaStream_t s) {
   if (!mla_map(&maps.q, a.q_cat, MH, a.B, MH) ||
       !mla_map(&maps.c, a.cache, a.L_max > 0 ? a.L_max : 1, a.B, TP))
     return cudaErrorInvalidValue;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // the opt-in done, per device (idempotent if raced)
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(mla_latent_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, M_SMEM);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true);
   }
   const int ns = a.n_split > 1 ? a.n_split : 1;
   mla_latent_kernel<<<dim3(a.B, ns), MLA_NT, M_SMEM, s>>>(a, maps);

@@ -17,6 +17,7 @@
 //                          is split on the CUDA cores into bf16 hi + lo (two products, the
 //                          sum good to ~2^-17 relative), W_V K-major by TMA; the epilogue
 //                          scales each row by sigmoid(gate) and writes bf16.
+#include <atomic>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -295,13 +296,13 @@ bool proj_map(CUtensorMap *m, const void *ptr, bool f32, uint64_t d0, uint64_t d
 // the dynamic shared-memory opt-in of one kernel, once per device (each kernel passes its own
 // flags: both kernels have the same signature, so a per-type cache would be shared)
 template <typename K>
-cudaError_t set_smem(K kernel, uint32_t bytes, bool (&done)[64]) {
+cudaError_t set_smem(K kernel, uint32_t bytes, std::atomic<bool> (&done)[64]) {
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !done[dev]) {
+  if (dev >= 0 && dev < 64 && !done[dev].load()) {  // idempotent if two threads race here
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    done[dev] = true;
+    done[dev].store(true);
   }
   return cudaSuccess;
 }
@@ -318,7 +319,7 @@ cudaError_t launch_mla_absorb(const MlaArgs &a, cudaStream_t s) {
   if (!proj_map(&maps.a, a.q_nope, false, PN, PH, (uint64_t)a.B, 64, 1, box_rows(a.B)) ||
       !proj_map(&maps.w, a.w_uk, false, PL, PN, PH, 64, PN, 1))
     return cudaErrorInvalidValue;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];
   cudaError_t e = set_smem(mla_absorb_tc_kernel, AB_SMEM, attr_set);
   if (e != cudaSuccess) return e;
   mla_absorb_tc_kernel<<<dim3(2, PH, (a.B + PB - 1) / PB), PT, AB_SMEM, s>>>(a, maps);
@@ -334,7 +335,7 @@ cudaError_t launch_mla_up_gate(const MlaArgs &a, cudaStream_t s) {
   if (!proj_map(&maps.z, a.z, true, PL, PH, (uint64_t)a.B, 32, 1, box_rows(a.B)) ||
       !proj_map(&maps.w, a.w_uv, false, PL, PV, PH, 64, PV, 1))
     return cudaErrorInvalidValue;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];
   cudaError_t e = set_smem(mla_up_gate_tc_kernel, UG_SMEM, attr_set);
   if (e != cudaSuccess) return e;
   mla_up_gate_tc_kernel<<<dim3(PH, (a.B + PB - 1) / PB), PT, UG_SMEM, s>>>(a, maps);
