@@ -91,9 +91,10 @@ def _prefill_flops(T, H, d, C=64):
     return T / C * H * per
 
 
-# the survey's triangle-aware count of the prefill's dense work per head and token at d = 128,
-# C = 64: 2 (3 d^2 + 2.5 C d)
-SURVEY_FLOPS_PER_HEAD_TOKEN = 2 * (3 * 128 * 128 + 2.5 * 64 * 128)
+# a triangle-aware count of the prefill's dense work per head and token at d = 128, C = 64:
+# 2 (3 d^2 + 2.5 C d) -- the state read, correction and update (3 d^2 multiply-adds) and the
+# intra-chunk products on their triangles (2.5 C d)
+TRIANGLE_FLOPS_PER_HEAD_TOKEN = 2 * (3 * 128 * 128 + 2.5 * 64 * 128)
 
 
 def _prefill_bytes_batch(lengths, H, d, *, gate, state_in, state_bytes=4):
@@ -466,9 +467,9 @@ def run_ours(args):
                                 "frac": pf_flops / (pf * 1e-3) / 1e12 / tflops,
                                 "peak_kind": f"{peak_kind} bf16_tflops (burst)",
                                 "algorithmic_flops_per_launch": pf_flops,
-                                # the survey's triangle-aware count, 139,264 flop per head-token
-                                "survey_flops_per_head_token": SURVEY_FLOPS_PER_HEAD_TOKEN,
-                                "survey_frac": SURVEY_FLOPS_PER_HEAD_TOKEN * T_PREFILL * H
+                                # the triangle-aware count, 139,264 flop per head-token
+                                "triangle_flops_per_head_token": TRIANGLE_FLOPS_PER_HEAD_TOKEN,
+                                "triangle_frac": TRIANGLE_FLOPS_PER_HEAD_TOKEN * T_PREFILL * H
                                                / (pf * 1e-3) / 1e12 / tflops}},
         "gpu_launches": int(launches),
         "gpu_launches_per_step": launches / args.steps,
@@ -563,7 +564,7 @@ def _long_context_bench(dev, kda, inputs, hbm, tflops, args):
     ms = _time_prefill(kda, p, inp, out, fin, gate=True, reps=min(args.steps, 5), flush=flush)
     b = _prefill_bytes_batch(lens, H, D, gate=True, state_in=True)
     gbs = b / (ms * 1e-3) / 1e9
-    tf = SURVEY_FLOPS_PER_HEAD_TOKEN * T * H / (ms * 1e-3) / 1e12
+    tf = TRIANGLE_FLOPS_PER_HEAD_TOKEN * T * H / (ms * 1e-3) / 1e12
     del inp, out, fin
     torch.cuda.empty_cache()
     return {"workload": "4 x 32768 tokens, H=64, d=128, bf16 q/k/v, fp32 g/beta/state, initial "

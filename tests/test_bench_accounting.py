@@ -92,7 +92,7 @@ def test_reference_arm_prints_one_contract_line(capsys):
 
 def test_batch_prefill_bytes_for_the_gated_and_varlen_workloads():
     """Per token q, k, v, out (bf16), g, beta (fp32) and the gate logits (bf16) when the output
-    norm and gate run: the survey's 114,944 bytes per token at 64 heads; per sequence the
+    norm and gate run: 114,944 bytes per token at 64 heads; per sequence the
     initial and final state."""
     lens = [32768] * 4
     per_tok = 3 * H * D * BF16 + H * D * F32 + H * F32 + H * D * BF16 + H * D * BF16
@@ -105,6 +105,6 @@ def test_batch_prefill_bytes_for_the_gated_and_varlen_workloads():
                                       state_bytes=2) == 128 * 98_560 + 2 * H * D * D * 2
 
 
-def test_survey_flop_count_per_head_token():
+def test_triangle_flop_count_per_head_token():
     # 2 (3 d^2 + 2.5 C d) at d = 128, C = 64
-    assert bench.SURVEY_FLOPS_PER_HEAD_TOKEN == 139_264
+    assert bench.TRIANGLE_FLOPS_PER_HEAD_TOKEN == 139_264
