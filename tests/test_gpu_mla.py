@@ -45,8 +45,8 @@ def _latent(m):
 
 @pytest.mark.parametrize("q_std", [1.0, 4.0])
 def test_latent_attention_matches_the_oracle(q_std):
-    """Ragged lengths around the 128-position tile (1, 127, 128, 129, 300), peaked scores
-    (q_std 4: the running max moves and Z is rescaled), NaN past every length."""
+    """Ragged lengths around the 64-position tile edges (1, 127, 128, 129, 300), peaked
+    scores (q_std 4: the running max moves and Z is rescaled), NaN past every length."""
     lengths = [1, 127, 128, 129, 300, 256]
     m = _case(lengths, 320, seed=800 + int(q_std), q_std=q_std)
     z = _latent(m)
@@ -195,3 +195,43 @@ def test_split_mla_decode_matches_the_expanded_oracle():
                                      clean[..., 512:], np.array(lengths), m["w_uk"], m["w_uv"],
                                      m["gate"], scale=kda.MLA_SCALE)
     assert out_error(out.cpu(), ref, torch.bfloat16) <= TOL
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_latent_attention_random_batches(seed):
+    """Seeded random batches: 1-20 sequences, lengths 0..cache length (tile edges, one-position
+    tails, empty sequences), cache lengths 64-1,100, peaked or flat scores, and a forced split
+    of 1, 2, 3 or 5 CTAs per sequence (the merge of partial sums): every sequence against the
+    oracle; an empty sequence gives exactly zero."""
+    rng = np.random.default_rng(1000 + seed)
+    B = int(rng.integers(1, 21))
+    L = int(rng.integers(1, 18)) * 64 + int(rng.integers(0, 2)) * int(rng.integers(1, 64))
+    lengths = [int(x) for x in rng.integers(0, L + 1, size=B)]
+    lengths[0] = L  # one full cache
+    if B > 2:
+        lengths[1] = 0
+    q_std = float(rng.choice([1.0, 4.0]))
+    split = int(rng.choice([1, 2, 3, 5]))
+    m = _case(lengths, L, seed=2000 + seed, q_std=q_std)
+    _gpu.lib()
+    n_ws = 0
+    with kda.mla_split(split):
+        n_ws = kda.mla_decode_workspace_size(B, L)
+        ws = torch.empty(max(n_ws // 4, 1), dtype=torch.float32, device="cuda") if n_ws else None
+        z = torch.full((B, 64, 512), 7.0, device="cuda")
+        kda.mla_decode_latent(m["q_cat"].cuda(), m["cache"].cuda(), m["lengths"].cuda(), z,
+                              workspace=ws)
+        torch.cuda.synchronize()
+    kda.kda_check_device_error()
+    assert torch.isfinite(z).all()
+    clean = m["cache"].clone()
+    for b, n in enumerate(lengths):
+        clean[b, n:] = 0
+    ref, _ = oracle.mla_latent_attention(m["q_cat"], clean, np.array(lengths),
+                                         scale=kda.MLA_SCALE)
+    for b in range(B):
+        if lengths[b] == 0:
+            assert bool((z[b] == 0).all()), f"sequence {b}: empty, not zero"
+            continue
+        e = max_err_rel_rms(z[b], ref[b])
+        assert e <= TOL, f"seed {seed}, split {split}, sequence {b} (length {lengths[b]}): {e:.3g}"
