@@ -101,3 +101,34 @@ def test_more_heads_than_sms():
     ref = _oracle(inp, False)
     assert out_error(out, ref["out"], torch.bfloat16) <= 1e-2
     assert max_err_rel_rms(fin, ref["final_state"]) <= 1e-3
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_prefill_random_batches(seed):
+    """Seeded random packed batches on both tensor-core forms: 1-6 sequences of 0-400 tokens
+    (chunk edges and one-token tails among them), 1-3 heads, the norm and gate on or off, an
+    initial state on all, some or none of the sequences; every (sequence, head) unit against
+    the oracle."""
+    rng = np.random.default_rng(3000 + seed)
+    n = int(rng.integers(1, 7))
+    lens = [int(x) for x in rng.integers(0, 401, size=n)]
+    edges = [0, 1, 63, 64, 65, 128, 129]
+    lens[int(rng.integers(0, n))] = edges[seed % len(edges)]
+    H = int(rng.integers(1, 4))
+    gate = bool(seed % 2)
+    init = [None, "all", "even"][seed % 3]
+    form = "pair" if seed % 4 < 2 else "fused"
+    inp = inputs.kda_inputs(lens, H, 128, seed=3100 + seed, init_state=init, gate=gate)
+    p = kda.params(H=H, d=128, prefill_form=form)
+    out, fin = _gpu.prefill(inp, p, gate=gate)
+    torch.cuda.synchronize()
+    kda.kda_check_device_error()
+    ref = _oracle(inp, gate)
+    cu = inp["cu_seqlens"].tolist()
+    for s in range(n):
+        if lens[s] == 0:
+            continue
+        for h in range(H):
+            e = out_error(out[cu[s]:cu[s + 1], h], ref["out"][cu[s]:cu[s + 1], h], torch.bfloat16)
+            assert e <= 1e-2, f"seed {seed}: sequence {s} (length {lens[s]}), head {h}: {e:.3g}"
+    assert max_err_rel_rms(fin, ref["final_state"]) <= 1e-3
