@@ -74,7 +74,8 @@ __device__ __forceinline__ uint32_t sw128_row(int r, int j) {
 
 // Warps 0-7: softmax and rescale (warp w reads TMEM lanes 32 (w & 3) .. + 31; in S, whose
 // M = 64 rows sit in lanes 32 (w & 3) + 0..15, lane l < 16 of warps w and w + 4 owns head
-// 16 (w & 3) + l, the first warp for a tile's positions 0-31 and the second for 32-63).
+// 16 (w & 3) + l, the first warp for a tile's positions 0-31 and the second for 32-63; each
+// owner hands the upper 16 of its 32 scores to lane l + 16, so every lane takes 16 weights).
 // Warps 8-11: TMA loads and tensor-core issue (S products on 8 and 9, Z products on 10 and
 // 11).  The sides meet only on mbarriers: C tile landed, S ready, S read, P ready, Z done.
 __global__ void __launch_bounds__(MLA_NT, 1)
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(MLA_NT, 1)
     //      scale by the same factor, so l is their sum at the end) -------------------------
     const int qw = warp & 3, hf = warp >> 2;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
-    const bool owner = lane < 16;          // lane l < 16 owns head 16 (w & 3) + l
+    const bool owner = lane < 16;          // lane l < 16 owns head 16 (w & 3) + l (with l + 16)
     const int hd = 16 * qw + (lane & 15);
     float m_run = -INFINITY, l_run = 0.f;
     for (int t = 0; t < ntiles; ++t) {
@@ -232,16 +233,24 @@ __global__ void __launch_bounds__(MLA_NT, 1)
         for (int c = 0; c < 32; ++c)
           x[c] = p0 + c < len ? (x[c] + v[c]) * a.scale_log2 : -INFINITY;
       }
-      float mt = -INFINITY;
-      if (owner) {
+      // the owner of head hd (lane l < 16) hands its scores for positions 16-31 of this half
+      // to lane l + 16, so all 32 lanes take 16 weights each
+      const int sub = lane >> 4;
+      float xs[16];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) mt = fmaxf(mt, x[c]);
-        s_pmax[hf][hd] = mt;
+      for (int c = 0; c < 16; ++c) {
+        const float up = __shfl_sync(0xffffffffu, x[16 + c], lane & 15);
+        xs[c] = sub ? up : x[c];
       }
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) mt = fmaxf(mt, xs[c]);
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+      if (owner) s_pmax[hf][hd] = mt;
       tc_fence_before();
       asm volatile("bar.sync 1, 256;" ::: "memory");
       if (tid == 0) mbar_arrive(bar(MB_SF0 + j));  // S buffer j has been read
-      if (owner) {
+      {
         // the running maximum: the largest weight is exactly 1 (no bf16 rounding on the
         // dominant term; a reference allowed to lag by up to 2^8 measured 1.04e-2 of RMS on
         // peaked rows, over the bound)
@@ -250,23 +259,23 @@ __global__ void __launch_bounds__(MLA_NT, 1)
         float ls = 0.f;
         uint8_t *prow = tile + (KB - 1) * BLK;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {  // this half's 32 weights: four 16-byte chunks of P's row
+        for (int q = 0; q < 2; ++q) {  // this lane's 16 weights: two 16-byte chunks of P's row
           uint32_t w[4];
 #pragma unroll
           for (int y = 0; y < 4; ++y) {
-            const float e0 = x[8 * q + 2 * y] == -INFINITY ? 0.f : ex2f_sfu(x[8 * q + 2 * y] - mn);
+            const float e0 = xs[8 * q + 2 * y] == -INFINITY ? 0.f : ex2f_sfu(xs[8 * q + 2 * y] - mn);
             const float e1 =
-                x[8 * q + 2 * y + 1] == -INFINITY ? 0.f : ex2f_sfu(x[8 * q + 2 * y + 1] - mn);
+                xs[8 * q + 2 * y + 1] == -INFINITY ? 0.f : ex2f_sfu(xs[8 * q + 2 * y + 1] - mn);
             const __nv_bfloat16 b0 = __float2bfloat16_rn(e0), b1 = __float2bfloat16_rn(e1);
             ls += __bfloat162float(b0) + __bfloat162float(b1);  // the weights the product uses
             w[y] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
           }
-          *reinterpret_cast<uint4 *>(prow + sw128_row(hd, 4 * hf + q)) =
+          *reinterpret_cast<uint4 *>(prow + sw128_row(hd, 4 * hf + 2 * sub + q)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
-        l_run = l_run * al + ls;
+        l_run = l_run * al + ls;  // this lane's part of the head's normaliser
         m_run = mn;
-        if (hf == 0) {
+        if (hf == 0 && owner) {
           s_alpha[hd] = al;
           if (t > 0 && al != 1.f) s_rescale[j] = 1;
         }
@@ -310,6 +319,7 @@ __global__ void __launch_bounds__(MLA_NT, 1)
       }
       if (s_stop) break;
     }
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);  // lanes l and l + 16: one head
     if (owner) {
       if (hf == 0) s_l[hd] = l_run, s_mfin[hd] = m_run;
       else s_lpart[hd] = l_run;
