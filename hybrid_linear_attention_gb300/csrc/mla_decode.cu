@@ -332,7 +332,9 @@ __global__ void __launch_bounds__(MLA_NT, 1)
   // ---- z = Z / l per head (softmax warps: thread = latent channel of its lane quarter;
   //      warps w and w + 4 take slices 0-1 and 2-3) ------------------------------------------
   if (warp < 8) {
-    const bool done = ntiles > 0 && !s_abort && wait(MB_Z, (uint32_t)((ntiles - 1) & 1));
+    // the warp shares the outcome (its tensor-memory loads below are warp-wide)
+    const bool done = __all_sync(0xffffffffu, ntiles > 0 && !s_abort &&
+                                                  wait(MB_Z, (uint32_t)((ntiles - 1) & 1))) != 0;
     tc_fence_after();
     const int qw = warp & 3, hf = warp >> 2;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
