@@ -380,20 +380,29 @@ __global__ void __launch_bounds__(MLA_NT, 1)
   if (warp == 0) tmem_dealloc(tm, 512);
 }
 
-// z[b][h] = sum_s 2^(m_s - M) Z_s / sum_s 2^(m_s - M) l_s over the splits (M = max_s m_s)
+// z[b][h] = sum_s 2^(m_s - M) Z_s / sum_s 2^(m_s - M) l_s over the splits (M = max_s m_s).
+// The splits' (m, l) come into shared memory once (one thread each); the partial sums' loads
+// do not depend on the running sums, so eight of them are in flight at a time.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaArgs a, int n_split) {
+  __shared__ float s_m[64], s_l[64];  // n_split <= 64
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const float *ml = a.part + (size_t)n_split * a.B * MH * ML;
+  if (tid < n_split) {
+    const float *p = ml + (((size_t)tid * a.B + b) * MH + h) * 2;
+    s_m[tid] = p[0];
+    s_l[tid] = p[1];
+  }
+  __syncthreads();
   float M = -INFINITY;
-  for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, ml[(((size_t)sp * a.B + b) * MH + h) * 2]);
+  for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, s_m[sp]);
   float acc[4] = {0.f, 0.f, 0.f, 0.f}, L = 0.f;
-  for (int sp = 0; sp < n_split; ++sp) {
+#pragma unroll 8
+  for (int sp = 0; sp < n_split; ++sp) {  // an empty split (m = -inf) has Z = 0, l = 0: weight 0
+    const float m = s_m[sp];
+    const float w = m == -INFINITY ? 0.f : exp2f(m - M);
     const size_t row = (size_t)sp * a.B + b;
-    const float m = ml[(row * MH + h) * 2];
-    if (m == -INFINITY) continue;
-    const float w = exp2f(m - M);
-    L = fmaf(w, ml[(row * MH + h) * 2 + 1], L);
     const float4 zz = *reinterpret_cast<const float4 *>(a.part + (row * MH + h) * ML + 4 * tid);
+    L = fmaf(w, s_l[sp], L);
     acc[0] = fmaf(w, zz.x, acc[0]), acc[1] = fmaf(w, zz.y, acc[1]);
     acc[2] = fmaf(w, zz.z, acc[2]), acc[3] = fmaf(w, zz.w, acc[3]);
   }
