@@ -139,17 +139,20 @@ __global__ void __launch_bounds__(PT, 1)
 }
 
 // ---- value up-projection and gate ----------------------------------------------------------
-// per stage s (latent channels 64 s .. 64 s + 63), double-buffered: z raw fp32 (two boxes of
-// [128 rows][32], 16 KB each), W_V [128 v][64 l] bf16 (16 KB), z hi | lo bf16 ([128][64], 16 KB each)
-constexpr uint32_t UG_STAGE = 32768 + 16384 + 32768;
-constexpr uint32_t UG_Z = 0, UG_W = 32768, UG_HI = 49152, UG_LO = 65536;
-constexpr uint32_t UG_SMEM = 2 * UG_STAGE + 1024;
+// per stage s (latent channels 64 s .. 64 s + 63), four stages in flight: z raw fp32 (two
+// boxes of [128 rows][32], 16 KB each), W_V [128 v][64 l] bf16 (16 KB).  Each thread turns its
+// own row of z into bf16 hi | lo in place: hi over the first box's row, lo over the second's
+// ([128][64] bf16 each, the same 128-byte pitch and swizzle)
+constexpr uint32_t UG_STAGE = 32768 + 16384;
+constexpr uint32_t UG_Z = 0, UG_W = 32768, UG_HI = 0, UG_LO = 16384;
+constexpr int UG_NB = 4;  // stage buffers
+constexpr uint32_t UG_SMEM = UG_NB * UG_STAGE + 1024;
 constexpr int UG_NS = PL / 64;
 
 __global__ void __launch_bounds__(PT, 1)
     mla_up_gate_tc_kernel(const MlaArgs a, const __grid_constant__ ProjMaps maps) {
   extern __shared__ uint8_t praw[];
-  __shared__ __align__(8) uint64_t s_bar[4];  // loads landed (by buffer), products done (by buffer)
+  __shared__ __align__(8) uint64_t s_bar[2 * UG_NB];  // loads landed, products done (by buffer)
   __shared__ uint32_t s_tmem;
   __shared__ int s_fail;
   const uint32_t raw = smem_u32(praw);
@@ -159,7 +162,7 @@ __global__ void __launch_bounds__(PT, 1)
   const int h = blockIdx.x, b0 = blockIdx.y * PB;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&s_bar[i]), 1);
+    for (int i = 0; i < 2 * UG_NB; ++i) mbar_init(smem_u32(&s_bar[i]), 1);
     mbar_fence_init();
     s_fail = 0;
   }
@@ -169,27 +172,28 @@ __global__ void __launch_bounds__(PT, 1)
   tc_fence_after();
   const uint32_t tm = s_tmem;
   auto ld_bar = [&](int j) { return smem_u32(&s_bar[j]); };
-  auto mm_bar = [&](int j) { return smem_u32(&s_bar[2 + j]); };
-  auto load = [&](int s) {  // thread 0: stage s into buffer s & 1
-    const uint32_t base = sb + (uint32_t)(s & 1) * UG_STAGE;
-    mbar_expect_tx(ld_bar(s & 1), 2u * 128u * box_rows(a.B) + 16384u);
-    tma_load_3d(base + UG_Z, &maps.z, 64 * s, h, b0, ld_bar(s & 1));
-    tma_load_3d(base + UG_Z + 16384, &maps.z, 64 * s + 32, h, b0, ld_bar(s & 1));
-    tma_load_3d(base + UG_W, &maps.w, 64 * s, 0, h, ld_bar(s & 1));
+  auto mm_bar = [&](int j) { return smem_u32(&s_bar[UG_NB + j]); };
+  auto load = [&](int s) {  // thread 0: stage s into buffer s % UG_NB
+    const int j = s % UG_NB;
+    const uint32_t base = sb + (uint32_t)j * UG_STAGE;
+    mbar_expect_tx(ld_bar(j), 2u * 128u * box_rows(a.B) + 16384u);
+    tma_load_3d(base + UG_Z, &maps.z, 64 * s, h, b0, ld_bar(j));
+    tma_load_3d(base + UG_Z + 16384, &maps.z, 64 * s + 32, h, b0, ld_bar(j));
+    tma_load_3d(base + UG_W, &maps.w, 64 * s, 0, h, ld_bar(j));
   };
-  if (tid == 0) {
-    load(0);
-    load(1);
-  }
+  if (tid == 0)
+    for (int s = 0; s < UG_NB && s < UG_NS; ++s) load(s);
   constexpr uint32_t ID = idesc(1, 128, 128, 0, 0);  // bf16, both K-major
   bool ok = true;
 #pragma unroll 1
   for (int s = 0; s < UG_NS && ok; ++s) {
-    const int j = s & 1;
+    const int j = s % UG_NB;
     uint8_t *stg = sm + (uint32_t)j * UG_STAGE;
-    if (!proj_wait(ld_bar(j), (uint32_t)((s >> 1) & 1))) s_fail = 1;
+    if (!proj_wait(ld_bar(j), (uint32_t)((s / UG_NB) & 1))) s_fail = 1;
     // row tid: its 64 fp32 values (two swizzled 128-byte rows) -> bf16 hi | lo, K-major
-    // [128 rows][64] with the same 128-byte swizzle
+    // [128 rows][64] with the same 128-byte swizzle, over the same two rows: every value of
+    // the row is read before the first write
+    float xa[2][4][8];
 #pragma unroll
     for (int box = 0; box < 2; ++box) {
       const uint8_t *zr = stg + UG_Z + 16384u * box + (uint32_t)tid * 128u;
@@ -197,7 +201,15 @@ __global__ void __launch_bounds__(PT, 1)
       for (int q = 0; q < 4; ++q) {  // 16-byte pieces of 8 fp32 = pieces 2q, 2q + 1
         const float4 x0 = *reinterpret_cast<const float4 *>(zr + (((2 * q) ^ (tid & 7)) << 4));
         const float4 x1 = *reinterpret_cast<const float4 *>(zr + (((2 * q + 1) ^ (tid & 7)) << 4));
-        const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        xa[box][q][0] = x0.x, xa[box][q][1] = x0.y, xa[box][q][2] = x0.z, xa[box][q][3] = x0.w;
+        xa[box][q][4] = x1.x, xa[box][q][5] = x1.y, xa[box][q][6] = x1.z, xa[box][q][7] = x1.w;
+      }
+    }
+#pragma unroll
+    for (int box = 0; box < 2; ++box) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float(&xs)[8] = xa[box][q];
         uint32_t hw[4], lw[4];
 #pragma unroll
         for (int y = 0; y < 4; ++y) {
@@ -230,18 +242,16 @@ __global__ void __launch_bounds__(PT, 1)
           mma_bf16_ss(tm, ad, bd, ID, (s | term | ks) != 0);
         }
       mma_commit(mm_bar(j));
-      if (s + 2 < UG_NS) {  // buffer j is free once these products have read it
-        if (!proj_wait(mm_bar(j), (uint32_t)((s >> 1) & 1))) s_fail = 1;
-        else load(s + 2);
+      if (s + UG_NB < UG_NS) {  // buffer j is free once these products have read it
+        if (!proj_wait(mm_bar(j), (uint32_t)((s / UG_NB) & 1))) s_fail = 1;
+        else load(s + UG_NB);
       }
     }
   }
-  // the last products (stages UG_NS - 2 and UG_NS - 1, one per buffer)
-  if (ok && tid == 0) {
-    if (!proj_wait(mm_bar(0), (uint32_t)(((UG_NS - 2) >> 1) & 1)) ||
-        !proj_wait(mm_bar(1), (uint32_t)(((UG_NS - 1) >> 1) & 1)))
-      s_fail = 1;
-  }
+  // the last products (stages UG_NS - UG_NB .. UG_NS - 1, one per buffer)
+  if (ok && tid == 0)
+    for (int s = UG_NS - UG_NB; s < UG_NS; ++s)
+      if (!proj_wait(mm_bar(s % UG_NB), (uint32_t)((s / UG_NB) & 1))) s_fail = 1;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -270,7 +280,7 @@ __global__ void __launch_bounds__(PT, 1)
     }
   } else if (tid == 0) {
     // a bounded wait ran out: let the copies and products in flight land (bounded), then report
-    for (int i = 0; i < 4; ++i) proj_wait(smem_u32(&s_bar[i]), 0), proj_wait(smem_u32(&s_bar[i]), 1);
+    for (int i = 0; i < 2 * UG_NB; ++i) proj_wait(smem_u32(&s_bar[i]), 0), proj_wait(smem_u32(&s_bar[i]), 1);
     if (a.err) atomicOr(a.err, ERR_MBAR_TIMEOUT);
   }
   tc_fence_before();
