@@ -975,13 +975,15 @@ __global__ void __launch_bounds__(NT, 1)
         for (int y = 0; y < 8; ++y) v[y] = a.scale * fmaf(s_pd[par][32 * grp + 8 * sl + y], u8[y], v[y]);
       };
       const float w = GATE ? (a.norm_w ? a.norm_w[j] : 1.f) : 1.f;
+      float ov[32];  // o of this thread's 32 rows: one tensor-memory round trip
+      if (GATE && !QUANT) load_o(ov);
       if (GATE) {
         wait(BAR_GT, par);  // the gate tile, loaded into the stage region after the Y pass
         {
           float sq[32];
-          load_o(sq);
+          if (QUANT) load_o(sq);
 #pragma unroll
-          for (int x = 0; x < 32; ++x) sq[x] *= sq[x];
+          for (int x = 0; x < 32; ++x) sq[x] = QUANT ? sq[x] * sq[x] : ov[x] * ov[x];
           transpose_reduce(sq, false);
           s_red[quarter][32 * grp + lane] = sq[0];
         }
@@ -1061,21 +1063,23 @@ __global__ void __launch_bounds__(NT, 1)
           }
         }
       } else if (GATE) {
-#pragma unroll 1
-        for (int sl = 0; sl < 4; ++sl) {  // 8 rows at a time, o re-read: a short loop body
-          float o8[8], u8[8];
-          tmem_ld8(tm + lane_off + TM_C + 64 + 32 * grp + 8 * sl, o8);
-          tmem_ld8(tm + lane_off + TM_B + 32 * grp + 8 * sl, u8);
-          tmem_wait_ld();
+        // sigma(gate) of the 32 rows first (every logit read before the outputs overwrite the
+        // stage region), then the outputs two rows per packed conversion from o in registers
+        float sg[32];
 #pragma unroll
-          for (int y = 0; y < 8; ++y) {
-            const int r = 32 * grp + 8 * sl + y;
-            if (r < nv) {  // each thread overwrites the gate logit it has just read
-              const float val = a.scale * fmaf(s_pd[par][r], u8[y], o8[y]) * s_nrm[r] * w *
-                                sigmoid_sfu(__bfloat162float(stage[r * D + j]));
-              if (tile) stage[r * D + j] = __float2bfloat16_rn(val);
-              else out[((size_t)(t0 + r) * H + h) * D + j] = __float2bfloat16_rn(val);
-            }
+        for (int x = 0; x < 32; ++x) sg[x] = sigmoid_sfu(__bfloat162float(stage[(32 * grp + x) * D + j]));
+#pragma unroll
+        for (int x = 0; x < 32; x += 2) {
+          const int r = 32 * grp + x;
+          const uint32_t pr = pack_bf2(ov[x] * s_nrm[r] * w * sg[x], ov[x + 1] * s_nrm[r + 1] * w * sg[x + 1]);
+          const uint16_t v0 = (uint16_t)(pr & 0xffffu), v1 = (uint16_t)(pr >> 16);
+          if (tile) {
+            reinterpret_cast<uint16_t *>(stage)[r * D + j] = v0;
+            reinterpret_cast<uint16_t *>(stage)[(r + 1) * D + j] = v1;
+          } else {
+            uint16_t *o16 = reinterpret_cast<uint16_t *>(out);
+            if (r < nv) o16[((size_t)(t0 + r) * H + h) * D + j] = v0;
+            if (r + 1 < nv) o16[((size_t)(t0 + r + 1) * H + h) * D + j] = v1;
           }
         }
       } else {
