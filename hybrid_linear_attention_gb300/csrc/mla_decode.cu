@@ -40,6 +40,7 @@ constexpr int MR = 64;        // positional-key width
 constexpr int MK = ML + MR;   // cached key width
 constexpr int TP = 64;        // cached positions per tile
 constexpr int KB = MK / 64;   // 64-element key blocks (128 bytes of bf16)
+constexpr int PFD = 2;       // tiles ahead of the one being loaded that are fetched into L2
 constexpr int MLA_NT = 384;   // eight softmax warps (two per TMEM lane quarter) + four issuer warps
 
 // shared memory of the latent kernel (1024-byte aligned base): Q [KB][64 heads][128 B]
@@ -66,6 +67,13 @@ __device__ __forceinline__ float ex2f_sfu(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// a tensor tile fetched into L2 only (no shared memory, no barrier)
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
 }
 // offset of (row r, 16-byte chunk j) in a 128-byte-swizzled block
 __device__ __forceinline__ uint32_t sw128_row(int r, int j) {
@@ -147,6 +155,10 @@ __global__ void __launch_bounds__(MLA_NT, 1)
         for (int kb = 0; kb < KB; ++kb)
           tma_load_3d(sb + M_OFF_C + j * TILE + kb * BLK, &maps.c, 64 * kb, TP * (tbase + t), b,
                       bar(MB_C0 + j));
+        if (t + PFD < ntiles)  // the tile PFD further on, into L2 while this one is used:
+                               // its own load then waits on L2, not on HBM
+          for (int kb = 0; kb < KB; ++kb)
+            tma_prefetch_3d(&maps.c, 64 * kb, TP * (tbase + t + PFD), b);
       };
       if (warp < 10) {
         // S = Q C^T: M = 64 heads (A = Q), N = 64 positions (B = C), both K-major
