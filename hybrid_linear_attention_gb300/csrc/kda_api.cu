@@ -166,8 +166,7 @@ kda_status kda_prologue(const kda_params *p, const void *x_raw, const void *conv
   a.q = q, a.k = k, a.v = v;
   a.beta = beta, a.g = g;
   a.err = device_error_ptr();
-  const int n_launch = (total_tokens > 0 ? 1 + ((g_raw || beta_logit) ? 1 : 0) : 0) +
-                       (conv_state ? 1 : 0);
+  const int n_launch = (total_tokens > 0 ? 1 : 0) + (conv_state ? 1 : 0);
   return finish(kda::launch_prologue(a, p->d_k, p->io_dtype == KDA_BF16, stream), n_launch);
 }
 

@@ -10,7 +10,8 @@
 //   prologue_kernel     packed prefill: conv + SiLU (+ per-head L2 of q, k) for a share of
 //                       the tokens x (stream, head) rows, 16-byte vectors, one read per
 //                       input, the next tokens' inputs always in flight.
-//   gate_act_kernel     the gate activations beta = sigmoid(logit), g = max(g_raw, g_min).
+//                       The gate activations beta = sigmoid(logit), g = max(g_raw, g_min)
+//                       are spread over the same CTAs after their tokens.
 //   conv_tail_kernel    afterwards, the new tail of every sequence (separate launch, so the
 //                       in-place update never races with the reads of the old tail).
 //   conv_update_kernel  decode: one new token per sequence, tail shifted in place.
@@ -109,6 +110,21 @@ template <> struct ConvW<float> {
   }
   __device__ __forceinline__ float tap(int y, int j) const { return w[y][j]; }
 };
+
+// Gate activations, elementwise: g = max(g_raw, g_min) (four at a time), beta = sigmoid;
+// thread e0 of nthr takes elements e0, e0 + nthr, ...  (without g_raw only the T * H gates)
+template <int D>
+__device__ __forceinline__ void gate_act(const ProArgs &a, int64_t e0, int64_t nthr) {
+  const int64_t n4 = a.g_raw ? a.T * a.H * (int64_t)D / 4 : 0, nb = a.T * a.H;
+  for (int64_t e = e0; e < n4; e += nthr) {
+    const float4 v = reinterpret_cast<const float4 *>(a.g_raw)[e];
+    reinterpret_cast<float4 *>(a.g)[e] = make_float4(fmaxf(v.x, a.g_min), fmaxf(v.y, a.g_min),
+                                                     fmaxf(v.z, a.g_min), fmaxf(v.w, a.g_min));
+    if (a.beta_logit && e < nb) a.beta[e] = sigmoidf_(a.beta_logit[e]);
+  }
+  if (a.beta_logit)
+    for (int64_t e = n4 + e0; e < nb; e += nthr) a.beta[e] = sigmoidf_(a.beta_logit[e]);
+}
 
 // One CTA: a share of the tokens x PNT/(D/8) rows of D channels (a row = one head of one of the
 // q, k, v streams); D/8 threads per row, eight channels each.  Every thread walks the tile's
@@ -210,24 +226,11 @@ __global__ void __launch_bounds__(PNT, 2) prologue_kernel(const ProArgs a) {
       dp += (int64_t)H * D;
     }
   }
-}
-
-// Gate activations, elementwise: g = max(g_raw, g_min) (four at a time), beta = sigmoid.
-template <int D>
-__global__ void gate_act_kernel(const ProArgs a) {
-  // without g_raw only the T * H gates are walked
-  const int64_t n4 = a.g_raw ? a.T * a.H * (int64_t)D / 4 : 0, nb = a.T * a.H;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n4; e += stride) {
-    if (a.g_raw) {
-      const float4 v = reinterpret_cast<const float4 *>(a.g_raw)[e];
-      reinterpret_cast<float4 *>(a.g)[e] = make_float4(fmaxf(v.x, a.g_min), fmaxf(v.y, a.g_min),
-                                                       fmaxf(v.z, a.g_min), fmaxf(v.w, a.g_min));
-    }
-    if (a.beta_logit && e < nb) a.beta[e] = sigmoidf_(a.beta_logit[e]);
-  }
-  for (int64_t e = n4 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nb; e += stride)
-    if (a.beta_logit) a.beta[e] = sigmoidf_(a.beta_logit[e]);
+  // the gate activations ride along: each CTA takes a grid-strided share after its tokens (no
+  // launch of their own)
+  if (a.beta_logit || a.g_raw)
+    gate_act<D>(a, ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) * PNT + tid,
+                (int64_t)gridDim.x * gridDim.y * PNT);
 }
 
 // New tail of sequence n: the last three raw inputs, reaching into the old tail when the
@@ -330,14 +333,6 @@ cudaError_t launch_pro(const ProArgs &a, cudaStream_t s) {
     prologue_kernel<D, IO><<<grid, PNT, 0, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (a.g_raw || a.beta_logit) {
-      const int64_t work = a.g_raw ? a.T * a.H * (int64_t)D / 4 : a.T * a.H;
-      const int64_t blocks = (work + 255) / 256;
-      const int64_t cap = (int64_t)nsm * 8;
-      gate_act_kernel<D><<<(unsigned)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap), 256, 0, s>>>(a);
-      e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
-    }
   }
   if (a.conv_state && a.n_seqs > 0) {
     const int C = 3 * a.H * D;
