@@ -852,10 +852,10 @@ __global__ void __launch_bounds__(NT, 1)
       }
       commit(mma_par);
   };
-  auto kbar = [&](int nv) {
-    // Kbar = k Gamma_C / Gamma (bf16 hi | lo, MN-major) into X[0, 32K) while u is formed;
-    // then k and g of the next chunk may be loaded
-    for (int it = tid; it < C * 16; it += NT) {  // Kbar hi | lo
+  // Kbar = k Gamma_C / Gamma (bf16 hi | lo, MN-major) into X[0, 32K), items [i0, i1) of the
+  // (token, 8-channel group) list by thread t of nt
+  auto kbar_items = [&](int nv, int i0, int i1, int t, int nt) {
+    for (int it = i0 + t; it < i1; it += nt) {  // Kbar hi | lo
       const int s = it >> 4, c8 = it & 15;
       uint32_t hw[4], lw[4];
       if (s < nv) {
@@ -883,6 +883,11 @@ __global__ void __launch_bounds__(NT, 1)
           make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
   };
+  // the whole of it, while u is formed; then k and g of the next chunk may be loaded
+  auto kbar = [&](int nv) { kbar_items(nv, 0, C * 16, tid, NT); };
+  // cluster-pair consumer: warp group 2 builds the first KB2 items once the state read is done
+  // (it frees X), in the Y phase it would otherwise idle through; the rest while u is formed
+  constexpr int KB2 = 256;
   auto p6 = [&]() {
     // ---- P6: u from TC[0, 64) (fp32 -> TB[0,64) for the output, tf32 -> TB[64,128) for
     //      P'u) and u hi | lo (bf16, K-major [j][s]) into X[32K, 64K) -----------------------
@@ -1198,6 +1203,8 @@ __global__ void __launch_bounds__(NT, 1)
         y_decay(nv, par, false, true);
       } else {  // S^T *= Gamma_C: MMA1 reads the split state in TA, not S
         decay(0, 4);
+        wait(BAR_X, par);  // the state read is done: X may be rewritten
+        kbar_items(nv, 0, KB2, tid - 256, 128);
       }
       fence_proxy_async();
       if (!(ok = sync())) break;
@@ -1211,7 +1218,7 @@ __global__ void __launch_bounds__(NT, 1)
           s_abort = 1;
         }
       }
-      kbar(nv);
+      kbar_items(nv, KB2, C * 16, tid, NT);
       fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0 && more) issue((1u << BAR_K) | (1u << BAR_G), c + 1);
