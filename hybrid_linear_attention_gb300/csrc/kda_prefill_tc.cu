@@ -915,6 +915,38 @@ __global__ void __launch_bounds__(NT, 1)
       tmem_wait_st();
     }
   };
+  auto p6_spread = [&]() {
+    // ---- the same in 8-column slices spread over the three warp groups (3, 3, 2): the
+    //      one-CTA form, whose group 2 is otherwise idle here (the pair's group 2 gains
+    //      nothing from it: it is the next chunk's P1 that waits) ----------------------------
+    float u[3][8];
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+      if (grp + 3 * q < 8) tmem_ld8(tm + lane_off + TM_C + 8 * (grp + 3 * q), u[q]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      const int s8 = grp + 3 * q;
+      if (s8 < 8) {
+        float t[8];
+        tmem_st8(tm + lane_off + TM_B + 8 * s8, u[q]);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) t[x] = to_tf32(u[q][x]);
+        tmem_st8(tm + lane_off + TM_B + 64 + 8 * s8, t);
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          const float a0 = u[q][2 * y], a1 = u[q][2 * y + 1];
+          hw[y] = pack_bf2(a0, a1);
+          lw[y] = pack_bf2(a0 - bf_lo(hw[y]), a1 - bf_hi(hw[y]));
+        }
+        const uint32_t off = kmaj_bf16_64(j, 8 * s8);
+        *reinterpret_cast<uint4 *>(sm + OFF_X + 32768 + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4 *>(sm + OFF_X + 49152 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+    }
+    tmem_wait_st();
+  };
   // ---- P7 (thread 0): O += P' u (tf32, P' at shared offset p_off); S^T += u^T Kbar as
   //      hi*hi + hi*lo + lo*hi (bf16)
   auto p7_issue = [&](uint32_t p_off) {
@@ -1150,25 +1182,25 @@ __global__ void __launch_bounds__(NT, 1)
         if (more) issue(1u << BAR_Q, c + 1);  // q is consumed
         mma1_issue(false, 0);
       }
-      if (grp == 2)  // in flight with MMA1 and the Y / decay work
+      if (grp == 2) {  // in flight with MMA1 and the Y / decay work
         inverse(sm + OFF_T, reinterpret_cast<const float *>(sm + OFF_A),
                 reinterpret_cast<float *>(sm + OFF_T), s_M);
-      else y_decay(nv, par, true, false);
+      } else {  // then Kbar (X is free once MMA1 is done) while group 2 still inverts
+        y_decay(nv, par, true, false);
+        kbar_items(nv, 0, C * 16, tid, 256);
+      }
       mma_par ^= 1;  // MMA1's phase (waited by groups 0 and 1)
       fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0) {
         mmau_issue(OFF_T);
         if (GATE) issue(1u << BAR_GT, c);  // V is consumed: the gate tile takes its place
+        if (more) issue((1u << BAR_K) | (1u << BAR_G), c + 1);  // k and g are consumed
       }
-      kbar(nv);  // while u is formed; then k and g of the next chunk may be loaded
-      fence_proxy_async();
-      if (!(ok = sync())) break;
-      if (tid == 0 && more) issue((1u << BAR_K) | (1u << BAR_G), c + 1);
       wait(BAR_MMA, mma_par);  // u ready
       mma_par ^= 1;
       tc_fence_after();
-      p6();
+      p6_spread();
       fence_proxy_async();
       if (!(ok = sync())) break;
       if (tid == 0) p7_issue(OFF_P);
