@@ -69,6 +69,9 @@ constexpr uint32_t OFF_T = 147456;   // 16 KB: T fp32 (plain) -> T tf32 (K-major
 constexpr uint32_t OFF_P = 163840;   // 16 KB: P' tf32 (K-major)
 constexpr uint32_t OFF_A = 180224;   // 17 KB: A fp32, rows of LDA floats
 constexpr int LDA = 68;              // A row stride: rows 16 bytes apart in the bank map
+// the one-CTA inverse's scratch, four 16 x 16 fp32 blocks past A, over the band lo rows of the
+// A/P product's B operand (dead once that product is done)
+constexpr uint32_t OFF_SCR = OFF_A + 64 * LDA * 4;
 // B operand of the A/P product (bf16, K-major), live until that product completes, over
 // T, P' and A: Khat^(R) rows, 48 far then 112 band (hi), and the band rows' lo parts
 constexpr uint32_t OFF_BH = 147456;  // 160 rows x 128 channels x 2 B = 40 KB
@@ -91,6 +94,7 @@ __host__ __device__ constexpr uint32_t off_lt(int b) { return 147456u + 32768u *
 __host__ __device__ constexpr uint32_t off_lp(int b) { return off_lt(b) + 16384u; }
 static_assert(off_lt(0) == OFF_T && off_lp(0) == OFF_P, "landing buffer 0 = T, P' regions");
 static_assert(off_lp(1) + 16384u <= 217088u, "landing buffers inside the shared memory map");
+static_assert(OFF_SCR % 16 == 0 && OFF_SCR + 4 * 256 * 4 <= 217088u, "inverse scratch inside the map");
 
 // K-major 128B-swizzled tf32 operand with NR rows: panels of 32 channels, NR*128 bytes each
 template <int NR>
@@ -762,15 +766,35 @@ __global__ void __launch_bounds__(NT, 1)
         for (int i = 0; i < 16; ++i) Tm[(b0 + i) * 64 + b0 + cc] = x[i];
       }
       asm volatile("bar.sync 3, 128;" ::: "memory");
-      // off-diagonal blocks by distance, one warp per block: M = sum_Q A_RQ T_QS (the A
-      // blocks of row R are contiguous in Q), then T_RS = -T_RR M
-      for (int dist = 1; dist <= 3; ++dist) {
-        if (wg < 4 - dist) {
-          const int R = dist + wg, S = R - dist;
+      if (PAIR) {  // the producer of a pair: by distance (beside its P1 and operand build, the
+                   // fewer warps of the last levels measured faster)
+        // off-diagonal blocks by distance, one warp per block: M = sum_Q A_RQ T_QS (the A
+        // blocks of row R are contiguous in Q), then T_RS = -T_RR M
+        for (int dist = 1; dist <= 3; ++dist) {
+          if (wg < 4 - dist) {
+            const int R = dist + wg, S = R - dist;
+            float dacc[2][4] = {};
+            for (int Q = S; Q < R; ++Q)
+              warp_mma16(dacc, Am + (16 * R) * LDA + 16 * Q, LDA, Tm + (16 * Q) * 64 + 16 * S, 64,
+                         2, lane);
+            warp_store16(scr + wg * 256, 16, dacc, lane, 1.f);
+            __syncwarp();
+            float tacc[2][4] = {};
+            warp_mma16(tacc, Tm + (16 * R) * 64 + 16 * R, 64, scr + wg * 256, 16, 2, lane);
+            warp_store16(Tm + (16 * R) * 64 + 16 * S, 64, tacc, lane, -1.f);
+          }
+          asm volatile("bar.sync 3, 128;" ::: "memory");
+        }
+      } else {
+        // off-diagonal blocks as a 2 x 2 block inverse of 32 x 32 halves, whose diagonal halves
+        // are themselves 2 x 2 block inverses: three levels of at most two 16 x 16 products
+        // each (against three by distance, the last of four on one warp).
+        // level 1 (warps 0, 1): T_10 = -T_11 (A_10 T_00), T_32 = -T_33 (A_32 T_22)
+        if (wg < 2) {
+          const int R = 1 + 2 * wg, S = R - 1;
           float dacc[2][4] = {};
-          for (int Q = S; Q < R; ++Q)
-            warp_mma16(dacc, Am + (16 * R) * LDA + 16 * Q, LDA, Tm + (16 * Q) * 64 + 16 * S, 64,
-                       2, lane);
+          warp_mma16(dacc, Am + (16 * R) * LDA + 16 * S, LDA, Tm + (16 * S) * 64 + 16 * S, 64, 2,
+                     lane);
           warp_store16(scr + wg * 256, 16, dacc, lane, 1.f);
           __syncwarp();
           float tacc[2][4] = {};
@@ -778,19 +802,44 @@ __global__ void __launch_bounds__(NT, 1)
           warp_store16(Tm + (16 * R) * 64 + 16 * S, 64, tacc, lane, -1.f);
         }
         asm volatile("bar.sync 3, 128;" ::: "memory");
+        // level 2 (warp wg: R = 2 + wg / 2, S = wg % 2): X_RS = sum_{Q = S..1} A_RQ T_QS, the
+        // lower-left half's product with the inverse of the upper-left one, into scratch block wg
+        {
+          const int R = 2 + (wg >> 1), S = wg & 1;
+          float dacc[2][4] = {};
+          for (int Q = S; Q < 2; ++Q)
+            warp_mma16(dacc, Am + (16 * R) * LDA + 16 * Q, LDA, Tm + (16 * Q) * 64 + 16 * S, 64,
+                       2, lane);
+          warp_store16(scr + wg * 256, 16, dacc, lane, 1.f);
+        }
+        asm volatile("bar.sync 3, 128;" ::: "memory");
+        // level 3: T_RS = -sum_{Q = 2..R} T_RQ X_QS (the inverse of the lower-right half times X)
+        {
+          const int R = 2 + (wg >> 1), S = wg & 1;
+          float tacc[2][4] = {};
+          for (int Q = 2; Q <= R; ++Q)
+            warp_mma16(tacc, Tm + (16 * R) * 64 + 16 * Q, 64, scr + (2 * (Q - 2) + S) * 256, 16, 2,
+                       lane);
+          warp_store16(Tm + (16 * R) * 64 + 16 * S, 64, tacc, lane, -1.f);
+        }
+        asm volatile("bar.sync 3, 128;" ::: "memory");
       }
-      // T (lower triangle incl. the unit diagonal) -> tf32, K-major [r][s], in place
-      float tv[32];
+      // T (lower triangle incl. the unit diagonal) -> tf32, K-major [r][s], in place, four
+      // consecutive s at a time (16-byte loads and stores: the swizzle moves whole 16-byte
+      // chunks)
+      float4 tv[8];
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int e = t + 128 * q, r = e >> 6, ss = e & 63;
-        tv[q] = ss <= r ? to_tf32(Tm[e]) : 0.f;
+      for (int q = 0; q < 8; ++q) {
+        const int e = 4 * (t + 128 * q), r = e >> 6, s0 = e & 63;
+        const float4 v = *reinterpret_cast<const float4 *>(Tm + e);
+        tv[q] = make_float4(s0 <= r ? to_tf32(v.x) : 0.f, s0 + 1 <= r ? to_tf32(v.y) : 0.f,
+                            s0 + 2 <= r ? to_tf32(v.z) : 0.f, s0 + 3 <= r ? to_tf32(v.w) : 0.f);
       }
       asm volatile("bar.sync 3, 128;" ::: "memory");
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int e = t + 128 * q;
-        *reinterpret_cast<float *>(tbase + kmaj_f32<64>(e >> 6, e & 63)) = tv[q];
+      for (int q = 0; q < 8; ++q) {
+        const int e = 4 * (t + 128 * q);
+        *reinterpret_cast<float4 *>(tbase + kmaj_f32<64>(e >> 6, e & 63)) = tv[q];
       }
   };
   // ---- S^T *= Gamma_C on 32-column blocks first .. first + nblk - 1 of this warp's lane
@@ -1184,7 +1233,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
       if (grp == 2) {  // in flight with MMA1 and the Y / decay work
         inverse(sm + OFF_T, reinterpret_cast<const float *>(sm + OFF_A),
-                reinterpret_cast<float *>(sm + OFF_T), s_M);
+                reinterpret_cast<float *>(sm + OFF_T), reinterpret_cast<float *>(sm + OFF_SCR));
       } else {  // then Kbar (X is free once MMA1 is done) while group 2 still inverts
         y_decay(nv, par, true, false);
         kbar_items(nv, 0, C * 16, tid, 256);

@@ -54,6 +54,10 @@ SCHEMES = {
     "kernel": dict(dt=np.float32, split_ap=True, band=True, p=tf32, inv=tf32, t=tf32,
                    x=tf32, s=tf32_trunc, xq="bf16x3", xk="bf16x3", y_split=True, y=tf32,
                    u=tf32, upd="bf16x3"),
+    # the one-CTA form: the same roundings, the inverse's off-diagonal blocks by halves
+    "kernel_1cta": dict(dt=np.float32, split_ap=True, band=True, p=tf32, inv=tf32, t=tf32,
+                        x=tf32, s=tf32_trunc, xq="bf16x3", xk="bf16x3", y_split=True, y=tf32,
+                        u=tf32, upd="bf16x3", inv_form="halves"),
     "all_bf16": dict(dt=np.float32, split_ap=False, band=False, p=bf16, inv=bf16, t=bf16,
                      x=bf16, s=bf16, y_split=False, y=bf16, u=bf16, upd="bf16"),
     "exact": dict(dt=np.float64, split_ap=False, band=False, p=_ident, inv=_ident, t=_ident,
@@ -77,21 +81,42 @@ def _prod(a, b, sc, band):
 
 def _inverse(A, sc):
     """(I + A)^-1 by 16 x 16 blocks: diagonal blocks exact in the working type, off-diagonal
-    blocks by distance from products of rounded operands."""
+    blocks from products of rounded operands, in one of the kernel's two orders:
+    "distance" (the cluster pair's producer): block (R, S) = -T_RR sum_Q A_RQ T_QS by distance
+    R - S; "halves" (the one-CTA form): a 2 x 2 block inverse of the 32 x 32 halves, whose
+    diagonal halves are 2 x 2 block inverses of their 16 x 16 blocks."""
     dt, rnd = sc["dt"], sc["inv"]
     n = A.shape[0]
     T = np.zeros_like(A)
-    for R in range(n // 16):
-        b = slice(16 * R, 16 * R + 16)
+    blk = [slice(16 * R, 16 * R + 16) for R in range(n // 16)]
+    for b in blk:
         T[b, b] = np.linalg.inv(np.eye(16) + A[b, b].astype(np.float64)).astype(dt)
+    if sc.get("inv_form", "distance") == "halves":
+        assert n == 64
+        for R in (1, 3):  # T_R,R-1 = -T_RR (A_R,R-1 T_R-1,R-1)
+            M = rnd(A[blk[R], blk[R - 1]]) @ rnd(T[blk[R - 1], blk[R - 1]])
+            T[blk[R], blk[R - 1]] = -(rnd(T[blk[R], blk[R]]) @ rnd(M))
+        X = {}
+        for R in (2, 3):  # X_RS = sum_{Q = S..1} A_RQ T_QS
+            for S_ in (0, 1):
+                M = np.zeros((16, 16), dtype=dt)
+                for Q in range(S_, 2):
+                    M = M + rnd(A[blk[R], blk[Q]]) @ rnd(T[blk[Q], blk[S_]])
+                X[R, S_] = M
+        for R in (2, 3):  # T_RS = -sum_{Q = 2..R} T_RQ X_QS
+            for S_ in (0, 1):
+                M = np.zeros((16, 16), dtype=dt)
+                for Q in range(2, R + 1):
+                    M = M + rnd(T[blk[R], blk[Q]]) @ rnd(X[Q, S_])
+                T[blk[R], blk[S_]] = -M
+        return T
     for dist in range(1, n // 16):
         for R in range(dist, n // 16):
             S_ = R - dist
-            rb, sb = slice(16 * R, 16 * R + 16), slice(16 * S_, 16 * S_ + 16)
+            rb, sb = blk[R], blk[S_]
             M = np.zeros((16, 16), dtype=dt)
             for Q in range(S_, R):
-                qb = slice(16 * Q, 16 * Q + 16)
-                M = M + rnd(A[rb, qb]) @ rnd(T[qb, sb])
+                M = M + rnd(A[rb, blk[Q]]) @ rnd(T[blk[Q], sb])
             T[rb, sb] = -(rnd(T[rb, rb]) @ rnd(M))
     return T
 

@@ -46,12 +46,32 @@ def test_model_without_rounding_is_the_recurrence(gate):
     assert eo < 1e-10 and es < 1e-10
 
 
+@pytest.mark.parametrize("scheme", ["kernel", "kernel_1cta"])
 @pytest.mark.parametrize("seed", [300, 301, 302])
-def test_kernel_roundings_meet_the_bounds(seed):
-    eo, es = _run(512, 2, seed, "kernel", gate=False, init="all")
+def test_kernel_roundings_meet_the_bounds(seed, scheme):
+    """Both kernel forms (the pair's inverse by distance, the one-CTA form's by halves)."""
+    eo, es = _run(512, 2, seed, scheme, gate=False, init="all")
     assert eo <= 1e-2 and es <= 1e-3, (eo, es)
-    eo_g, _ = _run(512, 2, seed, "kernel", gate=True)
+    eo_g, _ = _run(512, 2, seed, scheme, gate=True)
     assert eo_g <= 1e-2, eo_g
+
+
+def test_inverse_orders_agree():
+    """The two block orders of the inverse are the same matrix up to the tf32 rounding of their
+    products, and each is (I + A)^-1 to that rounding."""
+    from tests import _kernel_numerics as kn
+    rng = np.random.default_rng(7)
+    k = rng.standard_normal((64, 128))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    A = np.tril(0.5 * (k @ k.T), -1).astype(np.float32)
+    exact = np.linalg.inv(np.eye(64) + A.astype(np.float64))
+    t_d = kn._inverse(A, kn.SCHEMES["kernel"])
+    t_h = kn._inverse(A, kn.SCHEMES["kernel_1cta"])
+    scale = np.abs(exact).max()
+    assert np.abs(t_d - exact).max() <= 1e-3 * scale
+    assert np.abs(t_h - exact).max() <= 1e-3 * scale
+    assert np.abs(t_d - t_h).max() <= 1e-3 * scale
+    assert np.array_equal(np.triu(t_h, 1), np.zeros_like(t_h))
 
 
 def test_single_bf16_operands_miss_the_state_bound():
