@@ -178,10 +178,6 @@ __device__ __forceinline__ float sigmoid_sfu(float x) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + ex2(-1.4426950408889634f * x)));
   return r;
 }
-__device__ __forceinline__ void st_f32x8(uint8_t *p0, uint8_t *p1, const float (&o)[8]) {
-  *reinterpret_cast<float4 *>(p0) = make_float4(o[0], o[1], o[2], o[3]);
-  *reinterpret_cast<float4 *>(p1) = make_float4(o[4], o[5], o[6], o[7]);
-}
 
 // D(16x16) += A(16 x 8kk) B(8kk x 16) for row-major fp32 blocks in shared memory (row
 // strides la, lb), on the warp-level tensor-core MMA (m16n8k8, tf32 inputs, fp32
@@ -902,7 +898,8 @@ __global__ void __launch_bounds__(NT, 1)
       commit(mma_par);
   };
   // Kbar = k Gamma_C / Gamma (bf16 hi | lo, MN-major) into X[0, 32K), items [i0, i1) of the
-  // (token, 8-channel group) list by thread t of nt
+  // (token, 8-channel group) list by thread t of nt; once all of it is built, k and g of the
+  // next chunk may be loaded
   auto kbar_items = [&](int nv, int i0, int i1, int t, int nt) {
     for (int it = i0 + t; it < i1; it += nt) {  // Kbar hi | lo
       const int s = it >> 4, c8 = it & 15;
@@ -932,8 +929,6 @@ __global__ void __launch_bounds__(NT, 1)
           make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
   };
-  // the whole of it, while u is formed; then k and g of the next chunk may be loaded
-  auto kbar = [&](int nv) { kbar_items(nv, 0, C * 16, tid, NT); };
   // cluster-pair consumer: warp group 2 builds the first KB2 items once the state read is done
   // (it frees X), in the Y phase it would otherwise idle through; the rest while u is formed
   constexpr int KB2 = 256;
